@@ -1,0 +1,225 @@
+"""float64 CPU oracle for paged-KV-cache decode attention (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The product library
+never imports, links or loads anything here, and this package imports nothing
+from the product package.
+
+The arithmetic lives in ``pkv_oracle.c`` (plain C loops in double precision,
+compiled with ``-ffp-contract=off`` so that x86 and Arm give the same bits).
+This module only builds that file with gcc, loads it with ctypes and moves
+numpy arrays in and out.  Every function cites, in ``pkv_oracle.c``, the
+passage of the pages it follows:
+
+* ``kv_cache_bytes``  -- "推理优化这件事，为什么值得反复复盘", sec. 4.1
+  (2 x L x H x D x S x bytes) and the batch factor of
+  "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.1;
+* ``slot_mapping``, ``append`` -- in-place append into a paged cache
+  ("为什么“推理优化”不是锦上添花", sec. 3.1 and 3.2;
+  "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.3);
+* ``decode`` -- read every cached K/V, score, softmax, weighted sum
+  ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.2);
+* ``decode_partition``, ``merge`` -- the same over consecutive token ranges,
+  recombined by the log-sum-exp identity (not on the pages; see the C file).
+
+Every function is pinned by ``tests/test_oracle.py`` against something other
+than itself (numpy's binary16 decoder, a contiguous textbook softmax, closed
+forms, a pure-Python brute force, the pages' worked size example).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "pkv_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+
+_f64p = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+GCC_FLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c99", "-shared", "-fPIC"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc a C source into a shared object (no FP contraction)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *GCC_FLAGS, src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile pkv_oracle.c into liboracle.so next to it when missing or stale."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+            compile_source(SOURCE, _LIB)
+    return _LIB
+
+
+def _p(a: np.ndarray, ptr_t):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ptr_t)
+
+
+def _bits(a: np.ndarray) -> np.ndarray:
+    """fp16 (or raw uint16) array -> contiguous uint16 bit patterns."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        return a.view(np.uint16)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+class Oracle:
+    """numpy front end over one compiled copy of pkv_oracle.c."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        lib.oracle_half_to_double.restype = ctypes.c_double
+        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_halves_to_doubles.restype = None
+        lib.oracle_halves_to_doubles.argtypes = [_f64p, _u16p, ctypes.c_int64]
+        lib.oracle_kv_cache_bytes.restype = ctypes.c_int64
+        lib.oracle_kv_cache_bytes.argtypes = [ctypes.c_int64] * 6
+        lib.oracle_slot_mapping.restype = None
+        lib.oracle_slot_mapping.argtypes = [_i64p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int]
+        lib.oracle_append.restype = None
+        lib.oracle_append.argtypes = [_u16p, _u16p, _i64p, _u16p, _u16p] + [ctypes.c_int] * 4
+        lib.oracle_decode.restype = None
+        lib.oracle_decode.argtypes = ([_f64p, _u16p, _u16p, _u16p, _i32p, _i32p]
+                                      + [ctypes.c_int] * 6 + [ctypes.c_double])
+        lib.oracle_decode_partition.restype = None
+        lib.oracle_decode_partition.argtypes = ([_f64p, _f64p, _f64p, _u16p, _u16p, _u16p,
+                                                 _i32p, _i32p] + [ctypes.c_int] * 6
+                                                + [ctypes.c_double, ctypes.c_int, ctypes.c_int])
+        lib.oracle_merge.restype = None
+        lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
+        self.lib = lib
+        self.path = lib_path
+
+    def half_to_double(self, a: np.ndarray) -> np.ndarray:
+        """Decode binary16 values (fp16 or uint16 bit patterns) to float64."""
+        bits = _bits(a)
+        out = np.empty(bits.shape, np.float64)
+        self.lib.oracle_halves_to_doubles(_p(out, _f64p), _p(bits, _u16p), bits.size)
+        return out
+
+    def kv_cache_bytes(self, batch: int, layers: int, heads: int, head_dim: int, tokens: int,
+                       elem_bytes: int) -> int:
+        return int(self.lib.oracle_kv_cache_bytes(batch, layers, heads, head_dim, tokens,
+                                                  elem_bytes))
+
+    def slot_mapping(self, block_tables, positions, block_size: int) -> np.ndarray:
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        pos = np.ascontiguousarray(positions, dtype=np.int32)
+        out = np.empty(pos.shape[0], np.int64)
+        self.lib.oracle_slot_mapping(_p(out, _i64p), _p(bt, _i32p), _p(pos, _i32p), pos.shape[0],
+                                     bt.shape[1], block_size)
+        return out
+
+    def append(self, k_cache: np.ndarray, v_cache: np.ndarray, slots, k_new, v_new) -> None:
+        """In place on k_cache / v_cache ([NB, Hkv, bs, D] fp16 or uint16 arrays)."""
+        nb, hkv, bs, d = k_cache.shape
+        kc, vc = _bits(k_cache), _bits(v_cache)
+        assert np.shares_memory(kc, k_cache) and np.shares_memory(vc, v_cache)
+        kn, vn = _bits(k_new), _bits(v_new)
+        sl = np.ascontiguousarray(slots, dtype=np.int64)
+        assert kn.shape == (sl.shape[0], hkv, d) and vn.shape == kn.shape
+        self.lib.oracle_append(_p(kc, _u16p), _p(vc, _u16p), _p(sl, _i64p), _p(kn, _u16p),
+                               _p(vn, _u16p), sl.shape[0], hkv, d, bs)
+
+    def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
+        """float64 [B, Hq, D] attention output of one decode step."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        b, hq, d = qb.shape
+        nb, hkv, bs, d2 = kc.shape
+        assert d2 == d and hq % hkv == 0
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty((b, hq, d), np.float64)
+        self.lib.oracle_decode(_p(out, _f64p), _p(qb, _u16p), _p(kc, _u16p), _p(vc, _u16p),
+                               _p(bt, _i32p), _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs,
+                               float(scale))
+        return out
+
+    def decode_partition(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                         partition_size: int, max_partitions: int):
+        """(o [B,Hq,P,D], m [B,Hq,P], l [B,Hq,P]) float64 split-context partials."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        b, hq, d = qb.shape
+        nb, hkv, bs, _ = kc.shape
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        o = np.empty((b, hq, max_partitions, d), np.float64)
+        m = np.empty((b, hq, max_partitions), np.float64)
+        l = np.empty((b, hq, max_partitions), np.float64)
+        self.lib.oracle_decode_partition(_p(o, _f64p), _p(m, _f64p), _p(l, _f64p), _p(qb, _u16p),
+                                         _p(kc, _u16p), _p(vc, _u16p), _p(bt, _i32p),
+                                         _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs,
+                                         float(scale), partition_size, max_partitions)
+        return o, m, l
+
+    def merge(self, o_part, m_part, l_part, context_lens, partition_size: int) -> np.ndarray:
+        """float64 [B, Hq, D] log-sum-exp merge of split-context partials."""
+        o = np.ascontiguousarray(o_part, dtype=np.float64)
+        m = np.ascontiguousarray(m_part, dtype=np.float64)
+        l = np.ascontiguousarray(l_part, dtype=np.float64)
+        b, hq, p, d = o.shape
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty((b, hq, d), np.float64)
+        self.lib.oracle_merge(_p(out, _f64p), _p(o, _f64p), _p(m, _f64p), _p(l, _f64p),
+                              _p(cl, _i32p), b, hq, d, partition_size, p)
+        return out
+
+
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle built from pkv_oracle.c (compiled on first use)."""
+    global _default
+    if _default is None:
+        path = build()
+        with _lock:
+            if _default is None:
+                _default = Oracle(path)
+    return _default
+
+
+def half_to_double(a):
+    return default().half_to_double(a)
+
+
+def kv_cache_bytes(*args):
+    return default().kv_cache_bytes(*args)
+
+
+def slot_mapping(block_tables, positions, block_size):
+    return default().slot_mapping(block_tables, positions, block_size)
+
+
+def append(k_cache, v_cache, slots, k_new, v_new):
+    return default().append(k_cache, v_cache, slots, k_new, v_new)
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale):
+    return default().decode(q, k_cache, v_cache, block_tables, context_lens, scale)
+
+
+def decode_partition(q, k_cache, v_cache, block_tables, context_lens, scale, partition_size,
+                     max_partitions):
+    return default().decode_partition(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                      partition_size, max_partitions)
+
+
+def merge(o_part, m_part, l_part, context_lens, partition_size):
+    return default().merge(o_part, m_part, l_part, context_lens, partition_size)

@@ -1,0 +1,335 @@
+"""Pins of the float64 CPU oracle against things other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with
+
+* the pages' own worked example (the KV-size formula),
+* hand-worked fixtures under tests/golden/,
+* a textbook contiguous attention (scipy's softmax and numpy matmuls over
+  un-paged K/V, scattered into the paged pool block by block here),
+* closed forms (one key -> v; equal keys or q = 0 -> mean of V; a dominant
+  key -> its v; an empty context -> 0; merge of one partition -> identity),
+* a pure-Python brute force with math.exp and math.fsum,
+* invariances the definition implies (relabelling physical block ids, GQA
+  equal to MHA with K/V repeated per group, split size).
+
+``tests/test_oracle.py`` runs them on the oracle; ``tests/test_oracle_mutants.py``
+runs them on deliberately broken copies of the oracle to show that a
+plausible slip (a dropped term, a wrong sign or index, a swapped operand) is
+caught by at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+from scipy.special import softmax
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ test-side constructions
+
+def random_contiguous(rng, ctxs, hkv, d, value_scale=1.0):
+    """Per-request contiguous K, V: list of fp16 arrays [Hkv, ctx_b, D]."""
+    ks = [(rng.standard_normal((hkv, c, d)) * value_scale).astype(np.float16) for c in ctxs]
+    vs = [rng.standard_normal((hkv, c, d)).astype(np.float16) for c in ctxs]
+    return ks, vs
+
+
+def scatter_to_pool(ks, vs, bs, rng, extra_blocks=2):
+    """Store contiguous per-request K/V in a paged pool [NB, Hkv, bs, D] whose physical
+    block ids are a random permutation; block i of request b holds its tokens
+    [i*bs, (i+1)*bs).  Unused pool memory is filled with NaN so that any read outside the
+    context shows up."""
+    hkv, d = ks[0].shape[0], ks[0].shape[2]
+    need = [-(-k.shape[1] // bs) for k in ks]
+    nb = sum(need) + extra_blocks
+    perm = rng.permutation(nb)
+    kpool = np.full((nb, hkv, bs, d), np.nan, np.float16)
+    vpool = np.full((nb, hkv, bs, d), np.nan, np.float16)
+    bt = np.full((len(ks), max(1, max(need))), -1, np.int32)
+    nxt = 0
+    for b, (k, v) in enumerate(zip(ks, vs)):
+        for i in range(need[b]):
+            phys = perm[nxt]
+            nxt += 1
+            bt[b, i] = phys
+            lo, hi = i * bs, min((i + 1) * bs, k.shape[1])
+            kpool[phys, :, :hi - lo, :] = k[:, lo:hi, :]
+            vpool[phys, :, :hi - lo, :] = v[:, lo:hi, :]
+    ctx = np.array([k.shape[1] for k in ks], np.int32)
+    return kpool, vpool, bt, ctx
+
+
+def textbook_attention(q, ks, vs, scale):
+    """softmax(scale q K^T) V per request and q head on contiguous float64 K/V."""
+    b, hq, d = q.shape
+    hkv = ks[0].shape[0]
+    g = hq // hkv
+    out = np.zeros((b, hq, d))
+    for i in range(b):
+        if ks[i].shape[1] == 0:
+            continue
+        for h in range(hq):
+            kk = ks[i][h // g].astype(np.float64)
+            vv = vs[i][h // g].astype(np.float64)
+            w = softmax(scale * (kk @ q[i, h].astype(np.float64)))
+            out[i, h] = w @ vv
+    return out
+
+
+# ------------------------------------------------------------------ pins
+
+def pin_half_decoding(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def pin_kv_bytes_worked_example(orc):
+    g = golden("kv_cache_bytes.json")
+    got = orc.kv_cache_bytes(g["batch"], g["layers"], g["heads"], g["head_dim"], g["tokens"],
+                             g["elem_bytes"])
+    assert got == g["expected_bytes"]
+    assert round(got / 1e9, 1) == g["printed_gb"]
+    # the batch factor multiplies; a pool of S tokens per layer and kv head is NB*bs*D*2 per tensor
+    assert orc.kv_cache_bytes(8, 32, 8, 128, 2048, 2) == 8 * orc.kv_cache_bytes(1, 32, 8, 128,
+                                                                                  2048, 2)
+    nb, hkv, bs, d = 128, 8, 16, 128
+    assert orc.kv_cache_bytes(1, 1, hkv, d, nb * bs, 2) == 2 * nb * hkv * bs * d * 2
+
+
+def pin_append_golden(orc):
+    g = golden("append_tiny.json")
+    kc = np.array(g["k_cache_before"], np.float16)
+    vc = np.array(g["v_cache_before"], np.float16)
+    orc.append(kc, vc, np.array(g["slot_mapping"], np.int64),
+               np.array(g["k_new"], np.float16), np.array(g["v_new"], np.float16))
+    assert np.array_equal(kc, np.array(g["k_cache_after"], np.float16))
+    assert np.array_equal(vc, np.array(g["v_cache_after"], np.float16))
+
+
+def pin_slot_mapping_by_enumeration(orc):
+    """Walk every block table in order, naming each pool slot by the (request, position)
+    stored there; the slot mapping must be the inverse of that enumeration."""
+    rng = np.random.default_rng(11)
+    for bs in (1, 2, 16, 64):
+        ctxs = [0, 1, bs, 3 * bs + 1, 5 * bs - 1]
+        need = [-(-c // bs) for c in ctxs]
+        nb = sum(need) + 3
+        perm = rng.permutation(nb)
+        bt = np.full((len(ctxs), max(need)), -1, np.int32)
+        owner = {}
+        nxt = 0
+        for b, n in enumerate(need):
+            for i in range(n):
+                bt[b, i] = perm[nxt]
+                for o in range(bs):
+                    owner[(b, i * bs + o)] = int(perm[nxt]) * bs + o
+                nxt += 1
+        for b, c in enumerate(ctxs):
+            pos = np.full(len(ctxs), -1, np.int32)
+            for p in range(c):
+                pos[b] = p
+                got = orc.slot_mapping(bt, pos, bs)
+                assert got[b] == owner[(b, p)]
+                assert all(got[i] == -1 for i in range(len(ctxs)) if i != b)
+
+
+def pin_two_keys_golden(orc):
+    g = golden("attention_two_keys.json")
+    out = orc.decode(np.array(g["q"], np.float16), np.array(g["k_cache"], np.float16),
+                     np.array(g["v_cache"], np.float16), np.array(g["block_tables"], np.int32),
+                     np.array(g["context_lens"], np.int32), g["scale"])
+    assert np.allclose(out, np.array(g["expected_out"]), rtol=0, atol=g["tolerance"])
+
+
+def pin_textbook_contiguous(orc):
+    rng = np.random.default_rng(3)
+    for bs, hq, hkv, d, ctxs in [(16, 4, 2, 128, [1, 15, 16, 17, 100]),
+                                 (2, 3, 3, 8, [5, 2, 9]),
+                                 (64, 8, 1, 64, [200, 64, 1])]:
+        ks, vs = random_contiguous(rng, ctxs, hkv, d)
+        q = rng.standard_normal((len(ctxs), hq, d)).astype(np.float16)
+        kp, vp, bt, ctx = scatter_to_pool(ks, vs, bs, rng)
+        scale = 1.0 / math.sqrt(d)
+        got = orc.decode(q, kp, vp, bt, ctx, scale)
+        ref = textbook_attention(q, ks, vs, scale)
+        assert np.abs(got - ref).max() < 1e-12
+
+
+def pin_one_key_is_v(orc):
+    rng = np.random.default_rng(4)
+    ks, vs = random_contiguous(rng, [1, 1], 2, 16, value_scale=5.0)
+    q = rng.standard_normal((2, 4, 16)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 4, rng)
+    got = orc.decode(q, kp, vp, bt, ctx, 0.25)
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(got[b, h], vs[b][h // 2, 0].astype(np.float64))
+
+
+def pin_uniform_scores_mean_v(orc):
+    rng = np.random.default_rng(5)
+    ctxs = [37, 5]
+    # (a) every key identical -> all scores equal -> out = mean of V
+    k_row = rng.standard_normal(32).astype(np.float16)
+    ks = [np.broadcast_to(k_row, (1, c, 32)).copy() for c in ctxs]
+    vs = [rng.standard_normal((1, c, 32)).astype(np.float16) for c in ctxs]
+    q = rng.standard_normal((2, 1, 32)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 8, rng)
+    got = orc.decode(q, kp, vp, bt, ctx, 0.3)
+    for b in range(2):
+        assert np.abs(got[b, 0] - vs[b][0].astype(np.float64).mean(axis=0)).max() < 1e-14
+    # (b) q = 0 -> all scores zero -> out = mean of V, whatever K is
+    ks2, vs2 = random_contiguous(rng, ctxs, 1, 32, value_scale=3.0)
+    kp, vp, bt, ctx = scatter_to_pool(ks2, vs2, 8, rng)
+    got = orc.decode(np.zeros((2, 1, 32), np.float16), kp, vp, bt, ctx, 0.3)
+    for b in range(2):
+        assert np.abs(got[b, 0] - vs2[b][0].astype(np.float64).mean(axis=0)).max() < 1e-14
+
+
+def pin_dominant_key(orc):
+    rng = np.random.default_rng(6)
+    d, c = 8, 20
+    k = (rng.standard_normal((1, c, d)) * 0.1).astype(np.float16)
+    k[0, 13] = 0
+    k[0, 13, 2] = 8.0
+    v = rng.standard_normal((1, c, d)).astype(np.float16)
+    q = np.zeros((1, 1, d), np.float16)
+    q[0, 0, 2] = 8.0
+    kp, vp, bt, ctx = scatter_to_pool([k], [v], 4, rng)
+    got = orc.decode(q, kp, vp, bt, ctx, 1.0)          # score 64 vs |others| < ~3
+    assert np.abs(got[0, 0] - v[0, 13].astype(np.float64)).max() < 1e-20
+
+
+def pin_block_relabel_invariance(orc):
+    rng = np.random.default_rng(7)
+    ks, vs = random_contiguous(rng, [33, 7, 64], 2, 32)
+    q = rng.standard_normal((3, 4, 32)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 16, rng)
+    base = orc.decode(q, kp, vp, bt, ctx, 0.2)
+    relabel = rng.permutation(kp.shape[0])          # new id of old block i is relabel[i]
+    kp2 = np.empty_like(kp)
+    vp2 = np.empty_like(vp)
+    kp2[relabel] = kp
+    vp2[relabel] = vp
+    bt2 = np.where(bt >= 0, relabel[np.maximum(bt, 0)], -1).astype(np.int32)
+    again = orc.decode(q, kp2, vp2, bt2, ctx, 0.2)
+    assert np.array_equal(base, again)
+
+
+def pin_gqa_is_repeated_mha(orc):
+    rng = np.random.default_rng(8)
+    g = 4
+    ks, vs = random_contiguous(rng, [21, 50], 2, 16)
+    q = rng.standard_normal((2, 2 * g, 16)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 8, rng)
+    gqa = orc.decode(q, kp, vp, bt, ctx, 0.25)
+    ks_r = [np.repeat(k, g, axis=0) for k in ks]
+    vs_r = [np.repeat(v, g, axis=0) for v in vs]
+    kp_r, vp_r, bt_r, ctx_r = scatter_to_pool(ks_r, vs_r, 8, rng)
+    mha = orc.decode(q, kp_r, vp_r, bt_r, ctx_r, 0.25)
+    assert np.abs(gqa - mha).max() < 1e-15
+
+
+def pin_brute_force_python(orc):
+    rng = np.random.default_rng(9)
+    for trial in range(20):
+        ctxs = [int(x) for x in rng.integers(1, 6, size=2)]
+        ks, vs = random_contiguous(rng, ctxs, 1, 4)
+        q = rng.standard_normal((2, 2, 4)).astype(np.float16)
+        kp, vp, bt, ctx = scatter_to_pool(ks, vs, 2, rng)
+        scale = 0.7
+        got = orc.decode(q, kp, vp, bt, ctx, scale)
+        for b in range(2):
+            for h in range(2):
+                qq = [float(x) for x in q[b, h]]
+                sc = [scale * math.fsum(qq[d] * float(ks[b][0, p, d]) for d in range(4))
+                      for p in range(ctxs[b])]
+                mx = max(sc)
+                w = [math.exp(s - mx) for s in sc]
+                tot = math.fsum(w)
+                for d in range(4):
+                    ref = math.fsum(w[p] * float(vs[b][0, p, d]) for p in range(ctxs[b])) / tot
+                    assert abs(got[b, h, d] - ref) <= 1e-14 * max(1.0, abs(ref))
+
+
+def pin_empty_context(orc):
+    rng = np.random.default_rng(10)
+    ks, vs = random_contiguous(rng, [0, 3], 1, 8)
+    q = rng.standard_normal((2, 1, 8)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 2, rng)
+    got = orc.decode(q, kp, vp, bt, ctx, 1.0)
+    assert np.array_equal(got[0], np.zeros((1, 8)))
+    o, m, l = orc.decode_partition(q, kp, vp, bt, ctx, 1.0, 2, 2)
+    assert np.array_equal(orc.merge(o, m, l, ctx, 2)[0], np.zeros((1, 8)))
+
+
+def pin_partition_merge_is_decode(orc):
+    rng = np.random.default_rng(12)
+    ctxs = [1, 16, 17, 100, 511, 512, 513, 1300]
+    ks, vs = random_contiguous(rng, ctxs, 2, 32, value_scale=2.0)
+    q = rng.standard_normal((len(ctxs), 8, 32)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 16, rng)
+    ref = textbook_attention(q, ks, vs, 0.3)
+    for part in (16, 48, 512, 2048):
+        maxp = -(-max(ctxs) // part)
+        o, m, l = orc.decode_partition(q, kp, vp, bt, ctx, 0.3, part, maxp)
+        got = orc.merge(o, m, l, ctx, part)
+        assert np.abs(got - ref).max() < 1e-12, part
+        # unused partitions are marked empty
+        for b, c in enumerate(ctxs):
+            np_b = -(-c // part)
+            assert np.all(l[b, :, np_b:] == 0) and np.all(np.isneginf(m[b, :, np_b:]))
+
+
+def pin_partition_statistics(orc):
+    """One partition covering the whole context: m is the max score, l = sum exp(s - m),
+    o the normalised output -- checked against scores computed here with numpy."""
+    rng = np.random.default_rng(13)
+    ctxs = [9, 40]
+    ks, vs = random_contiguous(rng, ctxs, 1, 16, value_scale=3.0)
+    q = rng.standard_normal((2, 2, 16)).astype(np.float16)
+    kp, vp, bt, ctx = scatter_to_pool(ks, vs, 4, rng)
+    o, m, l = orc.decode_partition(q, kp, vp, bt, ctx, 0.5, 64, 1)
+    ref = textbook_attention(q, ks, vs, 0.5)
+    for b in range(2):
+        for h in range(2):
+            s = 0.5 * (ks[b][0].astype(np.float64) @ q[b, h].astype(np.float64))
+            assert abs(m[b, h, 0] - s.max()) < 1e-13
+            assert abs(l[b, h, 0] - np.exp(s - s.max()).sum()) < 1e-12
+            assert np.abs(o[b, h, 0] - ref[b, h]).max() < 1e-12
+    # merging a single partition returns it unchanged
+    merged = orc.merge(o, m, l, ctx, 64)
+    assert np.array_equal(merged, o[:, :, 0, :])
+
+
+ALL_PINS = [
+    pin_half_decoding,
+    pin_kv_bytes_worked_example,
+    pin_append_golden,
+    pin_slot_mapping_by_enumeration,
+    pin_two_keys_golden,
+    pin_textbook_contiguous,
+    pin_one_key_is_v,
+    pin_uniform_scores_mean_v,
+    pin_dominant_key,
+    pin_block_relabel_invariance,
+    pin_gqa_is_repeated_mha,
+    pin_brute_force_python,
+    pin_empty_context,
+    pin_partition_merge_is_decode,
+    pin_partition_statistics,
+]

@@ -1,0 +1,54 @@
+"""Each pin set must catch a plausible slip in the oracle.
+
+A mistake is planted in a copy of the oracle's C source (on the CPU, in a
+temporary directory), the copy is compiled, and at least one pin must fail on
+it.  This shows that the pins can tell a correct oracle from a nearly-correct
+one: a dropped term, a wrong sign, a wrong index, a swapped operand.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTANTS = {
+    "gqa_head_mapping": ("int j = h / group;\n            double *o = out",
+                         "int j = h % num_kv_heads;\n            double *o = out"),
+    "dropped_scale": ("s[p - p0] = scale * dot;", "s[p - p0] = dot;"),
+    "block_offset_off_by_one": ("        int off = p % bs;\n        double dot",
+                                "        int off = (p + 1) % bs;\n        double dot"),
+    "scores_read_v": ("oracle_half_to_double(k_cache[cache_index(phys, j, off, d, Hkv, bs, D)]);\n        s[",
+                      "oracle_half_to_double(k_cache[cache_index(phys, j, off, (d + 1) % D, Hkv, bs, D)]);\n        s["),
+    "softmax_sign": ("double w = exp(s[p - p0] - m);", "double w = exp(m - s[p - p0]);"),
+    "half_exponent_bias": ("expo - 25", "expo - 24"),
+    "merge_drops_l": ("double w = l_part[row0 + p] * exp(m_part[row0 + p] - M);",
+                      "double w = exp(m_part[row0 + p] - M);"),
+    "append_offset": ("int off = (int)(slot % block_size);", "int off = (int)(slot / block_size) % block_size;"),
+    "append_kv_swapped": ("k_cache[dst] = k_new[src];\n                v_cache[dst] = v_new[src];",
+                          "k_cache[dst] = k_new[src];\n                v_cache[dst] = k_new[src];"),
+    "slot_uses_next_block": ("block_tables[(int64_t)b * max_blocks_per_seq + pos / block_size]",
+                             "block_tables[(int64_t)b * max_blocks_per_seq + (pos + 1) / block_size]"),
+    "kv_bytes_missing_factor": ("return 2 * batch * L * H * D * S * elem_bytes;",
+                                "return batch * L * H * D * S * elem_bytes;"),
+    "max_not_subtracted_in_l": ("        l += w;\n", "        l += w * w;\n"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(oracle.SOURCE, encoding="utf-8") as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new), encoding="utf-8")
+    lib = oracle.compile_source(str(path), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutant {name}"
