@@ -1,0 +1,621 @@
+#!/usr/bin/env python
+"""Benchmark: one decode step (append + paged decode attention, every layer) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha7b] [--block-size 16]
+    python bench.py --impl reference ...      # the float64 CPU oracle on the host cores
+
+A step is the whole hot path over one batch: for each of the 32 layers, pkv_append writes the
+new token's K/V into its slot and pkv_decode_attention attends over every cached token
+(split into 512-token partitions + log-sum-exp merge where a context needs it).  The default
+workload is the 7B-shaped MHA decode: batch 16, 32 layers, 32 q = 32 kv heads, head_dim 128,
+block_size 16, context lengths uniform in [200, 4000] per request (seeded), fp16 K/V ~ N(0, 1),
+physical blocks a seeded permutation of the pool.  Each layer has its own 554 MB cache, so
+every step streams ~17.7 GB: far larger than L2, no flush needed.
+
+Printed (rank 0, one JSON line): decode-attention HBM GB/s over the whole step (value), the
+step time, tokens/s, the dominant kernel's roofline (algorithmic bytes / its CUDA-event time,
+against the measured HBM copy bandwidth), the end-to-end rate through the C ABI with host
+buffers (inputs copied host->device and outputs device->host inside the timed region), SM
+clocks sampled during the timed region, and the CPU oracle's rate on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention HBM GB/s & % of GB300 roofline; tokens/s per step at 1 GPU"
+LAYERS = 32
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "mha7b": "7B-shaped MHA decode: batch 16, 32 layers, 32 q / 32 kv heads, head_dim 128, block_size {bs}, "
+             "context U[200,4000] per request (seeded), fp16 K/V ~N(0,1), one append+decode per layer",
+    "gqa8b": "8B-shaped GQA decode: batch 64, 32 layers, 32 q / 8 kv heads, head_dim 128, block_size {bs}, "
+             "2048 prefilled tokens, decode step t appends position 2047+t (steps cycle 1..128)",
+    "shared_prefix": "shared-prefix batch: batch 32, 32 layers, 32 q / 8 kv heads, head_dim 128, block_size 16, "
+                     "1024-token common prefix (64 shared blocks) + private suffix U[128,1024]",
+    "long_context": "long context: batch 4, 32 layers, 32 q / 8 kv heads, head_dim 128, context 32768, "
+                    "block_size {bs}, 1% of K rows x8 (peaky softmax), 512-token split partitions",
+    "tiny": "tiny: batch 1, 1 layer, 32 q = 32 kv heads, head_dim 128, context 512, block_size 16",
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_over_ranks(ms_per_step: float, units: float, world: int):
+    """Whole-job timing: the slowest rank's time, the sum of every rank's units."""
+    if world <= 1:
+        return ms_per_step, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pkv_decode.cu", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_278_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str, bs: int):
+    """DRAM bytes per launch of the partition kernel from a committed ncu summary, valid only
+    while the kernel source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            fields = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if fields.get("workload") == workload and int(fields.get("block_size", "0")) == bs \
+                    and fields.get("kernel_sha") == want:
+                return float(fields["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons, with host timestamps."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, windows):
+        inside = [s for t, s in self.samples if any(a <= t <= b for a, b in windows)]
+        used = inside if inside else [s for _, s in self.samples]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in used if num(s[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in used:
+            for name, val in zip(names, s[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(used[0][1]),
+                "power_w_max": max((num(s[2]) or 0.0) for s in used),
+                "reasons": sorted(reasons),
+                "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+def gpu_uuid(dev_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+# ----------------------------------------------------------------------------- workload set-up
+
+def make_layer(workload: str, layer: int, bs: int, device, step: int = 1):
+    import workloads
+    if workload == "mha7b":
+        return workloads.mha7b(layer, device=device)
+    if workload == "gqa8b":
+        return workloads.gqa8b(layer, step, bs, device=device)
+    if workload == "shared_prefix":
+        return workloads.shared_prefix(layer, device=device)
+    if workload == "long_context":
+        return workloads.long_context(layer, bs, device=device)
+    if workload == "tiny":
+        return workloads.tiny(device=device)
+    raise ValueError(workload)
+
+
+def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tokens=0, num_seqs=None):
+    """Algorithmic bytes of one decode-attention call: K and V of every cached token read once
+    (a shared prefix once), q read, out written, block-table entries and context lengths read."""
+    b = len(ctx) if num_seqs is None else num_seqs
+    tokens = sum(ctx) - unique_prefix_tokens * (b - 1) if unique_prefix_tokens else sum(ctx)
+    kv = 2 * tokens * num_kv_heads * head_dim * 2
+    qo = 2 * b * num_q_heads * head_dim * 2
+    tables = sum(-(-c // bs) for c in ctx) * 4 + 4 * b
+    return kv + qo + tables
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_278_gb300 as pkv
+    from paged_kv_cache_278_gb300.build import build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build()
+    dev = torch.device("cuda", local)
+
+    bs = args.block_size
+    n_layers = 1 if args.workload == "tiny" else LAYERS
+    steps_cycle = 128 if args.workload == "gqa8b" else 1
+
+    # per-layer caches (distinct, like a real model) and per-layer new-token inputs in one block
+    cases = [make_layer(args.workload, l, bs, dev) for l in range(n_layers)]
+    c0 = cases[0]
+    B, Hq, Hkv, D = c0.num_seqs, c0.num_q_heads, c0.num_kv_heads, c0.head_dim
+    bs = c0.block_size
+    q_all = torch.stack([c.q for c in cases])
+    kn_all = torch.stack([c.k_new for c in cases])
+    vn_all = torch.stack([c.v_new for c in cases])
+    for l, c in enumerate(cases):
+        c.q, c.k_new, c.v_new = q_all[l], kn_all[l], vn_all[l]
+    out_all = torch.empty_like(q_all)
+    block_tables = c0.block_tables.clone()
+    max_ctx_cap = c0.max_blocks_per_seq * bs
+
+    # context lengths / slots of each step of the cycle (host pool logic -> device, once)
+    if args.workload == "gqa8b":
+        import workloads
+        ctx_steps = [[workloads.GQA_PREFILL + t] * B for t in range(1, steps_cycle + 1)]
+    else:
+        ctx_steps = [c0.context_lens.cpu().tolist()]
+    ctx_dev = torch.tensor(ctx_steps, dtype=torch.int32, device=dev)
+    slot_dev = torch.stack([
+        pkv.slot_mapping(block_tables.cpu(), torch.tensor(c, dtype=torch.int32) - 1, bs) for c in ctx_steps]).to(dev)
+    ctx_cur = ctx_dev[0].clone()
+    slot_cur = slot_dev[0].clone()
+    ws = pkv.make_workspace(B, Hq, max_ctx_cap, dev)
+
+    prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
+    bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens) for c in ctx_steps]
+    logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs) for c in ctx_steps]
+
+    split = ws is not None
+    launches_per_step = n_layers * (2 + (1 if split else 0))
+
+    def step():
+        for l, c in enumerate(cases):
+            pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
+            pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
+                                 workspace=ws)
+
+    def set_step(i):
+        j = i % steps_cycle
+        if steps_cycle > 1:
+            ctx_cur.copy_(ctx_dev[j], non_blocking=True)
+            slot_cur.copy_(slot_dev[j], non_blocking=True)
+        return j
+
+    # CPU baseline inputs: host copies of layer 0 taken before any of our kernels run
+    cpu_sample = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_sample = {k: getattr(c0, k).cpu().numpy() for k in
+                      ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            set_step(i)
+            step()
+    torch.cuda.synchronize(dev)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                set_step(i)
+                graph.replay()
+        torch.cuda.synchronize(dev)
+    assert pkv.device_error() == pkv.PKV_DEV_OK
+    assert torch.isfinite(out_all.float()).all()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(gpu_uuid(local))
+    clocks.start()
+    time.sleep(0.3)
+    windows = []
+
+    # ---- timed region 1: K whole steps (CUDA-graph replay of all layers)
+    barrier()
+    t0 = time.time()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    step_bytes = 0
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            j = set_step(i)
+            step_bytes += bytes_per_step[j % len(bytes_per_step)]
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+        e1.record(stream)
+    barrier()
+    windows.append((t0, time.time()))
+    ms_total = e0.elapsed_time(e1)
+    ms_per_step = ms_total / args.steps
+
+    # ---- timed region 2: the dominant kernel alone, CUDA events around every launch
+    maxp = -(-max_ctx_cap // pkv.PKV_DEFAULT_PARTITION)
+    o_part = torch.empty((B, Hq, maxp, D), dtype=torch.float32, device=dev)
+    m_part = torch.empty((B, Hq, maxp), dtype=torch.float32, device=dev)
+    l_part = torch.empty((B, Hq, maxp), dtype=torch.float32, device=dev)
+    kt_steps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(kt_steps * n_layers)]
+    kernel_bytes = 0
+    barrier()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(kt_steps):
+            j = set_step(i)
+            for l, c in enumerate(cases):
+                a, b = ev[i * n_layers + l]
+                a.record(stream)
+                pkv.decode_partition(o_part, m_part, l_part, c.q, c.k_cache, c.v_cache, block_tables, ctx_cur,
+                                     c.scale, pkv.PKV_DEFAULT_PARTITION)
+                b.record(stream)
+                pkv.merge(out_all[l], o_part, m_part, l_part, ctx_cur, pkv.PKV_DEFAULT_PARTITION)
+                kernel_bytes += bytes_per_step[j % len(bytes_per_step)] // n_layers
+    barrier()
+    windows.append((t0, time.time()))
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev)
+    kernel_launches = len(ev)
+
+    # ---- timed region 3: end to end through the public API with host buffers
+    q_h = q_all.cpu().pin_memory()
+    kn_h = kn_all.cpu().pin_memory()
+    vn_h = vn_all.cpu().pin_memory()
+    bt_h = block_tables.cpu().pin_memory()
+    ctx_h = ctx_dev.cpu().pin_memory()
+    slot_h = slot_dev.cpu().pin_memory()
+    out_h = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    h2d = (q_h.numel() + kn_h.numel() + vn_h.numel()) * 2 + bt_h.numel() * 4 + ctx_h[0].numel() * 4 + \
+        slot_h[0].numel() * 8
+    d2h = out_h.numel() * 2
+    e2e_bytes = 0
+    barrier()
+    t0 = time.time()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        x0.record(stream)
+        for i in range(args.steps):
+            j = i % steps_cycle
+            q_all.copy_(q_h, non_blocking=True)
+            kn_all.copy_(kn_h, non_blocking=True)
+            vn_all.copy_(vn_h, non_blocking=True)
+            block_tables.copy_(bt_h, non_blocking=True)
+            ctx_cur.copy_(ctx_h[j], non_blocking=True)
+            slot_cur.copy_(slot_h[j], non_blocking=True)
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+            out_h.copy_(out_all, non_blocking=True)
+            e2e_bytes += bytes_per_step[j % len(bytes_per_step)]
+        x1.record(stream)
+    x1.synchronize()
+    barrier()
+    windows.append((t0, time.time()))
+    e2e_ms = x0.elapsed_time(x1)
+    clocks.stop()
+    assert pkv.device_error() == pkv.PKV_DEV_OK
+    assert torch.isfinite(out_h.float()).all()
+
+    # ---- whole-job numbers
+    ms_job, bytes_job = reduce_over_ranks(ms_per_step, step_bytes / args.steps, world)
+    e2e_ms_job, e2e_bytes_job = reduce_over_ranks(e2e_ms / args.steps, e2e_bytes / args.steps, world)
+    kernel_avg_ms = kernel_ms / kernel_launches
+    kernel_bytes_avg = kernel_bytes / kernel_launches
+    if rank != 0:
+        return
+
+    peak, peak_src = read_peaks()
+    gbs = bytes_job / (ms_job * 1e-3) / 1e9
+    achieved = kernel_bytes_avg / (kernel_avg_ms * 1e-3) / 1e9
+    traffic = read_traffic(args.workload, bs)
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_job, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "accumulate": "f32",
+        "data": "synthetic (seeded N(0,1) fp16 K/V/q, seeded block permutation)",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.workload].format(bs=bs),
+            "layers": n_layers,
+            "batch": B,
+            "num_q_heads": Hq,
+            "num_kv_heads": Hkv,
+            "head_dim": D,
+            "block_size": bs,
+            "partition_size": pkv.PKV_DEFAULT_PARTITION,
+            "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
+                  % (cases[0].k_cache.numel() * 4 / 1e6, bytes_job / 1e9),
+            "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
+        },
+        "tokens_per_s": round(B * world / (ms_job * 1e-3), 1),
+        "pct_of_hbm_peak": round(100 * gbs / peak, 1),
+        "decode_bytes_per_step": int(bytes_job),
+        "logical_bytes_per_step": int(sum(logical_bytes_per_step) / len(logical_bytes_per_step)),
+        "roofline": {
+            "kernel": "decode_partition_kernel (packed-GQA paged decode, 512-token partitions)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(kernel_bytes_avg),
+            "avg_launch_us": round(kernel_avg_ms * 1e3, 2),
+            "launches_timed": kernel_launches,
+        },
+        "e2e": {
+            "value": round(e2e_bytes_job / (e2e_ms_job * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms_job, 4),
+            "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+            "note": "KV cache is device-resident state; each step copies the new tokens' q/k/v for all layers, "
+                    "block tables, context lengths and slots from pinned host memory and reads every layer's "
+                    "output back",
+        },
+        "gpu_launches": launches_per_step * args.steps + (2 * args.steps if steps_cycle > 1 else 0),
+        "clocks": clocks.summary(windows),
+        "kernel_source": kernel_source_hash(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    if cpu_sample is not None:
+        line["cpu_baseline"] = cpu_baseline(cpu_sample, c0, bs, Hkv, Hq, D, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None):
+    """The oracle (single-threaded C, float64) on a bounded sample of the workload: one layer's
+    append + decode for as many requests (in order) as fit the time budget."""
+    import numpy as np
+
+    import oracle
+    ctx = h["context_lens"].tolist()
+    b = len(ctx)
+    slots = oracle.slot_mapping(h["block_tables"], h["positions"], bs)
+    t0 = time.perf_counter()
+    oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"], h["v_new"])
+    done, nbytes = 0, 0
+    limit = b if max_requests is None else min(b, max_requests)
+    while done < limit:
+        sl = slice(done, done + 1)
+        oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl], h["context_lens"][sl],
+                      case.scale)
+        nbytes += decode_bytes(ctx[done:done + 1], hkv, hq, d, bs)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"layer 0: append of all {b} requests + decode of the first {done} of {b} requests "
+                      f"({sum(ctx[:done])} cached tokens), single-threaded C float64, {dt:.1f} s",
+            "cpu": cpu_model()}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle as it stands on the host cores: each step = append + decode of a bounded set of
+    requests of one layer of the same workload; steps sized so the run ends within minutes."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+
+    bs = args.block_size
+    case = make_layer(args.workload, 0, bs, "cpu")
+    bs = case.block_size
+    h = {k: getattr(case, k).numpy() for k in
+         ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
+    ctx = h["context_lens"].tolist()
+    b = len(ctx)
+    # calibrate: one request
+    t0 = time.perf_counter()
+    oracle.decode(h["q"][:1], h["k_cache"], h["v_cache"], h["block_tables"][:1], h["context_lens"][:1], case.scale)
+    per_token = (time.perf_counter() - t0) / max(ctx[0], 1)
+    per_step_budget = args.cpu_budget * 8 / max(args.steps + args.warmup, 1)
+    n_req, tok = 0, 0
+    while n_req < b and (tok + ctx[n_req]) * per_token <= per_step_budget:
+        tok += ctx[n_req]
+        n_req += 1
+    n_req = max(n_req, 1)
+    sl = slice(0, n_req)
+    slots = oracle.slot_mapping(h["block_tables"][sl], h["positions"][sl], bs)
+
+    def one():
+        oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"][sl], h["v_new"][sl])
+        oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl], h["context_lens"][sl],
+                      case.scale)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    nbytes = decode_bytes(ctx[:n_req], case.num_kv_heads, case.num_q_heads, case.head_dim, bs)
+    value = nbytes * args.steps / dt / 1e9
+    sample = (f"per step: layer 0, append + decode of {n_req} of {b} requests ({sum(ctx[:n_req])} cached tokens), "
+              f"single-threaded C float64")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) fp16 K/V/q, seeded block permutation)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload].format(bs=bs), "block_size": bs},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="mha7b")
+    ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

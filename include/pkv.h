@@ -1,0 +1,240 @@
+/*
+ * pkv.h -- C ABI of the paged-KV-cache decode-attention library (libpkv.so).
+ *
+ * One decode step of a transformer layer over a paged KV cache, for one GPU
+ * (NVIDIA GB300, sm_103a):
+ *
+ *   1. the new token's K and V are written in place into their cache slots
+ *      (pkv_append) -- no reallocation, old entries are never recomputed
+ *      ("为什么“推理优化”不是锦上添花", sec. 3.1; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ *      sec. 4.3);
+ *   2. every query head attends over all cached positions of its request,
+ *      out = softmax(scale * q . K^T) . V, with K/V gathered block by block
+ *      through the request's block table (pkv_decode_attention, or the
+ *      explicit split pair pkv_decode_partition + pkv_merge)
+ *      ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2 and 4.2).
+ *
+ * The cache is cut into fixed-size blocks that requests reference through
+ * per-request block tables; blocks can be shared between requests (a common
+ * prompt prefix) ("推理优化这件事，为什么值得反复复盘", sec. 4.2 and 4.3;
+ * "为什么“推理优化”不是锦上添花", sec. 3.2, scheme 1).  The host block pool
+ * (pkv_pool_*) hands out block ids, counts references and frees blocks.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *   * Cache layout: k_cache and v_cache are fp16 arrays
+ *     [num_blocks][num_kv_heads][block_size][head_dim], contiguous.  Slot s
+ *     is (block s / block_size, offset s % block_size).
+ *   * GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   * block_tables: int32 [num_seqs][max_blocks_per_seq]; entry i of row b
+ *     is the physical block holding logical tokens [i*bs, (i+1)*bs) of
+ *     request b.  Entries at or past ceil(context_lens[b] / block_size) are
+ *     never read.
+ *   * context_lens: int32 [num_seqs], the number of cached tokens of each
+ *     request INCLUDING the token appended in this step.  0 is allowed and
+ *     yields a zero output row.
+ *   * Pointers named *_cache, q, out, k_new, v_new, o_part, m_part, l_part,
+ *     block_tables, context_lens, slot_mapping and workspace are DEVICE
+ *     pointers owned by the caller.  The library never allocates, frees or
+ *     retains device memory and keeps no pointer after a call returns.
+ *   * Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream): they validate arguments on the host, enqueue
+ *     kernels and return without synchronising.  A call that returns an
+ *     error has enqueued nothing.
+ *   * Inside the kernels, indices that would leave a buffer (a block id
+ *     outside [0, num_blocks), a context longer than its table, a slot
+ *     outside the pool) are clamped or skipped and recorded in a per-device
+ *     error word; pkv_get_device_error reports and clears it.  No kernel
+ *     traps, asserts or spins without bound.
+ *   * Thread safety: calls may be issued from several host threads; the
+ *     pool object is not internally locked (one owner thread per pool).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG -1   /* null pointer, bad shape, misaligned pointer */
+#define PKV_ERR_UNSUPPORTED -2   /* valid but not implemented (head_dim, group size, ...) */
+#define PKV_ERR_CUDA -3          /* a CUDA runtime call or kernel launch failed */
+#define PKV_ERR_OUT_OF_BLOCKS -4 /* the pool has fewer free blocks than requested */
+#define PKV_ERR_WORKSPACE -5     /* workspace missing or smaller than required */
+#define PKV_ERR_DEVICE_CHECK -6  /* a kernel recorded an out-of-range index */
+
+/* Codes recorded in the device error word (see pkv_get_device_error). */
+#define PKV_DEV_OK 0
+#define PKV_DEV_BAD_BLOCK_ID 1   /* block table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_CONTEXT 2    /* context_lens[b] > max_blocks_per_seq * block_size */
+#define PKV_DEV_BAD_SLOT 3       /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEV_WAIT_TIMEOUT 4   /* an asynchronous copy did not complete in time */
+
+/* Defaults and limits of the decode kernels. */
+#define PKV_HEAD_DIM 128             /* the only head_dim the decode kernels take */
+#define PKV_DEFAULT_PARTITION 512    /* split-context partition used by pkv_decode_attention */
+#define PKV_MAX_PARTITION 4096       /* largest partition_size accepted */
+#define PKV_MIN_BLOCK_SIZE 16        /* block_size must be a multiple of 16 ... */
+#define PKV_MAX_BLOCK_SIZE 256       /* ... and at most 256 */
+
+typedef struct CUstream_st *pkv_stream_t; /* == cudaStream_t */
+typedef struct pkv_pool pkv_pool;         /* opaque host object */
+
+/* Human-readable name of a PKV_* status code (static storage, never NULL). */
+PKV_API const char *pkv_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+PKV_API int pkv_version(void);
+
+/* ================================================================ host pool
+ * Paged allocation of KV-cache blocks, freed on every exit path of a request,
+ * with reference counts for blocks shared as a common prefix
+ * ("推理优化这件事，为什么值得反复复盘", sec. 4.2: paged management, allocate on
+ * demand and free at request end including on failure, shared-prefix cache).
+ * All pool calls are host-only and synchronous.
+ */
+
+/* Create a pool of num_blocks (1 .. 2^31-1) free blocks.  The free list is a
+ * permutation of 0..num_blocks-1 drawn from `seed` (splitmix64 + Fisher-Yates),
+ * so consecutive allocations scatter over the pool.  *out receives the pool;
+ * release it with pkv_pool_destroy.  Errors: INVALID_ARG. */
+PKV_API int pkv_pool_create(int64_t num_blocks, uint64_t seed, pkv_pool **out);
+
+/* Release a pool (NULL is ignored).  Outstanding block ids become invalid. */
+PKV_API void pkv_pool_destroy(pkv_pool *pool);
+
+/* Allocate n blocks (all or nothing), each with reference count 1, writing
+ * their ids to ids[0..n-1].  Errors: INVALID_ARG, OUT_OF_BLOCKS (nothing is
+ * allocated and ids is untouched). */
+PKV_API int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *ids);
+
+/* Add one reference to each of n allocated blocks (prefix sharing).  All ids
+ * are checked before any count changes.  Errors: INVALID_ARG (an id that is
+ * out of range or not allocated). */
+PKV_API int pkv_pool_share(pkv_pool *pool, int n, const int32_t *ids);
+
+/* Drop one reference from each of n blocks; a block whose count reaches 0
+ * returns to the free list.  All ids are checked first (and an id listed
+ * more times than its count is an error), so a failed call changes nothing.
+ * Errors: INVALID_ARG. */
+PKV_API int pkv_pool_free(pkv_pool *pool, int n, const int32_t *ids);
+
+/* Number of free blocks, or -1 for a NULL pool. */
+PKV_API int64_t pkv_pool_num_free(const pkv_pool *pool);
+
+/* Reference count of block id (0 = free), or -1 if id is out of range. */
+PKV_API int pkv_pool_refcount(const pkv_pool *pool, int32_t id);
+
+/* Grow one request's block table so that it covers new_tokens tokens:
+ * table_row[0 .. ceil(cur_tokens/bs)) are the blocks the request holds; the
+ * blocks needed for tokens [cur_tokens, new_tokens) are allocated (all or
+ * nothing) and written after them.  Errors: INVALID_ARG (new_tokens would
+ * exceed max_blocks * block_size, or new_tokens < cur_tokens), OUT_OF_BLOCKS. */
+PKV_API int pkv_pool_reserve(pkv_pool *pool, int32_t *table_row, int max_blocks,
+                             int cur_tokens, int new_tokens, int block_size);
+
+/* Host slot mapping for one new token per request:
+ *   slots[b] = block_tables[b][positions[b] / bs] * bs + positions[b] % bs,
+ * and slots[b] = -1 when positions[b] < 0 (no token for that request).
+ * block_tables, positions and slots are HOST pointers.  Errors: INVALID_ARG
+ * (a position past the table or a negative block id in a read entry). */
+PKV_API int pkv_slot_mapping(int64_t *slots, const int32_t *block_tables, const int32_t *positions,
+                             int num_seqs, int max_blocks_per_seq, int block_size);
+
+/* ================================================================ device calls */
+
+/* In-place append of one decode step's new K/V into the cache.
+ *   k_cache, v_cache : fp16 [num_blocks][num_kv_heads][block_size][head_dim], 16-byte aligned
+ *   slot_mapping     : int64 [num_tokens]; token t goes to slot slot_mapping[t];
+ *                      a negative slot skips the token (padding)
+ *   k_new, v_new     : fp16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned
+ * Each (token, kv head) row is copied bit for bit with 16-byte stores.  Two
+ * tokens naming the same slot race (the caller must not do that).
+ * head_dim must be a multiple of 8; block_size >= 1.  A slot >= num_blocks *
+ * block_size is skipped and recorded as PKV_DEV_BAD_SLOT.
+ * Errors: INVALID_ARG, CUDA. */
+PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                       const void *k_new, const void *v_new, int num_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, pkv_stream_t stream);
+
+/* Bytes of workspace pkv_decode_attention needs for contexts up to
+ * max_context tokens (0 when one partition covers max_context). */
+PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                         int max_context, int partition_size);
+
+/* One decode step of attention for every request and query head:
+ *   out[b][h][:] = softmax(scale * q[b][h] . K_b^T) . V_b
+ * over the context_lens[b] cached tokens of request b, K_b/V_b gathered
+ * through block_tables (kv head h / (num_q_heads / num_kv_heads)).
+ *   out : fp16 [num_seqs][num_q_heads][head_dim]
+ *   q   : fp16 [num_seqs][num_q_heads][head_dim], 16-byte aligned
+ * Requirements: head_dim == 128; num_q_heads / num_kv_heads in {1, 2, 4, 8};
+ * block_size a multiple of 16 in [16, 256]; caches 16-byte aligned.
+ * When max_blocks_per_seq * block_size <= PKV_DEFAULT_PARTITION every request
+ * is done by one pass and the workspace is not used (may be NULL).  Otherwise
+ * contexts are split into partitions of PKV_DEFAULT_PARTITION tokens that run
+ * in parallel and are merged by log-sum-exp; requests that fit one partition
+ * still finish in one pass.  The split needs
+ * pkv_decode_workspace_size(num_seqs, num_q_heads, 128, max_blocks_per_seq *
+ * block_size, PKV_DEFAULT_PARTITION) bytes of 256-byte-aligned workspace.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, int num_seqs,
+                                 int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int64_t num_blocks, float scale,
+                                 void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Split-context partial attention.  Partition p of request b covers logical
+ * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each
+ * such partition and query head h it writes
+ *   m_part[b][h][p]      = max score (natural-log units, scale applied)
+ *   l_part[b][h][p]      = sum over the partition of exp(score - m)
+ *   o_part[b][h][p][:]   = sum exp(score - m) v / l   (normalised, fp32)
+ * o_part: fp32 [num_seqs][num_q_heads][max_partitions][head_dim];
+ * m_part, l_part: fp32 [num_seqs][num_q_heads][max_partitions].
+ * Partitions at or past ceil(ctx_b / partition_size) are not written, except
+ * that an empty request (ctx_b == 0) gets m = -inf, l = 0, o = 0 in partition 0.
+ * max_partitions must be >= ceil(max_blocks_per_seq * block_size / partition_size);
+ * partition_size a multiple of 16 in [16, PKV_MAX_PARTITION].  Other
+ * requirements as pkv_decode_attention.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+PKV_API int pkv_decode_partition(float *o_part, float *m_part, float *l_part, const void *q,
+                                 const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, const int32_t *context_lens,
+                                 int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int64_t num_blocks, float scale, int partition_size,
+                                 int max_partitions, pkv_stream_t stream);
+
+/* Log-sum-exp merge of the partials of pkv_decode_partition:
+ *   M = max_p m_p,  w_p = l_p * exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p
+ * over the ceil(ctx_b / partition_size) partitions of each request, rounded
+ * to fp16 (round to nearest even); an empty request gets a zero row.
+ * out: fp16 [num_seqs][num_q_heads][head_dim].  Errors: INVALID_ARG, CUDA. */
+PKV_API int pkv_merge(void *out, const float *o_part, const float *m_part, const float *l_part,
+                      const int32_t *context_lens, int num_seqs, int num_q_heads, int head_dim,
+                      int partition_size, int max_partitions, pkv_stream_t stream);
+
+/* Synchronise `stream`, then report (in *code) and clear the device error
+ * word of the current device: PKV_DEV_OK when no kernel recorded an index
+ * problem since the last call.  Returns PKV_OK, or CUDA when a runtime call
+ * fails.  This is the only library call that synchronises. */
+PKV_API int pkv_get_device_error(pkv_stream_t stream, int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

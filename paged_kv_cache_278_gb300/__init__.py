@@ -1,0 +1,241 @@
+"""paged_kv_cache_278_gb300 -- decode attention over a paged KV cache on GB300.
+
+A thin Python binding over libpkv.so (C ABI in include/pkv.h).  Every step of
+the hot path runs in the library's CUDA kernels; this module only checks
+tensor shapes/dtypes, passes raw device pointers and the current CUDA stream,
+and turns status codes into exceptions.  PyTorch is used for device memory
+and streams only.
+
+    import paged_kv_cache_278_gb300 as pkv
+    pkv.append(k_cache, v_cache, slot_mapping, k_new, v_new)          # in-place append
+    pkv.decode_attention(out, q, k_cache, v_cache, block_tables,        # softmax(q K^T) V
+                         context_lens, scale, workspace=ws)
+    o, m, l = ...; pkv.decode_partition(o, m, l, q, ...); pkv.merge(out, o, m, l, context_lens, 512)
+
+Cache tensors are fp16 [num_blocks, num_kv_heads, block_size, head_dim].
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
+                   PKV_DEV_OK, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION, PkvError)
+
+__all__ = [
+    "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
+    "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
+    "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
+    "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
+]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _L():
+    return _lib.load()
+
+
+def _stream(device: torch.device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cache_shape(k_cache, v_cache):
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4, k_cache.device)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    return tuple(k_cache.shape)
+
+
+def append(k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_new: torch.Tensor,
+           v_new: torch.Tensor, stream=None) -> None:
+    """Write k_new/v_new [T, Hkv, D] into the cache slots slot_mapping [T] (int64; -1 = skip)."""
+    nb, hkv, bs, d = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    t = slot_mapping.shape[0]
+    if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
+    st = _L().pkv_append(k_cache.data_ptr(), v_cache.data_ptr(), slot_mapping.data_ptr(), k_new.data_ptr(),
+                         v_new.data_ptr(), t, hkv, d, bs, nb, _stream(dev, stream))
+    _lib.check(st, "pkv_append")
+
+
+def decode_workspace_size(num_seqs: int, num_q_heads: int, max_context: int,
+                          partition_size: int = PKV_DEFAULT_PARTITION, head_dim: int = PKV_HEAD_DIM) -> int:
+    return int(_L().pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context, partition_size))
+
+
+def make_workspace(num_seqs: int, num_q_heads: int, max_context: int, device) -> torch.Tensor | None:
+    """Allocate (with torch) the workspace decode_attention needs; None when it needs none."""
+    n = decode_workspace_size(num_seqs, num_q_heads, max_context)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _decode_inputs(q, k_cache, v_cache, block_tables, context_lens):
+    nb, hkv, bs, d = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", torch.float16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    b, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q head_dim differs from the cache's")
+    if block_tables.shape[0] != b or context_lens.shape[0] != b:
+        raise ValueError("block_tables / context_lens batch differs from q")
+    return nb, hkv, bs, d, b, hq, dev
+
+
+def decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out [B, Hq, D] fp16 = softmax(scale q K^T) V over each request's paged context."""
+    nb, hkv, bs, d, b, hq, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.float16, 3, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    st = _L().pkv_decode_attention(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_tables.data_ptr(), context_lens.data_ptr(), b, block_tables.shape[1],
+                                   hq, hkv, d, bs, nb, float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
+    _lib.check(st, "pkv_decode_attention")
+    return out
+
+
+def decode_partition(o_part: torch.Tensor, m_part: torch.Tensor, l_part: torch.Tensor, q: torch.Tensor,
+                     k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, scale: float, partition_size: int = PKV_DEFAULT_PARTITION,
+                     stream=None) -> None:
+    """Split-context partials: o_part [B,Hq,P,D], m_part/l_part [B,Hq,P] (fp32)."""
+    nb, hkv, bs, d, b, hq, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(o_part, "o_part", torch.float32, 4, dev)
+    _need(m_part, "m_part", torch.float32, 3, dev)
+    _need(l_part, "l_part", torch.float32, 3, dev)
+    p = o_part.shape[2]
+    if o_part.shape != (b, hq, p, d) or m_part.shape != (b, hq, p) or l_part.shape != (b, hq, p):
+        raise ValueError("partial buffers must be [B, Hq, P, D] and [B, Hq, P]")
+    st = _L().pkv_decode_partition(o_part.data_ptr(), m_part.data_ptr(), l_part.data_ptr(), q.data_ptr(),
+                                   k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                   context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb,
+                                   float(scale), partition_size, p, _stream(dev, stream))
+    _lib.check(st, "pkv_decode_partition")
+
+
+def merge(out: torch.Tensor, o_part: torch.Tensor, m_part: torch.Tensor, l_part: torch.Tensor,
+          context_lens: torch.Tensor, partition_size: int = PKV_DEFAULT_PARTITION, stream=None) -> torch.Tensor:
+    """Log-sum-exp merge of decode_partition's partials into out [B, Hq, D] fp16."""
+    _need(o_part, "o_part", torch.float32, 4)
+    dev = o_part.device
+    _need(m_part, "m_part", torch.float32, 3, dev)
+    _need(l_part, "l_part", torch.float32, 3, dev)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    b, hq, p, d = o_part.shape
+    if out.shape != (b, hq, d) or m_part.shape != (b, hq, p) or l_part.shape != (b, hq, p):
+        raise ValueError("shape mismatch between out and the partial buffers")
+    st = _L().pkv_merge(out.data_ptr(), o_part.data_ptr(), m_part.data_ptr(), l_part.data_ptr(),
+                        context_lens.data_ptr(), b, hq, d, partition_size, p, _stream(dev, stream))
+    _lib.check(st, "pkv_merge")
+    return out
+
+
+def device_error(device=None, stream=None) -> int:
+    """Synchronise and return (then clear) the device error word: PKV_DEV_OK if no kernel
+    recorded an out-of-range index."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    code = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        st = _L().pkv_get_device_error(_stream(dev, stream), ctypes.byref(code))
+    _lib.check(st, "pkv_get_device_error")
+    return code.value
+
+
+def slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int) -> torch.Tensor:
+    """Host slot of each request's new token: int64 [B] (CPU tensors in, CPU tensor out)."""
+    bt = block_tables.to(torch.int32).contiguous().cpu()
+    pos = positions.to(torch.int32).contiguous().cpu()
+    out = torch.empty(pos.shape[0], dtype=torch.int64)
+    st = _L().pkv_slot_mapping(ctypes.cast(out.data_ptr(), _lib.c_i64p), ctypes.cast(bt.data_ptr(), _lib.c_i32p),
+                               ctypes.cast(pos.data_ptr(), _lib.c_i32p), pos.shape[0], bt.shape[1], block_size)
+    _lib.check(st, "pkv_slot_mapping")
+    return out
+
+
+class BlockPool:
+    """Host pool of KV-cache block ids (free list + reference counts), backed by pkv_pool_*."""
+
+    def __init__(self, num_blocks: int, seed: int = 0):
+        h = ctypes.c_void_p()
+        _lib.check(_L().pkv_pool_create(num_blocks, seed, ctypes.byref(h)), "pkv_pool_create")
+        self._h = h
+        self.num_blocks = num_blocks
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _L().pkv_pool_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _ids(ids):
+        arr = (ctypes.c_int32 * len(ids))(*[int(i) for i in ids])
+        return arr
+
+    def alloc(self, n: int) -> list[int]:
+        arr = (ctypes.c_int32 * max(n, 1))()
+        _lib.check(_L().pkv_pool_alloc(self._h, n, arr), "pkv_pool_alloc")
+        return list(arr[:n])
+
+    def share(self, ids) -> None:
+        _lib.check(_L().pkv_pool_share(self._h, len(ids), self._ids(ids)), "pkv_pool_share")
+
+    def free(self, ids) -> None:
+        _lib.check(_L().pkv_pool_free(self._h, len(ids), self._ids(ids)), "pkv_pool_free")
+
+    def num_free(self) -> int:
+        return int(_L().pkv_pool_num_free(self._h))
+
+    def refcount(self, block_id: int) -> int:
+        return int(_L().pkv_pool_refcount(self._h, block_id))
+
+    def reserve(self, table_row: torch.Tensor, cur_tokens: int, new_tokens: int, block_size: int) -> None:
+        """Grow a CPU int32 block-table row in place to cover new_tokens tokens."""
+        if table_row.dtype != torch.int32 or table_row.device.type != "cpu" or not table_row.is_contiguous():
+            raise ValueError("table_row must be a contiguous CPU int32 tensor")
+        st = _L().pkv_pool_reserve(self._h, ctypes.cast(table_row.data_ptr(), _lib.c_i32p), table_row.numel(),
+                                   cur_tokens, new_tokens, block_size)
+        _lib.check(st, "pkv_pool_reserve")

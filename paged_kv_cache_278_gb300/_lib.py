@@ -1,0 +1,97 @@
+"""ctypes loader for libpkv.so (the C ABI declared in include/pkv.h).
+
+The shared library is built in-tree by ``paged_kv_cache_278_gb300.build`` (or
+``__graft_entry__.build()``).  There is no fallback: if the library is missing
+or fails to load, importing the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+c_int, c_int64, c_size_t, c_float, c_void_p, c_uint64 = (
+    ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p, ctypes.c_uint64)
+c_i32p = ctypes.POINTER(ctypes.c_int32)
+c_i64p = ctypes.POINTER(ctypes.c_int64)
+
+# status codes (mirror include/pkv.h)
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_CUDA = -3
+PKV_ERR_OUT_OF_BLOCKS = -4
+PKV_ERR_WORKSPACE = -5
+PKV_ERR_DEVICE_CHECK = -6
+
+PKV_DEV_OK = 0
+PKV_DEV_BAD_BLOCK_ID = 1
+PKV_DEV_BAD_CONTEXT = 2
+PKV_DEV_BAD_SLOT = 3
+PKV_DEV_WAIT_TIMEOUT = 4
+
+PKV_HEAD_DIM = 128
+PKV_DEFAULT_PARTITION = 512
+PKV_MAX_PARTITION = 4096
+
+# every symbol include/pkv.h declares: name -> (restype, argtypes)
+SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [c_int]),
+    "pkv_version": (c_int, []),
+    "pkv_pool_create": (c_int, [c_int64, c_uint64, ctypes.POINTER(c_void_p)]),
+    "pkv_pool_destroy": (None, [c_void_p]),
+    "pkv_pool_alloc": (c_int, [c_void_p, c_int, c_i32p]),
+    "pkv_pool_share": (c_int, [c_void_p, c_int, c_i32p]),
+    "pkv_pool_free": (c_int, [c_void_p, c_int, c_i32p]),
+    "pkv_pool_num_free": (c_int64, [c_void_p]),
+    "pkv_pool_refcount": (c_int, [c_void_p, ctypes.c_int32]),
+    "pkv_pool_reserve": (c_int, [c_void_p, c_i32p, c_int, c_int, c_int, c_int]),
+    "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
+    "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                           c_int64, c_void_p]),
+    "pkv_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "pkv_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                     c_int, c_int, c_int, c_int, c_int64, c_float, c_void_p, c_size_t,
+                                     c_void_p]),
+    "pkv_decode_partition": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
+                                     c_int, c_int, c_void_p]),
+    "pkv_merge": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                          c_void_p]),
+    "pkv_get_device_error": (c_int, [c_void_p, ctypes.POINTER(c_int)]),
+}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpkv.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libpkv.so is not built ({path}); run `python -m paged_kv_cache_278_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def check(status: int, what: str) -> None:
+    if status != PKV_OK:
+        raise PkvError(status, what)

@@ -1,0 +1,93 @@
+// pkv_append.cu -- in-place append of one decode step's K/V into the paged cache.
+//
+// The new token's K and V go straight into their slots of the preallocated
+// pool; nothing is reallocated and no old entry is touched
+// ("为什么“推理优化”不是锦上添花", sec. 3.1: append into a preallocated tensor;
+// "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.3: an in-place append kernel
+// instead of concatenating a new tensor every step).
+//
+// One thread moves one 16-byte piece of one (token, kv head) row of K or V:
+// reads of k_new/v_new are fully coalesced; each row lands as a contiguous
+// head_dim*2-byte run inside its (block, kv head) tile.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ int g_append_error;
+
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads)
+    append_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                  const int64_t *__restrict__ slot_mapping, const uint4 *__restrict__ k_new,
+                  const uint4 *__restrict__ v_new, int64_t pieces_per_tensor, int num_kv_heads,
+                  int pieces_per_row, int block_size, int64_t num_slots) {
+    int64_t idx = static_cast<int64_t>(blockIdx.x) * kAppendThreads + threadIdx.x;
+    const bool is_v = idx >= pieces_per_tensor;
+    if (is_v) idx -= pieces_per_tensor;
+    if (idx >= pieces_per_tensor) return;
+    const int piece = static_cast<int>(idx % pieces_per_row);
+    const int64_t row = idx / pieces_per_row;  // = token * num_kv_heads + kv head
+    const int head = static_cast<int>(row % num_kv_heads);
+    const int64_t token = row / num_kv_heads;
+    const int64_t slot = __ldg(slot_mapping + token);
+    if (slot < 0) return;  // padding token
+    if (slot >= num_slots) {
+        pkv::record_error(&g_append_error, PKV_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t block = slot / block_size;
+    const int64_t offset = slot - block * block_size;
+    const int64_t dst = ((block * num_kv_heads + head) * block_size + offset) * pieces_per_row + piece;
+    if (is_v)
+        v_cache[dst] = __ldg(v_new + idx);
+    else
+        k_cache[dst] = __ldg(k_new + idx);
+}
+
+}  // namespace
+
+extern "C" PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                                  const void *k_new, const void *v_new, int num_tokens,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, pkv_stream_t stream) {
+    if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!pkv_internal::aligned16(k_cache) || !pkv_internal::aligned16(v_cache) ||
+        !pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new) ||
+        !pkv_internal::aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    const int pieces_per_row = head_dim / 8;
+    const int64_t pieces = static_cast<int64_t>(num_tokens) * num_kv_heads * pieces_per_row;
+    const int64_t blocks = (2 * pieces + kAppendThreads - 1) / kAppendThreads;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    append_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0,
+                    reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping,
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), pieces, num_kv_heads,
+        pieces_per_row, block_size, num_blocks * block_size);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+namespace pkv_internal {
+
+int append_take_error(int *code) {
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_append_error, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_append_error, &zero, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    *code = value;
+    return PKV_OK;
+}
+
+}  // namespace pkv_internal

@@ -1,0 +1,661 @@
+// pkv_decode.cu -- decode attention over a paged KV cache on sm_103a.
+//
+// What is computed ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.2: a decode
+// step reads every cached K/V of the request, scores it, normalises with
+// softmax and takes the weighted sum of V; sec. 3.2: the cache is paged and
+// addressed through a page table):
+//
+//     out[b][h] = softmax(scale * q[b][h] . K_b^T) . V_b
+//
+// How (GB300 design; the pages only give the operation):
+//   * One CTA owns one (request b, kv head, partition of the context).  All
+//     g = Hq/Hkv query heads that read that kv head are packed into the CTA,
+//     so every K/V byte is fetched from HBM exactly once per step.
+//   * The partition is cut into 16-token chunks.  A chunk never straddles a
+//     block (block_size is a multiple of 16), so its K rows (16 x 256 B) and V
+//     rows are each ONE contiguous 4 KiB run in the [block][kv head][slot][dim]
+//     layout, fetched by a single 1-D bulk copy (the TMA engine) into shared
+//     memory and counted on an mbarrier.
+//   * Each of the 4 warps streams its own chunks (w, w+4, w+8, ...) through a
+//     private 3-stage ring: no block-wide barrier inside the main loop, and up
+//     to 3 x 8 KiB in flight per warp, 2 CTAs per SM.
+//   * q . K: LPT lanes share a token row (each lane holds 128/LPT dims of q in
+//     fp32 registers, pre-multiplied by scale*log2(e)); partial dot products
+//     are combined with a reduce-scatter of warp shuffles, after which each
+//     lane holds finished scores for a fixed (token, head) subset.
+//   * Online softmax in fp32 with lazy rescaling: the running max is only
+//     raised (and the accumulators rescaled) when a score exceeds it by more
+//     than 2^8, so most chunks skip the rescale.  Probabilities go through a
+//     small per-warp shared buffer to the P.V stage, where each lane owns 4
+//     output dims of every packed head and walks the chunk's tokens.
+//   * At the end the 4 warps' (m, l, acc) are merged in shared memory; the CTA
+//     writes either the fp16 output (request fits one partition) or fp32
+//     partials (m, l, normalised o) for the log-sum-exp merge kernel.
+//   * Indices read from memory are checked (block ids, context length) and
+//     clamped; problems are recorded in the device error word.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ int g_decode_error;
+
+constexpr int kD = PKV_HEAD_DIM;        // 128
+constexpr int kChunk = 16;              // tokens per shared-memory tile
+constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
+constexpr int kTileBytes = kChunk * kRowBytes;  // 4 KiB
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr float kRescaleThreshold = 8.0f;          // log2 units
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+struct DecodeParams {
+    const __half *q;
+    const unsigned char *k_cache;
+    const unsigned char *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    __half *out;
+    float *o_part;
+    float *m_part;
+    float *l_part;
+    int max_blocks_per_seq;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    int64_t num_blocks;
+    float q_scale;            // scale * log2(e)
+    int partition_size;
+    int max_partitions;
+    int direct_single;        // write fp16 out directly for single-partition requests
+};
+
+// Shared-memory carve-up (bytes), identical on host and device.
+struct SmemLayout {
+    static constexpr int stages = 0;
+    static constexpr int stage_bytes = kWarps * kStages * 2 * kTileBytes;
+    static constexpr int bars = stages + stage_bytes;
+    static constexpr int probs = bars + kWarps * kStages * 8;
+    __host__ __device__ static constexpr int table(int g) { return probs + kWarps * kChunk * g * 4; }
+    __host__ __device__ static constexpr int total(int g, int partition_size) {
+        return table(g) + (partition_size / kChunk + 1) * 4;
+    }
+};
+
+template <int G, int LPT>
+__global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const DecodeParams P) {
+    constexpr int TG = 32 / LPT;            // token groups per warp (q.K stage)
+    constexpr int TPL = kChunk / TG;        // tokens per lane per chunk (q.K stage)
+    constexpr int NP = kD / LPT / 8;        // 16-byte pieces of a row per lane
+    constexpr int N = TPL * G;              // partial dot products per lane
+    constexpr int LOG_LPT = ilog2(LPT);
+    constexpr int LOG_N = ilog2(N);
+    constexpr int HALVING = LOG_LPT < LOG_N ? LOG_LPT : LOG_N;
+    constexpr int HELD = N >> HALVING;      // finished scores per lane
+    constexpr int DUP_BITS = LOG_LPT - HALVING;
+    static_assert((1 << LOG_LPT) == LPT && (1 << LOG_N) == N, "powers of two");
+    static_assert(NP >= 1 && NP * 8 * LPT == kD, "lane split of a row");
+
+    extern __shared__ __align__(1024) unsigned char smem[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int b = blockIdx.z;
+    const int Hq = P.num_q_heads;
+    const int bs = P.block_size;
+
+    // ---------------------------------------------------------------- extent
+    int ctx = __ldg(P.context_lens + b);
+    const int cap = P.max_blocks_per_seq * bs;
+    if (ctx > cap) {
+        if (part == 0 && kvh == 0 && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
+        ctx = cap;
+    }
+    if (ctx < 0) ctx = 0;
+    const int n_parts = (ctx + P.partition_size - 1) / P.partition_size;
+    const bool direct = P.direct_single && n_parts <= 1;
+
+    if (ctx == 0) {  // empty request: zero output (or an empty partial)
+        if (part != 0) return;
+        for (int i = threadIdx.x; i < G * kD; i += kThreads) {
+            const int hq = kvh * G + i / kD, d = i % kD;
+            const int64_t row = static_cast<int64_t>(b) * Hq + hq;
+            if (direct) {
+                P.out[row * kD + d] = __float2half_rn(0.f);
+            } else {
+                P.o_part[(row * P.max_partitions) * kD + d] = 0.f;
+                if (d == 0) {
+                    P.m_part[row * P.max_partitions] = -INFINITY;
+                    P.l_part[row * P.max_partitions] = 0.f;
+                }
+            }
+        }
+        return;
+    }
+    if (part >= n_parts) return;
+
+    const int start = part * P.partition_size;
+    const int n_tok = min(P.partition_size, ctx - start);
+    const int n_chunks = (n_tok + kChunk - 1) / kChunk;
+    const int lb0 = start / bs;
+    const int n_bt = (start + n_tok - 1) / bs - lb0 + 1;
+
+    int32_t *s_table = reinterpret_cast<int32_t *>(smem + SmemLayout::table(G));
+    float *s_prob = reinterpret_cast<float *>(smem + SmemLayout::probs) + warp * kChunk * G;
+    const uint32_t bar0 = pkv::smem_addr(smem + SmemLayout::bars) + warp * kStages * 8;
+    const uint32_t stage0 = pkv::smem_addr(smem + SmemLayout::stages) + warp * kStages * 2 * kTileBytes;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) pkv::mbar_init(bar0 + 8 * s, 1);
+        pkv::fence_mbar_init();
+    }
+    {
+        const int32_t *bt_row = P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq + lb0;
+        for (int i = threadIdx.x; i < n_bt; i += kThreads) {
+            int32_t id = __ldg(bt_row + i);
+            if (id < 0 || id >= P.num_blocks) {
+                pkv::record_error(&g_decode_error, PKV_DEV_BAD_BLOCK_ID);
+                id = 0;
+            }
+            s_table[i] = id;
+        }
+    }
+
+    // q of the G packed heads, this lane's dims, fp32, pre-scaled.
+    const int c = lane & (LPT - 1);   // dim slice within a token row
+    const int r = lane / LPT;         // token group
+    float qf[G][NP * 8];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(
+            P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD);
+#pragma unroll
+        for (int np = 0; np < NP; ++np) {
+            const uint4 raw = __ldg(qrow + c + LPT * np);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = pkv::half2_bits_to_float2(w[e]);
+                qf[hh][np * 8 + 2 * e] = f.x * P.q_scale;
+                qf[hh][np * 8 + 2 * e + 1] = f.y * P.q_scale;
+            }
+        }
+    }
+
+    // Which finished scores this lane ends up holding after the reduce-scatter.
+    int base = 0;
+#pragma unroll
+    for (int s = 0; s < HALVING; ++s)
+        if (lane & (LPT >> (s + 1))) base += N >> (s + 1);
+    const bool owner = (c & ((1 << DUP_BITS) - 1)) == 0;
+    // Finished score k of this lane is (packed head my_head, chunk token held_tok(k)); HELD divides
+    // TPL and base is a multiple of HELD, so all of a lane's scores share one head.
+    static_assert(TPL % HELD == 0, "a lane's finished scores must share one head");
+    const int my_head = base / TPL;
+    auto held_tok = [base, r](int k) { return r + TG * ((base + k) % TPL); };
+
+    __syncthreads();  // table + barrier init visible to every warp
+
+    const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
+    const int64_t head_stride = static_cast<int64_t>(bs) * kRowBytes;
+    const int64_t block_stride = head_stride * P.num_kv_heads;
+
+    auto issue = [=](int i) {
+        const int cidx = warp + i * kWarps;
+        const int tok0 = start + cidx * kChunk;
+        const int valid = min(kChunk, n_tok - cidx * kChunk);
+        const int lb = tok0 / bs;
+        const int off = tok0 - lb * bs;
+        const int64_t phys = s_table[lb - lb0];
+        const int64_t byte_off = phys * block_stride + kvh * head_stride + static_cast<int64_t>(off) * kRowBytes;
+        const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
+        const int st = i % kStages;
+        const uint32_t bar = bar0 + 8 * st;
+        const uint32_t dst = stage0 + st * 2 * kTileBytes;
+        pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
+        pkv::bulk_copy_g2s(dst, P.k_cache + byte_off, bytes, bar);
+        pkv::bulk_copy_g2s(dst + kTileBytes, P.v_cache + byte_off, bytes, bar);
+    };
+
+    if (lane == 0) {
+        const int pre = my_chunks < kStages ? my_chunks : kStages;
+        for (int i = 0; i < pre; ++i) issue(i);
+    }
+
+    // m_head: running max per packed head (warp-uniform); m_mine = m_head[my_head];
+    // l_lane: this lane's share of the softmax denominators; acc: P.V accumulators.
+    float m_head[G], l_lane[G], acc[G][4];
+    float m_mine = -INFINITY;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        m_head[hh] = -INFINITY;
+        l_lane[hh] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[hh][e] = 0.f;
+    }
+
+    int consumed = 0;
+    bool aborted = false;
+    for (int i = 0; i < my_chunks; ++i) {
+        const int st = i % kStages;
+        const bool landed = pkv::mbar_wait_bounded(bar0 + 8 * st, (i / kStages) & 1);
+        if (!__all_sync(pkv::kFullMask, landed)) {  // warp-uniform decision
+            if (lane == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
+            aborted = true;
+            break;
+        }
+        consumed = i + 1;
+        const int cidx = warp + i * kWarps;
+        const int valid = min(kChunk, n_tok - cidx * kChunk);
+        const uint32_t k_tile = stage0 + st * 2 * kTileBytes;
+        const uint32_t v_tile = k_tile + kTileBytes;
+
+        // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
+        float v[N];
+#pragma unroll
+        for (int it = 0; it < TPL; ++it) {
+            const int t = r + TG * it;
+            float kf[NP * 8];
+#pragma unroll
+            for (int np = 0; np < NP; ++np) {
+                const uint4 raw = pkv::lds128(k_tile + t * kRowBytes + (c + LPT * np) * 16);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = pkv::half2_bits_to_float2(w[e]);
+                    kf[np * 8 + 2 * e] = f.x;
+                    kf[np * 8 + 2 * e + 1] = f.y;
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                float sacc = 0.f;
+#pragma unroll
+                for (int e = 0; e < NP * 8; ++e) sacc = fmaf(qf[hh][e], kf[e], sacc);
+                v[hh * TPL + it] = sacc;
+            }
+        }
+        // ---- reduce-scatter across the LPT lanes of a token group
+#pragma unroll
+        for (int s = 0; s < HALVING; ++s) {
+            const int mask = LPT >> (s + 1);
+            const int half = N >> (s + 1);
+            const bool upper = (lane & mask) != 0;
+#pragma unroll
+            for (int k = 0; k < half; ++k) {
+                const float send = upper ? v[k] : v[k + half];
+                const float keep = upper ? v[k + half] : v[k];
+                v[k] = keep + __shfl_xor_sync(pkv::kFullMask, send, mask);
+            }
+        }
+#pragma unroll
+        for (int s = HALVING; s < LOG_LPT; ++s) v[0] += __shfl_xor_sync(pkv::kFullMask, v[0], LPT >> (s + 1));
+
+        // ---- online softmax (log2 domain) with lazy rescale
+        bool need = false;
+#pragma unroll
+        for (int k = 0; k < HELD; ++k) {
+            if (held_tok(k) >= valid) v[k] = -INFINITY;
+            need |= v[k] > m_mine + kRescaleThreshold;
+        }
+        if (__any_sync(pkv::kFullMask, need)) {
+            float mx[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) mx[hh] = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < HELD; ++k)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+                    mx[hh] = fmaxf(mx[hh], my_head == hh ? v[k] : -INFINITY);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+                for (int sh = 0; sh < 5; ++sh)
+                    mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(pkv::kFullMask, mx[hh], 16 >> sh));
+            }
+            m_mine = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float mn = fmaxf(m_head[hh], mx[hh]);
+                const float alpha = exp2f(m_head[hh] - mn);
+                m_head[hh] = mn;
+                l_lane[hh] *= alpha;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[hh][e] *= alpha;
+                m_mine += (my_head == hh) ? mn : 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < HELD; ++k) {
+            const float p = exp2f(v[k] - m_mine);  // 0 for masked tokens
+            if (owner) {
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) l_lane[hh] += (my_head == hh) ? p : 0.f;
+                if (held_tok(k) < valid) s_prob[held_tok(k) * G + my_head] = p;
+            }
+        }
+        __syncwarp();
+
+        // ---- P . V: this lane owns dims [4*lane, 4*lane+4) of every packed head
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t) {
+            if (t < valid) {
+                const uint2 raw = pkv::lds64(v_tile + t * kRowBytes + lane * 8);
+                const float2 v01 = pkv::half2_bits_to_float2(raw.x);
+                const float2 v23 = pkv::half2_bits_to_float2(raw.y);
+                float pr[G];
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) pr[hh] = s_prob[t * G + hh];
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    acc[hh][0] = fmaf(pr[hh], v01.x, acc[hh][0]);
+                    acc[hh][1] = fmaf(pr[hh], v01.y, acc[hh][1]);
+                    acc[hh][2] = fmaf(pr[hh], v23.x, acc[hh][2]);
+                    acc[hh][3] = fmaf(pr[hh], v23.y, acc[hh][3]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && i + kStages < my_chunks) {
+            pkv::fence_proxy_async_smem();
+            issue(i + kStages);
+        }
+    }
+    if (aborted) {
+        // Let this warp's copies still in flight land before the buffers are reused.
+        const int issued = my_chunks < consumed + kStages ? my_chunks : consumed + kStages;
+        for (int i = consumed + 1; i < issued; ++i) pkv::mbar_wait_bounded(bar0 + 8 * (i % kStages), (i / kStages) & 1);
+    }
+
+    // ---- per-warp softmax denominators
+    float l_head[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) l_head[hh] = l_lane[hh];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int sh = 0; sh < 5; ++sh)
+            l_head[hh] += __shfl_xor_sync(pkv::kFullMask, l_head[hh], 16 >> sh);
+
+    // ---- merge the 4 warps in shared memory (reusing the stage buffers)
+    __syncthreads();
+    float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][G][kD]
+    float *c_m = c_acc + kWarps * G * kD;                            // [kWarps][G]
+    float *c_l = c_m + kWarps * G;                                   // [kWarps][G]
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        *reinterpret_cast<float4 *>(c_acc + (warp * G + hh) * kD + lane * 4) =
+            make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            c_m[warp * G + hh] = m_head[hh];
+            c_l[warp * G + hh] = l_head[hh];
+        }
+    }
+    __syncthreads();
+    const int d = threadIdx.x;  // kThreads == kD
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, c_m[w * G + hh]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = exp2f(c_m[w * G + hh] - M);   // 0 for warps without chunks
+            L = fmaf(c_l[w * G + hh], f, L);
+            O = fmaf(c_acc[(w * G + hh) * kD + d], f, O);
+        }
+        const int64_t row = static_cast<int64_t>(b) * Hq + kvh * G + hh;
+        const float o = O / L;
+        if (direct) {
+            P.out[row * kD + d] = __float2half_rn(o);
+        } else {
+            const int64_t prow = row * P.max_partitions + part;
+            P.o_part[prow * kD + d] = o;
+            if (d == 0) {
+                P.m_part[prow] = M * kLn2;
+                P.l_part[prow] = L;
+            }
+        }
+    }
+}
+
+// One CTA per (q head, request); thread d owns output dim d.
+__global__ void __launch_bounds__(kD) merge_kernel(__half *__restrict__ out, const float *__restrict__ o_part,
+                                                   const float *__restrict__ m_part,
+                                                   const float *__restrict__ l_part,
+                                                   const int32_t *__restrict__ context_lens, int num_q_heads,
+                                                   int partition_size, int max_partitions, int skip_single) {
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    const int d = threadIdx.x;
+    int ctx = __ldg(context_lens + b);
+    if (ctx < 0) ctx = 0;
+    int n_parts = (ctx + partition_size - 1) / partition_size;
+    if (n_parts > max_partitions) {
+        if (h == 0 && d == 0) pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
+        n_parts = max_partitions;
+    }
+    if (skip_single && n_parts <= 1) return;  // written by the partition kernel
+    const int64_t row = static_cast<int64_t>(b) * num_q_heads + h;
+    if (n_parts == 0) {
+        out[row * kD + d] = __float2half_rn(0.f);
+        return;
+    }
+    const float *m = m_part + row * max_partitions;
+    const float *l = l_part + row * max_partitions;
+    float M = -INFINITY;
+    for (int p = 0; p < n_parts; ++p) M = fmaxf(M, __ldg(m + p));
+    float wsum = 0.f, acc = 0.f;
+    for (int p = 0; p < n_parts; ++p) {
+        const float w = __ldg(l + p) * expf(__ldg(m + p) - M);
+        wsum += w;
+        acc = fmaf(w, __ldg(o_part + (row * max_partitions + p) * kD + d), acc);
+    }
+    out[row * kD + d] = __float2half_rn(acc / wsum);
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int G>
+constexpr int lanes_per_token() {
+    return G >= 8 ? 16 : 8;
+}
+
+template <int G>
+int launch_partition(const DecodeParams &p, int num_seqs, cudaStream_t stream) {
+    constexpr int LPT = lanes_per_token<G>();
+    auto kernel = decode_partition_kernel<G, LPT>;
+    const int smem = SmemLayout::total(G, p.partition_size);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    static std::atomic<uint64_t> configured{0};  // one bit per device
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemLayout::total(G, PKV_MAX_PARTITION)) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const dim3 grid(p.max_partitions, p.num_kv_heads, num_seqs);
+    kernel<<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream) {
+    switch (group) {
+        case 1: return launch_partition<1>(p, num_seqs, stream);
+        case 2: return launch_partition<2>(p, num_seqs, stream);
+        case 4: return launch_partition<4>(p, num_seqs, stream);
+        case 8: return launch_partition<8>(p, num_seqs, stream);
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+}
+
+int check_common(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                 const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                 int num_kv_heads, int head_dim, int block_size, int64_t num_blocks) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != kD) return PKV_ERR_UNSUPPORTED;
+    if (block_size % PKV_MIN_BLOCK_SIZE != 0 || block_size > PKV_MAX_BLOCK_SIZE) return PKV_ERR_UNSUPPORTED;
+    if (num_blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    const int g = num_q_heads / num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return PKV_ERR_UNSUPPORTED;
+    if (!pkv_internal::aligned16(q) || !pkv_internal::aligned16(k_cache) || !pkv_internal::aligned16(v_cache) ||
+        !pkv_internal::aligned(block_tables, 4) || !pkv_internal::aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_context,
+                                                    int partition_size) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context <= 0 || partition_size <= 0) return 0;
+    const size_t parts = (static_cast<size_t>(max_context) + partition_size - 1) / partition_size;
+    if (parts <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * parts;
+    return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
+}
+
+extern "C" PKV_API int pkv_decode_partition(float *o_part, float *m_part, float *l_part, const void *q,
+                                            const void *k_cache, const void *v_cache,
+                                            const int32_t *block_tables, const int32_t *context_lens,
+                                            int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                            float scale, int partition_size, int max_partitions,
+                                            pkv_stream_t stream) {
+    int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
+    if (st != PKV_OK) return st;
+    if (!o_part || !m_part || !l_part) return PKV_ERR_INVALID_ARG;
+    if (!pkv_internal::aligned16(o_part) || !pkv_internal::aligned(m_part, 4) || !pkv_internal::aligned(l_part, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (partition_size < kChunk || partition_size > PKV_MAX_PARTITION || partition_size % kChunk != 0)
+        return PKV_ERR_UNSUPPORTED;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    if (max_partitions < (cap + partition_size - 1) / partition_size || max_partitions > 0x7fffffff)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    DecodeParams p{};
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const unsigned char *>(k_cache);
+    p.v_cache = static_cast<const unsigned char *>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.o_part = o_part;
+    p.m_part = m_part;
+    p.l_part = l_part;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.q_scale = scale * kLog2e;
+    p.partition_size = partition_size;
+    p.max_partitions = max_partitions;
+    p.direct_single = 0;
+    return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" PKV_API int pkv_merge(void *out, const float *o_part, const float *m_part, const float *l_part,
+                                 const int32_t *context_lens, int num_seqs, int num_q_heads, int head_dim,
+                                 int partition_size, int max_partitions, pkv_stream_t stream) {
+    if (!out || !o_part || !m_part || !l_part || !context_lens) return PKV_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_q_heads <= 0 || partition_size <= 0 || max_partitions <= 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != kD) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    merge_kernel<<<dim3(num_q_heads, num_seqs), kD, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<__half *>(out), o_part, m_part, l_part, context_lens, num_q_heads, partition_size,
+        max_partitions, 0);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *block_tables, const int32_t *context_lens,
+                                            int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                            float scale, void *workspace, size_t workspace_bytes,
+                                            pkv_stream_t stream) {
+    int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
+    if (st != PKV_OK) return st;
+    if (!out) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    const int part = PKV_DEFAULT_PARTITION;
+    const int max_parts = static_cast<int>((cap + part - 1) / part);
+    DecodeParams p{};
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const unsigned char *>(k_cache);
+    p.v_cache = static_cast<const unsigned char *>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<__half *>(out);
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.q_scale = scale * kLog2e;
+    p.partition_size = part;
+    p.max_partitions = max_parts;
+    p.direct_single = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
+
+    const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, static_cast<int>(cap), part);
+    if (!workspace || workspace_bytes < need || !pkv_internal::aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    p.o_part = reinterpret_cast<float *>(ws);
+    p.m_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)));
+    p.l_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)) + align256(rows * sizeof(float)));
+    st = dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
+    if (st != PKV_OK) return st;
+    merge_kernel<<<dim3(num_q_heads, num_seqs), kD, 0, s>>>(p.out, p.o_part, p.m_part, p.l_part, context_lens,
+                                                            num_q_heads, part, max_parts, 1);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+namespace pkv_internal {
+
+int decode_take_error(int *code) {
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_decode_error, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    *code = value;
+    return PKV_OK;
+}
+
+}  // namespace pkv_internal
