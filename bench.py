@@ -229,7 +229,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     bs = args.block_size
-    n_layers = 1 if args.workload == "tiny" else LAYERS
+    n_layers = 1 if args.workload == "tiny" else (args.layers or LAYERS)
     steps_cycle = 128 if args.workload == "gqa8b" else 1
 
     # per-layer caches (distinct, like a real model) and per-layer new-token inputs in one block
@@ -599,6 +599,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="mha7b")
     ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default 32; fewer only for profiling)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")

@@ -23,9 +23,10 @@
 //     fp32 registers, pre-multiplied by scale*log2(e)); partial dot products
 //     are combined with a reduce-scatter of warp shuffles, after which each
 //     lane holds finished scores for a fixed (token, head) subset.
-//   * Online softmax in fp32 with lazy rescaling: the running max is only
+//   * Online softmax in fp32 with lazy rescaling: the reference max is only
 //     raised (and the accumulators rescaled) when a score exceeds it by more
-//     than 2^8, so most chunks skip the rescale.  Probabilities go through a
+//     than 2^8, so most chunks skip the rescale; the true max is tracked on
+//     the side and everything is re-referenced to it once at the end.  Probabilities go through a
 //     small per-warp shared buffer to the P.V stage, where each lane owns 4
 //     output dims of every packed head and walks the chunk's tokens.
 //   * At the end the 4 warps' (m, l, acc) are merged in shared memory; the CTA
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     // l_lane: this lane's share of the softmax denominators; acc: P.V accumulators.
     float m_head[G], l_lane[G], acc[G][4];
     float m_mine = -INFINITY;
+    float top_mine = -INFINITY;  // true running max of this lane's scores (m_head may lag it by < 2^8)
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
         m_head[hh] = -INFINITY;
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         for (int k = 0; k < HELD; ++k) {
             if (held_tok(k) >= valid) v[k] = -INFINITY;
             need |= v[k] > m_mine + kRescaleThreshold;
+            top_mine = fmaxf(top_mine, v[k]);
         }
         if (__any_sync(pkv::kFullMask, need)) {
             float mx[G];
@@ -382,15 +385,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         for (int i = consumed + 1; i < issued; ++i) pkv::mbar_wait_bounded(bar0 + 8 * (i % kStages), (i / kStages) & 1);
     }
 
-    // ---- per-warp softmax denominators
+    // ---- per-warp softmax denominators, re-referenced to the true max of each head
     float l_head[G];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) l_head[hh] = l_lane[hh];
+    for (int hh = 0; hh < G; ++hh) {
+        l_head[hh] = l_lane[hh];
+        float top = my_head == hh ? top_mine : -INFINITY;
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int sh = 0; sh < 5; ++sh)
+        for (int sh = 0; sh < 5; ++sh) {
             l_head[hh] += __shfl_xor_sync(pkv::kFullMask, l_head[hh], 16 >> sh);
+            top = fmaxf(top, __shfl_xor_sync(pkv::kFullMask, top, 16 >> sh));
+        }
+        if (top > -INFINITY) {  // this warp saw tokens: m_head <= top < m_head + 2^8
+            const float f = exp2f(m_head[hh] - top);
+            l_head[hh] *= f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[hh][e] *= f;
+            m_head[hh] = top;
+        }
+    }
 
     // ---- merge the 4 warps in shared memory (reusing the stage buffers)
     __syncthreads();
