@@ -494,20 +494,23 @@ def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None):
     slots = oracle.slot_mapping(h["block_tables"], h["positions"], bs)
     t0 = time.perf_counter()
     oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"], h["v_new"])
-    done, nbytes = 0, 0
+    done, nbytes, tokens = 0, 0, 0
     limit = b if max_requests is None else min(b, max_requests)
-    while done < limit:
-        sl = slice(done, done + 1)
+    # requests of layer 0 in order, cycling, until the time budget is spent (at least one pass)
+    while done < limit or time.perf_counter() - t0 < budget_s:
+        i = done % b
+        sl = slice(i, i + 1)
         oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl], h["context_lens"][sl],
                       case.scale)
-        nbytes += decode_bytes(ctx[done:done + 1], hkv, hq, d, bs)
+        nbytes += decode_bytes(ctx[i:i + 1], hkv, hq, d, bs)
+        tokens += ctx[i]
         done += 1
-        if time.perf_counter() - t0 > budget_s:
+        if max_requests is not None and done >= limit:
             break
     dt = time.perf_counter() - t0
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"layer 0: append of all {b} requests + decode of the first {done} of {b} requests "
-                      f"({sum(ctx[:done])} cached tokens), single-threaded C float64, {dt:.1f} s",
+            "sample": f"layer 0: append of all {b} requests, then {done} single-request decodes cycling over "
+                      f"the {b} requests ({tokens} cached tokens attended), single-threaded C float64, {dt:.1f} s",
             "cpu": cpu_model()}
 
 
