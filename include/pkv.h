@@ -227,6 +227,45 @@ PKV_API int pkv_merge(void *out, const float *o_part, const float *m_part, const
                       const int32_t *context_lens, int num_seqs, int num_q_heads, int head_dim,
                       int partition_size, int max_partitions, pkv_stream_t stream);
 
+/* Size of the library's built-in scratch array used by pkv_decode_attention_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+
+/* Allocation-free form of pkv_decode_attention.  The paper has no counterpart:
+ * this call exists for callers that cannot allocate device memory.
+ *
+ * Who needs it: code running while a stream is captured into a CUDA graph in
+ * global capture mode (cudaMalloc synchronises the device, which that mode
+ * forbids); plugins hosted by another runtime that owns all device memory and
+ * hands them only input and output pointers; latency-bound serving loops that
+ * ban allocator calls after start-up.  None of them can supply the split
+ * workspace pkv_decode_attention asks for.
+ *
+ * Same arguments, semantics and results as pkv_decode_attention, minus the
+ * workspace: the split partials live in a file-scope static __device__ array
+ * of PKV_NOALLOC_SCRATCH_BYTES bytes inside libpkv.so.  Every GPU on which the
+ * library's kernels are loaded holds that array until the process exits.  The
+ * first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture begins.  Nothing here calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *
+ * Limit and sharing: a call whose split needs more than
+ * PKV_NOALLOC_SCRATCH_BYTES (pkv_decode_workspace_size with max_context =
+ * max_blocks_per_seq * block_size and partition PKV_DEFAULT_PARTITION) is
+ * refused with PKV_ERR_WORKSPACE before anything is enqueued.  All calls share
+ * the one array, and it keeps the previous call's contents; nothing in it has
+ * to start at zero (each call writes every partial it later reads).  Calls
+ * whose kernels overlap on the GPU (unordered streams, or several host
+ * threads) race on the array: order them on one stream.
+ * Errors: as pkv_decode_attention, plus WORKSPACE for oversize requests and
+ * CUDA if the address look-up fails. */
+PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, int num_seqs,
+                                         int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int64_t num_blocks,
+                                         float scale, pkv_stream_t stream);
+
 /* Synchronise `stream`, then report (in *code) and clear the device error
  * word of the current device: PKV_DEV_OK when no kernel recorded an index
  * problem since the last call.  Returns PKV_OK, or CUDA when a runtime call

@@ -34,6 +34,7 @@ PKV_DEV_WAIT_TIMEOUT = 4
 PKV_HEAD_DIM = 128
 PKV_DEFAULT_PARTITION = 512
 PKV_MAX_PARTITION = 4096
+PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/pkv.h declares: name -> (restype, argtypes)
 SIGNATURES = {
@@ -54,6 +55,8 @@ SIGNATURES = {
     "pkv_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                      c_int, c_int, c_int, c_int, c_int64, c_float, c_void_p, c_size_t,
                                      c_void_p]),
+    "pkv_decode_attention_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                             c_int, c_int, c_int, c_int, c_int, c_int64, c_float, c_void_p]),
     "pkv_decode_partition": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
                                      c_int, c_int, c_void_p]),

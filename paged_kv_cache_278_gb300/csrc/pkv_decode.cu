@@ -40,6 +40,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "pkv.h"
 #include "pkv_device.cuh"
@@ -656,6 +657,51 @@ extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void
     merge_kernel<<<dim3(num_q_heads, num_seqs), kD, 0, s>>>(p.out, p.o_part, p.m_part, p.l_part, context_lens,
                                                             num_q_heads, part, max_parts, 1);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ allocation-free variant
+//
+// For callers that cannot allocate device memory (global-mode stream capture, hosted plugins
+// that only receive input/output pointers, allocator-free serving loops): the split partials
+// go to this file-scope array instead of a caller workspace.  On the host the symbol names a
+// stand-in, not device memory, so it is never passed to a kernel directly; its device address
+// is looked up once per device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_address[kMaxDevices] = {};
+}  // namespace
+
+extern "C" PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                                    const void *v_cache, const int32_t *block_tables,
+                                                    const int32_t *context_lens, int num_seqs,
+                                                    int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                                                    int head_dim, int block_size, int64_t num_blocks, float scale,
+                                                    pkv_stream_t stream) {
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    if (cap > 0 && cap <= 0x7fffffffLL) {
+        const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, static_cast<int>(cap),
+                                                      PKV_DEFAULT_PARTITION);
+        if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_address[dev]) {
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) return PKV_ERR_CUDA;
+            g_noalloc_address[dev] = addr;
+        }
+        scratch = g_noalloc_address[dev];
+    }
+    return pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, scratch,
+                                PKV_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 namespace pkv_internal {
