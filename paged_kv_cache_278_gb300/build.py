@@ -55,10 +55,10 @@ def stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/ translation unit for sm_103a and link libpkv.so."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB_PATH) -> str:
+    """Compile every csrc/ translation unit for sm_103a and link libpkv.so (or `lib_path`)."""
     with _lock:
-        if not force and not stale():
+        if not force and lib_path == LIB_PATH and not stale():
             return LIB_PATH
         nvcc = nvcc_path()
         tmp = tempfile.mkdtemp(prefix="pkv_build_")
@@ -89,11 +89,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if res.returncode != 0:
                 sys.stderr.write(res.stdout)
                 raise RuntimeError("link of libpkv.so failed")
-            shutil.copy2(out_tmp, LIB_PATH + f".tmp{os.getpid()}")
-            os.replace(LIB_PATH + f".tmp{os.getpid()}", LIB_PATH)
+            shutil.copy2(out_tmp, lib_path + f".tmp{os.getpid()}")
+            os.replace(lib_path + f".tmp{os.getpid()}", lib_path)
         finally:
             shutil.rmtree(tmp, ignore_errors=True)
-    return LIB_PATH
+    return lib_path
 
 
 def main(argv=None):

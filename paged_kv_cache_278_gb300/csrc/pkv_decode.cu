@@ -54,9 +54,19 @@ constexpr int kD = PKV_HEAD_DIM;        // 128
 constexpr int kChunk = 16;              // tokens per shared-memory tile
 constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 constexpr int kTileBytes = kChunk * kRowBytes;  // 4 KiB
-constexpr int kWarps = 4;
+// Warps per CTA and bulk-copy stages per warp (each stage holds one 16-token chunk of K and V).
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 3
+#endif
+#ifndef PKV_DECODE_MIN_CTAS
+#define PKV_DECODE_MIN_CTAS 2
+#endif
+constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = PKV_DECODE_STAGES;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -97,7 +107,7 @@ struct SmemLayout {
 };
 
 template <int G, int LPT>
-__global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const DecodeParams P) {
+__global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partition_kernel(const DecodeParams P) {
     constexpr int TG = 32 / LPT;            // token groups per warp (q.K stage)
     constexpr int TPL = kChunk / TG;        // tokens per lane per chunk (q.K stage)
     constexpr int NP = kD / LPT / 8;        // 16-byte pieces of a row per lane
@@ -208,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     // Finished score k of this lane is (packed head my_head, chunk token held_tok(k)); HELD divides
     // TPL and base is a multiple of HELD, so all of a lane's scores share one head.
     static_assert(TPL % HELD == 0, "a lane's finished scores must share one head");
+    static_assert(kWarps * G * (kD + 2) * 4 <= SmemLayout::stage_bytes, "combine area must fit the stages");
     const int my_head = base / TPL;
     auto held_tok = [base, r](int k) { return r + TG * ((base + k) % TPL); };
 
@@ -424,9 +435,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         }
     }
     __syncthreads();
-    const int d = threadIdx.x;  // kThreads == kD
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
+    for (int idx = threadIdx.x; idx < G * kD; idx += kThreads) {
+        const int hh = idx / kD, d = idx % kD;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, c_m[w * G + hh]);
@@ -452,15 +462,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     }
 }
 
-// One CTA per (q head, request); thread d owns output dim d.
+// One CTA per (q head, request); thread d owns output dim d.  Partitions are taken in tiles
+// of 128: the tile's (m, l) pairs are loaded in parallel (one per thread), the weights
+// w_p = l_p exp(m_p - M) go to shared memory, then every thread issues its tile of o loads
+// independently, so a tile costs a few memory round trips instead of one per partition.
 __global__ void __launch_bounds__(kD) merge_kernel(__half *__restrict__ out, const float *__restrict__ o_part,
                                                    const float *__restrict__ m_part,
                                                    const float *__restrict__ l_part,
                                                    const int32_t *__restrict__ context_lens, int num_q_heads,
                                                    int partition_size, int max_partitions, int skip_single) {
+    __shared__ float s_w[kD];
+    __shared__ float s_red[kD / 32];
     const int h = blockIdx.x;
     const int b = blockIdx.y;
     const int d = threadIdx.x;
+    const int lane = d & 31, warp = d >> 5;
     int ctx = __ldg(context_lens + b);
     if (ctx < 0) ctx = 0;
     int n_parts = (ctx + partition_size - 1) / partition_size;
@@ -476,13 +492,41 @@ __global__ void __launch_bounds__(kD) merge_kernel(__half *__restrict__ out, con
     }
     const float *m = m_part + row * max_partitions;
     const float *l = l_part + row * max_partitions;
+    const float *o = o_part + row * max_partitions * kD + d;
+
+    // M = max over partitions (block reduction)
     float M = -INFINITY;
-    for (int p = 0; p < n_parts; ++p) M = fmaxf(M, __ldg(m + p));
+    for (int p = d; p < n_parts; p += kD) M = fmaxf(M, __ldg(m + p));
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
+    if (lane == 0) s_red[warp] = M;
+    __syncthreads();
+    M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kD / 32; ++w) M = fmaxf(M, s_red[w]);
+
     float wsum = 0.f, acc = 0.f;
-    for (int p = 0; p < n_parts; ++p) {
-        const float w = __ldg(l + p) * expf(__ldg(m + p) - M);
-        wsum += w;
-        acc = fmaf(w, __ldg(o_part + (row * max_partitions + p) * kD + d), acc);
+    for (int p0 = 0; p0 < n_parts; p0 += kD) {
+        const int n = min(kD, n_parts - p0);
+        __syncthreads();  // previous tile's weights consumed
+        if (d < n) s_w[d] = __ldg(l + p0 + d) * expf(__ldg(m + p0 + d) - M);
+        __syncthreads();
+        int p = 0;
+        for (; p + 4 <= n; p += 4) {
+            const float o0 = __ldg(o + static_cast<int64_t>(p0 + p) * kD);
+            const float o1 = __ldg(o + static_cast<int64_t>(p0 + p + 1) * kD);
+            const float o2 = __ldg(o + static_cast<int64_t>(p0 + p + 2) * kD);
+            const float o3 = __ldg(o + static_cast<int64_t>(p0 + p + 3) * kD);
+            acc = fmaf(s_w[p], o0, acc);
+            acc = fmaf(s_w[p + 1], o1, acc);
+            acc = fmaf(s_w[p + 2], o2, acc);
+            acc = fmaf(s_w[p + 3], o3, acc);
+            wsum += s_w[p] + s_w[p + 1] + s_w[p + 2] + s_w[p + 3];
+        }
+        for (; p < n; ++p) {
+            acc = fmaf(s_w[p], __ldg(o + static_cast<int64_t>(p0 + p) * kD), acc);
+            wsum += s_w[p];
+        }
     }
     out[row * kD + d] = __float2half_rn(acc / wsum);
 }
