@@ -169,7 +169,9 @@ PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping
                        int head_dim, int block_size, int64_t num_blocks, pkv_stream_t stream);
 
 /* Bytes of workspace pkv_decode_attention needs for contexts up to
- * max_context tokens (0 when one partition covers max_context). */
+ * max_context tokens (0 when one partition covers max_context): fp32 partials
+ * for every (request, q head, partition) followed by one int completion
+ * counter per (request, q head). */
 PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                          int max_context, int partition_size);
 
@@ -184,10 +186,14 @@ PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head
  * When max_blocks_per_seq * block_size <= PKV_DEFAULT_PARTITION every request
  * is done by one pass and the workspace is not used (may be NULL).  Otherwise
  * contexts are split into partitions of PKV_DEFAULT_PARTITION tokens that run
- * in parallel and are merged by log-sum-exp; requests that fit one partition
- * still finish in one pass.  The split needs
+ * in parallel and are merged by log-sum-exp inside the same kernel (the last
+ * partition of a request to finish merges them); requests that fit one
+ * partition still finish in one pass.  The split needs
  * pkv_decode_workspace_size(num_seqs, num_q_heads, 128, max_blocks_per_seq *
- * block_size, PKV_DEFAULT_PARTITION) bytes of 256-byte-aligned workspace.
+ * block_size, PKV_DEFAULT_PARTITION) bytes of 256-byte-aligned workspace whose
+ * counter region is zero when the workspace is first used (zero-fill a new
+ * workspace once, e.g. cudaMemsetAsync); every call leaves the counters zero.
+ * Calls that share a workspace must be ordered (one stream).
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache,
                                  const void *v_cache, const int32_t *block_tables,
@@ -253,10 +259,12 @@ PKV_API int pkv_merge(void *out, const float *o_part, const float *m_part, const
  * PKV_NOALLOC_SCRATCH_BYTES (pkv_decode_workspace_size with max_context =
  * max_blocks_per_seq * block_size and partition PKV_DEFAULT_PARTITION) is
  * refused with PKV_ERR_WORKSPACE before anything is enqueued.  All calls share
- * the one array, and it keeps the previous call's contents; nothing in it has
- * to start at zero (each call writes every partial it later reads).  Calls
- * whose kernels overlap on the GPU (unordered streams, or several host
- * threads) race on the array: order them on one stream.
+ * the one array, and it keeps the previous call's contents; the only part
+ * that must start at zero (the split's completion counters) is cleared by
+ * each call on `stream` before its kernel runs, and every partial a call
+ * reads it has written itself.  Calls whose kernels overlap on the GPU
+ * (unordered streams, or several host threads) race on the array: order them
+ * on one stream.
  * Errors: as pkv_decode_attention, plus WORKSPACE for oversize requests and
  * CUDA if the address look-up fails. */
 PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, const void *k_cache,

@@ -91,11 +91,12 @@ def decode_workspace_size(num_seqs: int, num_q_heads: int, max_context: int,
 
 
 def make_workspace(num_seqs: int, num_q_heads: int, max_context: int, device) -> torch.Tensor | None:
-    """Allocate (with torch) the workspace decode_attention needs; None when it needs none."""
+    """Allocate (with torch) the zero-filled workspace decode_attention needs; None when it needs
+    none.  Its completion counters start at zero and every call leaves them zero."""
     n = decode_workspace_size(num_seqs, num_q_heads, max_context)
     if n == 0:
         return None
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def _decode_inputs(q, k_cache, v_cache, block_tables, context_lens):

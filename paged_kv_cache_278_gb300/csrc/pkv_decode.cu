@@ -59,10 +59,10 @@ constexpr int kTileBytes = kChunk * kRowBytes;  // 4 KiB
 #define PKV_DECODE_WARPS 4
 #endif
 #ifndef PKV_DECODE_STAGES
-#define PKV_DECODE_STAGES 3
+#define PKV_DECODE_STAGES 2
 #endif
 #ifndef PKV_DECODE_MIN_CTAS
-#define PKV_DECODE_MIN_CTAS 2
+#define PKV_DECODE_MIN_CTAS 3
 #endif
 constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
@@ -92,7 +92,10 @@ struct DecodeParams {
     int partition_size;
     int max_partitions;
     int direct_single;        // write fp16 out directly for single-partition requests
+    int *counters;            // per (request, kv head) completion counters: fused merge when non-null
 };
+
+constexpr int kMergeTile = 128;  // partitions whose weights the fused merge stages at a time
 
 // Shared-memory carve-up (bytes), identical on host and device.
 struct SmemLayout {
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
     static_assert((1 << LOG_LPT) == LPT && (1 << LOG_N) == N, "powers of two");
     static_assert(NP >= 1 && NP * 8 * LPT == kD, "lane split of a row");
 
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -435,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
         }
     }
     __syncthreads();
+#pragma unroll 1
     for (int idx = threadIdx.x; idx < G * kD; idx += kThreads) {
         const int hh = idx / kD, d = idx % kD;
         float M = -INFINITY;
@@ -460,6 +464,60 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
             }
         }
     }
+    if (direct || P.counters == nullptr) return;
+
+    // ---- fused log-sum-exp merge: the last partition CTA of (b, kv head) to finish merges them all.
+    // Every writer fences its partials at device scope before the counter increment (release);
+    // the last CTA fences again after seeing the final count (acquire) and reads the partials
+    // from L2 (ld.global.cg), then returns the counter to zero for the next call.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    int *counter = P.counters + static_cast<int64_t>(b) * P.num_kv_heads + kvh;
+    if (threadIdx.x == 0) s_last = atomicAdd(counter, 1) == n_parts - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    static_assert(kThreads == kD, "the fused merge gives each thread one output dim");
+    static_assert(G * (kMergeTile + 1) * 4 <= SmemLayout::stage_bytes, "merge tile must fit the stages");
+    float *s_wt = reinterpret_cast<float *>(smem);        // [G][kMergeTile] weights of the current tile
+    float *s_max = s_wt + G * kMergeTile;                  // [G] max of m over the partitions
+    const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
+    for (int hh = warp; hh < G; hh += kWarps) {
+        const float *m = P.m_part + (row0 + hh) * P.max_partitions;
+        float M = -INFINITY;
+        for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(m + pp));
+#pragma unroll
+        for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
+        if (lane == 0) s_max[hh] = M;
+    }
+    const int d = threadIdx.x;
+    float macc[G], wsum[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) macc[hh] = wsum[hh] = 0.f;
+    for (int p0 = 0; p0 < n_parts; p0 += kMergeTile) {
+        const int n = min(kMergeTile, n_parts - p0);
+        __syncthreads();  // s_max ready / previous tile consumed
+        for (int i = threadIdx.x; i < G * n; i += kThreads) {
+            const int hh = i / n, pp = i - hh * n;
+            const int64_t prow = (row0 + hh) * P.max_partitions + p0 + pp;
+            s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int pp = 0; pp < n; ++pp) {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float w = s_wt[hh * kMergeTile + pp];
+                const float o = __ldcg(P.o_part + ((row0 + hh) * P.max_partitions + p0 + pp) * kD + d);
+                macc[hh] = fmaf(w, o, macc[hh]);
+                wsum[hh] += w;
+            }
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) P.out[(row0 + hh) * kD + d] = __float2half_rn(macc[hh] / wsum[hh]);
+    if (threadIdx.x == 0) *counter = 0;
 }
 
 // One CTA per (q head, request); thread d owns output dim d.  Partitions are taken in tiles
@@ -591,6 +649,11 @@ int check_common(const void *q, const void *k_cache, const void *v_cache, const 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Split workspace layout: o_part | m_part | l_part | counters, each 256-byte aligned.
+size_t counters_offset(size_t rows) {
+    return align256(rows * kD * sizeof(float)) + 2 * align256(rows * sizeof(float));
+}
+
 }  // namespace
 
 extern "C" PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_context,
@@ -599,7 +662,8 @@ extern "C" PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_head
     const size_t parts = (static_cast<size_t>(max_context) + partition_size - 1) / partition_size;
     if (parts <= 1) return 0;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * parts;
-    return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
+    return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float)) +
+           align256(static_cast<size_t>(num_seqs) * num_q_heads * sizeof(int));
 }
 
 extern "C" PKV_API int pkv_decode_partition(float *o_part, float *m_part, float *l_part, const void *q,
@@ -696,11 +760,8 @@ extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void
     p.o_part = reinterpret_cast<float *>(ws);
     p.m_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)));
     p.l_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)) + align256(rows * sizeof(float)));
-    st = dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
-    if (st != PKV_OK) return st;
-    merge_kernel<<<dim3(num_q_heads, num_seqs), kD, 0, s>>>(p.out, p.o_part, p.m_part, p.l_part, context_lens,
-                                                            num_q_heads, part, max_parts, 1);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    p.counters = reinterpret_cast<int *>(ws + counters_offset(rows));
+    return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
 }
 
 // ------------------------------------------------------------------ allocation-free variant
@@ -742,6 +803,16 @@ extern "C" PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, co
             g_noalloc_address[dev] = addr;
         }
         scratch = g_noalloc_address[dev];
+    }
+    // The split's completion counters must start at zero; every call leaves them zero, but the
+    // array is shared by all calls, so clear them here rather than trust an earlier call.
+    const int max_parts = cap > 0 ? static_cast<int>((cap + PKV_DEFAULT_PARTITION - 1) / PKV_DEFAULT_PARTITION) : 0;
+    if (max_parts > 1 && num_seqs > 0 && num_q_heads > 0 && head_dim == kD) {
+        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+        if (cudaMemsetAsync(static_cast<unsigned char *>(scratch) + counters_offset(rows), 0,
+                            static_cast<size_t>(num_seqs) * num_q_heads * sizeof(int),
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return PKV_ERR_CUDA;
     }
     return pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, scratch,

@@ -139,3 +139,25 @@ def test_side_stream_and_graph_capture():
     torch.cuda.synchronize()
     assert torch.equal(out_g, out)
     assert_no_device_error()
+
+
+def test_workspace_reuse_leaves_counters_zero():
+    # one workspace across calls with different contexts: the fused merge's completion counters
+    # must come back to zero after every call, or later calls would merge too early or never
+    first = workloads.random_case(21, [4000, 513, 1025, 77], 16, 4, block_size=16, extra_blocks=8)
+    ws = pkv.make_workspace(first.num_seqs, first.num_q_heads, first.max_blocks_per_seq * 16, "cuda")
+    for seed, ctxs in [(21, [4000, 513, 1025, 77]), (22, [600, 3999, 0, 2048]), (23, [1, 2, 3, 4000])]:
+        case = workloads.random_case(seed, ctxs, 16, 4, block_size=16, extra_blocks=8)
+        case.block_tables = torch.nn.functional.pad(case.block_tables,
+                                                    (0, first.max_blocks_per_seq - case.max_blocks_per_seq),
+                                                    value=-1)
+        h = host_inputs(case)
+        ref = oracle_step(h, case)
+        out = gpu_step(case.to("cuda"), workspace=ws)
+        assert max_err(out, ref) <= ATTN_TOL
+        torch.cuda.synchronize()
+        rows = 4 * 16 * -(-first.max_blocks_per_seq * 16 // 512)
+        up = lambda x: x + (-x) % 256
+        counters = ws[up(rows * 128 * 4) + 2 * up(rows * 4):].view(torch.int32)
+        assert int(counters.abs().sum()) == 0
+    assert_no_device_error()

@@ -91,7 +91,8 @@ def test_invalid_arguments_rejected_without_launch(lib):
 def test_workspace_size(lib):
     assert lib.pkv_decode_workspace_size(4, 32, 128, 512, 512) == 0
     rows = 4 * 32 * 64
-    expect = rows * 128 * 4 + 2 * (rows * 4 + (-rows * 4) % 256)
+    up = lambda x: x + (-x) % 256
+    expect = up(rows * 128 * 4) + 2 * up(rows * 4) + up(4 * 32 * 4)
     assert lib.pkv_decode_workspace_size(4, 32, 128, 32768, 512) == expect
 
 
