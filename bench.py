@@ -337,29 +337,29 @@ def run_ours(args):
     ms_total = e0.elapsed_time(e1)
     ms_per_step = ms_total / args.steps
 
-    # ---- timed region 2: the dominant kernel alone, CUDA events around every launch.  A
-    # pkv_decode_attention call is exactly one launch of the partition kernel (its log-sum-exp
-    # merge runs inside it), so the events bracket that kernel and nothing else.
+    # ---- timed region 2: the dominant kernel alone.  A pkv_decode_attention call is exactly one
+    # launch of the partition kernel (its log-sum-exp merge runs inside it); per step the layers'
+    # launches run back to back between one pair of CUDA events on the launching stream, so the
+    # average launch duration is (event interval) / launches, with no other kernel in between.
     kt_steps = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(kt_steps * n_layers)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kt_steps)]
     kernel_bytes = 0
     barrier()
     t0 = time.time()
     with torch.cuda.stream(stream):
         for i in range(kt_steps):
             j = set_step(i)
+            a, b = ev[i]
+            a.record(stream)
             for l, c in enumerate(cases):
-                a, b = ev[i * n_layers + l]
-                a.record(stream)
                 pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
                                      workspace=ws)
-                b.record(stream)
-                kernel_bytes += bytes_per_step[j % len(bytes_per_step)] // n_layers
+            b.record(stream)
+            kernel_bytes += bytes_per_step[j % len(bytes_per_step)]
     barrier()
     windows.append((t0, time.time()))
     kernel_ms = sum(a.elapsed_time(b) for a, b in ev)
-    kernel_launches = len(ev)
+    kernel_launches = kt_steps * n_layers
 
     # ---- timed region 3: end to end through the public API with host buffers
     q_h = q_all.cpu().pin_memory()
