@@ -179,7 +179,7 @@ PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head
  *   out[b][h][:] = softmax(scale * q[b][h] . K_b^T) . V_b
  * over the context_lens[b] cached tokens of request b, K_b/V_b gathered
  * through block_tables (kv head h / (num_q_heads / num_kv_heads)).
- *   out : fp16 [num_seqs][num_q_heads][head_dim]
+ *   out : fp16 [num_seqs][num_q_heads][head_dim], 8-byte aligned
  *   q   : fp16 [num_seqs][num_q_heads][head_dim], 16-byte aligned
  * Requirements: head_dim == 128; num_q_heads / num_kv_heads in {1, 2, 4, 8};
  * block_size a multiple of 16 in [16, 256]; caches 16-byte aligned.

@@ -95,7 +95,7 @@ struct DecodeParams {
     int *counters;            // per (request, kv head) completion counters: fused merge when non-null
 };
 
-constexpr int kMergeTile = 128;  // partitions whose weights the fused merge stages at a time
+constexpr int kMergeTile = 1024;  // partitions whose weights the fused merge stages at a time
 
 // Shared-memory carve-up (bytes), identical on host and device.
 struct SmemLayout {
@@ -478,23 +478,38 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    static_assert(kThreads == kD, "the fused merge gives each thread one output dim");
-    static_assert(G * (kMergeTile + 1) * 4 <= SmemLayout::stage_bytes, "merge tile must fit the stages");
-    float *s_wt = reinterpret_cast<float *>(smem);        // [G][kMergeTile] weights of the current tile
-    float *s_max = s_wt + G * kMergeTile;                  // [G] max of m over the partitions
+    // Slots: (packed head, 4 consecutive dims) -> float4 loads of o; partitions are split over
+    // GROUPS thread groups when there are fewer slots than threads, and loads are unrolled so a
+    // thread keeps 8 rows in flight.  All weights w = l exp(m - M) of a tile are staged first.
+    constexpr int SLOTS = G * (kD / 4);
+    constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
+    constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
+    static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
+    static_assert(G * kMergeTile * 4 + G * 4 + GROUPS * SLOTS * 20 <= SmemLayout::stage_bytes,
+                  "merge staging must fit the stages");
+    float *s_wt = reinterpret_cast<float *>(smem);                  // [G][kMergeTile]
+    float *s_max = s_wt + G * kMergeTile;                            // [G]
+    float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
+    float *s_sum = reinterpret_cast<float *>(s_acc + GROUPS * SLOTS);                     // [GROUPS][SLOTS]
     const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
     for (int hh = warp; hh < G; hh += kWarps) {
         const float *m = P.m_part + (row0 + hh) * P.max_partitions;
         float M = -INFINITY;
+#pragma unroll 4
         for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(m + pp));
 #pragma unroll
         for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
         if (lane == 0) s_max[hh] = M;
     }
-    const int d = threadIdx.x;
-    float macc[G], wsum[G];
+    const int grp = GROUPS > 1 ? threadIdx.x / SLOTS : 0;
+    const int slot0 = GROUPS > 1 ? threadIdx.x % SLOTS : threadIdx.x;
+    float4 macc[PER_THREAD];
+    float msum[PER_THREAD];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) macc[hh] = wsum[hh] = 0.f;
+    for (int k = 0; k < PER_THREAD; ++k) {
+        macc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        msum[k] = 0.f;
+    }
     for (int p0 = 0; p0 < n_parts; p0 += kMergeTile) {
         const int n = min(kMergeTile, n_parts - p0);
         __syncthreads();  // s_max ready / previous tile consumed
@@ -504,19 +519,50 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
             s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
         }
         __syncthreads();
-#pragma unroll 4
-        for (int pp = 0; pp < n; ++pp) {
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float w = s_wt[hh * kMergeTile + pp];
-                const float o = __ldcg(P.o_part + ((row0 + hh) * P.max_partitions + p0 + pp) * kD + d);
-                macc[hh] = fmaf(w, o, macc[hh]);
-                wsum[hh] += w;
+        for (int k = 0; k < PER_THREAD; ++k) {
+            const int slot = slot0 + k * kThreads;
+            const int hh = slot / (kD / 4), d4 = slot % (kD / 4);
+            const float4 *o = reinterpret_cast<const float4 *>(P.o_part + ((row0 + hh) * P.max_partitions + p0) * kD) + d4;
+            const float *w = s_wt + hh * kMergeTile;
+#pragma unroll 8
+            for (int pp = grp; pp < n; pp += GROUPS) {
+                const float4 v = __ldcg(o + static_cast<int64_t>(pp) * (kD / 4));
+                const float wp = w[pp];
+                macc[k].x = fmaf(wp, v.x, macc[k].x);
+                macc[k].y = fmaf(wp, v.y, macc[k].y);
+                macc[k].z = fmaf(wp, v.z, macc[k].z);
+                macc[k].w = fmaf(wp, v.w, macc[k].w);
+                msum[k] += wp;
             }
         }
     }
+    if (GROUPS > 1) {
+        s_acc[grp * SLOTS + slot0] = macc[0];
+        s_sum[grp * SLOTS + slot0] = msum[0];
+        __syncthreads();
+        if (grp != 0) return;
+        for (int g2 = 1; g2 < GROUPS; ++g2) {
+            const float4 v = s_acc[g2 * SLOTS + slot0];
+            macc[0].x += v.x;
+            macc[0].y += v.y;
+            macc[0].z += v.z;
+            macc[0].w += v.w;
+            msum[0] += s_sum[g2 * SLOTS + slot0];
+        }
+    }
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) P.out[(row0 + hh) * kD + d] = __float2half_rn(macc[hh] / wsum[hh]);
+    for (int k = 0; k < PER_THREAD; ++k) {
+        const int slot = slot0 + k * kThreads;
+        const int hh = slot / (kD / 4), d4 = slot % (kD / 4);
+        const float inv = 1.f / msum[k];
+        __half2 lo = __floats2half2_rn(macc[k].x * inv, macc[k].y * inv);
+        __half2 hi = __floats2half2_rn(macc[k].z * inv, macc[k].w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(P.out + (row0 + hh) * kD + d4 * 4) = packed;
+    }
     if (threadIdx.x == 0) *counter = 0;
 }
 
@@ -729,7 +775,7 @@ extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
-    if (!out) return PKV_ERR_INVALID_ARG;
+    if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int part = PKV_DEFAULT_PARTITION;
