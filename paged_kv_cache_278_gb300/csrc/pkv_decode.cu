@@ -64,6 +64,10 @@ constexpr int kTileBytes = kChunk * kRowBytes;  // 4 KiB
 #ifndef PKV_DECODE_MIN_CTAS
 #define PKV_DECODE_MIN_CTAS 3
 #endif
+// 1: q.K and P.V use packed two-lane FMAs (fma.rn.f32x2), halving FMA issue slots.
+#ifndef PKV_DECODE_FFMA2
+#define PKV_DECODE_FFMA2 1
+#endif
 constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = PKV_DECODE_STAGES;
@@ -301,10 +305,17 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
             }
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
+#if PKV_DECODE_FFMA2
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < NP * 8; e += 2) pkv::fma2(s0, s1, qf[hh][e], qf[hh][e + 1], kf[e], kf[e + 1]);
+                v[hh * TPL + it] = s0 + s1;
+#else
                 float sacc = 0.f;
 #pragma unroll
                 for (int e = 0; e < NP * 8; ++e) sacc = fmaf(qf[hh][e], kf[e], sacc);
                 v[hh * TPL + it] = sacc;
+#endif
             }
         }
         // ---- reduce-scatter across the LPT lanes of a token group
@@ -381,10 +392,15 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
                 for (int hh = 0; hh < G; ++hh) pr[hh] = s_prob[t * G + hh];
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
+#if PKV_DECODE_FFMA2
+                    pkv::fma2(acc[hh][0], acc[hh][1], pr[hh], pr[hh], v01.x, v01.y);
+                    pkv::fma2(acc[hh][2], acc[hh][3], pr[hh], pr[hh], v23.x, v23.y);
+#else
                     acc[hh][0] = fmaf(pr[hh], v01.x, acc[hh][0]);
                     acc[hh][1] = fmaf(pr[hh], v01.y, acc[hh][1]);
                     acc[hh][2] = fmaf(pr[hh], v23.x, acc[hh][2]);
                     acc[hh][3] = fmaf(pr[hh], v23.y, acc[hh][3]);
+#endif
                 }
             }
         }
@@ -467,17 +483,15 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
     if (direct || P.counters == nullptr) return;
 
     // ---- fused log-sum-exp merge: the last partition CTA of (b, kv head) to finish merges them all.
-    // Every writer fences its partials at device scope before the counter increment (release);
-    // the last CTA fences again after seeing the final count (acquire) and reads the partials
-    // from L2 (ld.global.cg), then returns the counter to zero for the next call.
+    // The CTA's partial writes are ordered before one acquire-release increment of the counter by
+    // thread 0 (barrier, then atom.acq_rel.gpu); the CTA that sees the final count reads every
+    // partial from L2 (ld.global.cg) after a second barrier, then returns the counter to zero.
     __shared__ int s_last;
-    __threadfence();
     __syncthreads();
     int *counter = P.counters + static_cast<int64_t>(b) * P.num_kv_heads + kvh;
-    if (threadIdx.x == 0) s_last = atomicAdd(counter, 1) == n_parts - 1;
+    if (threadIdx.x == 0) s_last = pkv::atomic_add_acq_rel_gpu(counter, 1) == n_parts - 1;
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     // Slots: (packed head, 4 consecutive dims) -> float4 loads of o; partitions are split over
     // GROUPS thread groups when there are fewer slots than threads, and loads are unrolled so a
     // thread keeps 8 rows in flight.  All weights w = l exp(m - M) of a tile are staged first.

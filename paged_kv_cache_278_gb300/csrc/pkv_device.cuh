@@ -97,6 +97,26 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t bits) {
     return __half22float2(h);
 }
 
+// (c0, c1) += (a0, a1) * (b0, b1): one packed two-lane fp32 FMA (Blackwell FFMA2), each lane
+// rounded exactly like fmaf.
+__device__ __forceinline__ void fma2(float &c0, float &c1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Release-acquire increment at GPU scope; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void record_error(int *word, int code) { atomicCAS(word, 0, code); }
 
