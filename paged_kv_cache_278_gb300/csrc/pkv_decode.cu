@@ -99,7 +99,7 @@ struct DecodeParams {
     int *counters;            // per (request, kv head) completion counters: fused merge when non-null
 };
 
-constexpr int kMergeTile = 1024;  // partitions whose weights the fused merge stages at a time
+constexpr int kMergeTile = 512;  // partitions whose weights the fused merge stages at a time
 
 // Shared-memory carve-up (bytes), identical on host and device.
 struct SmemLayout {
@@ -499,22 +499,13 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
     constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
     constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
     static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
-    static_assert(G * kMergeTile * 4 + G * 4 + GROUPS * SLOTS * 20 <= SmemLayout::stage_bytes,
+    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout::stage_bytes,
                   "merge staging must fit the stages");
-    float *s_wt = reinterpret_cast<float *>(smem);                  // [G][kMergeTile]
-    float *s_max = s_wt + G * kMergeTile;                            // [G]
+    float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][kMergeTile]
+    float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
     float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
     float *s_sum = reinterpret_cast<float *>(s_acc + GROUPS * SLOTS);                     // [GROUPS][SLOTS]
     const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
-    for (int hh = warp; hh < G; hh += kWarps) {
-        const float *m = P.m_part + (row0 + hh) * P.max_partitions;
-        float M = -INFINITY;
-#pragma unroll 4
-        for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(m + pp));
-#pragma unroll
-        for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
-        if (lane == 0) s_max[hh] = M;
-    }
     const int grp = GROUPS > 1 ? threadIdx.x / SLOTS : 0;
     const int slot0 = GROUPS > 1 ? threadIdx.x % SLOTS : threadIdx.x;
     float4 macc[PER_THREAD];
@@ -524,30 +515,85 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
         macc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         msum[k] = 0.f;
     }
-    for (int p0 = 0; p0 < n_parts; p0 += kMergeTile) {
-        const int n = min(kMergeTile, n_parts - p0);
-        __syncthreads();  // s_max ready / previous tile consumed
-        for (int i = threadIdx.x; i < G * n; i += kThreads) {
-            const int hh = i / n, pp = i - hh * n;
-            const int64_t prow = (row0 + hh) * P.max_partitions + p0 + pp;
-            s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
+    auto o_row = [&](int hh, int d4) {
+        return reinterpret_cast<const float4 *>(P.o_part + (row0 + hh) * P.max_partitions * kD) + d4;
+    };
+    auto accumulate = [&](int k, float w, float4 v) {
+        macc[k].x = fmaf(w, v.x, macc[k].x);
+        macc[k].y = fmaf(w, v.y, macc[k].y);
+        macc[k].z = fmaf(w, v.z, macc[k].z);
+        macc[k].w = fmaf(w, v.w, macc[k].w);
+        msum[k] += w;
+    };
+    if (n_parts <= kMergeTile) {
+        // Fast path, about one L2 round trip: issue this thread's first PRE partial rows, stage
+        // every (m, l) of the group in shared memory meanwhile, then weight the rows in registers.
+        constexpr int PRE = 8;
+        float4 pre[PER_THREAD][PRE];
+#pragma unroll
+        for (int k = 0; k < PER_THREAD; ++k) {
+            const int slot = slot0 + k * kThreads;
+            const float4 *o = o_row(slot / (kD / 4), slot % (kD / 4));
+#pragma unroll
+            for (int jj = 0; jj < PRE; ++jj) {
+                const int pp = grp + jj * GROUPS;
+                pre[k][jj] = pp < n_parts ? __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float *s_mm = s_wt;
+        float *s_ll = s_wt + G * kMergeTile;
+        for (int i = threadIdx.x; i < G * n_parts; i += kThreads) {
+            const int hh = i / n_parts, pp = i - hh * n_parts;
+            const int64_t prow = (row0 + hh) * P.max_partitions + pp;
+            s_mm[hh * kMergeTile + pp] = __ldcg(P.m_part + prow);
+            s_ll[hh * kMergeTile + pp] = __ldcg(P.l_part + prow);
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < PER_THREAD; ++k) {
             const int slot = slot0 + k * kThreads;
-            const int hh = slot / (kD / 4), d4 = slot % (kD / 4);
-            const float4 *o = reinterpret_cast<const float4 *>(P.o_part + ((row0 + hh) * P.max_partitions + p0) * kD) + d4;
-            const float *w = s_wt + hh * kMergeTile;
+            const int hh = slot / (kD / 4);
+            const float *mm = s_mm + hh * kMergeTile;
+            const float *ll = s_ll + hh * kMergeTile;
+            float M = -INFINITY;
+            for (int pp = 0; pp < n_parts; ++pp) M = fmaxf(M, mm[pp]);
+#pragma unroll
+            for (int jj = 0; jj < PRE; ++jj) {
+                const int pp = grp + jj * GROUPS;
+                if (pp < n_parts) accumulate(k, ll[pp] * expf(mm[pp] - M), pre[k][jj]);
+            }
+            const float4 *o = o_row(hh, slot % (kD / 4));
+            for (int pp = grp + PRE * GROUPS; pp < n_parts; pp += GROUPS)
+                accumulate(k, ll[pp] * expf(mm[pp] - M), __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
+        }
+    } else {
+        // Long contexts: maxima first, then tiles of weights, each tile's rows streamed.
+        for (int hh = warp; hh < G; hh += kWarps) {
+            const float *m = P.m_part + (row0 + hh) * P.max_partitions;
+            float M = -INFINITY;
+#pragma unroll 4
+            for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(m + pp));
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
+            if (lane == 0) s_max[hh] = M;
+        }
+        for (int p0 = 0; p0 < n_parts; p0 += kMergeTile) {
+            const int n = min(kMergeTile, n_parts - p0);
+            __syncthreads();  // s_max ready / previous tile consumed
+            for (int i = threadIdx.x; i < G * n; i += kThreads) {
+                const int hh = i / n, pp = i - hh * n;
+                const int64_t prow = (row0 + hh) * P.max_partitions + p0 + pp;
+                s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < PER_THREAD; ++k) {
+                const int slot = slot0 + k * kThreads;
+                const int hh = slot / (kD / 4);
+                const float4 *o = o_row(hh, slot % (kD / 4)) + static_cast<int64_t>(p0) * (kD / 4);
+                const float *w = s_wt + hh * kMergeTile;
 #pragma unroll 8
-            for (int pp = grp; pp < n; pp += GROUPS) {
-                const float4 v = __ldcg(o + static_cast<int64_t>(pp) * (kD / 4));
-                const float wp = w[pp];
-                macc[k].x = fmaf(wp, v.x, macc[k].x);
-                macc[k].y = fmaf(wp, v.y, macc[k].y);
-                macc[k].z = fmaf(wp, v.z, macc[k].z);
-                macc[k].w = fmaf(wp, v.w, macc[k].w);
-                msum[k] += wp;
+                for (int pp = grp; pp < n; pp += GROUPS) accumulate(k, w[pp], __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
             }
         }
     }

@@ -161,3 +161,10 @@ def test_workspace_reuse_leaves_counters_zero():
         counters = ws[up(rows * 128 * 4) + 2 * up(rows * 4):].view(torch.int32)
         assert int(counters.abs().sum()) == 0
     assert_no_device_error()
+
+
+def test_context_beyond_one_merge_tile():
+    # 270,000 tokens = 528 partitions of 512: the fused merge takes its tiled branch
+    case = workloads.random_case(31, [270000, 700], 2, 1, block_size=128)
+    err, _, _ = run_parity(case)
+    assert err <= ATTN_TOL, err
