@@ -257,20 +257,32 @@ def run_ours(args):
         pkv.slot_mapping(block_tables.cpu(), torch.tensor(c, dtype=torch.int32) - 1, bs) for c in ctx_steps]).to(dev)
     ctx_cur = ctx_dev[0].clone()
     slot_cur = slot_dev[0].clone()
-    ws = pkv.make_workspace(B, Hq, max_ctx_cap, dev)
+    cascade = args.workload == "shared_prefix" and not args.no_cascade
+    prefix_len = 1024 if args.workload == "shared_prefix" else 0
+    if cascade:
+        ws = pkv.make_shared_prefix_workspace(B, Hq, max_ctx_cap, prefix_len, dev)
+    else:
+        ws = pkv.make_workspace(B, Hq, max_ctx_cap, dev)
+
+    def decode(l, c):
+        if cascade:
+            pkv.decode_attention_shared_prefix(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur,
+                                               c.scale, prefix_len, ws)
+        else:
+            pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
+                                 workspace=ws)
 
     prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
     bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens) for c in ctx_steps]
     logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs) for c in ctx_steps]
 
-    split = ws is not None
-    launches_per_step = n_layers * 2     # append + decode (the split's merge runs inside the decode kernel)
+    # append + decode (the split's merge runs inside the decode kernel; the cascade adds its prefix kernel)
+    launches_per_step = n_layers * (3 if cascade else 2)
 
     def step():
         for l, c in enumerate(cases):
             pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
-            pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
-                                 workspace=ws)
+            decode(l, c)
 
     def set_step(i):
         j = i % steps_cycle
@@ -352,8 +364,7 @@ def run_ours(args):
             a, b = ev[i]
             a.record(stream)
             for l, c in enumerate(cases):
-                pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
-                                     workspace=ws)
+                decode(l, c)
             b.record(stream)
             kernel_bytes += bytes_per_step[j % len(bytes_per_step)]
     barrier()
@@ -440,6 +451,8 @@ def run_ours(args):
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
                   % (cases[0].k_cache.numel() * 4 / 1e6, bytes_job / 1e9),
             "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
+            "decode_call": "pkv_decode_attention_shared_prefix (prefix 1024 tokens)" if cascade
+            else "pkv_decode_attention",
         },
         "tokens_per_s": round(B * world / (ms_job * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * gbs / peak, 1),
@@ -601,6 +614,7 @@ def main(argv=None):
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--layers", type=int, default=0, help="layers per step (default 32; fewer only for profiling)")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cascade", action="store_true", help="shared_prefix: plain decode instead of the cascade")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)

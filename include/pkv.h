@@ -80,6 +80,7 @@ extern "C" {
 #define PKV_DEV_BAD_CONTEXT 2    /* context_lens[b] > max_blocks_per_seq * block_size */
 #define PKV_DEV_BAD_SLOT 3       /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEV_WAIT_TIMEOUT 4   /* an asynchronous copy did not complete in time */
+#define PKV_DEV_PREFIX_MISMATCH 5 /* a block table does not start with the shared prefix's blocks */
 
 /* Defaults and limits of the decode kernels. */
 #define PKV_HEAD_DIM 128             /* the only head_dim the decode kernels take */
@@ -201,6 +202,40 @@ PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache,
                                  int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
                                  int head_dim, int block_size, int64_t num_blocks, float scale,
                                  void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Bytes of workspace pkv_decode_attention_shared_prefix needs: fp32 partials for
+ * ceil(prefix_len / 64) prefix chunks plus ceil((max_context - prefix_len) / 512)
+ * suffix partitions per (request, q head), then one int counter per
+ * (request, q head).  0 for invalid arguments. */
+PKV_API size_t pkv_shared_prefix_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                                int max_context, int prefix_len);
+
+/* Decode attention for a batch whose block tables all begin with the same
+ * prefix_len / block_size blocks (a shared prompt prefix: "推理优化这件事，为什么值得
+ * 反复复盘", sec. 4.2; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2).  The
+ * result equals pkv_decode_attention on the same arguments, but the prefix's
+ * K/V is read once per kv head for the whole batch instead of once per
+ * request: a first kernel scores every request's query rows against the
+ * prefix in 64-token chunks (tensor-core MMA over the B x G rows of each kv
+ * head), a second runs the split decode over each request's suffix (tokens
+ * from prefix_len on) and merges prefix chunks and suffix partitions by
+ * log-sum-exp.
+ * Requirements (besides those of pkv_decode_attention): prefix_len > 0 and a
+ * multiple of block_size; context_lens[b] >= prefix_len; row b of
+ * block_tables starts with the same prefix_len / block_size ids as row 0
+ * (checked on the device: PKV_DEV_PREFIX_MISMATCH); workspace of
+ * pkv_shared_prefix_workspace_size(num_seqs, num_q_heads, 128,
+ * max_blocks_per_seq * block_size, prefix_len) bytes, 256-byte aligned, whose
+ * counter region is zero before first use (calls leave it zero).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+PKV_API int pkv_decode_attention_shared_prefix(void *out, const void *q, const void *k_cache,
+                                               const void *v_cache, const int32_t *block_tables,
+                                               const int32_t *context_lens, int num_seqs,
+                                               int max_blocks_per_seq, int num_q_heads,
+                                               int num_kv_heads, int head_dim, int block_size,
+                                               int64_t num_blocks, float scale, int prefix_len,
+                                               void *workspace, size_t workspace_bytes,
+                                               pkv_stream_t stream);
 
 /* Split-context partial attention.  Partition p of request b covers logical
  * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each

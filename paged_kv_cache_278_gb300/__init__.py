@@ -22,10 +22,12 @@ import torch
 
 from . import _lib
 from ._lib import (PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
-                   PKV_DEV_OK, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION, PkvError)
+                   PKV_DEV_OK, PKV_DEV_PREFIX_MISMATCH, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION,
+                   PkvError)
 
 __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
+    "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -129,6 +131,33 @@ def decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, 
                                    block_tables.data_ptr(), context_lens.data_ptr(), b, block_tables.shape[1],
                                    hq, hkv, d, bs, nb, float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
     _lib.check(st, "pkv_decode_attention")
+    return out
+
+
+def make_shared_prefix_workspace(num_seqs: int, num_q_heads: int, max_context: int, prefix_len: int,
+                                 device) -> torch.Tensor:
+    """Allocate (with torch) the zero-filled workspace decode_attention_shared_prefix needs."""
+    n = int(_L().pkv_shared_prefix_workspace_size(num_seqs, num_q_heads, PKV_HEAD_DIM, max_context, prefix_len))
+    if n == 0:
+        raise ValueError("invalid shared-prefix workspace request")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_attention_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   scale: float, prefix_len: int, workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """Same result as decode_attention for tables that all start with the same prefix_len tokens'
+    blocks; the prefix's K/V is read once per kv head for the whole batch."""
+    nb, hkv, bs, d, b, hq, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    st = _L().pkv_decode_attention_shared_prefix(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), int(prefix_len),
+        workspace.data_ptr(), workspace.numel(), _stream(dev, stream))
+    _lib.check(st, "pkv_decode_attention_shared_prefix")
     return out
 
 

@@ -30,6 +30,7 @@ PKV_DEV_BAD_BLOCK_ID = 1
 PKV_DEV_BAD_CONTEXT = 2
 PKV_DEV_BAD_SLOT = 3
 PKV_DEV_WAIT_TIMEOUT = 4
+PKV_DEV_PREFIX_MISMATCH = 5
 
 PKV_HEAD_DIM = 128
 PKV_DEFAULT_PARTITION = 512
@@ -57,6 +58,10 @@ SIGNATURES = {
                                      c_void_p]),
     "pkv_decode_attention_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                              c_int, c_int, c_int, c_int, c_int, c_int64, c_float, c_void_p]),
+    "pkv_shared_prefix_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "pkv_decode_attention_shared_prefix": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                   c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
+                                                   c_int, c_void_p, c_size_t, c_void_p]),
     "pkv_decode_partition": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
                                      c_int, c_int, c_void_p]),

@@ -97,6 +97,8 @@ struct DecodeParams {
     int max_partitions;
     int direct_single;        // write fp16 out directly for single-partition requests
     int *counters;            // per (request, kv head) completion counters: fused merge when non-null
+    int token_offset;         // first logical token covered by partition 0 (shared-prefix length, else 0)
+    int slot_offset;          // partial slots [0, slot_offset) already hold the shared prefix's partials
 };
 
 constexpr int kMergeTile = 512;  // partitions whose weights the fused merge stages at a time
@@ -112,6 +114,146 @@ struct SmemLayout {
         return table(g) + (partition_size / kChunk + 1) * 4;
     }
 };
+
+// Log-sum-exp merge of partial slots [0, n_total) of the G query heads of (request b, kv head
+// kvh) into fp16 out; called by every thread of one CTA (it synchronises the CTA).
+template <int G>
+__device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, unsigned char *smem) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int Hq = P.num_q_heads;
+    // Slots: (packed head, 4 consecutive dims) -> float4 loads of o; partitions are split over
+    // GROUPS thread groups when there are fewer slots than threads, and loads are unrolled so a
+    // thread keeps 8 rows in flight.  All weights w = l exp(m - M) of a tile are staged first.
+    constexpr int SLOTS = G * (kD / 4);
+    constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
+    constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
+    static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
+    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout::stage_bytes,
+                  "merge staging must fit the stages");
+    float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][kMergeTile]
+    float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
+    float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
+    float *s_sum = reinterpret_cast<float *>(s_acc + GROUPS * SLOTS);                     // [GROUPS][SLOTS]
+    const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
+    const int grp = GROUPS > 1 ? threadIdx.x / SLOTS : 0;
+    const int slot0 = GROUPS > 1 ? threadIdx.x % SLOTS : threadIdx.x;
+    float4 macc[PER_THREAD];
+    float msum[PER_THREAD];
+#pragma unroll
+    for (int k = 0; k < PER_THREAD; ++k) {
+        macc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        msum[k] = 0.f;
+    }
+    auto o_row = [&](int hh, int d4) {
+        return reinterpret_cast<const float4 *>(P.o_part + (row0 + hh) * P.max_partitions * kD) + d4;
+    };
+    auto accumulate = [&](int k, float w, float4 v) {
+        macc[k].x = fmaf(w, v.x, macc[k].x);
+        macc[k].y = fmaf(w, v.y, macc[k].y);
+        macc[k].z = fmaf(w, v.z, macc[k].z);
+        macc[k].w = fmaf(w, v.w, macc[k].w);
+        msum[k] += w;
+    };
+    if (n_total <= kMergeTile) {
+        // Fast path, about one L2 round trip: issue this thread's first PRE partial rows, stage
+        // every (m, l) of the group in shared memory meanwhile, then weight the rows in registers.
+        constexpr int PRE = 8;
+        float4 pre[PER_THREAD][PRE];
+#pragma unroll
+        for (int k = 0; k < PER_THREAD; ++k) {
+            const int slot = slot0 + k * kThreads;
+            const float4 *o = o_row(slot / (kD / 4), slot % (kD / 4));
+#pragma unroll
+            for (int jj = 0; jj < PRE; ++jj) {
+                const int pp = grp + jj * GROUPS;
+                pre[k][jj] = pp < n_total ? __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float *s_mm = s_wt;
+        float *s_ll = s_wt + G * kMergeTile;
+        for (int i = threadIdx.x; i < G * n_total; i += kThreads) {
+            const int hh = i / n_total, pp = i - hh * n_total;
+            const int64_t prow = (row0 + hh) * P.max_partitions + pp;
+            s_mm[hh * kMergeTile + pp] = __ldcg(P.m_part + prow);
+            s_ll[hh * kMergeTile + pp] = __ldcg(P.l_part + prow);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < PER_THREAD; ++k) {
+            const int slot = slot0 + k * kThreads;
+            const int hh = slot / (kD / 4);
+            const float *mm = s_mm + hh * kMergeTile;
+            const float *ll = s_ll + hh * kMergeTile;
+            float M = -INFINITY;
+            for (int pp = 0; pp < n_total; ++pp) M = fmaxf(M, mm[pp]);
+#pragma unroll
+            for (int jj = 0; jj < PRE; ++jj) {
+                const int pp = grp + jj * GROUPS;
+                if (pp < n_total) accumulate(k, ll[pp] * expf(mm[pp] - M), pre[k][jj]);
+            }
+            const float4 *o = o_row(hh, slot % (kD / 4));
+            for (int pp = grp + PRE * GROUPS; pp < n_total; pp += GROUPS)
+                accumulate(k, ll[pp] * expf(mm[pp] - M), __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
+        }
+    } else {
+        // Long contexts: maxima first, then tiles of weights, each tile's rows streamed.
+        for (int hh = warp; hh < G; hh += kWarps) {
+            const float *m = P.m_part + (row0 + hh) * P.max_partitions;
+            float M = -INFINITY;
+#pragma unroll 4
+            for (int pp = lane; pp < n_total; pp += 32) M = fmaxf(M, __ldcg(m + pp));
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
+            if (lane == 0) s_max[hh] = M;
+        }
+        for (int p0 = 0; p0 < n_total; p0 += kMergeTile) {
+            const int n = min(kMergeTile, n_total - p0);
+            __syncthreads();  // s_max ready / previous tile consumed
+            for (int i = threadIdx.x; i < G * n; i += kThreads) {
+                const int hh = i / n, pp = i - hh * n;
+                const int64_t prow = (row0 + hh) * P.max_partitions + p0 + pp;
+                s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < PER_THREAD; ++k) {
+                const int slot = slot0 + k * kThreads;
+                const int hh = slot / (kD / 4);
+                const float4 *o = o_row(hh, slot % (kD / 4)) + static_cast<int64_t>(p0) * (kD / 4);
+                const float *w = s_wt + hh * kMergeTile;
+#pragma unroll 8
+                for (int pp = grp; pp < n; pp += GROUPS) accumulate(k, w[pp], __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
+            }
+        }
+    }
+    if (GROUPS > 1) {
+        s_acc[grp * SLOTS + slot0] = macc[0];
+        s_sum[grp * SLOTS + slot0] = msum[0];
+        __syncthreads();
+        if (grp != 0) return;
+        for (int g2 = 1; g2 < GROUPS; ++g2) {
+            const float4 v = s_acc[g2 * SLOTS + slot0];
+            macc[0].x += v.x;
+            macc[0].y += v.y;
+            macc[0].z += v.z;
+            macc[0].w += v.w;
+            msum[0] += s_sum[g2 * SLOTS + slot0];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < PER_THREAD; ++k) {
+        const int slot = slot0 + k * kThreads;
+        const int hh = slot / (kD / 4), d4 = slot % (kD / 4);
+        const float inv = 1.f / msum[k];
+        __half2 lo = __floats2half2_rn(macc[k].x * inv, macc[k].y * inv);
+        __half2 hi = __floats2half2_rn(macc[k].z * inv, macc[k].w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(P.out + (row0 + hh) * kD + d4 * 4) = packed;
+    }
+}
 
 template <int G, int LPT>
 __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partition_kernel(const DecodeParams P) {
@@ -145,8 +287,13 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
         ctx = cap;
     }
     if (ctx < 0) ctx = 0;
-    const int n_parts = (ctx + P.partition_size - 1) / P.partition_size;
-    const bool direct = P.direct_single && n_parts <= 1;
+    const int tok_begin = P.token_offset;  // > 0 only for the suffix pass after a shared prefix
+    if (tok_begin > 0 && ctx < tok_begin) {
+        if (part == 0 && kvh == 0 && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
+        ctx = tok_begin;
+    }
+    const int n_parts = (ctx - tok_begin + P.partition_size - 1) / P.partition_size;
+    const bool direct = P.direct_single && n_parts <= 1 && P.slot_offset == 0;
 
     if (ctx == 0) {  // empty request: zero output (or an empty partial)
         if (part != 0) return;
@@ -165,9 +312,13 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
         }
         return;
     }
+    if (n_parts == 0) {  // shared-prefix pass: the whole context is the prefix, merge its chunks only
+        if (part == 0 && P.counters != nullptr) merge_group<G>(P, b, kvh, P.slot_offset, smem);
+        return;
+    }
     if (part >= n_parts) return;
 
-    const int start = part * P.partition_size;
+    const int start = tok_begin + part * P.partition_size;
     const int n_tok = min(P.partition_size, ctx - start);
     const int n_chunks = (n_tok + kChunk - 1) / kChunk;
     const int lb0 = start / bs;
@@ -192,6 +343,11 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
                 id = 0;
             }
             s_table[i] = id;
+        }
+        if (tok_begin > 0 && part == 0 && kvh == 0 && b > 0) {  // every table must start with the shared prefix
+            const int32_t *row_b = P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq;
+            for (int i = threadIdx.x; i < tok_begin / bs; i += kThreads)
+                if (__ldg(row_b + i) != __ldg(P.block_tables + i)) pkv::record_error(&g_decode_error, PKV_DEV_PREFIX_MISMATCH);
         }
     }
 
@@ -472,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
         if (direct) {
             P.out[row * kD + d] = __float2half_rn(o);
         } else {
-            const int64_t prow = row * P.max_partitions + part;
+            const int64_t prow = row * P.max_partitions + P.slot_offset + part;
             P.o_part[prow * kD + d] = o;
             if (d == 0) {
                 P.m_part[prow] = M * kLn2;
@@ -492,137 +648,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
     if (threadIdx.x == 0) s_last = pkv::atomic_add_acq_rel_gpu(counter, 1) == n_parts - 1;
     __syncthreads();
     if (!s_last) return;
-    // Slots: (packed head, 4 consecutive dims) -> float4 loads of o; partitions are split over
-    // GROUPS thread groups when there are fewer slots than threads, and loads are unrolled so a
-    // thread keeps 8 rows in flight.  All weights w = l exp(m - M) of a tile are staged first.
-    constexpr int SLOTS = G * (kD / 4);
-    constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
-    constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
-    static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
-    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout::stage_bytes,
-                  "merge staging must fit the stages");
-    float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][kMergeTile]
-    float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
-    float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
-    float *s_sum = reinterpret_cast<float *>(s_acc + GROUPS * SLOTS);                     // [GROUPS][SLOTS]
-    const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
-    const int grp = GROUPS > 1 ? threadIdx.x / SLOTS : 0;
-    const int slot0 = GROUPS > 1 ? threadIdx.x % SLOTS : threadIdx.x;
-    float4 macc[PER_THREAD];
-    float msum[PER_THREAD];
-#pragma unroll
-    for (int k = 0; k < PER_THREAD; ++k) {
-        macc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        msum[k] = 0.f;
-    }
-    auto o_row = [&](int hh, int d4) {
-        return reinterpret_cast<const float4 *>(P.o_part + (row0 + hh) * P.max_partitions * kD) + d4;
-    };
-    auto accumulate = [&](int k, float w, float4 v) {
-        macc[k].x = fmaf(w, v.x, macc[k].x);
-        macc[k].y = fmaf(w, v.y, macc[k].y);
-        macc[k].z = fmaf(w, v.z, macc[k].z);
-        macc[k].w = fmaf(w, v.w, macc[k].w);
-        msum[k] += w;
-    };
-    if (n_parts <= kMergeTile) {
-        // Fast path, about one L2 round trip: issue this thread's first PRE partial rows, stage
-        // every (m, l) of the group in shared memory meanwhile, then weight the rows in registers.
-        constexpr int PRE = 8;
-        float4 pre[PER_THREAD][PRE];
-#pragma unroll
-        for (int k = 0; k < PER_THREAD; ++k) {
-            const int slot = slot0 + k * kThreads;
-            const float4 *o = o_row(slot / (kD / 4), slot % (kD / 4));
-#pragma unroll
-            for (int jj = 0; jj < PRE; ++jj) {
-                const int pp = grp + jj * GROUPS;
-                pre[k][jj] = pp < n_parts ? __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        float *s_mm = s_wt;
-        float *s_ll = s_wt + G * kMergeTile;
-        for (int i = threadIdx.x; i < G * n_parts; i += kThreads) {
-            const int hh = i / n_parts, pp = i - hh * n_parts;
-            const int64_t prow = (row0 + hh) * P.max_partitions + pp;
-            s_mm[hh * kMergeTile + pp] = __ldcg(P.m_part + prow);
-            s_ll[hh * kMergeTile + pp] = __ldcg(P.l_part + prow);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < PER_THREAD; ++k) {
-            const int slot = slot0 + k * kThreads;
-            const int hh = slot / (kD / 4);
-            const float *mm = s_mm + hh * kMergeTile;
-            const float *ll = s_ll + hh * kMergeTile;
-            float M = -INFINITY;
-            for (int pp = 0; pp < n_parts; ++pp) M = fmaxf(M, mm[pp]);
-#pragma unroll
-            for (int jj = 0; jj < PRE; ++jj) {
-                const int pp = grp + jj * GROUPS;
-                if (pp < n_parts) accumulate(k, ll[pp] * expf(mm[pp] - M), pre[k][jj]);
-            }
-            const float4 *o = o_row(hh, slot % (kD / 4));
-            for (int pp = grp + PRE * GROUPS; pp < n_parts; pp += GROUPS)
-                accumulate(k, ll[pp] * expf(mm[pp] - M), __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
-        }
-    } else {
-        // Long contexts: maxima first, then tiles of weights, each tile's rows streamed.
-        for (int hh = warp; hh < G; hh += kWarps) {
-            const float *m = P.m_part + (row0 + hh) * P.max_partitions;
-            float M = -INFINITY;
-#pragma unroll 4
-            for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(m + pp));
-#pragma unroll
-            for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
-            if (lane == 0) s_max[hh] = M;
-        }
-        for (int p0 = 0; p0 < n_parts; p0 += kMergeTile) {
-            const int n = min(kMergeTile, n_parts - p0);
-            __syncthreads();  // s_max ready / previous tile consumed
-            for (int i = threadIdx.x; i < G * n; i += kThreads) {
-                const int hh = i / n, pp = i - hh * n;
-                const int64_t prow = (row0 + hh) * P.max_partitions + p0 + pp;
-                s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int k = 0; k < PER_THREAD; ++k) {
-                const int slot = slot0 + k * kThreads;
-                const int hh = slot / (kD / 4);
-                const float4 *o = o_row(hh, slot % (kD / 4)) + static_cast<int64_t>(p0) * (kD / 4);
-                const float *w = s_wt + hh * kMergeTile;
-#pragma unroll 8
-                for (int pp = grp; pp < n; pp += GROUPS) accumulate(k, w[pp], __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
-            }
-        }
-    }
-    if (GROUPS > 1) {
-        s_acc[grp * SLOTS + slot0] = macc[0];
-        s_sum[grp * SLOTS + slot0] = msum[0];
-        __syncthreads();
-        if (grp != 0) return;
-        for (int g2 = 1; g2 < GROUPS; ++g2) {
-            const float4 v = s_acc[g2 * SLOTS + slot0];
-            macc[0].x += v.x;
-            macc[0].y += v.y;
-            macc[0].z += v.z;
-            macc[0].w += v.w;
-            msum[0] += s_sum[g2 * SLOTS + slot0];
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < PER_THREAD; ++k) {
-        const int slot = slot0 + k * kThreads;
-        const int hh = slot / (kD / 4), d4 = slot % (kD / 4);
-        const float inv = 1.f / msum[k];
-        __half2 lo = __floats2half2_rn(macc[k].x * inv, macc[k].y * inv);
-        __half2 hi = __floats2half2_rn(macc[k].z * inv, macc[k].w * inv);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t *>(&lo);
-        packed.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(P.out + (row0 + hh) * kD + d4 * 4) = packed;
-    }
+    merge_group<G>(P, b, kvh, P.slot_offset + n_parts, smem);
     if (threadIdx.x == 0) *counter = 0;
 }
 
@@ -703,7 +729,7 @@ constexpr int lanes_per_token() {
 }
 
 template <int G>
-int launch_partition(const DecodeParams &p, int num_seqs, cudaStream_t stream) {
+int launch_partition(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
     auto kernel = decode_partition_kernel<G, LPT>;
     const int smem = SmemLayout::total(G, p.partition_size);
@@ -717,17 +743,17 @@ int launch_partition(const DecodeParams &p, int num_seqs, cudaStream_t stream) {
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const dim3 grid(p.max_partitions, p.num_kv_heads, num_seqs);
+    const dim3 grid(grid_parts > 0 ? grid_parts : p.max_partitions, p.num_kv_heads, num_seqs);
     kernel<<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream) {
+int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream, int grid_parts = 0) {
     switch (group) {
-        case 1: return launch_partition<1>(p, num_seqs, stream);
-        case 2: return launch_partition<2>(p, num_seqs, stream);
-        case 4: return launch_partition<4>(p, num_seqs, stream);
-        case 8: return launch_partition<8>(p, num_seqs, stream);
+        case 1: return launch_partition<1>(p, num_seqs, stream, grid_parts);
+        case 2: return launch_partition<2>(p, num_seqs, stream, grid_parts);
+        case 4: return launch_partition<4>(p, num_seqs, stream, grid_parts);
+        case 8: return launch_partition<8>(p, num_seqs, stream, grid_parts);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }
@@ -753,7 +779,7 @@ int check_common(const void *q, const void *k_cache, const void *v_cache, const 
     return PKV_OK;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+using pkv_internal::align256;
 
 // Split workspace layout: o_part | m_part | l_part | counters, each 256-byte aligned.
 size_t counters_offset(size_t rows) {
@@ -926,6 +952,40 @@ extern "C" PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, co
 }
 
 namespace pkv_internal {
+
+int check_decode_args(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                      const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks) {
+    return check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq, num_q_heads,
+                        num_kv_heads, head_dim, block_size, num_blocks);
+}
+
+int launch_split_pass(const SplitPass &a, void *stream) {
+    DecodeParams p{};
+    p.q = static_cast<const __half *>(a.q);
+    p.k_cache = static_cast<const unsigned char *>(a.k_cache);
+    p.v_cache = static_cast<const unsigned char *>(a.v_cache);
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.out = static_cast<__half *>(a.out);
+    p.o_part = a.o_part;
+    p.m_part = a.m_part;
+    p.l_part = a.l_part;
+    p.max_blocks_per_seq = a.max_blocks_per_seq;
+    p.num_q_heads = a.num_q_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.block_size = a.block_size;
+    p.num_blocks = a.num_blocks;
+    p.q_scale = a.scale * kLog2e;
+    p.partition_size = a.partition_size;
+    p.max_partitions = a.max_partitions;
+    p.direct_single = 0;
+    p.counters = a.counters;
+    p.token_offset = a.token_offset;
+    p.slot_offset = a.slot_offset;
+    return dispatch_partition(p, a.num_seqs, a.num_q_heads / a.num_kv_heads, reinterpret_cast<cudaStream_t>(stream),
+                              a.grid_partitions);
+}
 
 int decode_take_error(int *code) {
     int value = 0;

@@ -169,12 +169,14 @@ PKV_API int pkv_get_device_error(pkv_stream_t stream, int *code) {
     if (!code) return PKV_ERR_INVALID_ARG;
     *code = PKV_DEV_OK;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
-    int a = 0, d = 0;
+    int a = 0, d = 0, p = 0;
     int st = pkv_internal::append_take_error(&a);
     if (st != PKV_OK) return st;
     st = pkv_internal::decode_take_error(&d);
     if (st != PKV_OK) return st;
-    *code = a ? a : d;
+    st = pkv_internal::prefix_take_error(&p);
+    if (st != PKV_OK) return st;
+    *code = a ? a : (d ? d : p);
     return PKV_OK;
 }
 

@@ -1,6 +1,7 @@
 // pkv_internal.h -- host-side helpers shared by the library's translation units.
 #pragma once
 
+#include <stddef.h>
 #include <stdint.h>
 
 namespace pkv_internal {
@@ -12,5 +13,29 @@ inline bool aligned16(const void *p) { return aligned(p, 16); }
 // the current device and reset it to zero.  Return PKV_OK or PKV_ERR_CUDA.
 int append_take_error(int *code);
 int decode_take_error(int *code);
+int prefix_take_error(int *code);
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Host-side argument checks shared by every decode entry point (PKV_OK or an error status).
+int check_decode_args(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                      const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks);
+
+// One split pass of the decode kernel writing partial slots [slot_offset, slot_offset + parts)
+// for the tokens from token_offset on, with the log-sum-exp merge of slots
+// [0, slot_offset + parts) fused in (counters must be zero; they are left zero).
+struct SplitPass {
+    void *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    int num_seqs, max_blocks_per_seq, num_q_heads, num_kv_heads, block_size;
+    int64_t num_blocks;
+    float scale;
+    int partition_size, max_partitions, token_offset, slot_offset, grid_partitions;
+    float *o_part, *m_part, *l_part;
+    int *counters;
+};
+int launch_split_pass(const SplitPass &a, void *stream);
 
 }  // namespace pkv_internal

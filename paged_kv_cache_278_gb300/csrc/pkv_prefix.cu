@@ -1,0 +1,351 @@
+// pkv_prefix.cu -- decode attention for a batch whose block tables share a common prefix.
+//
+// Requests that start with the same system prompt reference the same KV blocks for it
+// ("推理优化这件事，为什么值得反复复盘", sec. 4.2: a shared-prefix cache lets many requests use
+// one copy of the prompt's KV; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2: pages
+// shared across requests with the same prompt).  Attention over such a batch is computed in
+// two passes that together equal softmax(scale q K^T) V over each full context:
+//
+//   1. prefix_kernel: for every kv head and every 64-token chunk of the shared prefix, the
+//      scores of ALL requests' query rows that read this kv head (B x G rows) against the
+//      chunk, their exact chunk softmax statistics and the normalised P.V, written as
+//      partial slots [0, n_chunks) of the split layout.  The prefix's K/V is read once per
+//      step instead of once per request.  With B x G rows the scores form a dense
+//      (rows x 64 x 128) contraction, so it runs on the tensor cores: warp-level
+//      m16n8k16 MMAs, fp16 operands with fp32 accumulation; P is split into fp16 hi + lo
+//      parts for the P.V product so the weights keep ~22 bits.
+//   2. The ordinary split decode kernel over each request's private suffix (tokens from
+//      prefix_len on), writing slots n_chunks.. and merging all slots by log-sum-exp in the
+//      same kernel (last partition of each request to finish).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ int g_prefix_error;
+
+constexpr int kD = PKV_HEAD_DIM;       // 128
+constexpr int kChunkTok = 64;          // prefix tokens per CTA
+constexpr int kWarps = 8;              // 16 query rows per warp
+constexpr int kRows = kWarps * 16;     // query rows per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kPad = kD + 8;           // halves per shared-memory row: 272 B keeps ldmatrix conflict-free
+constexpr int kSmemBytes = (2 * kChunkTok + kRows) * kPad * 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct PrefixParams {
+    const __half *q;
+    const __half *k_cache;
+    const __half *v_cache;
+    const int32_t *block_tables;  // row 0 holds the shared prefix's blocks
+    float *o_part;
+    float *m_part;
+    float *l_part;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    int prefix_len;
+    int max_partitions;
+    int64_t num_blocks;
+    float q_scale;  // scale * log2(e)
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(pkv::smem_addr(p)));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(pkv::smem_addr(p)));
+}
+
+// d += a (16x16 fp16, row) * b (16x8 fp16, col), fp32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Grid (prefix chunks, kv heads, ceil(B*G / 128)); 8 warps, each owning 16 query rows.
+__global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __half *sK = reinterpret_cast<__half *>(smem);      // [kChunkTok][kPad]
+    __half *sV = sK + kChunkTok * kPad;                   // [kChunkTok][kPad]
+    __half *sQ = sV + kChunkTok * kPad;                   // [kRows][kPad]
+    const int chunk = blockIdx.x, kvh = blockIdx.y, rtile = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hq = P.num_q_heads, Hkv = P.num_kv_heads, G = Hq / Hkv, bs = P.block_size;
+    const int rows = P.num_seqs * G;
+    const int row0 = rtile * kRows;
+    const int tok0 = chunk * kChunkTok;
+    const int ntok = min(kChunkTok, P.prefix_len - tok0);
+
+    // K/V chunk (zero rows past the prefix) and the CTA's query rows, 16 bytes per thread access
+    for (int i = threadIdx.x; i < kChunkTok * (kD / 8); i += kThreads) {
+        const int t = i / (kD / 8), piece = i % (kD / 8);
+        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+        if (t < ntok) {
+            const int tok = tok0 + t;
+            int32_t id = __ldg(P.block_tables + tok / bs);
+            if (id < 0 || id >= P.num_blocks) {
+                pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
+                id = 0;
+            }
+            const int64_t src = ((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs) * kD + piece * 8;
+            kv = __ldg(reinterpret_cast<const uint4 *>(P.k_cache + src));
+            vv = __ldg(reinterpret_cast<const uint4 *>(P.v_cache + src));
+        }
+        *reinterpret_cast<uint4 *>(sK + t * kPad + piece * 8) = kv;
+        *reinterpret_cast<uint4 *>(sV + t * kPad + piece * 8) = vv;
+    }
+    for (int i = threadIdx.x; i < kRows * (kD / 8); i += kThreads) {
+        const int r = i / (kD / 8), piece = i % (kD / 8);
+        const int gr = row0 + r;
+        uint4 qv = make_uint4(0, 0, 0, 0);
+        if (gr < rows) {
+            const int b = gr / G, hh = gr % G;
+            qv = __ldg(reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD) + piece);
+        }
+        *reinterpret_cast<uint4 *>(sQ + r * kPad + piece * 8) = qv;
+    }
+    __syncthreads();
+    if (row0 + warp * 16 >= rows) return;  // no barrier follows
+
+    // ---- S = Q K^T for this warp's 16 rows x 64 tokens (8 n-tiles), K = 128 dims (8 k-steps)
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kD / 16; ++ks) {
+        uint32_t a[4];
+        ldmatrix_x4(a, sQ + (warp * 16 + (lane & 15)) * kPad + ks * 16 + (lane >> 4) * 8);
+#pragma unroll
+        for (int nt = 0; nt < 8; nt += 2) {
+            uint32_t bfr[4];
+            ldmatrix_x4(bfr, sK + (nt * 8 + (lane & 7) + (lane >> 4) * 8) * kPad + ks * 16 + ((lane >> 3) & 1) * 8);
+            mma16816(s[nt], a, bfr[0], bfr[1]);
+            mma16816(s[nt + 1], a, bfr[2], bfr[3]);
+        }
+    }
+    // ---- exact softmax over the chunk for rows g = lane/4 (regs 0,1) and g + 8 (regs 2,3)
+    float m_lo = -INFINITY, m_hi = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int col = nt * 8 + (lane & 3) * 2 + (e & 1);
+            s[nt][e] = col < ntok ? s[nt][e] * P.q_scale : -INFINITY;
+        }
+        m_lo = fmaxf(m_lo, fmaxf(s[nt][0], s[nt][1]));
+        m_hi = fmaxf(m_hi, fmaxf(s[nt][2], s[nt][3]));
+    }
+#pragma unroll
+    for (int sh = 1; sh <= 2; sh <<= 1) {
+        m_lo = fmaxf(m_lo, __shfl_xor_sync(pkv::kFullMask, m_lo, sh));
+        m_hi = fmaxf(m_hi, __shfl_xor_sync(pkv::kFullMask, m_hi, sh));
+    }
+    float l_lo = 0.f, l_hi = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] = exp2f(s[nt][0] - m_lo);
+        s[nt][1] = exp2f(s[nt][1] - m_lo);
+        s[nt][2] = exp2f(s[nt][2] - m_hi);
+        s[nt][3] = exp2f(s[nt][3] - m_hi);
+        l_lo += s[nt][0] + s[nt][1];
+        l_hi += s[nt][2] + s[nt][3];
+    }
+#pragma unroll
+    for (int sh = 1; sh <= 2; sh <<= 1) {
+        l_lo += __shfl_xor_sync(pkv::kFullMask, l_lo, sh);
+        l_hi += __shfl_xor_sync(pkv::kFullMask, l_hi, sh);
+    }
+
+    // ---- O = P V: 16 rows x 128 dims (16 n-tiles), K = 64 tokens (4 k-steps), P = hi + lo
+    float o[16][4];
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+#pragma unroll
+    for (int kt = 0; kt < kChunkTok / 16; ++kt) {
+        const float src[8] = {s[2 * kt][0],     s[2 * kt][1],     s[2 * kt][2],     s[2 * kt][3],
+                              s[2 * kt + 1][0], s[2 * kt + 1][1], s[2 * kt + 1][2], s[2 * kt + 1][3]};
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            // fragment r: (row g | g+8) x (tokens 16kt + {0..7} | {8..15}): C-fragment pairs
+            const float x0 = src[(r >> 1) * 4 + (r & 1) * 2], x1 = src[(r >> 1) * 4 + (r & 1) * 2 + 1];
+            const __half2 hi = __floats2half2_rn(x0, x1);
+            const float2 hf = __half22float2(hi);
+            ph[r] = *reinterpret_cast<const uint32_t *>(&hi);
+            pl[r] = pack_half2(x0 - hf.x, x1 - hf.y);
+        }
+#pragma unroll
+        for (int dt = 0; dt < 16; dt += 2) {
+            uint32_t vb[4];
+            ldmatrix_x4_trans(vb, sV + (kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7)) * kPad + (dt + (lane >> 4)) * 8);
+            mma16816(o[dt], ph, vb[0], vb[1]);
+            mma16816(o[dt], pl, vb[0], vb[1]);
+            mma16816(o[dt + 1], ph, vb[2], vb[3]);
+            mma16816(o[dt + 1], pl, vb[2], vb[3]);
+        }
+    }
+
+    // ---- partial slot `chunk` of each valid row: normalised o, m in natural-log units, l
+    const int g = lane >> 2;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int gr = row0 + warp * 16 + g + half * 8;
+        if (gr >= rows) continue;
+        const int b = gr / G, hh = gr % G;
+        const int64_t prow = (static_cast<int64_t>(b) * Hq + kvh * G + hh) * P.max_partitions + chunk;
+        const float l = half ? l_hi : l_lo;
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) {
+            const float2 v = make_float2(o[dt][half * 2] * inv, o[dt][half * 2 + 1] * inv);
+            *reinterpret_cast<float2 *>(P.o_part + prow * kD + dt * 8 + (lane & 3) * 2) = v;
+        }
+        if ((lane & 3) == 0) {
+            P.m_part[prow] = (half ? m_hi : m_lo) * kLn2;
+            P.l_part[prow] = l;
+        }
+    }
+}
+
+struct SharedLayout {
+    int n_pre, n_suf, max_parts;
+    size_t rows, o_bytes, m_bytes, counter_off, total;
+};
+
+SharedLayout shared_layout(int num_seqs, int num_q_heads, int max_context, int prefix_len) {
+    SharedLayout L{};
+    L.n_pre = (prefix_len + kChunkTok - 1) / kChunkTok;
+    const int rest = max_context - prefix_len;
+    L.n_suf = rest > 0 ? (rest + PKV_DEFAULT_PARTITION - 1) / PKV_DEFAULT_PARTITION : 0;
+    L.max_parts = L.n_pre + L.n_suf;
+    L.rows = static_cast<size_t>(num_seqs) * num_q_heads * L.max_parts;
+    L.o_bytes = pkv_internal::align256(L.rows * kD * sizeof(float));
+    L.m_bytes = pkv_internal::align256(L.rows * sizeof(float));
+    L.counter_off = L.o_bytes + 2 * L.m_bytes;
+    L.total = L.counter_off + pkv_internal::align256(static_cast<size_t>(num_seqs) * num_q_heads * sizeof(int));
+    return L;
+}
+
+}  // namespace
+
+extern "C" PKV_API size_t pkv_shared_prefix_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                                           int max_context, int prefix_len) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim != kD || prefix_len <= 0 || max_context < prefix_len) return 0;
+    return shared_layout(num_seqs, num_q_heads, max_context, prefix_len).total;
+}
+
+extern "C" PKV_API int pkv_decode_attention_shared_prefix(
+    void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+    const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int64_t num_blocks, float scale, int prefix_len, void *workspace,
+    size_t workspace_bytes, pkv_stream_t stream) {
+    int st = pkv_internal::check_decode_args(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                             max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                                             num_blocks);
+    if (st != PKV_OK) return st;
+    if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    if (prefix_len <= 0 || prefix_len % block_size != 0 || prefix_len > cap) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    const SharedLayout L = shared_layout(num_seqs, num_q_heads, static_cast<int>(cap), prefix_len);
+    if (!workspace || workspace_bytes < L.total || !pkv_internal::aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+    const int rows = num_seqs * (num_q_heads / num_kv_heads);
+    if (num_seqs > 65535 || (rows + kRows - 1) / kRows > 65535) return PKV_ERR_UNSUPPORTED;
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    PrefixParams p{};
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const __half *>(k_cache);
+    p.v_cache = static_cast<const __half *>(v_cache);
+    p.block_tables = block_tables;
+    p.o_part = reinterpret_cast<float *>(ws);
+    p.m_part = reinterpret_cast<float *>(ws + L.o_bytes);
+    p.l_part = reinterpret_cast<float *>(ws + L.o_bytes + L.m_bytes);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.prefix_len = prefix_len;
+    p.max_partitions = L.max_parts;
+    p.num_blocks = num_blocks;
+    p.q_scale = scale * kLog2e;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const dim3 grid(L.n_pre, num_kv_heads, (rows + kRows - 1) / kRows);
+    prefix_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+
+    pkv_internal::SplitPass a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.partition_size = PKV_DEFAULT_PARTITION;
+    a.max_partitions = L.max_parts;
+    a.token_offset = prefix_len;
+    a.slot_offset = L.n_pre;
+    a.grid_partitions = L.n_suf > 0 ? L.n_suf : 1;
+    a.o_part = p.o_part;
+    a.m_part = p.m_part;
+    a.l_part = p.l_part;
+    a.counters = reinterpret_cast<int *>(ws + L.counter_off);
+    return pkv_internal::launch_split_pass(a, stream);
+}
+
+namespace pkv_internal {
+
+int prefix_take_error(int *code) {
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_prefix_error, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_prefix_error, &zero, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    *code = value;
+    return PKV_OK;
+}
+
+}  // namespace pkv_internal
