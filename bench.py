@@ -258,30 +258,34 @@ def run_ours(args):
     ctx_cur = ctx_dev[0].clone()
     slot_cur = slot_dev[0].clone()
     cascade = args.workload == "shared_prefix" and not args.no_cascade
-    prefix_len = 1024 if args.workload == "shared_prefix" else 0
-    if cascade:
-        ws = pkv.make_shared_prefix_workspace(B, Hq, max_ctx_cap, prefix_len, dev)
-    else:
-        ws = pkv.make_workspace(B, Hq, max_ctx_cap, dev)
+    prefix_len = 1024 if cascade else 0
+    ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev)
 
     def decode(l, c):
-        if cascade:
-            pkv.decode_attention_shared_prefix(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur,
-                                               c.scale, prefix_len, ws)
+        """One layer of the step: the append is fused into the decode kernel (pkv_decode_step) unless
+        --separate-append asks for the two-call path (pkv_append + attention)."""
+        if args.separate_append:
+            pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
+            if cascade:
+                pkv.decode_attention_shared_prefix(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur,
+                                                   c.scale, prefix_len, ws)
+            else:
+                pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
+                                     workspace=ws)
         else:
-            pkv.decode_attention(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
-                                 workspace=ws)
+            pkv.decode_step(out_all[l], c.q, c.k_new, c.v_new, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
+                            prefix_len, ws)
 
     prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
     bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens) for c in ctx_steps]
     logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs) for c in ctx_steps]
 
-    # append + decode (the split's merge runs inside the decode kernel; the cascade adds its prefix kernel)
-    launches_per_step = n_layers * (3 if cascade else 2)
+    # per layer: the decode kernel (append and the split's merge fused in), plus the prefix kernel with the
+    # cascade, plus the append kernel on the two-call path
+    launches_per_step = n_layers * (1 + (1 if cascade else 0) + (1 if args.separate_append else 0))
 
     def step():
         for l, c in enumerate(cases):
-            pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
             decode(l, c)
 
     def set_step(i):
@@ -349,10 +353,10 @@ def run_ours(args):
     ms_total = e0.elapsed_time(e1)
     ms_per_step = ms_total / args.steps
 
-    # ---- timed region 2: the dominant kernel alone.  A pkv_decode_attention call is exactly one
-    # launch of the partition kernel (its log-sum-exp merge runs inside it); per step the layers'
-    # launches run back to back between one pair of CUDA events on the launching stream, so the
-    # average launch duration is (event interval) / launches, with no other kernel in between.
+    # ---- timed region 2: the dominant kernel alone.  A pkv_decode_step call is exactly one launch of
+    # the decode kernel (the append and the split's log-sum-exp merge run inside it; the cascade adds
+    # its small prefix kernel); per step the layers' launches run back to back between one pair of
+    # CUDA events on the launching stream: average launch duration = event interval / launches.
     kt_steps = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kt_steps)]
     kernel_bytes = 0
@@ -451,8 +455,8 @@ def run_ours(args):
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
                   % (cases[0].k_cache.numel() * 4 / 1e6, bytes_job / 1e9),
             "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
-            "decode_call": "pkv_decode_attention_shared_prefix (prefix 1024 tokens)" if cascade
-            else "pkv_decode_attention",
+            "decode_call": ("pkv_append + " if args.separate_append else "pkv_decode_step ")
+            + ("shared prefix 1024 tokens" if cascade else ""),
         },
         "tokens_per_s": round(B * world / (ms_job * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * gbs / peak, 1),
@@ -615,6 +619,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="layers per step (default 32; fewer only for profiling)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cascade", action="store_true", help="shared_prefix: plain decode instead of the cascade")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="two calls per layer (pkv_append, then attention) instead of pkv_decode_step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)

@@ -204,8 +204,9 @@ PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache,
                                  void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* Bytes of workspace pkv_decode_attention_shared_prefix needs: fp32 partials for
- * ceil(prefix_len / 64) prefix chunks plus ceil((max_context - prefix_len) / 512)
- * suffix partitions per (request, q head), then one int counter per
+ * ceil(prefix_len / 64) prefix chunks plus up to ceil((max_context - prefix_len) / 64)
+ * suffix partitions per (request, q head) (the call picks the suffix partition,
+ * 64..512 tokens, from the grid it gives), then one int counter per
  * (request, q head).  0 for invalid arguments. */
 PKV_API size_t pkv_shared_prefix_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                                 int max_context, int prefix_len);
@@ -236,6 +237,37 @@ PKV_API int pkv_decode_attention_shared_prefix(void *out, const void *q, const v
                                                int64_t num_blocks, float scale, int prefix_len,
                                                void *workspace, size_t workspace_bytes,
                                                pkv_stream_t stream);
+
+/* Workspace for pkv_decode_step: pkv_decode_workspace_size(..., max_context,
+ * PKV_DEFAULT_PARTITION) when prefix_len is 0, else
+ * pkv_shared_prefix_workspace_size(..., prefix_len). */
+PKV_API size_t pkv_decode_step_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                              int max_context, int prefix_len);
+
+/* One whole decode step in one call: append each request's new token in
+ * place, then attend over every cached token including it
+ * ("为什么“推理优化”不是锦上添花", sec. 3.1; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 4.2 and 4.3).
+ *   k_new, v_new : fp16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned; the
+ *                  token of request b goes to logical position context_lens[b] - 1,
+ *                  i.e. slot block_tables[b][(ctx-1)/bs] * bs + (ctx-1) % bs, which
+ *                  must lie in an allocated block (a request with context 0
+ *                  appends nothing; an invalid block id skips the write and is
+ *                  recorded as PKV_DEV_BAD_BLOCK_ID)
+ *   k_cache, v_cache : written (the new rows) and read.
+ * prefix_len 0: same result as pkv_slot_mapping(positions = ctx - 1) +
+ * pkv_append + pkv_decode_attention.  prefix_len > 0: same as pkv_append +
+ * pkv_decode_attention_shared_prefix (the new token must lie past the prefix).
+ * The append is fused into the decode kernel: the CTA that owns a request's
+ * last position writes the row to the cache and uses it directly, so a step
+ * is one kernel launch (two with a shared prefix).  Workspace rules as for the
+ * matching attention call.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+PKV_API int pkv_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
+                            void *k_cache, void *v_cache, const int32_t *block_tables,
+                            const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, float scale, int prefix_len, void *workspace,
+                            size_t workspace_bytes, pkv_stream_t stream);
 
 /* Split-context partial attention.  Partition p of request b covers logical
  * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each

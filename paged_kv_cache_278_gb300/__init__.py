@@ -28,6 +28,7 @@ from ._lib import (PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONT
 __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
     "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
+    "decode_step", "make_step_workspace",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -158,6 +159,41 @@ def decode_attention_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: 
         context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), int(prefix_len),
         workspace.data_ptr(), workspace.numel(), _stream(dev, stream))
     _lib.check(st, "pkv_decode_attention_shared_prefix")
+    return out
+
+
+def make_step_workspace(num_seqs: int, num_q_heads: int, max_context: int, prefix_len: int = 0,
+                        device=None) -> torch.Tensor | None:
+    """Zero-filled workspace for decode_step (None when it needs none)."""
+    n = int(_L().pkv_decode_step_workspace_size(num_seqs, num_q_heads, PKV_HEAD_DIM, max_context, prefix_len))
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                context_lens: torch.Tensor, scale: float, prefix_len: int = 0,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode step: write each request's new token [B, Hkv, D] at position context_lens - 1,
+    then out = softmax(scale q K^T) V over the whole context (append fused into the decode kernel)."""
+    nb, hkv, bs, d, b, hq, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if k_new.shape != (b, hkv, d) or v_new.shape != (b, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{b}, {hkv}, {d}]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    st = _L().pkv_decode_step(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                              v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), b,
+                              block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), int(prefix_len), ws_ptr,
+                              ws_bytes, _stream(dev, stream))
+    _lib.check(st, "pkv_decode_step")
     return out
 
 

@@ -62,6 +62,10 @@ SIGNATURES = {
     "pkv_decode_attention_shared_prefix": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                    c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
                                                    c_int, c_void_p, c_size_t, c_void_p]),
+    "pkv_decode_step_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "pkv_decode_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float, c_int, c_void_p,
+                                c_size_t, c_void_p]),
     "pkv_decode_partition": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
                                      c_int, c_int, c_void_p]),

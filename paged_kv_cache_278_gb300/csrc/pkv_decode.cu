@@ -99,6 +99,10 @@ struct DecodeParams {
     int *counters;            // per (request, kv head) completion counters: fused merge when non-null
     int token_offset;         // first logical token covered by partition 0 (shared-prefix length, else 0)
     int slot_offset;          // partial slots [0, slot_offset) already hold the shared prefix's partials
+    const __half *k_new;      // non-null: append k_new/v_new [B][Hkv][D] at position ctx_b - 1 first
+    const __half *v_new;
+    __half *k_cache_w;        // writable views of the caches for that append
+    __half *v_cache_w;
 };
 
 constexpr int kMergeTile = 512;  // partitions whose weights the fused merge stages at a time
@@ -109,7 +113,8 @@ struct SmemLayout {
     static constexpr int stage_bytes = kWarps * kStages * 2 * kTileBytes;
     static constexpr int bars = stages + stage_bytes;
     static constexpr int probs = bars + kWarps * kStages * 8;
-    __host__ __device__ static constexpr int table(int g) { return probs + kWarps * kChunk * g * 4; }
+    __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * kChunk * g * 4; }
+    __host__ __device__ static constexpr int table(int g) { return newrow(g) + 2 * kRowBytes; }
     __host__ __device__ static constexpr int total(int g, int partition_size) {
         return table(g) + (partition_size / kChunk + 1) * 4;
     }
@@ -256,7 +261,8 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
 }
 
 template <int G, int LPT>
-__global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partition_kernel(const DecodeParams P) {
+__global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
+    decode_partition_kernel(const DecodeParams P) {
     constexpr int TG = 32 / LPT;            // token groups per warp (q.K stage)
     constexpr int TPL = kChunk / TG;        // tokens per lane per chunk (q.K stage)
     constexpr int NP = kD / LPT / 8;        // 16-byte pieces of a row per lane
@@ -385,6 +391,27 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
     const int my_head = base / TPL;
     auto held_tok = [base, r](int k) { return r + TG * ((base + k) % TPL); };
 
+    // ---- fused append: the CTA holding the request's last position writes the new token's K/V
+    // row for its kv head into the cache (lanes 0-15: K, 16-31: V of warp own_warp) and patches the
+    // row in its shared-memory tile once the chunk has landed, so the attention sees the new token
+    // whatever the order of the global write and the bulk copy.
+    const int new_pos = ctx - 1;
+    const bool appends = P.k_new != nullptr && part == n_parts - 1;
+    const int own_chunk = appends ? (new_pos - start) / kChunk : -1;
+    const int own_warp = own_chunk % kWarps;
+    unsigned char *s_newrow = smem + SmemLayout::newrow(G);  // [K row | V row] of the new token
+    if (appends && warp == own_warp) {
+        const int64_t src = (static_cast<int64_t>(b) * P.num_kv_heads + kvh) * kD + (lane & 15) * 8;
+        const uint4 new_row = __ldg(reinterpret_cast<const uint4 *>((lane < 16 ? P.k_new : P.v_new) + src));
+        *reinterpret_cast<uint4 *>(s_newrow + lane * 16) = new_row;
+        const int32_t id = __ldg(P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq + new_pos / bs);
+        if (id >= 0 && id < P.num_blocks) {
+            const int64_t dst = ((static_cast<int64_t>(id) * P.num_kv_heads + kvh) * bs + new_pos % bs) * kD +
+                                (lane & 15) * 8;
+            *reinterpret_cast<uint4 *>((lane < 16 ? P.k_cache_w : P.v_cache_w) + dst) = new_row;
+        }
+    }
+
     __syncthreads();  // table + barrier init visible to every warp
 
     const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
@@ -441,6 +468,14 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) decode_partitio
         const int valid = min(kChunk, n_tok - cidx * kChunk);
         const uint32_t k_tile = stage0 + st * 2 * kTileBytes;
         const uint32_t v_tile = k_tile + kTileBytes;
+        if (cidx == own_chunk) {  // the appended token's row: overwrite what the copy brought
+            const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
+            const uint32_t row = ((new_pos - start) % kChunk) * kRowBytes + (lane & 15) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"((lane < 16 ? k_tile : v_tile) + row),
+                         "r"(nr.x), "r"(nr.y), "r"(nr.z), "r"(nr.w)
+                         : "memory");
+            __syncwarp();
+        }
 
         // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
         float v[N];
@@ -852,16 +887,20 @@ extern "C" PKV_API int pkv_merge(void *out, const float *o_part, const float *m_
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                            const int32_t *block_tables, const int32_t *context_lens,
-                                            int num_seqs, int max_blocks_per_seq, int num_q_heads,
-                                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                                            float scale, void *workspace, size_t workspace_bytes,
-                                            pkv_stream_t stream) {
+namespace {
+
+// pkv_decode_attention, optionally appending the new token first (k_new/v_new non-null).
+int decode_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                          int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int64_t num_blocks, float scale, const void *k_new, const void *v_new, void *workspace,
+                          size_t workspace_bytes, pkv_stream_t stream) {
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
     if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+    if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int part = PKV_DEFAULT_PARTITION;
@@ -882,6 +921,10 @@ extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void
     p.partition_size = part;
     p.max_partitions = max_parts;
     p.direct_single = 1;
+    p.k_new = static_cast<const __half *>(k_new);
+    p.v_new = static_cast<const __half *>(v_new);
+    p.k_cache_w = static_cast<__half *>(const_cast<void *>(k_cache));
+    p.v_cache_w = static_cast<__half *>(const_cast<void *>(v_cache));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
 
@@ -894,6 +937,44 @@ extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void
     p.l_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)) + align256(rows * sizeof(float)));
     p.counters = reinterpret_cast<int *>(ws + counters_offset(rows));
     return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
+}
+
+}  // namespace
+
+extern "C" PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *block_tables, const int32_t *context_lens,
+                                            int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                            float scale, void *workspace, size_t workspace_bytes,
+                                            pkv_stream_t stream) {
+    return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, nullptr, nullptr,
+                                 workspace, workspace_bytes, stream);
+}
+
+extern "C" PKV_API size_t pkv_decode_step_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                                         int max_context, int prefix_len) {
+    if (prefix_len > 0)
+        return pkv_shared_prefix_workspace_size(num_seqs, num_q_heads, head_dim, max_context, prefix_len);
+    return pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context, PKV_DEFAULT_PARTITION);
+}
+
+extern "C" PKV_API int pkv_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
+                                       void *k_cache, void *v_cache, const int32_t *block_tables,
+                                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                       int64_t num_blocks, float scale, int prefix_len, void *workspace,
+                                       size_t workspace_bytes, pkv_stream_t stream) {
+    if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+    if (prefix_len > 0)
+        return pkv_internal::shared_prefix_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                                  max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                                                  num_blocks, scale, prefix_len, k_new, v_new, workspace,
+                                                  workspace_bytes, stream);
+    if (prefix_len < 0) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
+                                 workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free variant
@@ -983,6 +1064,10 @@ int launch_split_pass(const SplitPass &a, void *stream) {
     p.counters = a.counters;
     p.token_offset = a.token_offset;
     p.slot_offset = a.slot_offset;
+    p.k_new = static_cast<const __half *>(a.k_new);
+    p.v_new = static_cast<const __half *>(a.v_new);
+    p.k_cache_w = static_cast<__half *>(const_cast<void *>(a.k_cache));
+    p.v_cache_w = static_cast<__half *>(const_cast<void *>(a.v_cache));
     return dispatch_partition(p, a.num_seqs, a.num_q_heads / a.num_kv_heads, reinterpret_cast<cudaStream_t>(stream),
                               a.grid_partitions);
 }

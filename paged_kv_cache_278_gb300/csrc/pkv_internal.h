@@ -35,7 +35,15 @@ struct SplitPass {
     int partition_size, max_partitions, token_offset, slot_offset, grid_partitions;
     float *o_part, *m_part, *l_part;
     int *counters;
+    const void *k_new, *v_new;  // non-null: fused append of the new token (caches are written)
 };
 int launch_split_pass(const SplitPass &a, void *stream);
+
+// Shared-prefix decode (prefix kernel + suffix pass), optionally appending the new tokens.
+int shared_prefix_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                         int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, float scale, int prefix_len, const void *k_new, const void *v_new,
+                         void *workspace, size_t workspace_bytes, void *stream);
 
 }  // namespace pkv_internal

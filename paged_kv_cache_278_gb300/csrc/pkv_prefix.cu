@@ -100,10 +100,32 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     const int tok0 = chunk * kChunkTok;
     const int ntok = min(kChunkTok, P.prefix_len - tok0);
 
-    // K/V chunk (zero rows past the prefix) and the CTA's query rows, 16 bytes per thread access
-    for (int i = threadIdx.x; i < kChunkTok * (kD / 8); i += kThreads) {
+    // K/V chunk (zero rows past the prefix) and the CTA's query rows, 16 bytes per access.  All
+    // loads of a thread are issued before any store so they overlap (about two L2/HBM round
+    // trips in all: block ids, then rows).
+    constexpr int KV_PER_THREAD = kChunkTok * (kD / 8) / kThreads;  // 4
+    constexpr int Q_PER_THREAD = kRows * (kD / 8) / kThreads;        // 8
+    static_assert(KV_PER_THREAD * kThreads == kChunkTok * (kD / 8) && Q_PER_THREAD * kThreads == kRows * (kD / 8),
+                  "load split");
+    uint4 qv[Q_PER_THREAD];
+#pragma unroll
+    for (int k = 0; k < Q_PER_THREAD; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        const int r = i / (kD / 8), piece = i % (kD / 8);
+        const int gr = row0 + r;
+        qv[k] = make_uint4(0, 0, 0, 0);
+        if (gr < rows) {
+            const int b = gr / G, hh = gr % G;
+            qv[k] = __ldg(reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD) +
+                          piece);
+        }
+    }
+    int64_t src[KV_PER_THREAD];
+#pragma unroll
+    for (int k = 0; k < KV_PER_THREAD; ++k) {
+        const int i = threadIdx.x + k * kThreads;
         const int t = i / (kD / 8), piece = i % (kD / 8);
-        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+        src[k] = -1;
         if (t < ntok) {
             const int tok = tok0 + t;
             int32_t id = __ldg(P.block_tables + tok / bs);
@@ -111,22 +133,26 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
                 pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
                 id = 0;
             }
-            const int64_t src = ((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs) * kD + piece * 8;
-            kv = __ldg(reinterpret_cast<const uint4 *>(P.k_cache + src));
-            vv = __ldg(reinterpret_cast<const uint4 *>(P.v_cache + src));
+            src[k] = ((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs) * kD + piece * 8;
         }
-        *reinterpret_cast<uint4 *>(sK + t * kPad + piece * 8) = kv;
-        *reinterpret_cast<uint4 *>(sV + t * kPad + piece * 8) = vv;
     }
-    for (int i = threadIdx.x; i < kRows * (kD / 8); i += kThreads) {
-        const int r = i / (kD / 8), piece = i % (kD / 8);
-        const int gr = row0 + r;
-        uint4 qv = make_uint4(0, 0, 0, 0);
-        if (gr < rows) {
-            const int b = gr / G, hh = gr % G;
-            qv = __ldg(reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD) + piece);
-        }
-        *reinterpret_cast<uint4 *>(sQ + r * kPad + piece * 8) = qv;
+    uint4 kv[KV_PER_THREAD], vv[KV_PER_THREAD];
+#pragma unroll
+    for (int k = 0; k < KV_PER_THREAD; ++k) {
+        kv[k] = src[k] >= 0 ? __ldg(reinterpret_cast<const uint4 *>(P.k_cache + src[k])) : make_uint4(0, 0, 0, 0);
+        vv[k] = src[k] >= 0 ? __ldg(reinterpret_cast<const uint4 *>(P.v_cache + src[k])) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < Q_PER_THREAD; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        *reinterpret_cast<uint4 *>(sQ + (i / (kD / 8)) * kPad + (i % (kD / 8)) * 8) = qv[k];
+    }
+#pragma unroll
+    for (int k = 0; k < KV_PER_THREAD; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        const int t = i / (kD / 8), piece = i % (kD / 8);
+        *reinterpret_cast<uint4 *>(sK + t * kPad + piece * 8) = kv[k];
+        *reinterpret_cast<uint4 *>(sV + t * kPad + piece * 8) = vv[k];
     }
     __syncthreads();
     if (row0 + warp * 16 >= rows) return;  // no barrier follows
@@ -231,16 +257,21 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     }
 }
 
+constexpr int kMinSuffixPartition = 64;
+
 struct SharedLayout {
-    int n_pre, n_suf, max_parts;
+    int n_pre, n_suf, max_parts, suffix_partition;
     size_t rows, o_bytes, m_bytes, counter_off, total;
 };
 
-SharedLayout shared_layout(int num_seqs, int num_q_heads, int max_context, int prefix_len) {
+// Partial-slot layout for a suffix partition size; the workspace size function uses the
+// smallest partition, which bounds every layout a call can pick.
+SharedLayout shared_layout(int num_seqs, int num_q_heads, int max_context, int prefix_len, int suffix_partition) {
     SharedLayout L{};
+    L.suffix_partition = suffix_partition;
     L.n_pre = (prefix_len + kChunkTok - 1) / kChunkTok;
     const int rest = max_context - prefix_len;
-    L.n_suf = rest > 0 ? (rest + PKV_DEFAULT_PARTITION - 1) / PKV_DEFAULT_PARTITION : 0;
+    L.n_suf = rest > 0 ? (rest + suffix_partition - 1) / suffix_partition : 0;
     L.max_parts = L.n_pre + L.n_suf;
     L.rows = static_cast<size_t>(num_seqs) * num_q_heads * L.max_parts;
     L.o_bytes = pkv_internal::align256(L.rows * kD * sizeof(float));
@@ -255,7 +286,7 @@ SharedLayout shared_layout(int num_seqs, int num_q_heads, int max_context, int p
 extern "C" PKV_API size_t pkv_shared_prefix_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                                            int max_context, int prefix_len) {
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim != kD || prefix_len <= 0 || max_context < prefix_len) return 0;
-    return shared_layout(num_seqs, num_q_heads, max_context, prefix_len).total;
+    return shared_layout(num_seqs, num_q_heads, max_context, prefix_len, kMinSuffixPartition).total;
 }
 
 extern "C" PKV_API int pkv_decode_attention_shared_prefix(
@@ -263,16 +294,48 @@ extern "C" PKV_API int pkv_decode_attention_shared_prefix(
     const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
     int head_dim, int block_size, int64_t num_blocks, float scale, int prefix_len, void *workspace,
     size_t workspace_bytes, pkv_stream_t stream) {
-    int st = pkv_internal::check_decode_args(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                                             max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
-                                             num_blocks);
+    return pkv_internal::shared_prefix_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                              max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                                              num_blocks, scale, prefix_len, nullptr, nullptr, workspace,
+                                              workspace_bytes, stream);
+}
+
+namespace pkv_internal {
+
+int shared_prefix_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                         int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, float scale, int prefix_len, const void *k_new, const void *v_new,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                               num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
     if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+    if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     if (prefix_len <= 0 || prefix_len % block_size != 0 || prefix_len > cap) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
-    const SharedLayout L = shared_layout(num_seqs, num_q_heads, static_cast<int>(cap), prefix_len);
-    if (!workspace || workspace_bytes < L.total || !pkv_internal::aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+    const SharedLayout bound = shared_layout(num_seqs, num_q_heads, static_cast<int>(cap), prefix_len,
+                                             kMinSuffixPartition);
+    if (!workspace || workspace_bytes < bound.total || !pkv_internal::aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+    // Suffix partition: halve from 512 tokens (down to 64) until the suffix grid offers about four
+    // CTAs per resident CTA slot (3 per SM), so short private suffixes still fill the GPU.
+    int dev_sm = 0;
+    int suffix_part = PKV_DEFAULT_PARTITION;
+    {
+        int d = 0;
+        if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&dev_sm, cudaDevAttrMultiProcessorCount, d) !=
+                                                      cudaSuccess)
+            return PKV_ERR_CUDA;
+        const int64_t want = 4LL * 3 * dev_sm;
+        const int64_t rest = cap - prefix_len;
+        while (suffix_part > kMinSuffixPartition &&
+               static_cast<int64_t>(num_seqs) * num_kv_heads * ((rest + suffix_part - 1) / suffix_part) < want)
+            suffix_part /= 2;
+    }
+    const SharedLayout L = shared_layout(num_seqs, num_q_heads, static_cast<int>(cap), prefix_len, suffix_part);
     const int rows = num_seqs * (num_q_heads / num_kv_heads);
     if (num_seqs > 65535 || (rows + kRows - 1) / kRows > 65535) return PKV_ERR_UNSUPPORTED;
 
@@ -304,7 +367,7 @@ extern "C" PKV_API int pkv_decode_attention_shared_prefix(
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(L.n_pre, num_kv_heads, (rows + kRows - 1) / kRows);
     prefix_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -323,7 +386,7 @@ extern "C" PKV_API int pkv_decode_attention_shared_prefix(
     a.block_size = block_size;
     a.num_blocks = num_blocks;
     a.scale = scale;
-    a.partition_size = PKV_DEFAULT_PARTITION;
+    a.partition_size = L.suffix_partition;
     a.max_partitions = L.max_parts;
     a.token_offset = prefix_len;
     a.slot_offset = L.n_pre;
@@ -332,8 +395,12 @@ extern "C" PKV_API int pkv_decode_attention_shared_prefix(
     a.m_part = p.m_part;
     a.l_part = p.l_part;
     a.counters = reinterpret_cast<int *>(ws + L.counter_off);
+    a.k_new = k_new;
+    a.v_new = v_new;
     return pkv_internal::launch_split_pass(a, stream);
 }
+
+}  // namespace pkv_internal
 
 namespace pkv_internal {
 
