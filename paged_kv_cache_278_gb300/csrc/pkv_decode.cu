@@ -41,6 +41,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "pkv.h"
 #include "pkv_device.cuh"
@@ -67,6 +68,10 @@ constexpr int kTileBytes = kChunk * kRowBytes;  // 4 KiB
 // 1: q.K and P.V use packed two-lane FMAs (fma.rn.f32x2), halving FMA issue slots.
 #ifndef PKV_DECODE_FFMA2
 #define PKV_DECODE_FFMA2 1
+#endif
+// 1: with 4 or 8 query heads per kv head, q.K and P.V run on the tensor cores (mma.m16n8k16).
+#ifndef PKV_DECODE_TC
+#define PKV_DECODE_TC 1
 #endif
 constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
@@ -107,13 +112,19 @@ struct DecodeParams {
 
 constexpr int kMergeTile = 512;  // partitions whose weights the fused merge stages at a time
 
-// Shared-memory carve-up (bytes), identical on host and device.
+// Shared-memory carve-up (bytes), identical on host and device.  TC selects the tensor-core
+// engine's padded rows (272 B) and its fp16 P buffer.
+constexpr int kPadRowBytes = kRowBytes + 16;
+template <bool TC>
 struct SmemLayout {
+    static constexpr int row = TC ? kPadRowBytes : kRowBytes;
+    static constexpr int tile = kChunk * row;
     static constexpr int stages = 0;
-    static constexpr int stage_bytes = kWarps * kStages * 2 * kTileBytes;
+    static constexpr int stage_bytes = kWarps * kStages * 2 * tile;
     static constexpr int bars = stages + stage_bytes;
     static constexpr int probs = bars + kWarps * kStages * 8;
-    __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * kChunk * g * 4; }
+    __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? 2 * 8 * kChunk * 2 : kChunk * g * 4; }
+    __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
     __host__ __device__ static constexpr int table(int g) { return newrow(g) + 2 * kRowBytes; }
     __host__ __device__ static constexpr int total(int g, int partition_size) {
         return table(g) + (partition_size / kChunk + 1) * 4;
@@ -134,7 +145,7 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
     constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
     constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
     static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
-    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout::stage_bytes,
+    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout<false>::stage_bytes,
                   "merge staging must fit the stages");
     float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][kMergeTile]
     float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
@@ -260,20 +271,373 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
     }
 }
 
+// ---------------------------------------------------------------- CUDA-core engine
+// LPT lanes share a token row for q . K (each holding 128/LPT dims of q in fp32, pre-scaled by
+// scale*log2 e); partial dots are finished with a shuffle reduce-scatter after which each lane
+// holds scores of one packed head for a few tokens; P goes through a per-warp shared buffer to
+// P . V, where each lane owns 4 output dims of every packed head.  Used for G <= 2, where the
+// packed-head tile would leave most of a tensor-core MMA empty.
 template <int G, int LPT>
-__global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
-    decode_partition_kernel(const DecodeParams P) {
-    constexpr int TG = 32 / LPT;            // token groups per warp (q.K stage)
-    constexpr int TPL = kChunk / TG;        // tokens per lane per chunk (q.K stage)
-    constexpr int NP = kD / LPT / 8;        // 16-byte pieces of a row per lane
-    constexpr int N = TPL * G;              // partial dot products per lane
-    constexpr int LOG_LPT = ilog2(LPT);
-    constexpr int LOG_N = ilog2(N);
-    constexpr int HALVING = LOG_LPT < LOG_N ? LOG_LPT : LOG_N;
-    constexpr int HELD = N >> HALVING;      // finished scores per lane
-    constexpr int DUP_BITS = LOG_LPT - HALVING;
+struct FmaEngine {
+    static constexpr int TG = 32 / LPT;            // token groups per warp (q.K stage)
+    static constexpr int TPL = kChunk / TG;        // tokens per lane per chunk (q.K stage)
+    static constexpr int NP = kD / LPT / 8;        // 16-byte pieces of a row per lane
+    static constexpr int N = TPL * G;              // partial dot products per lane
+    static constexpr int LOG_LPT = ilog2(LPT);
+    static constexpr int LOG_N = ilog2(N);
+    static constexpr int HALVING = LOG_LPT < LOG_N ? LOG_LPT : LOG_N;
+    static constexpr int HELD = N >> HALVING;      // finished scores per lane
+    static constexpr int DUP_BITS = LOG_LPT - HALVING;
+    static constexpr int kRow = kRowBytes;         // shared-memory row stride
     static_assert((1 << LOG_LPT) == LPT && (1 << LOG_N) == N, "powers of two");
     static_assert(NP >= 1 && NP * 8 * LPT == kD, "lane split of a row");
+    // A lane's finished scores are (packed head my_head, chunk token held_tok(k)); HELD divides TPL
+    // and base is a multiple of HELD, so all of a lane's scores share one head.
+    static_assert(TPL % HELD == 0, "a lane's finished scores must share one head");
+
+    float qf[G][NP * 8];
+    float m_head[G], l_lane[G], acc[G][4];  // reference max (warp-uniform), lane share of l, P.V sums
+    float m_mine, top_mine;                 // m_head[my_head]; true running max of this lane's scores
+    int c, r, base, my_head;
+    bool owner;
+
+    __device__ __forceinline__ int held_tok(int k) const { return r + TG * ((base + k) % TPL); }
+
+    __device__ __forceinline__ void init(const DecodeParams &P, int b, int kvh, int lane) {
+        c = lane & (LPT - 1);
+        r = lane / LPT;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            const uint4 *qrow =
+                reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(b) * P.num_q_heads + kvh * G + hh) * kD);
+#pragma unroll
+            for (int np = 0; np < NP; ++np) {
+                const uint4 raw = __ldg(qrow + c + LPT * np);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = pkv::half2_bits_to_float2(w[e]);
+                    qf[hh][np * 8 + 2 * e] = f.x * P.q_scale;
+                    qf[hh][np * 8 + 2 * e + 1] = f.y * P.q_scale;
+                }
+            }
+        }
+        base = 0;
+#pragma unroll
+        for (int s = 0; s < HALVING; ++s)
+            if (lane & (LPT >> (s + 1))) base += N >> (s + 1);
+        owner = (c & ((1 << DUP_BITS) - 1)) == 0;
+        my_head = base / TPL;
+        m_mine = -INFINITY;
+        top_mine = -INFINITY;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            m_head[hh] = -INFINITY;
+            l_lane[hh] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[hh][e] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, int valid, int lane,
+                                          unsigned char *scratch) {
+        float *s_prob = reinterpret_cast<float *>(scratch);
+        // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
+        float v[N];
+#pragma unroll
+        for (int it = 0; it < TPL; ++it) {
+            const int t = r + TG * it;
+            float kf[NP * 8];
+#pragma unroll
+            for (int np = 0; np < NP; ++np) {
+                const uint4 raw = pkv::lds128(k_tile + t * kRow + (c + LPT * np) * 16);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = pkv::half2_bits_to_float2(w[e]);
+                    kf[np * 8 + 2 * e] = f.x;
+                    kf[np * 8 + 2 * e + 1] = f.y;
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+#if PKV_DECODE_FFMA2
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < NP * 8; e += 2) pkv::fma2(s0, s1, qf[hh][e], qf[hh][e + 1], kf[e], kf[e + 1]);
+                v[hh * TPL + it] = s0 + s1;
+#else
+                float sacc = 0.f;
+#pragma unroll
+                for (int e = 0; e < NP * 8; ++e) sacc = fmaf(qf[hh][e], kf[e], sacc);
+                v[hh * TPL + it] = sacc;
+#endif
+            }
+        }
+        // ---- reduce-scatter across the LPT lanes of a token group
+#pragma unroll
+        for (int s = 0; s < HALVING; ++s) {
+            const int mask = LPT >> (s + 1);
+            const int half = N >> (s + 1);
+            const bool upper = (lane & mask) != 0;
+#pragma unroll
+            for (int k = 0; k < half; ++k) {
+                const float send = upper ? v[k] : v[k + half];
+                const float keep = upper ? v[k + half] : v[k];
+                v[k] = keep + __shfl_xor_sync(pkv::kFullMask, send, mask);
+            }
+        }
+#pragma unroll
+        for (int s = HALVING; s < LOG_LPT; ++s) v[0] += __shfl_xor_sync(pkv::kFullMask, v[0], LPT >> (s + 1));
+
+        // ---- online softmax (log2 domain) with lazy rescale
+        bool need = false;
+#pragma unroll
+        for (int k = 0; k < HELD; ++k) {
+            if (held_tok(k) >= valid) v[k] = -INFINITY;
+            need |= v[k] > m_mine + kRescaleThreshold;
+            top_mine = fmaxf(top_mine, v[k]);
+        }
+        if (__any_sync(pkv::kFullMask, need)) {
+            float mx[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) mx[hh] = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < HELD; ++k)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) mx[hh] = fmaxf(mx[hh], my_head == hh ? v[k] : -INFINITY);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+                for (int sh = 0; sh < 5; ++sh) mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(pkv::kFullMask, mx[hh], 16 >> sh));
+            }
+            m_mine = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float mn = fmaxf(m_head[hh], mx[hh]);
+                const float alpha = exp2f(m_head[hh] - mn);
+                m_head[hh] = mn;
+                l_lane[hh] *= alpha;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[hh][e] *= alpha;
+                m_mine += (my_head == hh) ? mn : 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < HELD; ++k) {
+            const float p = exp2f(v[k] - m_mine);  // 0 for masked tokens
+            if (owner) {
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) l_lane[hh] += (my_head == hh) ? p : 0.f;
+                if (held_tok(k) < valid) s_prob[held_tok(k) * G + my_head] = p;
+            }
+        }
+        __syncwarp();
+
+        // ---- P . V: this lane owns dims [4*lane, 4*lane+4) of every packed head
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t) {
+            if (t < valid) {
+                const uint2 raw = pkv::lds64(v_tile + t * kRow + lane * 8);
+                const float2 v01 = pkv::half2_bits_to_float2(raw.x);
+                const float2 v23 = pkv::half2_bits_to_float2(raw.y);
+                float pr[G];
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) pr[hh] = s_prob[t * G + hh];
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+#if PKV_DECODE_FFMA2
+                    pkv::fma2(acc[hh][0], acc[hh][1], pr[hh], pr[hh], v01.x, v01.y);
+                    pkv::fma2(acc[hh][2], acc[hh][3], pr[hh], pr[hh], v23.x, v23.y);
+#else
+                    acc[hh][0] = fmaf(pr[hh], v01.x, acc[hh][0]);
+                    acc[hh][1] = fmaf(pr[hh], v01.y, acc[hh][1]);
+                    acc[hh][2] = fmaf(pr[hh], v23.x, acc[hh][2]);
+                    acc[hh][3] = fmaf(pr[hh], v23.y, acc[hh][3]);
+#endif
+                }
+            }
+        }
+    }
+
+    // Per-warp (m, l, acc) of every packed head, re-referenced to the true max, into shared memory.
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float l = l_lane[hh];
+            float top = my_head == hh ? top_mine : -INFINITY;
+#pragma unroll
+            for (int sh = 0; sh < 5; ++sh) {
+                l += __shfl_xor_sync(pkv::kFullMask, l, 16 >> sh);
+                top = fmaxf(top, __shfl_xor_sync(pkv::kFullMask, top, 16 >> sh));
+            }
+            float m = m_head[hh];
+            if (top > -INFINITY) {  // this warp saw tokens: m_head <= top < m_head + 2^8
+                const float f = exp2f(m - top);
+                l *= f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[hh][e] *= f;
+                m = top;
+            }
+            *reinterpret_cast<float4 *>(c_acc + (warp * G + hh) * kD + lane * 4) =
+                make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+            if (lane == 0) {
+                c_m[warp * G + hh] = m;
+                c_l[warp * G + hh] = l;
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------- tensor-core engine
+// With G >= 4 query heads per kv head both products are real MMA tiles (N = 8 head columns,
+// G of them live): per 16-token chunk
+//   S^T[16 tok x 8] = K_tile[16 x 128] . Q^T[128 x 8]        8 x mma.m16n8k16 (K from shared
+//                                                           memory by ldmatrix, Q^T as fp16
+//                                                           fragments held in registers)
+//   O^T[128 x 8]  += V_tile^T[128 x 16] . P^T[16 x 8]        8 m-tiles x 2 (P = hi + lo fp16)
+// with fp32 accumulation throughout.  K/V rows sit in shared memory at a 272-byte stride (one
+// bulk copy per row) so every ldmatrix is bank-conflict free.  Each lane owns heads
+// 2*(lane%4) and +1 of the fragments; lanes whose heads are >= G carry padding columns.
+template <int G>
+struct TcEngine {
+    static_assert(G == 4 || G == 8, "tensor-core engine packs 4 or 8 heads into the 8 MMA columns");
+    static constexpr int kRow = kPadRowBytes;
+
+    uint32_t qb[kD / 16][2];  // Q^T B-fragments of the 8 k-steps (fp16x2)
+    float o[kD / 16][4];      // O^T accumulators: (dim 16 mt + lane/4 (+8), head h0 (+1))
+    float m_ref[2], top[2], l_part[2];
+    float q_scale;
+
+    __device__ __forceinline__ void init(const DecodeParams &P, int b, int kvh, int lane) {
+        const int head = lane >> 2;
+        const __half *qrow =
+            P.q + (static_cast<int64_t>(b) * P.num_q_heads + kvh * G + (head < G ? head : 0)) * kD;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                qb[ks][j] = head < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + (lane & 3) * 2 + j * 8))
+                                     : 0u;
+#pragma unroll
+        for (int mt = 0; mt < kD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m_ref[0] = m_ref[1] = top[0] = top[1] = -INFINITY;
+        l_part[0] = l_part[1] = 0.f;
+        q_scale = P.q_scale;
+    }
+
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, int valid, int lane,
+                                          unsigned char *scratch) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t a[4];
+            pkv::ldsm_x4(a, k_tile + (lane & 15) * kRow + ks * 32 + (lane >> 4) * 16);
+            pkv::mma16816(s, a, qb[ks][0], qb[ks][1]);
+        }
+        const int g = lane >> 2;
+        s[0] = g < valid ? s[0] * q_scale : -INFINITY;
+        s[1] = g < valid ? s[1] * q_scale : -INFINITY;
+        s[2] = g + 8 < valid ? s[2] * q_scale : -INFINITY;
+        s[3] = g + 8 < valid ? s[3] * q_scale : -INFINITY;
+        float cm0 = fmaxf(s[0], s[2]), cm1 = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int sh = 4; sh <= 16; sh <<= 1) {
+            cm0 = fmaxf(cm0, __shfl_xor_sync(pkv::kFullMask, cm0, sh));
+            cm1 = fmaxf(cm1, __shfl_xor_sync(pkv::kFullMask, cm1, sh));
+        }
+        top[0] = fmaxf(top[0], cm0);
+        top[1] = fmaxf(top[1], cm1);
+        if (__any_sync(pkv::kFullMask, cm0 > m_ref[0] + kRescaleThreshold || cm1 > m_ref[1] + kRescaleThreshold)) {
+            const float n0 = fmaxf(m_ref[0], cm0), n1 = fmaxf(m_ref[1], cm1);
+            const float a0 = exp2f(m_ref[0] - n0), a1 = exp2f(m_ref[1] - n1);
+            m_ref[0] = n0;
+            m_ref[1] = n1;
+            l_part[0] *= a0;
+            l_part[1] *= a1;
+#pragma unroll
+            for (int mt = 0; mt < kD / 16; ++mt) {
+                o[mt][0] *= a0;
+                o[mt][1] *= a1;
+                o[mt][2] *= a0;
+                o[mt][3] *= a1;
+            }
+        }
+        const float p[4] = {exp2f(s[0] - m_ref[0]), exp2f(s[1] - m_ref[1]), exp2f(s[2] - m_ref[0]),
+                            exp2f(s[3] - m_ref[1])};
+        l_part[0] += p[0] + p[2];
+        l_part[1] += p[1] + p[3];
+        // P^T through shared memory as fp16 hi / lo: [2][8 heads][16 tokens]
+        __half *ph = reinterpret_cast<__half *>(scratch);
+        __half *pl = ph + 8 * kChunk;
+        const int h0 = (lane & 3) * 2;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = (h0 + (e & 1)) * kChunk + g + (e >> 1) * 8;
+            const __half hi = __float2half_rn(p[e]);
+            ph[idx] = hi;
+            pl[idx] = __float2half_rn(p[e] - __half2float(hi));
+        }
+        __syncwarp();
+        const int n = lane >> 2, k0 = (lane & 3) * 2;
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + n * kChunk + k0);
+        const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + n * kChunk + k0 + 8);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(pl + n * kChunk + k0);
+        const uint32_t bl1 = *reinterpret_cast<const uint32_t *>(pl + n * kChunk + k0 + 8);
+#pragma unroll
+        for (int mt = 0; mt < kD / 16; ++mt) {
+            uint32_t a[4];
+            pkv::ldsm_x4_trans(a, v_tile + ((lane >> 4) * 8 + (lane & 7)) * kRow + (mt * 16 + ((lane >> 3) & 1) * 8) * 2);
+            pkv::mma16816(o[mt], a, bh0, bh1);
+            pkv::mma16816(o[mt], a, bl0, bl1);
+        }
+    }
+
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+        float l[2] = {l_part[0], l_part[1]};
+#pragma unroll
+        for (int sh = 4; sh <= 16; sh <<= 1) {
+            l[0] += __shfl_xor_sync(pkv::kFullMask, l[0], sh);
+            l[1] += __shfl_xor_sync(pkv::kFullMask, l[1], sh);
+        }
+        float f[2] = {1.f, 1.f}, m[2] = {m_ref[0], m_ref[1]};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (top[j] > -INFINITY) {  // re-reference to the true max: m_ref <= top < m_ref + 2^8
+                f[j] = exp2f(m_ref[j] - top[j]);
+                l[j] *= f[j];
+                m[j] = top[j];
+            }
+        }
+        const int g = lane >> 2, h0 = (lane & 3) * 2;
+#pragma unroll
+        for (int mt = 0; mt < kD / 16; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = h0 + (e & 1);
+                if (h < G) c_acc[(warp * G + h) * kD + mt * 16 + g + (e >> 1) * 8] = o[mt][e] * f[e & 1];
+            }
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (h0 + j < G) {
+                    c_m[warp * G + h0 + j] = m[j];
+                    c_l[warp * G + h0 + j] = l[j];
+                }
+        }
+    }
+};
+
+template <int G, int LPT, bool TC>
+using EngineFor = typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type;
+
+template <int G, int LPT, bool TC>
+__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN_CTAS)
+    decode_partition_kernel(const DecodeParams P) {
+    using L = SmemLayout<TC>;
+    using Engine = EngineFor<G, LPT, TC>;
+    constexpr int kRow = L::row;
+    constexpr int kTile = L::tile;
 
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -330,10 +694,10 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
     const int lb0 = start / bs;
     const int n_bt = (start + n_tok - 1) / bs - lb0 + 1;
 
-    int32_t *s_table = reinterpret_cast<int32_t *>(smem + SmemLayout::table(G));
-    float *s_prob = reinterpret_cast<float *>(smem + SmemLayout::probs) + warp * kChunk * G;
-    const uint32_t bar0 = pkv::smem_addr(smem + SmemLayout::bars) + warp * kStages * 8;
-    const uint32_t stage0 = pkv::smem_addr(smem + SmemLayout::stages) + warp * kStages * 2 * kTileBytes;
+    int32_t *s_table = reinterpret_cast<int32_t *>(smem + L::table(G));
+    unsigned char *scratch = smem + L::probs + warp * L::probs_per_warp(G);
+    const uint32_t bar0 = pkv::smem_addr(smem + L::bars) + warp * kStages * 8;
+    const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * 2 * kTile;
 
     if (lane == 0) {
 #pragma unroll
@@ -353,43 +717,14 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
         if (tok_begin > 0 && part == 0 && kvh == 0 && b > 0) {  // every table must start with the shared prefix
             const int32_t *row_b = P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq;
             for (int i = threadIdx.x; i < tok_begin / bs; i += kThreads)
-                if (__ldg(row_b + i) != __ldg(P.block_tables + i)) pkv::record_error(&g_decode_error, PKV_DEV_PREFIX_MISMATCH);
+                if (__ldg(row_b + i) != __ldg(P.block_tables + i))
+                    pkv::record_error(&g_decode_error, PKV_DEV_PREFIX_MISMATCH);
         }
     }
 
-    // q of the G packed heads, this lane's dims, fp32, pre-scaled.
-    const int c = lane & (LPT - 1);   // dim slice within a token row
-    const int r = lane / LPT;         // token group
-    float qf[G][NP * 8];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        const uint4 *qrow = reinterpret_cast<const uint4 *>(
-            P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD);
-#pragma unroll
-        for (int np = 0; np < NP; ++np) {
-            const uint4 raw = __ldg(qrow + c + LPT * np);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = pkv::half2_bits_to_float2(w[e]);
-                qf[hh][np * 8 + 2 * e] = f.x * P.q_scale;
-                qf[hh][np * 8 + 2 * e + 1] = f.y * P.q_scale;
-            }
-        }
-    }
-
-    // Which finished scores this lane ends up holding after the reduce-scatter.
-    int base = 0;
-#pragma unroll
-    for (int s = 0; s < HALVING; ++s)
-        if (lane & (LPT >> (s + 1))) base += N >> (s + 1);
-    const bool owner = (c & ((1 << DUP_BITS) - 1)) == 0;
-    // Finished score k of this lane is (packed head my_head, chunk token held_tok(k)); HELD divides
-    // TPL and base is a multiple of HELD, so all of a lane's scores share one head.
-    static_assert(TPL % HELD == 0, "a lane's finished scores must share one head");
-    static_assert(kWarps * G * (kD + 2) * 4 <= SmemLayout::stage_bytes, "combine area must fit the stages");
-    const int my_head = base / TPL;
-    auto held_tok = [base, r](int k) { return r + TG * ((base + k) % TPL); };
+    Engine eng;
+    eng.init(P, b, kvh, lane);
+    static_assert(kWarps * G * (kD + 2) * 4 <= L::stage_bytes, "combine area must fit the stages");
 
     // ---- fused append: the CTA holding the request's last position writes the new token's K/V
     // row for its kv head into the cache (lanes 0-15: K, 16-31: V of warp own_warp) and patches the
@@ -399,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
     const bool appends = P.k_new != nullptr && part == n_parts - 1;
     const int own_chunk = appends ? (new_pos - start) / kChunk : -1;
     const int own_warp = own_chunk % kWarps;
-    unsigned char *s_newrow = smem + SmemLayout::newrow(G);  // [K row | V row] of the new token
+    unsigned char *s_newrow = smem + L::newrow(G);  // [K row | V row] of the new token
     if (appends && warp == own_warp) {
         const int64_t src = (static_cast<int64_t>(b) * P.num_kv_heads + kvh) * kD + (lane & 15) * 8;
         const uint4 new_row = __ldg(reinterpret_cast<const uint4 *>((lane < 16 ? P.k_new : P.v_new) + src));
@@ -418,6 +753,8 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
     const int64_t head_stride = static_cast<int64_t>(bs) * kRowBytes;
     const int64_t block_stride = head_stride * P.num_kv_heads;
 
+    // Stage chunk i of this warp (called by all 32 lanes): the CUDA-core engine takes the K and V
+    // rows as two contiguous bulk copies; the tensor-core engine copies row by row into padded rows.
     auto issue = [=](int i) {
         const int cidx = warp + i * kWarps;
         const int tok0 = start + cidx * kChunk;
@@ -429,28 +766,26 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
         const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
         const int st = i % kStages;
         const uint32_t bar = bar0 + 8 * st;
-        const uint32_t dst = stage0 + st * 2 * kTileBytes;
-        pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
-        pkv::bulk_copy_g2s(dst, P.k_cache + byte_off, bytes, bar);
-        pkv::bulk_copy_g2s(dst + kTileBytes, P.v_cache + byte_off, bytes, bar);
+        const uint32_t dst = stage0 + st * 2 * kTile;
+        if constexpr (TC) {
+            if (lane == 0) pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
+            __syncwarp();
+            const int row = lane & 15;
+            if (row < valid)
+                pkv::bulk_copy_g2s(dst + (lane < 16 ? 0 : kTile) + row * kRow,
+                                   (lane < 16 ? P.k_cache : P.v_cache) + byte_off + row * kRowBytes, kRowBytes, bar);
+        } else {
+            if (lane == 0) {
+                pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
+                pkv::bulk_copy_g2s(dst, P.k_cache + byte_off, bytes, bar);
+                pkv::bulk_copy_g2s(dst + kTile, P.v_cache + byte_off, bytes, bar);
+            }
+        }
     };
 
-    if (lane == 0) {
+    {
         const int pre = my_chunks < kStages ? my_chunks : kStages;
         for (int i = 0; i < pre; ++i) issue(i);
-    }
-
-    // m_head: running max per packed head (warp-uniform); m_mine = m_head[my_head];
-    // l_lane: this lane's share of the softmax denominators; acc: P.V accumulators.
-    float m_head[G], l_lane[G], acc[G][4];
-    float m_mine = -INFINITY;
-    float top_mine = -INFINITY;  // true running max of this lane's scores (m_head may lag it by < 2^8)
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        m_head[hh] = -INFINITY;
-        l_lane[hh] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[hh][e] = 0.f;
     }
 
     int consumed = 0;
@@ -466,137 +801,27 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
         consumed = i + 1;
         const int cidx = warp + i * kWarps;
         const int valid = min(kChunk, n_tok - cidx * kChunk);
-        const uint32_t k_tile = stage0 + st * 2 * kTileBytes;
-        const uint32_t v_tile = k_tile + kTileBytes;
+        const uint32_t k_tile = stage0 + st * 2 * kTile;
+        const uint32_t v_tile = k_tile + kTile;
+        bool touched = false;
+        if (TC && valid < kChunk) {  // the MMA reads all 16 V rows: make the unused ones finite (zero)
+            for (int x = lane; x < (kChunk - valid) * (kRow / 16); x += 32)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + valid * kRow + x * 16), "r"(0)
+                             : "memory");
+            touched = true;
+        }
         if (cidx == own_chunk) {  // the appended token's row: overwrite what the copy brought
             const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
-            const uint32_t row = ((new_pos - start) % kChunk) * kRowBytes + (lane & 15) * 16;
+            const uint32_t row = ((new_pos - start) % kChunk) * kRow + (lane & 15) * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"((lane < 16 ? k_tile : v_tile) + row),
                          "r"(nr.x), "r"(nr.y), "r"(nr.z), "r"(nr.w)
                          : "memory");
-            __syncwarp();
+            touched = true;
         }
-
-        // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
-        float v[N];
-#pragma unroll
-        for (int it = 0; it < TPL; ++it) {
-            const int t = r + TG * it;
-            float kf[NP * 8];
-#pragma unroll
-            for (int np = 0; np < NP; ++np) {
-                const uint4 raw = pkv::lds128(k_tile + t * kRowBytes + (c + LPT * np) * 16);
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = pkv::half2_bits_to_float2(w[e]);
-                    kf[np * 8 + 2 * e] = f.x;
-                    kf[np * 8 + 2 * e + 1] = f.y;
-                }
-            }
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-#if PKV_DECODE_FFMA2
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int e = 0; e < NP * 8; e += 2) pkv::fma2(s0, s1, qf[hh][e], qf[hh][e + 1], kf[e], kf[e + 1]);
-                v[hh * TPL + it] = s0 + s1;
-#else
-                float sacc = 0.f;
-#pragma unroll
-                for (int e = 0; e < NP * 8; ++e) sacc = fmaf(qf[hh][e], kf[e], sacc);
-                v[hh * TPL + it] = sacc;
-#endif
-            }
-        }
-        // ---- reduce-scatter across the LPT lanes of a token group
-#pragma unroll
-        for (int s = 0; s < HALVING; ++s) {
-            const int mask = LPT >> (s + 1);
-            const int half = N >> (s + 1);
-            const bool upper = (lane & mask) != 0;
-#pragma unroll
-            for (int k = 0; k < half; ++k) {
-                const float send = upper ? v[k] : v[k + half];
-                const float keep = upper ? v[k + half] : v[k];
-                v[k] = keep + __shfl_xor_sync(pkv::kFullMask, send, mask);
-            }
-        }
-#pragma unroll
-        for (int s = HALVING; s < LOG_LPT; ++s) v[0] += __shfl_xor_sync(pkv::kFullMask, v[0], LPT >> (s + 1));
-
-        // ---- online softmax (log2 domain) with lazy rescale
-        bool need = false;
-#pragma unroll
-        for (int k = 0; k < HELD; ++k) {
-            if (held_tok(k) >= valid) v[k] = -INFINITY;
-            need |= v[k] > m_mine + kRescaleThreshold;
-            top_mine = fmaxf(top_mine, v[k]);
-        }
-        if (__any_sync(pkv::kFullMask, need)) {
-            float mx[G];
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) mx[hh] = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < HELD; ++k)
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    mx[hh] = fmaxf(mx[hh], my_head == hh ? v[k] : -INFINITY);
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-                for (int sh = 0; sh < 5; ++sh)
-                    mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(pkv::kFullMask, mx[hh], 16 >> sh));
-            }
-            m_mine = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float mn = fmaxf(m_head[hh], mx[hh]);
-                const float alpha = exp2f(m_head[hh] - mn);
-                m_head[hh] = mn;
-                l_lane[hh] *= alpha;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[hh][e] *= alpha;
-                m_mine += (my_head == hh) ? mn : 0.f;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < HELD; ++k) {
-            const float p = exp2f(v[k] - m_mine);  // 0 for masked tokens
-            if (owner) {
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) l_lane[hh] += (my_head == hh) ? p : 0.f;
-                if (held_tok(k) < valid) s_prob[held_tok(k) * G + my_head] = p;
-            }
-        }
+        if (touched) __syncwarp();
+        eng.chunk(k_tile, v_tile, valid, lane, scratch);
         __syncwarp();
-
-        // ---- P . V: this lane owns dims [4*lane, 4*lane+4) of every packed head
-#pragma unroll
-        for (int t = 0; t < kChunk; ++t) {
-            if (t < valid) {
-                const uint2 raw = pkv::lds64(v_tile + t * kRowBytes + lane * 8);
-                const float2 v01 = pkv::half2_bits_to_float2(raw.x);
-                const float2 v23 = pkv::half2_bits_to_float2(raw.y);
-                float pr[G];
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) pr[hh] = s_prob[t * G + hh];
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-#if PKV_DECODE_FFMA2
-                    pkv::fma2(acc[hh][0], acc[hh][1], pr[hh], pr[hh], v01.x, v01.y);
-                    pkv::fma2(acc[hh][2], acc[hh][3], pr[hh], pr[hh], v23.x, v23.y);
-#else
-                    acc[hh][0] = fmaf(pr[hh], v01.x, acc[hh][0]);
-                    acc[hh][1] = fmaf(pr[hh], v01.y, acc[hh][1]);
-                    acc[hh][2] = fmaf(pr[hh], v23.x, acc[hh][2]);
-                    acc[hh][3] = fmaf(pr[hh], v23.y, acc[hh][3]);
-#endif
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && i + kStages < my_chunks) {
+        if (i + kStages < my_chunks) {
             pkv::fence_proxy_async_smem();
             issue(i + kStages);
         }
@@ -607,43 +832,12 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 2 : PKV_DECODE_MIN_CTAS)
         for (int i = consumed + 1; i < issued; ++i) pkv::mbar_wait_bounded(bar0 + 8 * (i % kStages), (i / kStages) & 1);
     }
 
-    // ---- per-warp softmax denominators, re-referenced to the true max of each head
-    float l_head[G];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        l_head[hh] = l_lane[hh];
-        float top = my_head == hh ? top_mine : -INFINITY;
-#pragma unroll
-        for (int sh = 0; sh < 5; ++sh) {
-            l_head[hh] += __shfl_xor_sync(pkv::kFullMask, l_head[hh], 16 >> sh);
-            top = fmaxf(top, __shfl_xor_sync(pkv::kFullMask, top, 16 >> sh));
-        }
-        if (top > -INFINITY) {  // this warp saw tokens: m_head <= top < m_head + 2^8
-            const float f = exp2f(m_head[hh] - top);
-            l_head[hh] *= f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[hh][e] *= f;
-            m_head[hh] = top;
-        }
-    }
-
     // ---- merge the 4 warps in shared memory (reusing the stage buffers)
     __syncthreads();
     float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][G][kD]
     float *c_m = c_acc + kWarps * G * kD;                            // [kWarps][G]
     float *c_l = c_m + kWarps * G;                                   // [kWarps][G]
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        *reinterpret_cast<float4 *>(c_acc + (warp * G + hh) * kD + lane * 4) =
-            make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            c_m[warp * G + hh] = m_head[hh];
-            c_l[warp * G + hh] = l_head[hh];
-        }
-    }
+    eng.finish(warp, lane, c_acc, c_m, c_l);
     __syncthreads();
 #pragma unroll 1
     for (int idx = threadIdx.x; idx < G * kD; idx += kThreads) {
@@ -766,15 +960,16 @@ constexpr int lanes_per_token() {
 template <int G>
 int launch_partition(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
-    auto kernel = decode_partition_kernel<G, LPT>;
-    const int smem = SmemLayout::total(G, p.partition_size);
+    constexpr bool TC = PKV_DECODE_TC && G >= 4;
+    auto kernel = decode_partition_kernel<G, LPT, TC>;
+    const int smem = SmemLayout<TC>::total(G, p.partition_size);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SmemLayout::total(G, PKV_MAX_PARTITION)) != cudaSuccess)
+                                 SmemLayout<TC>::total(G, PKV_MAX_PARTITION)) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }

@@ -60,26 +60,13 @@ struct PrefixParams {
     float q_scale;  // scale * log2(e)
 };
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(pkv::smem_addr(p)));
-}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) { pkv::ldsm_x4(r, pkv::smem_addr(p)); }
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(pkv::smem_addr(p)));
+    pkv::ldsm_x4_trans(r, pkv::smem_addr(p));
 }
 
-// d += a (16x16 fp16, row) * b (16x8 fp16, col), fp32 accumulators
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+using pkv::mma16816;
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
