@@ -650,8 +650,21 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     const int bs = P.block_size;
 
     // ---------------------------------------------------------------- extent
-    int ctx = __ldg(P.context_lens + b);
+    // The block ids of this warp's first chunks and q depend only on (b, kv head, partition):
+    // load them now, in parallel with the context length.
     const int cap = P.max_blocks_per_seq * bs;
+    const int start = P.token_offset + part * P.partition_size;
+    int32_t first_ids[kStages];
+#pragma unroll
+    for (int k = 0; k < kStages; ++k) {
+        const int tok = start + (warp + k * kWarps) * kChunk;
+        first_ids[k] = (lane == 0 && tok < cap)
+                           ? __ldg(P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq + tok / bs)
+                           : 0;
+    }
+    Engine eng;
+    eng.init(P, b, kvh, lane);
+    int ctx = __ldg(P.context_lens + b);
     if (ctx > cap) {
         if (part == 0 && kvh == 0 && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
         ctx = cap;
@@ -688,7 +701,6 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     }
     if (part >= n_parts) return;
 
-    const int start = tok_begin + part * P.partition_size;
     const int n_tok = min(P.partition_size, ctx - start);
     const int n_chunks = (n_tok + kChunk - 1) / kChunk;
     const int lb0 = start / bs;
@@ -704,6 +716,58 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         for (int s = 0; s < kStages; ++s) pkv::mbar_init(bar0 + 8 * s, 1);
         pkv::fence_mbar_init();
     }
+    const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
+    const int64_t head_stride = static_cast<int64_t>(bs) * kRowBytes;
+    const int64_t block_stride = head_stride * P.num_kv_heads;
+
+    // Stage chunk i of this warp (called by all 32 lanes): the CUDA-core engine takes the K and V
+    // rows as two contiguous bulk copies; the tensor-core engine copies row by row into padded rows.
+    auto issue_from = [=](int i, int64_t phys) {
+        const int cidx = warp + i * kWarps;
+        const int tok0 = start + cidx * kChunk;
+        const int valid = min(kChunk, n_tok - cidx * kChunk);
+        const int lb = tok0 / bs;
+        const int off = tok0 - lb * bs;
+        const int64_t byte_off = phys * block_stride + kvh * head_stride + static_cast<int64_t>(off) * kRowBytes;
+        const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
+        const int st = i % kStages;
+        const uint32_t bar = bar0 + 8 * st;
+        const uint32_t dst = stage0 + st * 2 * kTile;
+        if constexpr (TC) {
+            if (lane == 0) pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
+            __syncwarp();
+            const int row = lane & 15;
+            if (row < valid)
+                pkv::bulk_copy_g2s(dst + (lane < 16 ? 0 : kTile) + row * kRow,
+                                   (lane < 16 ? P.k_cache : P.v_cache) + byte_off + row * kRowBytes, kRowBytes, bar);
+        } else {
+            if (lane == 0) {
+                pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
+                pkv::bulk_copy_g2s(dst, P.k_cache + byte_off, bytes, bar);
+                pkv::bulk_copy_g2s(dst + kTile, P.v_cache + byte_off, bytes, bar);
+            }
+        }
+    };
+
+    auto issue = [=](int i) {
+        const int tok0 = start + (warp + i * kWarps) * kChunk;
+        issue_from(i, s_table[tok0 / bs - lb0]);
+    };
+
+    // Start-up: each warp reads the block ids of its first chunks straight from the table and
+    // issues their copies before the CTA-wide barrier, so the copy latency overlaps the
+    // prologue (table slice, q, barrier).
+    {
+        const int pre = my_chunks < kStages ? my_chunks : kStages;
+#pragma unroll
+        for (int k = 0; k < kStages; ++k) {
+            if (k < pre) {
+                const int32_t id = __shfl_sync(pkv::kFullMask, first_ids[k], 0);
+                issue_from(k, (id < 0 || id >= P.num_blocks) ? 0 : id);  // bad ids: recorded by the table pass
+            }
+        }
+    }
+
     {
         const int32_t *bt_row = P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq + lb0;
         for (int i = threadIdx.x; i < n_bt; i += kThreads) {
@@ -722,8 +786,6 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         }
     }
 
-    Engine eng;
-    eng.init(P, b, kvh, lane);
     static_assert(kWarps * G * (kD + 2) * 4 <= L::stage_bytes, "combine area must fit the stages");
 
     // ---- fused append: the CTA holding the request's last position writes the new token's K/V
@@ -749,44 +811,6 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
 
     __syncthreads();  // table + barrier init visible to every warp
 
-    const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
-    const int64_t head_stride = static_cast<int64_t>(bs) * kRowBytes;
-    const int64_t block_stride = head_stride * P.num_kv_heads;
-
-    // Stage chunk i of this warp (called by all 32 lanes): the CUDA-core engine takes the K and V
-    // rows as two contiguous bulk copies; the tensor-core engine copies row by row into padded rows.
-    auto issue = [=](int i) {
-        const int cidx = warp + i * kWarps;
-        const int tok0 = start + cidx * kChunk;
-        const int valid = min(kChunk, n_tok - cidx * kChunk);
-        const int lb = tok0 / bs;
-        const int off = tok0 - lb * bs;
-        const int64_t phys = s_table[lb - lb0];
-        const int64_t byte_off = phys * block_stride + kvh * head_stride + static_cast<int64_t>(off) * kRowBytes;
-        const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
-        const int st = i % kStages;
-        const uint32_t bar = bar0 + 8 * st;
-        const uint32_t dst = stage0 + st * 2 * kTile;
-        if constexpr (TC) {
-            if (lane == 0) pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
-            __syncwarp();
-            const int row = lane & 15;
-            if (row < valid)
-                pkv::bulk_copy_g2s(dst + (lane < 16 ? 0 : kTile) + row * kRow,
-                                   (lane < 16 ? P.k_cache : P.v_cache) + byte_off + row * kRowBytes, kRowBytes, bar);
-        } else {
-            if (lane == 0) {
-                pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
-                pkv::bulk_copy_g2s(dst, P.k_cache + byte_off, bytes, bar);
-                pkv::bulk_copy_g2s(dst + kTile, P.v_cache + byte_off, bytes, bar);
-            }
-        }
-    };
-
-    {
-        const int pre = my_chunks < kStages ? my_chunks : kStages;
-        for (int i = 0; i < pre; ++i) issue(i);
-    }
 
     int consumed = 0;
     bool aborted = false;
