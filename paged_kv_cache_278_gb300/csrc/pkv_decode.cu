@@ -34,6 +34,7 @@
 //     partials (m, l, normalised o) for the log-sum-exp merge kernel.
 //   * Indices read from memory are checked (block ids, context length) and
 //     clamped; problems are recorded in the device error word.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -54,7 +55,6 @@ __device__ int g_decode_error;
 constexpr int kD = PKV_HEAD_DIM;        // 128
 constexpr int kChunk = 16;              // tokens per shared-memory tile
 constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
-constexpr int kTileBytes = kChunk * kRowBytes;  // 4 KiB
 // Warps per CTA and bulk-copy stages per warp (each stage holds one 16-token chunk of K and V).
 #ifndef PKV_DECODE_WARPS
 #define PKV_DECODE_WARPS 4
@@ -108,16 +108,19 @@ struct DecodeParams {
     const __half *v_new;
     __half *k_cache_w;        // writable views of the caches for that append
     __half *v_cache_w;
+    CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
+    CUtensorMap tmap_v;       //   16 x 64 boxes, 128-byte swizzle
 };
 
 constexpr int kMergeTile = 512;  // partitions whose weights the fused merge stages at a time
 
 // Shared-memory carve-up (bytes), identical on host and device.  TC selects the tensor-core
-// engine's padded rows (272 B) and its fp16 P buffer.
-constexpr int kPadRowBytes = kRowBytes + 16;
+// engine's fp16 P buffer; its K/V tiles are two 2 KB halves (dims 0-63, 64-127) of 16 rows x
+// 128 B in the tensor copies' 128-byte swizzle (16-byte chunk c of row r stored at c ^ (r % 8)).
+constexpr int kHalfTile = kChunk * 128;
 template <bool TC>
 struct SmemLayout {
-    static constexpr int row = TC ? kPadRowBytes : kRowBytes;
+    static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
     static constexpr int stages = 0;
     static constexpr int stage_bytes = kWarps * kStages * 2 * tile;
@@ -496,13 +499,17 @@ struct FmaEngine {
 //                                                           memory by ldmatrix, Q^T as fp16
 //                                                           fragments held in registers)
 //   O^T[128 x 8]  += V_tile^T[128 x 16] . P^T[16 x 8]        8 m-tiles x 2 (P = hi + lo fp16)
-// with fp32 accumulation throughout.  K/V rows sit in shared memory at a 272-byte stride (one
-// bulk copy per row) so every ldmatrix is bank-conflict free.  Each lane owns heads
-// 2*(lane%4) and +1 of the fragments; lanes whose heads are >= G carry padding columns.
+// with fp32 accumulation throughout.  K/V tiles arrive by 2-D tensor copies in the 128-byte
+// swizzle, which keeps every ldmatrix bank-conflict free.  Each lane owns heads 2*(lane%4) and +1
+// of the fragments; lanes whose heads are >= G carry padding columns.
 template <int G>
 struct TcEngine {
     static_assert(G == 4 || G == 8, "tensor-core engine packs 4 or 8 heads into the 8 MMA columns");
-    static constexpr int kRow = kPadRowBytes;
+
+    // Byte offset of 16-byte chunk `c16` (0..15 across the 128 dims) of row r in a swizzled tile.
+    __device__ __forceinline__ static uint32_t swz(int r, int c16) {
+        return (c16 >> 3) * kHalfTile + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
+    }
 
     uint32_t qb[kD / 16][2];  // Q^T B-fragments of the 8 k-steps (fp16x2)
     float o[kD / 16][4];      // O^T accumulators: (dim 16 mt + lane/4 (+8), head h0 (+1))
@@ -532,7 +539,7 @@ struct TcEngine {
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t a[4];
-            pkv::ldsm_x4(a, k_tile + (lane & 15) * kRow + ks * 32 + (lane >> 4) * 16);
+            pkv::ldsm_x4(a, k_tile + swz(lane & 15, ks * 2 + (lane >> 4)));
             pkv::mma16816(s, a, qb[ks][0], qb[ks][1]);
         }
         const int g = lane >> 2;
@@ -587,7 +594,7 @@ struct TcEngine {
 #pragma unroll
         for (int mt = 0; mt < kD / 16; ++mt) {
             uint32_t a[4];
-            pkv::ldsm_x4_trans(a, v_tile + ((lane >> 4) * 8 + (lane & 7)) * kRow + (mt * 16 + ((lane >> 3) & 1) * 8) * 2);
+            pkv::ldsm_x4_trans(a, v_tile + swz((lane >> 4) * 8 + (lane & 7), mt * 2 + ((lane >> 3) & 1)));
             pkv::mma16816(o[mt], a, bh0, bh1);
             pkv::mma16816(o[mt], a, bl0, bl1);
         }
@@ -633,13 +640,13 @@ using EngineFor = typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngin
 
 template <int G, int LPT, bool TC>
 __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN_CTAS)
-    decode_partition_kernel(const DecodeParams P) {
+    decode_partition_kernel(const __grid_constant__ DecodeParams P) {
     using L = SmemLayout<TC>;
     using Engine = EngineFor<G, LPT, TC>;
     constexpr int kRow = L::row;
     constexpr int kTile = L::tile;
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -711,6 +718,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     const uint32_t bar0 = pkv::smem_addr(smem + L::bars) + warp * kStages * 8;
     const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * 2 * kTile;
 
+    if (TC && (pkv::smem_addr(smem) & 1023) != 0) {  // the 128-byte swizzle needs 1 KB-aligned tiles
+        if (threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
+        return;
+    }
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) pkv::mbar_init(bar0 + 8 * s, 1);
@@ -721,7 +732,14 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     const int64_t block_stride = head_stride * P.num_kv_heads;
 
     // Stage chunk i of this warp (called by all 32 lanes): the CUDA-core engine takes the K and V
-    // rows as two contiguous bulk copies; the tensor-core engine copies row by row into padded rows.
+    // rows as two contiguous bulk copies, the tensor-core engine four swizzled 2-D tensor boxes.
+    // The lambdas capture plain values only: the tensor maps must be read where the grid-constant
+    // parameter lives, never from a local copy.
+    const unsigned char *kc = P.k_cache;
+    const unsigned char *vc = P.v_cache;
+    const void *tmap_k = &P.tmap_k;
+    const void *tmap_v = &P.tmap_v;
+    const int hkv = P.num_kv_heads;
     auto issue_from = [=](int i, int64_t phys) {
         const int cidx = warp + i * kWarps;
         const int tok0 = start + cidx * kChunk;
@@ -734,17 +752,22 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         const uint32_t bar = bar0 + 8 * st;
         const uint32_t dst = stage0 + st * 2 * kTile;
         if constexpr (TC) {
-            if (lane == 0) pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
-            __syncwarp();
-            const int row = lane & 15;
-            if (row < valid)
-                pkv::bulk_copy_g2s(dst + (lane < 16 ? 0 : kTile) + row * kRow,
-                                   (lane < 16 ? P.k_cache : P.v_cache) + byte_off + row * kRowBytes, kRowBytes, bar);
+            // Whole 16-row boxes (a ragged tail's extra rows stay inside the block and are masked).
+            if (lane == 0) {
+                const int y = static_cast<int>((phys * hkv + kvh) * bs + off);
+                pkv::mbar_arrive_expect_tx(bar, 4 * kHalfTile);
+                pkv::tma_load_2d(dst, tmap_k, 0, y, bar);
+                pkv::tma_load_2d(dst + kHalfTile, tmap_k, 64, y, bar);
+                pkv::tma_load_2d(dst + kTile, tmap_v, 0, y, bar);
+                pkv::tma_load_2d(dst + kTile + kHalfTile, tmap_v, 64, y, bar);
+            }
+            (void)byte_off;
+            (void)bytes;
         } else {
             if (lane == 0) {
                 pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
-                pkv::bulk_copy_g2s(dst, P.k_cache + byte_off, bytes, bar);
-                pkv::bulk_copy_g2s(dst + kTile, P.v_cache + byte_off, bytes, bar);
+                pkv::bulk_copy_g2s(dst, kc + byte_off, bytes, bar);
+                pkv::bulk_copy_g2s(dst + kTile, vc + byte_off, bytes, bar);
             }
         }
     };
@@ -829,14 +852,16 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         const uint32_t v_tile = k_tile + kTile;
         bool touched = false;
         if (TC && valid < kChunk) {  // the MMA reads all 16 V rows: make the unused ones finite (zero)
-            for (int x = lane; x < (kChunk - valid) * (kRow / 16); x += 32)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + valid * kRow + x * 16), "r"(0)
+            for (int x = lane; x < (kChunk - valid) * 16; x += 32)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + TcEngine<4>::swz(valid + x / 16, x % 16)),
+                             "r"(0)
                              : "memory");
             touched = true;
         }
         if (cidx == own_chunk) {  // the appended token's row: overwrite what the copy brought
             const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
-            const uint32_t row = ((new_pos - start) % kChunk) * kRow + (lane & 15) * 16;
+            const int nr_row = (new_pos - start) % kChunk;
+            const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"((lane < 16 ? k_tile : v_tile) + row),
                          "r"(nr.x), "r"(nr.y), "r"(nr.z), "r"(nr.w)
                          : "memory");
@@ -981,11 +1006,51 @@ constexpr int lanes_per_token() {
     return G >= 8 ? 16 : 8;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// The cache as a 2-D fp16 tensor [rows][128] (rows = NB * Hkv * bs, 256-byte row stride) read in
+// 16-row x 64-dim boxes with the 128-byte swizzle.
+int encode_cache_map(CUtensorMap *map, const void *base, int64_t rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return PKV_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 template <int G>
-int launch_partition(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
+int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
     constexpr bool TC = PKV_DECODE_TC && G >= 4;
     auto kernel = decode_partition_kernel<G, LPT, TC>;
+    DecodeParams p = p_in;
+    if (TC) {
+        const int64_t rows = p.num_blocks * p.num_kv_heads * p.block_size;
+        if (rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // box row coordinates are signed 32-bit
+        int st = encode_cache_map(&p.tmap_k, p.k_cache, rows);
+        if (st == PKV_OK) st = encode_cache_map(&p.tmap_v, p.v_cache, rows);
+        if (st != PKV_OK) return st;
+    }
     const int smem = SmemLayout<TC>::total(G, p.partition_size);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
