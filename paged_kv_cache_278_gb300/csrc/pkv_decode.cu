@@ -703,7 +703,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         return;
     }
     if (n_parts == 0) {  // shared-prefix pass: the whole context is the prefix, merge its chunks only
-        if (part == 0 && P.counters != nullptr) merge_group<G>(P, b, kvh, P.slot_offset, smem);
+        if (part == 0 && P.counters != nullptr) {
+            pkv::pdl_wait_primary();  // the prefix kernel's partials
+            merge_group<G>(P, b, kvh, P.slot_offset, smem);
+        }
         return;
     }
     if (part >= n_parts) return;
@@ -926,6 +929,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     if (threadIdx.x == 0) s_last = pkv::atomic_add_acq_rel_gpu(counter, 1) == n_parts - 1;
     __syncthreads();
     if (!s_last) return;
+    if (P.slot_offset > 0) pkv::pdl_wait_primary();  // shared-prefix pass: the prefix kernel's partials
     merge_group<G>(P, b, kvh, P.slot_offset + n_parts, smem);
     if (threadIdx.x == 0) *counter = 0;
 }
@@ -1063,8 +1067,23 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const dim3 grid(grid_parts > 0 ? grid_parts : p.max_partitions, p.num_kv_heads, num_seqs);
-    kernel<<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (p.slot_offset == 0) {
+        kernel<<<grid, kThreads, smem, stream>>>(p);
+        return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    }
+    // Suffix pass after the shared-prefix kernel: launched as a programmatic dependent so it
+    // streams the suffixes while the prefix kernel runs; only its merges wait for the prefix.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream, int grid_parts = 0) {

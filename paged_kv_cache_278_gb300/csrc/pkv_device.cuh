@@ -148,6 +148,12 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
     return old;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start launching now, and
+// (in that kernel) wait until the preceding grid has completed and its writes are visible.
+// Both are no-ops when the launch carries no programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void record_error(int *word, int code) { atomicCAS(word, 0, code); }
 

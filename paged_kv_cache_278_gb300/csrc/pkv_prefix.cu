@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     __half *sK = reinterpret_cast<__half *>(smem);      // [kChunkTok][kPad]
     __half *sV = sK + kChunkTok * kPad;                   // [kChunkTok][kPad]
     __half *sQ = sV + kChunkTok * kPad;                   // [kRows][kPad]
+    pkv::pdl_launch_dependents();  // the suffix pass may start streaming right away
     const int chunk = blockIdx.x, kvh = blockIdx.y, rtile = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hq = P.num_q_heads, Hkv = P.num_kv_heads, G = Hq / Hkv, bs = P.block_size;
@@ -245,6 +246,11 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
 }
 
 constexpr int kMinSuffixPartition = 64;
+// The suffix partition is halved (from 512) until the suffix grid offers this many CTAs per
+// resident CTA slot.
+#ifndef PKV_SUFFIX_WAVES
+#define PKV_SUFFIX_WAVES 2
+#endif
 
 struct SharedLayout {
     int n_pre, n_suf, max_parts, suffix_partition;
@@ -307,8 +313,9 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
                                              kMinSuffixPartition);
     if (!workspace || workspace_bytes < bound.total || !pkv_internal::aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
-    // Suffix partition: halve from 512 tokens (down to 64) until the suffix grid offers about four
-    // CTAs per resident CTA slot (3 per SM), so short private suffixes still fill the GPU.
+    // Suffix partition: halve from 512 tokens (down to 64) until the suffix grid offers
+    // PKV_SUFFIX_WAVES CTAs per resident CTA slot (3 per SM), so short private suffixes still fill
+    // the GPU.
     int dev_sm = 0;
     int suffix_part = PKV_DEFAULT_PARTITION;
     {
@@ -316,7 +323,7 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
         if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&dev_sm, cudaDevAttrMultiProcessorCount, d) !=
                                                       cudaSuccess)
             return PKV_ERR_CUDA;
-        const int64_t want = 4LL * 3 * dev_sm;
+        const int64_t want = static_cast<int64_t>(PKV_SUFFIX_WAVES) * 3 * dev_sm;
         const int64_t rest = cap - prefix_len;
         while (suffix_part > kMinSuffixPartition &&
                static_cast<int64_t>(num_seqs) * num_kv_heads * ((rest + suffix_part - 1) / suffix_part) < want)
