@@ -249,7 +249,7 @@ constexpr int kMinSuffixPartition = 64;
 // The suffix partition is halved (from 512) until the suffix grid offers this many CTAs per
 // resident CTA slot.
 #ifndef PKV_SUFFIX_WAVES
-#define PKV_SUFFIX_WAVES 2
+#define PKV_SUFFIX_WAVES 1
 #endif
 
 struct SharedLayout {
