@@ -145,6 +145,31 @@ PKV_API int pkv_pool_refcount(const pkv_pool *pool, int32_t id);
 PKV_API int pkv_pool_reserve(pkv_pool *pool, int32_t *table_row, int max_blocks,
                              int cur_tokens, int new_tokens, int block_size);
 
+/* Fork: a new request starts as a copy of the first num_tokens tokens of another.
+ * dst_row[0 .. ceil(num_tokens/bs)) receives the same block ids as src_row and
+ * every one of those blocks gains a reference (shared, not copied).  Errors:
+ * INVALID_ARG (an id not allocated, or more blocks than max_blocks). */
+PKV_API int pkv_pool_fork(pkv_pool *pool, const int32_t *src_row, int32_t *dst_row, int max_blocks,
+                          int num_tokens, int block_size);
+
+/* Make position `cur_tokens` of a request writable before its token is
+ * appended.  If the position starts a new block, one block is allocated and
+ * written to table_row.  If it falls inside a block that other requests also
+ * reference (reference count > 1), that block is copied on write: a fresh
+ * block replaces it in table_row, the old block loses this request's
+ * reference, and *copy_src / *copy_dst receive the pair the caller must copy
+ * on the device (pkv_copy_blocks) before appending; *n_copies is 1 then, else
+ * 0.  Errors: INVALID_ARG, OUT_OF_BLOCKS (nothing changed). */
+PKV_API int pkv_pool_prepare_append(pkv_pool *pool, int32_t *table_row, int max_blocks,
+                                    int cur_tokens, int block_size, int32_t *copy_src,
+                                    int32_t *copy_dst, int *n_copies);
+
+/* Drop the request's reference to each of its ceil(num_tokens/bs) blocks (the
+ * end of a request, whether it finished or failed); all-or-nothing as
+ * pkv_pool_free.  Errors: INVALID_ARG. */
+PKV_API int pkv_pool_free_table(pkv_pool *pool, const int32_t *table_row, int num_tokens,
+                                int block_size);
+
 /* Host slot mapping for one new token per request:
  *   slots[b] = block_tables[b][positions[b] / bs] * bs + positions[b] % bs,
  * and slots[b] = -1 when positions[b] < 0 (no token for that request).
@@ -168,6 +193,17 @@ PKV_API int pkv_slot_mapping(int64_t *slots, const int32_t *block_tables, const 
 PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping,
                        const void *k_new, const void *v_new, int num_tokens, int num_kv_heads,
                        int head_dim, int block_size, int64_t num_blocks, pkv_stream_t stream);
+
+/* Copy whole blocks (every kv head, every slot) of both caches:
+ *   k_cache[dst[i]] <- k_cache[src[i]], v_cache[dst[i]] <- v_cache[src[i]], i < n,
+ * bit for bit (copy-on-write of a shared block).  src and dst are DEVICE int32
+ * arrays; a destination must not appear twice nor also be a source.  Ids
+ * outside [0, num_blocks) skip the pair and are recorded as
+ * PKV_DEV_BAD_BLOCK_ID.  head_dim must be a multiple of 8.
+ * Errors: INVALID_ARG, CUDA. */
+PKV_API int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst, int n,
+                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                            pkv_stream_t stream);
 
 /* Bytes of workspace pkv_decode_attention needs for contexts up to
  * max_context tokens (0 when one partition covers max_context): fp32 partials

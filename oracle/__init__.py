@@ -101,6 +101,8 @@ class Oracle:
         lib.oracle_decode_partition.argtypes = ([_f64p, _f64p, _f64p, _u16p, _u16p, _u16p,
                                                  _i32p, _i32p] + [ctypes.c_int] * 6
                                                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int])
+        lib.oracle_copy_blocks.restype = None
+        lib.oracle_copy_blocks.argtypes = [_u16p, _u16p, _i32p, _i32p] + [ctypes.c_int] * 4
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
         self.lib = lib
@@ -136,6 +138,16 @@ class Oracle:
         assert kn.shape == (sl.shape[0], hkv, d) and vn.shape == kn.shape
         self.lib.oracle_append(_p(kc, _u16p), _p(vc, _u16p), _p(sl, _i64p), _p(kn, _u16p),
                                _p(vn, _u16p), sl.shape[0], hkv, d, bs)
+
+    def copy_blocks(self, k_cache: np.ndarray, v_cache: np.ndarray, src, dst) -> None:
+        """In place: whole blocks dst[i] <- src[i] of both caches."""
+        nb, hkv, bs, d = k_cache.shape
+        kc, vc = _bits(k_cache), _bits(v_cache)
+        assert np.shares_memory(kc, k_cache) and np.shares_memory(vc, v_cache)
+        sr = np.ascontiguousarray(src, dtype=np.int32)
+        ds = np.ascontiguousarray(dst, dtype=np.int32)
+        self.lib.oracle_copy_blocks(_p(kc, _u16p), _p(vc, _u16p), _p(sr, _i32p), _p(ds, _i32p), sr.shape[0], hkv,
+                                    d, bs)
 
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
         """float64 [B, Hq, D] attention output of one decode step."""
@@ -223,3 +235,7 @@ def decode_partition(q, k_cache, v_cache, block_tables, context_lens, scale, par
 
 def merge(o_part, m_part, l_part, context_lens, partition_size):
     return default().merge(o_part, m_part, l_part, context_lens, partition_size)
+
+
+def copy_blocks(k_cache, v_cache, src, dst):
+    return default().copy_blocks(k_cache, v_cache, src, dst)

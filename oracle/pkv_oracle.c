@@ -121,6 +121,22 @@ void oracle_append(uint16_t *k_cache, uint16_t *v_cache, const int64_t *slot_map
     }
 }
 
+/* Copy-on-write of whole blocks: k_cache[dst[i]] <- k_cache[src[i]] and the same for V,
+ * every kv head and slot of the block, as raw 16-bit patterns (copying a shared page
+ * before a request appends into it; the pages share prefix blocks between requests:
+ * "推理优化这件事，为什么值得反复复盘", sec. 4.2). */
+void oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *src, const int32_t *dst, int n,
+                        int num_kv_heads, int head_dim, int block_size)
+{
+    int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < n; ++i) {
+        for (int64_t e = 0; e < per_block; ++e) {
+            k_cache[(int64_t)dst[i] * per_block + e] = k_cache[(int64_t)src[i] * per_block + e];
+            v_cache[(int64_t)dst[i] * per_block + e] = v_cache[(int64_t)src[i] * per_block + e];
+        }
+    }
+}
+
 /* scores s_p = scale * q . K[p] for p in [p0, p1) of request b, kv head j. */
 static void scores_range(double *s, const uint16_t *q_row, const uint16_t *k_cache,
                          const int32_t *bt_row, int p0, int p1, int j,

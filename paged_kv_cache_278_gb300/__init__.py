@@ -28,7 +28,7 @@ from ._lib import (PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONT
 __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
     "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
-    "decode_step", "make_step_workspace",
+    "decode_step", "make_step_workspace", "copy_blocks",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -245,6 +245,20 @@ def device_error(device=None, stream=None) -> int:
     return code.value
 
 
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
+                stream=None) -> None:
+    """k_cache[dst[i]] <- k_cache[src[i]] (and V), whole blocks, bit for bit (copy-on-write)."""
+    nb, hkv, bs, d = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(src, "src", torch.int32, 1, dev)
+    _need(dst, "dst", torch.int32, 1, dev)
+    if src.shape != dst.shape:
+        raise ValueError("src and dst differ in length")
+    st = _L().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), src.data_ptr(), dst.data_ptr(), src.numel(),
+                              hkv, d, bs, nb, _stream(dev, stream))
+    _lib.check(st, "pkv_copy_blocks")
+
+
 def slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int) -> torch.Tensor:
     """Host slot of each request's new token: int64 [B] (CPU tensors in, CPU tensor out)."""
     bt = block_tables.to(torch.int32).contiguous().cpu()
@@ -297,6 +311,30 @@ class BlockPool:
 
     def refcount(self, block_id: int) -> int:
         return int(_L().pkv_pool_refcount(self._h, block_id))
+
+    @staticmethod
+    def _row(table_row: torch.Tensor) -> "ctypes._Pointer":
+        if table_row.dtype != torch.int32 or table_row.device.type != "cpu" or not table_row.is_contiguous():
+            raise ValueError("table rows must be contiguous CPU int32 tensors")
+        return ctypes.cast(table_row.data_ptr(), _lib.c_i32p)
+
+    def fork(self, src_row: torch.Tensor, dst_row: torch.Tensor, num_tokens: int, block_size: int) -> None:
+        """dst_row shares the blocks holding src_row's first num_tokens tokens."""
+        st = _L().pkv_pool_fork(self._h, self._row(src_row), self._row(dst_row), dst_row.numel(), num_tokens,
+                                block_size)
+        _lib.check(st, "pkv_pool_fork")
+
+    def prepare_append(self, table_row: torch.Tensor, cur_tokens: int, block_size: int):
+        """Make position cur_tokens writable; returns (src, dst) block ids to copy first, or None."""
+        src, dst, n = ctypes.c_int32(-1), ctypes.c_int32(-1), ctypes.c_int(0)
+        st = _L().pkv_pool_prepare_append(self._h, self._row(table_row), table_row.numel(), cur_tokens, block_size,
+                                          ctypes.byref(src), ctypes.byref(dst), ctypes.byref(n))
+        _lib.check(st, "pkv_pool_prepare_append")
+        return (src.value, dst.value) if n.value else None
+
+    def free_table(self, table_row: torch.Tensor, num_tokens: int, block_size: int) -> None:
+        _lib.check(_L().pkv_pool_free_table(self._h, self._row(table_row), num_tokens, block_size),
+                   "pkv_pool_free_table")
 
     def reserve(self, table_row: torch.Tensor, cur_tokens: int, new_tokens: int, block_size: int) -> None:
         """Grow a CPU int32 block-table row in place to cover new_tokens tokens."""

@@ -49,6 +49,11 @@ SIGNATURES = {
     "pkv_pool_num_free": (c_int64, [c_void_p]),
     "pkv_pool_refcount": (c_int, [c_void_p, ctypes.c_int32]),
     "pkv_pool_reserve": (c_int, [c_void_p, c_i32p, c_int, c_int, c_int, c_int]),
+    "pkv_pool_fork": (c_int, [c_void_p, c_i32p, c_i32p, c_int, c_int, c_int]),
+    "pkv_pool_prepare_append": (c_int, [c_void_p, c_i32p, c_int, c_int, c_int, c_i32p, c_i32p,
+                                        ctypes.POINTER(c_int)]),
+    "pkv_pool_free_table": (c_int, [c_void_p, c_i32p, c_int, c_int]),
+    "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
     "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                            c_int64, c_void_p]),

@@ -50,7 +50,43 @@ __global__ void __launch_bounds__(kAppendThreads)
         k_cache[dst] = __ldg(k_new + idx);
 }
 
+// Copy-on-write: one thread per 16-byte piece of a block (all kv heads), K then V.
+__global__ void __launch_bounds__(kAppendThreads)
+    copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, const int32_t *__restrict__ src,
+                       const int32_t *__restrict__ dst, int64_t pieces_per_block, int n, int64_t num_blocks) {
+    int64_t idx = static_cast<int64_t>(blockIdx.x) * kAppendThreads + threadIdx.x;
+    const int64_t per_tensor = pieces_per_block * n;
+    const bool is_v = idx >= per_tensor;
+    if (is_v) idx -= per_tensor;
+    if (idx >= per_tensor) return;
+    const int pair = static_cast<int>(idx / pieces_per_block);
+    const int64_t piece = idx - pair * pieces_per_block;
+    const int32_t s = __ldg(src + pair), d = __ldg(dst + pair);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (piece == 0) pkv::record_error(&g_append_error, PKV_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    uint4 *cache = is_v ? v_cache : k_cache;
+    cache[d * pieces_per_block + piece] = cache[s * pieces_per_block + piece];
+}
+
 }  // namespace
+
+extern "C" PKV_API int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst, int n,
+                                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                       pkv_stream_t stream) {
+    if (!k_cache || !v_cache || (n > 0 && (!src || !dst))) return PKV_ERR_INVALID_ARG;
+    if (n < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!pkv_internal::aligned16(k_cache) || !pkv_internal::aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    const int64_t pieces = static_cast<int64_t>(num_kv_heads) * block_size * head_dim / 8;
+    const int64_t blocks = (2 * pieces * n + kAppendThreads - 1) / kAppendThreads;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    copy_blocks_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src, dst, pieces, n, num_blocks);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 extern "C" PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping,
                                   const void *k_new, const void *v_new, int num_tokens,

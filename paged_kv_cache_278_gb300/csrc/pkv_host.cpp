@@ -142,6 +142,49 @@ PKV_API int pkv_pool_reserve(pkv_pool *pool, int32_t *table_row, int max_blocks,
     return pkv_pool_alloc(pool, static_cast<int>(want - have), table_row + have);
 }
 
+PKV_API int pkv_pool_fork(pkv_pool *pool, const int32_t *src_row, int32_t *dst_row, int max_blocks, int num_tokens,
+                          int block_size) {
+    if (!pool || !src_row || !dst_row || max_blocks <= 0 || block_size <= 0 || num_tokens < 0)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t n = (static_cast<int64_t>(num_tokens) + block_size - 1) / block_size;
+    if (n > max_blocks) return PKV_ERR_INVALID_ARG;
+    const int st = pkv_pool_share(pool, static_cast<int>(n), src_row);
+    if (st != PKV_OK) return st;
+    for (int64_t i = 0; i < n; ++i) dst_row[i] = src_row[i];
+    return PKV_OK;
+}
+
+PKV_API int pkv_pool_prepare_append(pkv_pool *pool, int32_t *table_row, int max_blocks, int cur_tokens,
+                                    int block_size, int32_t *copy_src, int32_t *copy_dst, int *n_copies) {
+    if (!pool || !table_row || max_blocks <= 0 || block_size <= 0 || cur_tokens < 0 || !copy_src || !copy_dst ||
+        !n_copies)
+        return PKV_ERR_INVALID_ARG;
+    *n_copies = 0;
+    const int64_t blk = cur_tokens / block_size;
+    if (blk >= max_blocks) return PKV_ERR_INVALID_ARG;
+    if (cur_tokens % block_size == 0) return pkv_pool_alloc(pool, 1, table_row + blk);  // a fresh block
+    const int32_t old = table_row[blk];
+    const int64_t nb = static_cast<int64_t>(pool->refcount.size());
+    if (old < 0 || old >= nb || pool->refcount[old] <= 0) return PKV_ERR_INVALID_ARG;
+    if (pool->refcount[old] == 1) return PKV_OK;  // private: append in place
+    int32_t fresh = -1;
+    const int st = pkv_pool_alloc(pool, 1, &fresh);
+    if (st != PKV_OK) return st;
+    --pool->refcount[old];  // still >= 1: the other requests keep it
+    table_row[blk] = fresh;
+    *copy_src = old;
+    *copy_dst = fresh;
+    *n_copies = 1;
+    return PKV_OK;
+}
+
+PKV_API int pkv_pool_free_table(pkv_pool *pool, const int32_t *table_row, int num_tokens, int block_size) {
+    if (!pool || !table_row || num_tokens < 0 || block_size <= 0) return PKV_ERR_INVALID_ARG;
+    const int64_t n = (static_cast<int64_t>(num_tokens) + block_size - 1) / block_size;
+    if (n > 0x7fffffff) return PKV_ERR_INVALID_ARG;
+    return pkv_pool_free(pool, static_cast<int>(n), table_row);
+}
+
 PKV_API int pkv_slot_mapping(int64_t *slots, const int32_t *block_tables, const int32_t *positions, int num_seqs,
                              int max_blocks_per_seq, int block_size) {
     if (!slots || !block_tables || !positions || num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0)

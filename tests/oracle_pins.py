@@ -120,6 +120,45 @@ def pin_append_golden(orc):
     assert np.array_equal(vc, np.array(g["v_cache_after"], np.float16))
 
 
+def pin_copy_blocks_golden(orc):
+    g = golden("copy_blocks_tiny.json")
+    kc = np.array(g["k_cache_before"], np.float16)
+    vc = np.array(g["v_cache_before"], np.float16)
+    orc.copy_blocks(kc, vc, g["src"], g["dst"])
+    assert np.array_equal(kc, np.array(g["k_cache_after"], np.float16))
+    assert np.array_equal(vc, np.array(g["v_cache_after"], np.float16))
+
+
+def pin_copy_on_write_keeps_attention(orc):
+    """A request whose table points at a copied block must attend exactly as before the copy,
+    and appending into the copy must leave the original block's readers unchanged."""
+    rng = np.random.default_rng(11)
+    hkv, d, bs, ctx = 2, 16, 4, 10
+    ks, vs = random_contiguous(rng, [ctx, ctx], hkv, d)
+    ks[1], vs[1] = ks[0].copy(), vs[0].copy()
+    kpool, vpool, bt, _ = scatter_to_pool(ks, vs, bs, rng, extra_blocks=3)
+    bt[1] = bt[0]                                     # request 1 forks request 0
+    q = rng.standard_normal((2, 2 * hkv, d)).astype(np.float16)
+    ctxs = np.array([ctx, ctx], np.int32)
+    before = orc.decode(q, kpool, vpool, bt, ctxs, 0.25)
+    free = [i for i in range(kpool.shape[0]) if i not in set(bt[0].tolist())]
+    last = ctx // bs                                  # block holding position ctx (partially full)
+    orc.copy_blocks(kpool, vpool, [int(bt[1, last])], [free[0]])
+    bt[1, last] = free[0]
+    after = orc.decode(q, kpool, vpool, bt, ctxs, 0.25)
+    assert np.array_equal(before, after)
+    # request 1 appends its own token into the copy; request 0 is unaffected
+    k_new = rng.standard_normal((1, hkv, d)).astype(np.float16)
+    v_new = rng.standard_normal((1, hkv, d)).astype(np.float16)
+    orc.append(kpool, vpool, np.array([free[0] * bs + ctx % bs], np.int64), k_new, v_new)
+    ctxs2 = np.array([ctx, ctx + 1], np.int32)
+    out = orc.decode(q, kpool, vpool, bt, ctxs2, 0.25)
+    assert np.array_equal(out[0], before[0])
+    ref = textbook_attention(q[1:], [np.concatenate([ks[1], k_new.transpose(1, 0, 2)], axis=1)],
+                             [np.concatenate([vs[1], v_new.transpose(1, 0, 2)], axis=1)], 0.25)
+    assert np.abs(out[1] - ref[0]).max() < 1e-12
+
+
 def pin_slot_mapping_by_enumeration(orc):
     """Walk every block table in order, naming each pool slot by the (request, position)
     stored there; the slot mapping must be the inverse of that enumeration."""
@@ -320,6 +359,8 @@ ALL_PINS = [
     pin_half_decoding,
     pin_kv_bytes_worked_example,
     pin_append_golden,
+    pin_copy_blocks_golden,
+    pin_copy_on_write_keeps_attention,
     pin_slot_mapping_by_enumeration,
     pin_two_keys_golden,
     pin_textbook_contiguous,

@@ -168,3 +168,84 @@ def test_slot_mapping_matches_oracle(lib):
         assert np.array_equal(got, ref)
     with pytest.raises(pkv.PkvError):        # position beyond the table
         pkv.slot_mapping(torch.zeros((1, 2), dtype=torch.int32), torch.tensor([32], dtype=torch.int32), 16)
+
+
+def test_pool_fork_and_copy_on_write(lib):
+    pool = pkv.BlockPool(20, seed=9)
+    parent = torch.full((6,), -1, dtype=torch.int32)
+    pool.reserve(parent, 0, 40, 16)                     # 3 blocks, the last one half full
+    child = torch.full((6,), -1, dtype=torch.int32)
+    pool.fork(parent, child, 40, 16)
+    assert torch.equal(child[:3], parent[:3]) and (child[3:] == -1).all()
+    assert all(pool.refcount(int(i)) == 2 for i in parent[:3])
+    assert pool.num_free() == 17
+    # the child writes position 40, inside the shared third block: copy on write
+    shared = int(parent[2])
+    pair = pool.prepare_append(child, 40, 16)
+    assert pair is not None and pair[0] == shared and pair[1] == int(child[2]) and pair[1] != shared
+    assert pool.refcount(shared) == 1 and pool.refcount(pair[1]) == 1
+    assert torch.equal(child[:2], parent[:2])
+    # the parent now owns its third block alone: it appends in place
+    assert pool.prepare_append(parent, 40, 16) is None
+    assert int(parent[2]) == shared
+    # position 48 starts a fresh block for each
+    assert pool.prepare_append(child, 48, 16) is None and int(child[3]) >= 0
+    assert pool.num_free() == 15
+    pool.free_table(child, 49, 16)                      # child ends: only its private blocks return
+    assert pool.num_free() == 17
+    assert all(pool.refcount(int(i)) == 1 for i in parent[:3])
+    pool.free_table(parent, 41, 16)
+    assert pool.num_free() == 20
+
+
+def test_pool_copy_on_write_failure_changes_nothing(lib):
+    pool = pkv.BlockPool(4, seed=2)
+    a = torch.full((4,), -1, dtype=torch.int32)
+    pool.reserve(a, 0, 64, 16)                          # the whole pool
+    b = torch.full((4,), -1, dtype=torch.int32)
+    pool.fork(a, b, 64, 16)
+    before = b.clone()
+    with pytest.raises(pkv.PkvError) as e:
+        pool.prepare_append(b, 20, 16)                  # shared block, no free block to copy into
+    assert e.value.status == _lib.PKV_ERR_OUT_OF_BLOCKS
+    assert torch.equal(b, before) and all(pool.refcount(int(i)) == 2 for i in a)
+    with pytest.raises(pkv.PkvError):
+        pool.prepare_append(b, 64, 16)                  # beyond the table row
+    with pytest.raises(pkv.PkvError):
+        pool.fork(a, torch.full((2,), -1, dtype=torch.int32), 64, 16)   # row too short
+    stale = torch.tensor([0, 1, 2, 3], dtype=torch.int32)
+    pool.free_table(a, 64, 16)
+    pool.free_table(b, 64, 16)
+    with pytest.raises(pkv.PkvError):
+        pool.prepare_append(stale, 5, 16)               # block not allocated
+    assert pool.num_free() == 4
+
+
+def test_copy_on_write_flow_against_the_oracle(lib):
+    """Host pool + oracle copy and append: a forked request that diverges attends to its own
+    tokens, and its parent's output does not move."""
+    rng = np.random.default_rng(4)
+    hkv, hq, d, bs, ctx = 2, 4, 128, 16, 37
+    nb = 12
+    kpool = rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)
+    vpool = rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)
+    pool = pkv.BlockPool(nb, seed=1)
+    parent = torch.full((4,), -1, dtype=torch.int32)
+    pool.reserve(parent, 0, ctx, bs)
+    child = torch.full((4,), -1, dtype=torch.int32)
+    pool.fork(parent, child, ctx, bs)
+    q = np.repeat(rng.standard_normal((1, hq, d)).astype(np.float16), 2, axis=0)
+    bt = torch.stack([parent, child]).numpy()
+    before = oracle.decode(q, kpool, vpool, bt, np.array([ctx, ctx], np.int32), 0.1)
+    assert np.array_equal(before[0], before[1])
+    pair = pool.prepare_append(child, ctx, bs)
+    assert pair is not None
+    oracle.copy_blocks(kpool, vpool, [pair[0]], [pair[1]])
+    k_new = rng.standard_normal((1, hkv, d)).astype(np.float16)
+    v_new = rng.standard_normal((1, hkv, d)).astype(np.float16)
+    slot = int(child[ctx // bs]) * bs + ctx % bs
+    oracle.append(kpool, vpool, np.array([slot], np.int64), k_new, v_new)
+    bt = torch.stack([parent, child]).numpy()
+    after = oracle.decode(q, kpool, vpool, bt, np.array([ctx, ctx + 1], np.int32), 0.1)
+    assert np.array_equal(after[0], before[0])
+    assert not np.allclose(after[1], before[1])

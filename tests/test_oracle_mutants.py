@@ -32,6 +32,10 @@ MUTANTS = {
     "kv_bytes_missing_factor": ("return 2 * batch * L * H * D * S * elem_bytes;",
                                 "return batch * L * H * D * S * elem_bytes;"),
     "max_not_subtracted_in_l": ("        l += w;\n", "        l += w * w;\n"),
+    "copy_blocks_drops_v": ("            v_cache[(int64_t)dst[i] * per_block + e] = v_cache[(int64_t)src[i] * per_block + e];\n",
+                            ""),
+    "copy_blocks_one_head": ("int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;",
+                             "int64_t per_block = (int64_t)block_size * head_dim;"),
 }
 
 
