@@ -44,6 +44,8 @@ _f64p = ctypes.POINTER(ctypes.c_double)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
+_i8p = ctypes.POINTER(ctypes.c_int8)
+_f32p = ctypes.POINTER(ctypes.c_float)
 
 GCC_FLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c99", "-shared", "-fPIC"]
 
@@ -103,6 +105,13 @@ class Oracle:
                                                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int])
         lib.oracle_copy_blocks.restype = None
         lib.oracle_copy_blocks.argtypes = [_u16p, _u16p, _i32p, _i32p] + [ctypes.c_int] * 4
+        lib.oracle_quantize_k_row.restype = None
+        lib.oracle_quantize_k_row.argtypes = [_i8p, ctypes.POINTER(ctypes.c_float), _u16p, ctypes.c_int]
+        lib.oracle_append_quant_k.restype = None
+        lib.oracle_append_quant_k.argtypes = [_i8p, _f32p, _u16p, _i64p, _u16p, _u16p] + [ctypes.c_int] * 4
+        lib.oracle_decode_quant_k.restype = None
+        lib.oracle_decode_quant_k.argtypes = [_f64p, _u16p, _i8p, _f32p, _u16p, _i32p, _i32p] + \
+            [ctypes.c_int] * 6 + [ctypes.c_double]
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
         self.lib = lib
@@ -148,6 +157,43 @@ class Oracle:
         ds = np.ascontiguousarray(dst, dtype=np.int32)
         self.lib.oracle_copy_blocks(_p(kc, _u16p), _p(vc, _u16p), _p(sr, _i32p), _p(ds, _i32p), sr.shape[0], hkv,
                                     d, bs)
+
+    def quantize_k_row(self, k_row) -> tuple[np.ndarray, float]:
+        """(int8 codes [D], float32 scale) of one fp16 K row."""
+        kb = _bits(np.ascontiguousarray(k_row))
+        codes = np.empty(kb.shape[0], np.int8)
+        sc = ctypes.c_float(0.0)
+        self.lib.oracle_quantize_k_row(_p(codes, _i8p), ctypes.byref(sc), _p(kb, _u16p), kb.shape[0])
+        return codes, np.float32(sc.value)
+
+    def append_quant_k(self, k_codes: np.ndarray, k_scale: np.ndarray, v_cache: np.ndarray, slots, k_new,
+                       v_new) -> None:
+        """In place on k_codes (int8 [NB,Hkv,bs,D]), k_scale (float32 [NB,Hkv,bs]) and v_cache (fp16)."""
+        nb, hkv, bs, d = k_codes.shape
+        assert k_codes.dtype == np.int8 and k_codes.flags.c_contiguous
+        assert k_scale.dtype == np.float32 and k_scale.shape == (nb, hkv, bs) and k_scale.flags.c_contiguous
+        vc = _bits(v_cache)
+        assert np.shares_memory(vc, v_cache)
+        kn, vn = _bits(k_new), _bits(v_new)
+        sl = np.ascontiguousarray(slots, dtype=np.int64)
+        assert kn.shape == (sl.shape[0], hkv, d) and vn.shape == kn.shape
+        self.lib.oracle_append_quant_k(_p(k_codes, _i8p), _p(k_scale, _f32p), _p(vc, _u16p), _p(sl, _i64p),
+                                       _p(kn, _u16p), _p(vn, _u16p), sl.shape[0], hkv, d, bs)
+
+    def decode_quant_k(self, q, k_codes, k_scale, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
+        """float64 [B, Hq, D] decode over the int8-K / fp16-V cache (keys dequantised exactly)."""
+        qb, vc = _bits(q), _bits(v_cache)
+        kc = np.ascontiguousarray(k_codes, dtype=np.int8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        b, hq, d = qb.shape
+        nb, hkv, bs, d2 = kc.shape
+        assert d2 == d and hq % hkv == 0 and ks.shape == (nb, hkv, bs)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty((b, hq, d), np.float64)
+        self.lib.oracle_decode_quant_k(_p(out, _f64p), _p(qb, _u16p), _p(kc, _i8p), _p(ks, _f32p), _p(vc, _u16p),
+                                       _p(bt, _i32p), _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs, float(scale))
+        return out
 
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
         """float64 [B, Hq, D] attention output of one decode step."""
@@ -239,3 +285,15 @@ def merge(o_part, m_part, l_part, context_lens, partition_size):
 
 def copy_blocks(k_cache, v_cache, src, dst):
     return default().copy_blocks(k_cache, v_cache, src, dst)
+
+
+def quantize_k_row(k_row):
+    return default().quantize_k_row(k_row)
+
+
+def append_quant_k(k_codes, k_scale, v_cache, slots, k_new, v_new):
+    return default().append_quant_k(k_codes, k_scale, v_cache, slots, k_new, v_new)
+
+
+def decode_quant_k(q, k_codes, k_scale, v_cache, block_tables, context_lens, scale):
+    return default().decode_quant_k(q, k_codes, k_scale, v_cache, block_tables, context_lens, scale)

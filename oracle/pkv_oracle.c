@@ -36,6 +36,15 @@
  *     applied to consecutive token ranges, so merge(partition(x)) must equal
  *     decode(x).
  *
+ *   - Key-only int8 cache: the pages advise quantising K alone and keeping V
+ *     in full precision ("推理优化这件事，为什么值得反复复盘", sec. 4.4; the
+ *     int8 halving of cache memory also in "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ *     sec. 4.2).  They give no scheme; the reading taken is symmetric int8 with
+ *     one float32 scale per (token, kv head): s = max_d |k_d| / 127 and
+ *     code_d = round-half-even(k_d / s), both in float32, so that the integer
+ *     decision is taken in the precision the kernels use; an all-zero row has
+ *     s = 0 and zero codes.  Attention then uses k_d = code_d * s exactly.
+ *
  * fp16 values are carried as raw uint16 bit patterns and decoded to double by
  * the IEEE-754 binary16 definition (sign, 5-bit exponent with bias 15, 10-bit
  * fraction, subnormals, inf/nan) in oracle_half_to_double.
@@ -208,6 +217,96 @@ void oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache, cons
                          block_size, scale);
             softmax_weighted_sum(o, &m, &l, s, v_cache, bt_row, 0, ctx, j, num_kv_heads,
                                  head_dim, block_size);
+        }
+        free(s);
+    }
+}
+
+/* Symmetric int8 quantisation of one K row of D binary16 values, in float32:
+ * scale = max |k| / 127, code_d = round-half-even(k_d / scale) in [-127, 127].
+ * The float32 division and rintf (round to nearest even in the default mode)
+ * are the IEEE-754 operations; an all-zero row gives scale 0 and zero codes. */
+void oracle_quantize_k_row(int8_t *codes, float *scale, const uint16_t *k_row, int D)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf((float)oracle_half_to_double(k_row[d]));
+        if (a > amax)
+            amax = a;
+    }
+    float s = amax / 127.0f;
+    *scale = s;
+    for (int d = 0; d < D; ++d) {
+        if (s == 0.0f) {
+            codes[d] = 0;
+            continue;
+        }
+        float r = rintf((float)oracle_half_to_double(k_row[d]) / s);
+        if (r > 127.0f)
+            r = 127.0f;
+        if (r < -127.0f)
+            r = -127.0f;
+        codes[d] = (int8_t)r;
+    }
+}
+
+/* Append into the K-int8 / V-fp16 cache: for each token t with a slot >= 0 and
+ * each kv head j, k_codes[slot][j] and k_scale[slot][j] receive the quantised
+ * K row and v_cache[slot][j] the raw V row.  Layouts: k_codes int8 and v_cache
+ * fp16 [num_blocks][num_kv_heads][block_size][head_dim], k_scale float32
+ * [num_blocks][num_kv_heads][block_size]. */
+void oracle_append_quant_k(int8_t *k_codes, float *k_scale, uint16_t *v_cache, const int64_t *slot_mapping,
+                           const uint16_t *k_new, const uint16_t *v_new, int num_tokens,
+                           int num_kv_heads, int head_dim, int block_size)
+{
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t blk = slot / block_size;
+        int off = (int)(slot % block_size);
+        for (int j = 0; j < num_kv_heads; ++j) {
+            int64_t row = (blk * num_kv_heads + j) * block_size + off;
+            const uint16_t *src = k_new + ((int64_t)t * num_kv_heads + j) * head_dim;
+            oracle_quantize_k_row(k_codes + row * head_dim, k_scale + row, src, head_dim);
+            for (int d = 0; d < head_dim; ++d)
+                v_cache[row * head_dim + d] = v_new[((int64_t)t * num_kv_heads + j) * head_dim + d];
+        }
+    }
+}
+
+/* Decode attention over the K-int8 / V-fp16 cache: the plain definition with
+ * every key dequantised, k_d = code_d * scale (float64), and V as stored.  Same
+ * shapes, table and context rules as oracle_decode. */
+void oracle_decode_quant_k(double *out, const uint16_t *q, const int8_t *k_codes, const float *k_scale,
+                           const uint16_t *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                           int num_seqs, int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, double scale)
+{
+    int group = num_q_heads / num_kv_heads;
+    for (int b = 0; b < num_seqs; ++b) {
+        int ctx = context_lens[b];
+        const int32_t *bt_row = block_tables + (int64_t)b * max_blocks_per_seq;
+        double *s = (double *)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+        for (int h = 0; h < num_q_heads; ++h) {
+            int kvh = h / group;
+            double *o = out + ((int64_t)b * num_q_heads + h) * head_dim;
+            if (ctx <= 0) {
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                continue;
+            }
+            const uint16_t *q_row = q + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int p = 0; p < ctx; ++p) {
+                int64_t row = ((int64_t)bt_row[p / block_size] * num_kv_heads + kvh) * block_size + p % block_size;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += oracle_half_to_double(q_row[d]) * ((double)k_codes[row * head_dim + d] * k_scale[row]);
+                s[p] = scale * dot;
+            }
+            double m, l;
+            softmax_weighted_sum(o, &m, &l, s, v_cache, bt_row, 0, ctx, kvh, num_kv_heads, head_dim,
+                                 block_size);
         }
         free(s);
     }

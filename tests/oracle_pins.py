@@ -159,6 +159,91 @@ def pin_copy_on_write_keeps_attention(orc):
     assert np.abs(out[1] - ref[0]).max() < 1e-12
 
 
+def pin_quantize_golden(orc):
+    g = golden("quantize_k_rows.json")
+    for row in g["rows"]:
+        codes, sc = orc.quantize_k_row(np.array(row["k"], np.float16))
+        assert sc == np.float32(row["scale"]), (row["note"], sc)
+        assert codes.tolist() == row["codes"], (row["note"], codes)
+
+
+def pin_quantize_properties(orc):
+    """On random rows: every code in [-127, 127], the largest |k| maps to +-127, the rounding
+    error is at most half a step (plus the float32 quotient's rounding), and doubling the row
+    doubles the scale and keeps the codes."""
+    rng = np.random.default_rng(5)
+    for i in range(50):
+        k = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 2)).astype(np.float16)
+        codes, sc = orc.quantize_k_row(k)
+        kd = k.astype(np.float64)
+        assert np.abs(codes.astype(np.int32)).max() == 127
+        assert codes[np.argmax(np.abs(kd))] == (127 if kd[np.argmax(np.abs(kd))] > 0 else -127)
+        assert np.all(np.abs(kd - codes * np.float64(sc)) <= np.float64(sc) * (0.5 + 1e-5))
+        codes2, sc2 = orc.quantize_k_row((k.astype(np.float32) * 2).astype(np.float16))
+        assert sc2 == 2 * sc and np.array_equal(codes2, codes)
+
+
+def pin_append_quant_k(orc):
+    """The int8 append stores, per (token, kv head), the quantiser's codes and scale, and V bit
+    for bit as the fp16 append does; negative slots write nothing."""
+    rng = np.random.default_rng(6)
+    nb, hkv, bs, d, t = 5, 3, 4, 16, 6
+    codes = np.zeros((nb, hkv, bs, d), np.int8)
+    scales = np.full((nb, hkv, bs), -1.0, np.float32)
+    vq = np.zeros((nb, hkv, bs, d), np.float16)
+    vref = vq.copy()
+    kref = vq.copy()
+    slots = np.array([7, -1, 0, 19, 12, -5], np.int64)
+    kn = rng.standard_normal((t, hkv, d)).astype(np.float16)
+    vn = rng.standard_normal((t, hkv, d)).astype(np.float16)
+    orc.append_quant_k(codes, scales, vq, slots, kn, vn)
+    orc.append(kref, vref, slots, kn, vn)
+    assert np.array_equal(vq.view(np.uint16), vref.view(np.uint16))
+    for ti, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        for j in range(hkv):
+            c, sc = orc.quantize_k_row(kn[ti, j])
+            assert np.array_equal(codes[sl // bs, j, sl % bs], c) and scales[sl // bs, j, sl % bs] == sc
+    written = np.zeros((nb, bs), bool)
+    for sl in slots[slots >= 0]:
+        written[sl // bs, sl % bs] = True
+    assert np.all(scales.transpose(0, 2, 1)[~written] == -1.0)
+    assert not codes.transpose(0, 2, 1, 3)[~written].any()
+
+
+def pin_decode_quant_k(orc):
+    """With scales that are powers of two the dequantised keys are exact fp16 values: decode over
+    the int8 cache must equal decode over that fp16 cache; with arbitrary scales it must equal a
+    textbook contiguous attention over the dequantised keys."""
+    rng = np.random.default_rng(8)
+    hq, hkv, d, bs = 4, 2, 32, 4
+    ctxs = [9, 1, 0, 16]
+    nb = 20
+    codes = rng.integers(-127, 128, size=(nb, hkv, bs, d)).astype(np.int8)
+    scales = (2.0 ** rng.integers(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    v = rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)
+    bt = rng.permutation(nb)[:16].reshape(4, 4).astype(np.int32)
+    q = rng.standard_normal((4, hq, d)).astype(np.float16)
+    ctx = np.array(ctxs, np.int32)
+    kf16 = (codes.astype(np.float64) * scales[..., None]).astype(np.float16)
+    assert np.array_equal(kf16.astype(np.float64), codes.astype(np.float64) * scales[..., None])
+    got = orc.decode_quant_k(q, codes, scales, v, bt, ctx, 0.3)
+    ref = orc.decode(q, kf16, v, bt, ctx, 0.3)
+    assert np.abs(got - ref).max() <= 1e-15
+    scales = rng.uniform(1e-3, 5e-2, size=(nb, hkv, bs)).astype(np.float32)
+    got = orc.decode_quant_k(q, codes, scales, v, bt, ctx, 0.3)
+    kdq = codes.astype(np.float64) * scales[..., None].astype(np.float64)
+    ks, vs = [], []
+    for b, c in enumerate(ctxs):
+        rows_k = [kdq[bt[b, p // bs], :, p % bs] for p in range(c)]
+        rows_v = [v[bt[b, p // bs], :, p % bs] for p in range(c)]
+        ks.append(np.stack(rows_k, 1) if c else np.zeros((hkv, 0, d)))
+        vs.append(np.stack(rows_v, 1) if c else np.zeros((hkv, 0, d), np.float16))
+    ref = textbook_attention(q, ks, vs, 0.3)
+    assert np.abs(got - ref).max() <= 1e-12
+
+
 def pin_slot_mapping_by_enumeration(orc):
     """Walk every block table in order, naming each pool slot by the (request, position)
     stored there; the slot mapping must be the inverse of that enumeration."""
@@ -361,6 +446,10 @@ ALL_PINS = [
     pin_append_golden,
     pin_copy_blocks_golden,
     pin_copy_on_write_keeps_attention,
+    pin_quantize_golden,
+    pin_quantize_properties,
+    pin_append_quant_k,
+    pin_decode_quant_k,
     pin_slot_mapping_by_enumeration,
     pin_two_keys_golden,
     pin_textbook_contiguous,

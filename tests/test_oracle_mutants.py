@@ -24,7 +24,8 @@ MUTANTS = {
     "half_exponent_bias": ("expo - 25", "expo - 24"),
     "merge_drops_l": ("double w = l_part[row0 + p] * exp(m_part[row0 + p] - M);",
                       "double w = exp(m_part[row0 + p] - M);"),
-    "append_offset": ("int off = (int)(slot % block_size);", "int off = (int)(slot / block_size) % block_size;"),
+    "append_offset": ("int off = (int)(slot % block_size);\n        for (int j = 0; j < num_kv_heads; ++j) {\n            for",
+                      "int off = (int)(slot / block_size) % block_size;\n        for (int j = 0; j < num_kv_heads; ++j) {\n            for"),
     "append_kv_swapped": ("k_cache[dst] = k_new[src];\n                v_cache[dst] = v_new[src];",
                           "k_cache[dst] = k_new[src];\n                v_cache[dst] = k_new[src];"),
     "slot_uses_next_block": ("block_tables[(int64_t)b * max_blocks_per_seq + pos / block_size]",
@@ -34,6 +35,12 @@ MUTANTS = {
     "max_not_subtracted_in_l": ("        l += w;\n", "        l += w * w;\n"),
     "copy_blocks_drops_v": ("            v_cache[(int64_t)dst[i] * per_block + e] = v_cache[(int64_t)src[i] * per_block + e];\n",
                             ""),
+    "quant_truncates": ("float r = rintf(", "float r = truncf("),
+    "quant_step_128": ("float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    "dequant_drops_scale": ("((double)k_codes[row * head_dim + d] * k_scale[row])",
+                            "((double)k_codes[row * head_dim + d])"),
+    "quant_append_head_zero": ("int64_t row = (blk * num_kv_heads + j) * block_size + off;",
+                               "int64_t row = (blk * num_kv_heads) * block_size + off;"),
     "copy_blocks_one_head": ("int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;",
                              "int64_t per_block = (int64_t)block_size * head_dim;"),
 }
