@@ -200,12 +200,15 @@ def make_layer(workload: str, layer: int, bs: int, device, step: int = 1):
     raise ValueError(workload)
 
 
-def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tokens=0, num_seqs=None):
+def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tokens=0, num_seqs=None,
+                 kv="fp16"):
     """Algorithmic bytes of one decode-attention call: K and V of every cached token read once
-    (a shared prefix once), q read, out written, block-table entries and context lengths read."""
+    (a shared prefix once), q read, out written, block-table entries and context lengths read.
+    kv="int8k": a key row is head_dim int8 codes plus one float32 scale."""
     b = len(ctx) if num_seqs is None else num_seqs
     tokens = sum(ctx) - unique_prefix_tokens * (b - 1) if unique_prefix_tokens else sum(ctx)
-    kv = 2 * tokens * num_kv_heads * head_dim * 2
+    k_row = head_dim + 4 if kv == "int8k" else head_dim * 2
+    kv = tokens * num_kv_heads * (k_row + head_dim * 2)
     qo = 2 * b * num_q_heads * head_dim * 2
     tables = sum(-(-c // bs) for c in ctx) * 4 + 4 * b
     return kv + qo + tables
@@ -235,6 +238,24 @@ def run_ours(args):
     # per-layer caches (distinct, like a real model) and per-layer new-token inputs in one block
     cases = [make_layer(args.workload, l, bs, dev) for l in range(n_layers)]
     c0 = cases[0]
+    cpu_sample = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # host copies taken before any of our kernels run
+        cpu_sample = {k: getattr(c0, k).cpu().numpy() for k in
+                      ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
+    int8k = args.kv == "int8k"
+    if int8k:
+        # int8-key cache per layer: every pool row of the generated fp16 keys quantised by the library's own
+        # append kernel (set-up, outside the timed regions); V stays as generated
+        for c in cases:
+            nb_, hkv_, bs_, d_ = c.k_cache.shape
+            c.k_codes, c.k_scale, _ = pkv.empty_int8k_cache(nb_, hkv_, bs_, dev)
+            rows_k = c.k_cache.permute(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_).contiguous()
+            rows_v = c.v_cache.permute(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_).contiguous()
+            pkv.append_int8k(c.k_codes, c.k_scale, c.v_cache, torch.arange(nb_ * bs_, device=dev), rows_k, rows_v)
+            del rows_k, rows_v
+            c.k_cache = None
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
     B, Hq, Hkv, D = c0.num_seqs, c0.num_q_heads, c0.num_kv_heads, c0.head_dim
     bs = c0.block_size
     q_all = torch.stack([c.q for c in cases])
@@ -264,7 +285,15 @@ def run_ours(args):
     def decode(l, c):
         """One layer of the step: the append is fused into the decode kernel (pkv_decode_step) unless
         --separate-append asks for the two-call path (pkv_append + attention)."""
-        if args.separate_append:
+        if int8k:
+            if args.separate_append:
+                pkv.append_int8k(c.k_codes, c.k_scale, c.v_cache, slot_cur, c.k_new, c.v_new)
+                pkv.decode_attention_int8k(out_all[l], c.q, c.k_codes, c.k_scale, c.v_cache, block_tables, ctx_cur,
+                                           c.scale, workspace=ws)
+            else:
+                pkv.decode_step_int8k(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_cache,
+                                      block_tables, ctx_cur, c.scale, workspace=ws)
+        elif args.separate_append:
             pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
             if cascade:
                 pkv.decode_attention_shared_prefix(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur,
@@ -277,8 +306,8 @@ def run_ours(args):
                             prefix_len, ws)
 
     prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
-    bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens) for c in ctx_steps]
-    logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs) for c in ctx_steps]
+    bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens, kv=args.kv) for c in ctx_steps]
+    logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, kv=args.kv) for c in ctx_steps]
 
     # per layer: the decode kernel (append and the split's merge fused in), plus the prefix kernel with the
     # cascade, plus the append kernel on the two-call path
@@ -294,12 +323,6 @@ def run_ours(args):
             ctx_cur.copy_(ctx_dev[j], non_blocking=True)
             slot_cur.copy_(slot_dev[j], non_blocking=True)
         return j
-
-    # CPU baseline inputs: host copies of layer 0 taken before any of our kernels run
-    cpu_sample = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_sample = {k: getattr(c0, k).cpu().numpy() for k in
-                      ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
@@ -428,7 +451,7 @@ def run_ours(args):
     peak, peak_src = read_peaks()
     gbs = bytes_job / (ms_job * 1e-3) / 1e9
     achieved = kernel_bytes_avg / (kernel_avg_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload, bs)
+    traffic = read_traffic(args.workload + ("/int8k" if int8k else ""), bs)
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -440,7 +463,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        "dtype": "i8 keys (f32 row scales), f16 values" if int8k else "f16",
         "accumulate": "f32",
         "data": "synthetic (seeded N(0,1) fp16 K/V/q, seeded block permutation)",
         "config": {
@@ -452,10 +475,12 @@ def run_ours(args):
             "head_dim": D,
             "block_size": bs,
             "partition_size": pkv.PKV_DEFAULT_PARTITION,
+            "kv_cache": "int8 keys + float32 scale per (token, kv head), fp16 values" if int8k else "fp16 K and V",
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
-                  % (cases[0].k_cache.numel() * 4 / 1e6, bytes_job / 1e9),
+                  % (cases[0].v_cache.numel() * (3 if int8k else 4) / 1e6, bytes_job / 1e9),
             "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
-            "decode_call": ("pkv_append + " if args.separate_append else "pkv_decode_step ")
+            "decode_call": ("pkv_append" + ("_int8k" if int8k else "") + " + " if args.separate_append
+                            else "pkv_decode_step" + ("_int8k" if int8k else "") + " ")
             + ("shared prefix 1024 tokens" if cascade else ""),
         },
         "tokens_per_s": round(B * world / (ms_job * 1e-3), 1),
@@ -491,13 +516,28 @@ def run_ours(args):
         "gpu": torch.cuda.get_device_name(dev),
     }
     if cpu_sample is not None:
-        line["cpu_baseline"] = cpu_baseline(cpu_sample, c0, bs, Hkv, Hq, D, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(cpu_sample, c0, bs, Hkv, Hq, D, budget_s=args.cpu_budget, kv=args.kv)
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None):
+def oracle_int8k_pool(h):
+    """Host int8-key pool (codes, scales) of the sample's fp16 keys, quantised by the oracle."""
+    import numpy as np
+
+    import oracle
+    nb, hkv, bs, d = h["k_cache"].shape
+    codes = np.zeros((nb, hkv, bs, d), np.int8)
+    scales = np.zeros((nb, hkv, bs), np.float32)
+    v = h["v_cache"].copy()
+    rows = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    oracle.append_quant_k(codes, scales, v, np.arange(nb * bs, dtype=np.int64), rows(h["k_cache"]),
+                          rows(h["v_cache"]))
+    return codes, scales
+
+
+def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None, kv="fp16"):
     """The oracle (single-threaded C, float64) on a bounded sample of the workload: one layer's
     append + decode for as many requests (in order) as fit the time budget."""
     import numpy as np
@@ -506,17 +546,24 @@ def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None):
     ctx = h["context_lens"].tolist()
     b = len(ctx)
     slots = oracle.slot_mapping(h["block_tables"], h["positions"], bs)
-    t0 = time.perf_counter()
-    oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"], h["v_new"])
+    if kv == "int8k":
+        codes, scales = oracle_int8k_pool(h)
+        t0 = time.perf_counter()
+        oracle.append_quant_k(codes, scales, h["v_cache"], slots, h["k_new"], h["v_new"])
+        decode_one = lambda sl: oracle.decode_quant_k(h["q"][sl], codes, scales, h["v_cache"], h["block_tables"][sl],
+                                                      h["context_lens"][sl], case.scale)
+    else:
+        t0 = time.perf_counter()
+        oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"], h["v_new"])
+        decode_one = lambda sl: oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl],
+                                              h["context_lens"][sl], case.scale)
     done, nbytes, tokens = 0, 0, 0
     limit = b if max_requests is None else min(b, max_requests)
     # requests of layer 0 in order, cycling, until the time budget is spent (at least one pass)
     while done < limit or time.perf_counter() - t0 < budget_s:
         i = done % b
-        sl = slice(i, i + 1)
-        oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl], h["context_lens"][sl],
-                      case.scale)
-        nbytes += decode_bytes(ctx[i:i + 1], hkv, hq, d, bs)
+        decode_one(slice(i, i + 1))
+        nbytes += decode_bytes(ctx[i:i + 1], hkv, hq, d, bs, kv=kv)
         tokens += ctx[i]
         done += 1
         if max_requests is not None and done >= limit:
@@ -571,10 +618,18 @@ def run_reference(args):
     sl = slice(0, n_req)
     slots = oracle.slot_mapping(h["block_tables"][sl], h["positions"][sl], bs)
 
-    def one():
-        oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"][sl], h["v_new"][sl])
-        oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl], h["context_lens"][sl],
-                      case.scale)
+    if args.kv == "int8k":
+        codes, scales = oracle_int8k_pool(h)
+
+        def one():
+            oracle.append_quant_k(codes, scales, h["v_cache"], slots, h["k_new"][sl], h["v_new"][sl])
+            oracle.decode_quant_k(h["q"][sl], codes, scales, h["v_cache"], h["block_tables"][sl],
+                                  h["context_lens"][sl], case.scale)
+    else:
+        def one():
+            oracle.append(h["k_cache"], h["v_cache"], slots, h["k_new"][sl], h["v_new"][sl])
+            oracle.decode(h["q"][sl], h["k_cache"], h["v_cache"], h["block_tables"][sl], h["context_lens"][sl],
+                          case.scale)
 
     for _ in range(args.warmup):
         one()
@@ -582,7 +637,7 @@ def run_reference(args):
     for _ in range(args.steps):
         one()
     dt = time.perf_counter() - t0
-    nbytes = decode_bytes(ctx[:n_req], case.num_kv_heads, case.num_q_heads, case.head_dim, bs)
+    nbytes = decode_bytes(ctx[:n_req], case.num_kv_heads, case.num_q_heads, case.head_dim, bs, kv=args.kv)
     value = nbytes * args.steps / dt / 1e9
     sample = (f"per step: layer 0, append + decode of {n_req} of {b} requests ({sum(ctx[:n_req])} cached tokens), "
               f"single-threaded C float64")
@@ -600,7 +655,9 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) fp16 K/V/q, seeded block permutation)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload].format(bs=bs), "block_size": bs},
+        "config": {"workload": WORKLOAD_TEXT[args.workload].format(bs=bs), "block_size": bs,
+                   "kv_cache": "int8 keys + float32 scale per (token, kv head), fp16 values" if args.kv == "int8k"
+                   else "fp16 K and V"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -621,11 +678,15 @@ def main(argv=None):
     ap.add_argument("--no-cascade", action="store_true", help="shared_prefix: plain decode instead of the cascade")
     ap.add_argument("--separate-append", action="store_true",
                     help="two calls per layer (pkv_append, then attention) instead of pkv_decode_step")
+    ap.add_argument("--kv", choices=["fp16", "int8k"], default="fp16",
+                    help="cache format: fp16 K/V, or int8 keys with float32 row scales and fp16 values")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.kv == "int8k" and args.workload == "shared_prefix" and not args.no_cascade:
+        ap.error("the shared-prefix cascade reads fp16 keys; use --no-cascade with --kv int8k")
     if args.impl == "reference":
         run_reference(args)
     else:

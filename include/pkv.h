@@ -305,6 +305,51 @@ PKV_API int pkv_decode_step(void *out, const void *q, const void *k_new, const v
                             int64_t num_blocks, float scale, int prefix_len, void *workspace,
                             size_t workspace_bytes, pkv_stream_t stream);
 
+/* ---- int8 key cache ------------------------------------------------------
+ * Keys stored as int8 codes with one float32 scale per (block, kv head, slot);
+ * values stay fp16.  The pages report that int8 halves cache memory but that
+ * quality suffers on long sequences, and advise quantising only the keys
+ * ("推理优化这件事，为什么值得反复复盘", sec. 4.4; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 4.2).  Scheme (the pages give none): per key row of 128 dims,
+ *   scale = max_d |k_d| / 127           (float32, IEEE division)
+ *   code_d = round-half-even(k_d / scale), in [-127, 127]   (float32 quotient)
+ * and an all-zero row stores scale 0 and zero codes.  Attention uses
+ * k_d = code_d * scale.  Layouts:
+ *   k_codes : int8 [num_blocks][num_kv_heads][block_size][128], 16-byte aligned
+ *   k_scale : float32 [num_blocks][num_kv_heads][block_size], 16-byte aligned
+ *   v_cache : fp16 [num_blocks][num_kv_heads][block_size][128] as for pkv_append.
+ * Per cached token and kv head this reads 128 + 4 + 256 bytes instead of 512. */
+
+/* Append into the int8-key cache: for each token t with slot_mapping[t] >= 0,
+ * quantise k_new[t][j] into k_codes/k_scale at that slot and copy v_new[t][j]
+ * into v_cache.  Argument rules, skips and errors as pkv_append (k_new/v_new
+ * 8-byte aligned).  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+PKV_API int pkv_append_int8k(void *k_codes, float *k_scale, void *v_cache, const int64_t *slot_mapping,
+                             const void *k_new, const void *v_new, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, pkv_stream_t stream);
+
+/* pkv_decode_attention over the int8-key cache: the same result definition with
+ * every key dequantised, the same shapes, workspace (pkv_decode_workspace_size)
+ * and error rules.  Any group size 1, 2, 4 or 8 runs on the tensor cores. */
+PKV_API int pkv_decode_attention_int8k(void *out, const void *q, const void *k_codes, const float *k_scale,
+                                       const void *v_cache, const int32_t *block_tables,
+                                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                       int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                       pkv_stream_t stream);
+
+/* pkv_decode_step over the int8-key cache: the new token's key is quantised and
+ * written (codes and scale) with its value by the decode kernel itself, then
+ * attended.  Same as pkv_append_int8k at positions ctx - 1 followed by
+ * pkv_decode_attention_int8k.  No shared-prefix form.  Workspace as
+ * pkv_decode_attention_int8k.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+PKV_API int pkv_decode_step_int8k(void *out, const void *q, const void *k_new, const void *v_new, void *k_codes,
+                                  float *k_scale, void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                  pkv_stream_t stream);
+
 /* Split-context partial attention.  Partition p of request b covers logical
  * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each
  * such partition and query head h it writes

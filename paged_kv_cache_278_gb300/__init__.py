@@ -28,7 +28,8 @@ from ._lib import (PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONT
 __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
     "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
-    "decode_step", "make_step_workspace", "copy_blocks",
+    "decode_step", "make_step_workspace", "copy_blocks", "append_int8k", "decode_attention_int8k",
+    "decode_step_int8k", "empty_int8k_cache",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -243,6 +244,94 @@ def device_error(device=None, stream=None) -> int:
         st = _L().pkv_get_device_error(_stream(dev, stream), ctypes.byref(code))
     _lib.check(st, "pkv_get_device_error")
     return code.value
+
+
+# ---------------------------------------------------------------- int8 key cache
+
+def _int8k_shape(k_codes, k_scale, v_cache):
+    _need(k_codes, "k_codes", torch.int8, 4)
+    dev = k_codes.device
+    _need(k_scale, "k_scale", torch.float32, 3, dev)
+    _need(v_cache, "v_cache", torch.float16, 4, dev)
+    if k_codes.shape != v_cache.shape or k_scale.shape != k_codes.shape[:3]:
+        raise ValueError("k_codes [NB,Hkv,bs,D], k_scale [NB,Hkv,bs] and v_cache [NB,Hkv,bs,D] disagree")
+    return tuple(k_codes.shape)
+
+
+def empty_int8k_cache(num_blocks: int, num_kv_heads: int, block_size: int, device,
+                      head_dim: int = PKV_HEAD_DIM):
+    """Zero-filled (k_codes int8, k_scale float32, v_cache fp16) for the int8-key cache."""
+    return (torch.zeros((num_blocks, num_kv_heads, block_size, head_dim), dtype=torch.int8, device=device),
+            torch.zeros((num_blocks, num_kv_heads, block_size), dtype=torch.float32, device=device),
+            torch.zeros((num_blocks, num_kv_heads, block_size, head_dim), dtype=torch.float16, device=device))
+
+
+def append_int8k(k_codes: torch.Tensor, k_scale: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Quantise k_new [T, Hkv, D] into k_codes/k_scale and copy v_new into v_cache at slot_mapping [T]."""
+    nb, hkv, bs, d = _int8k_shape(k_codes, k_scale, v_cache)
+    dev = k_codes.device
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    t = slot_mapping.shape[0]
+    if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
+    st = _L().pkv_append_int8k(k_codes.data_ptr(), k_scale.data_ptr(), v_cache.data_ptr(), slot_mapping.data_ptr(),
+                               k_new.data_ptr(), v_new.data_ptr(), t, hkv, d, bs, nb, _stream(dev, stream))
+    _lib.check(st, "pkv_append_int8k")
+
+
+def _int8k_decode_inputs(q, k_codes, k_scale, v_cache, block_tables, context_lens, out, workspace):
+    nb, hkv, bs, d = _int8k_shape(k_codes, k_scale, v_cache)
+    dev = k_codes.device
+    _need(q, "q", torch.float16, 3, dev)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    b, hq, dq = q.shape
+    if dq != d or out.shape != q.shape:
+        raise ValueError("q / out shapes disagree with the cache")
+    if block_tables.shape[0] != b or context_lens.shape[0] != b:
+        raise ValueError("block_tables / context_lens batch differs from q")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    return nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes
+
+
+def decode_attention_int8k(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor, k_scale: torch.Tensor,
+                           v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """decode_attention over the int8-key cache (keys dequantised as code * row scale)."""
+    nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes = _int8k_decode_inputs(q, k_codes, k_scale, v_cache, block_tables,
+                                                                        context_lens, out, workspace)
+    st = _L().pkv_decode_attention_int8k(out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), k_scale.data_ptr(),
+                                         v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), b,
+                                         block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), ws_ptr, ws_bytes,
+                                         _stream(dev, stream))
+    _lib.check(st, "pkv_decode_attention_int8k")
+    return out
+
+
+def decode_step_int8k(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_codes: torch.Tensor, k_scale: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """decode_step over the int8-key cache: quantise + write the new token at ctx - 1, then attend."""
+    nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes = _int8k_decode_inputs(q, k_codes, k_scale, v_cache, block_tables,
+                                                                        context_lens, out, workspace)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    if k_new.shape != (b, hkv, d) or v_new.shape != (b, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{b}, {hkv}, {d}]")
+    st = _L().pkv_decode_step_int8k(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                    k_codes.data_ptr(), k_scale.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                    context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb, float(scale),
+                                    ws_ptr, ws_bytes, _stream(dev, stream))
+    _lib.check(st, "pkv_decode_step_int8k")
+    return out
 
 
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,

@@ -53,6 +53,12 @@ SIGNATURES = {
     "pkv_pool_prepare_append": (c_int, [c_void_p, c_i32p, c_int, c_int, c_int, c_i32p, c_i32p,
                                         ctypes.POINTER(c_int)]),
     "pkv_pool_free_table": (c_int, [c_void_p, c_i32p, c_int, c_int]),
+    "pkv_append_int8k": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                 c_int, c_int64, c_void_p]),
+    "pkv_decode_attention_int8k": (c_int, [c_void_p] * 7 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
+                                                                           c_void_p]),
+    "pkv_decode_step_int8k": (c_int, [c_void_p] * 9 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
+                                                                      c_void_p]),
     "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
     "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,

@@ -108,8 +108,10 @@ struct DecodeParams {
     const __half *v_new;
     __half *k_cache_w;        // writable views of the caches for that append
     __half *v_cache_w;
+    const float *k_scale;     // int8 key cache: float32 scale per (block, kv head, slot); null for fp16 keys
+    float *k_scale_w;         // writable view of k_scale for the fused append
     CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
-    CUtensorMap tmap_v;       //   16 x 64 boxes, 128-byte swizzle
+    CUtensorMap tmap_v;       //   16 x 64 boxes, 128-byte swizzle (int8 keys: 16 x 128-byte boxes)
 };
 
 constexpr int kMergeTile = 512;  // partitions whose weights the fused merge stages at a time
@@ -117,14 +119,19 @@ constexpr int kMergeTile = 512;  // partitions whose weights the fused merge sta
 // Shared-memory carve-up (bytes), identical on host and device.  TC selects the tensor-core
 // engine's fp16 P buffer; its K/V tiles are two 2 KB halves (dims 0-63, 64-127) of 16 rows x
 // 128 B in the tensor copies' 128-byte swizzle (16-byte chunk c of row r stored at c ^ (r % 8)).
+// KQ (int8 keys): the K tile is one 2 KB box of 16 int8 rows in the same swizzle, and each stage
+// also holds the chunk's 16 float32 key scales.
 constexpr int kHalfTile = kChunk * 128;
-template <bool TC>
+template <bool TC, bool KQ = false>
 struct SmemLayout {
     static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
+    static constexpr int k_tile = KQ ? kChunk * kD : tile;
+    static constexpr int stage = k_tile + tile;
     static constexpr int stages = 0;
-    static constexpr int stage_bytes = kWarps * kStages * 2 * tile;
-    static constexpr int bars = stages + stage_bytes;
+    static constexpr int stage_bytes = kWarps * kStages * stage;
+    static constexpr int scales = stages + stage_bytes;
+    static constexpr int bars = scales + (KQ ? kWarps * kStages * kChunk * 4 : 0);
     static constexpr int probs = bars + kWarps * kStages * 8;
     __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? 2 * 8 * kChunk * 2 : kChunk * g * 4; }
     __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
@@ -148,7 +155,7 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
     constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
     constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
     static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
-    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout<false>::stage_bytes,
+    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout<true, true>::stage_bytes,
                   "merge staging must fit the stages");
     float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][kMergeTile]
     float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
@@ -342,7 +349,7 @@ struct FmaEngine {
         }
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, int valid, int lane,
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
                                           unsigned char *scratch) {
         float *s_prob = reinterpret_cast<float *>(scratch);
         // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
@@ -504,7 +511,7 @@ struct FmaEngine {
 // of the fragments; lanes whose heads are >= G carry padding columns.
 template <int G>
 struct TcEngine {
-    static_assert(G == 4 || G == 8, "tensor-core engine packs 4 or 8 heads into the 8 MMA columns");
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "up to 8 heads in the 8 MMA columns");
 
     // Byte offset of 16-byte chunk `c16` (0..15 across the 128 dims) of row r in a swizzled tile.
     __device__ __forceinline__ static uint32_t swz(int r, int c16) {
@@ -516,6 +523,14 @@ struct TcEngine {
     float m_ref[2], top[2], l_part[2];
     float q_scale;
 
+    __device__ __forceinline__ void reset(const DecodeParams &P) {
+#pragma unroll
+        for (int mt = 0; mt < kD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m_ref[0] = m_ref[1] = top[0] = top[1] = -INFINITY;
+        l_part[0] = l_part[1] = 0.f;
+        q_scale = P.q_scale;
+    }
+
     __device__ __forceinline__ void init(const DecodeParams &P, int b, int kvh, int lane) {
         const int head = lane >> 2;
         const __half *qrow =
@@ -526,14 +541,10 @@ struct TcEngine {
             for (int j = 0; j < 2; ++j)
                 qb[ks][j] = head < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + (lane & 3) * 2 + j * 8))
                                      : 0u;
-#pragma unroll
-        for (int mt = 0; mt < kD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-        m_ref[0] = m_ref[1] = top[0] = top[1] = -INFINITY;
-        l_part[0] = l_part[1] = 0.f;
-        q_scale = P.q_scale;
+        reset(P);
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, int valid, int lane,
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
                                           unsigned char *scratch) {
         float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -547,6 +558,13 @@ struct TcEngine {
         s[1] = g < valid ? s[1] * q_scale : -INFINITY;
         s[2] = g + 8 < valid ? s[2] * q_scale : -INFINITY;
         s[3] = g + 8 < valid ? s[3] * q_scale : -INFINITY;
+        softmax_pv(s, v_tile, lane, scratch);
+    }
+
+    // Online softmax of the chunk's scaled, masked log2-domain scores s (token g / g + 8, heads
+    // h0 / h0 + 1) and the P.V product into the O^T accumulators.
+    __device__ __forceinline__ void softmax_pv(float (&s)[4], uint32_t v_tile, int lane, unsigned char *scratch) {
+        const int g = lane >> 2;
         float cm0 = fmaxf(s[0], s[2]), cm1 = fmaxf(s[1], s[3]);
 #pragma unroll
         for (int sh = 4; sh <= 16; sh <<= 1) {
@@ -635,16 +653,69 @@ struct TcEngine {
     }
 };
 
-template <int G, int LPT, bool TC>
-using EngineFor = typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type;
+// ---------------------------------------------------------------- int8-key tensor-core engine
+// Same products as TcEngine with K stored as int8 codes (one float32 scale per token row).  The
+// dot product is over all 128 dims, so any fixed permutation of the dims applied to both Q and K
+// leaves it unchanged: MMA k-slot 2t+e (e = 0, 1) of k-step ks stands for dim 32t + 4ks + e and
+// slot 2t+8+e for dim 32t + 4ks + 2 + e (t = lane % 4).  A lane then needs dims [32t, 32t+32) of
+// its two token rows g and g+8: four conflict-free 16-byte shared loads per chunk from the
+// swizzled int8 tile, converted to exact fp16 integers in registers (byte permute + one fp16x2
+// subtract).  The row scale multiplies the finished dot product of each token.
+template <int G>
+struct TcEngineQ : TcEngine<G> {
+    __device__ __forceinline__ static uint32_t swz8(int r, int c16) { return r * 128 + ((c16 ^ (r & 7)) << 4); }
 
-template <int G, int LPT, bool TC>
+    __device__ __forceinline__ void init(const DecodeParams &P, int b, int kvh, int lane) {
+        const int head = lane >> 2;
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(
+            P.q + (static_cast<int64_t>(b) * P.num_q_heads + kvh * G + (head < G ? head : 0)) * kD + 32 * (lane & 3));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 w = head < G ? __ldg(qrow + i) : make_uint4(0u, 0u, 0u, 0u);
+            this->qb[2 * i][0] = w.x;
+            this->qb[2 * i][1] = w.y;
+            this->qb[2 * i + 1][0] = w.z;
+            this->qb[2 * i + 1][1] = w.w;
+        }
+        this->reset(P);
+    }
+
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t s_tile, int valid, int lane,
+                                          unsigned char *scratch) {
+        const int g = lane >> 2, t = lane & 3;
+        const uint4 r0 = pkv::lds128(k_tile + swz8(g, 2 * t)), r1 = pkv::lds128(k_tile + swz8(g, 2 * t + 1));
+        const uint4 r8 = pkv::lds128(k_tile + swz8(g + 8, 2 * t)), r9 = pkv::lds128(k_tile + swz8(g + 8, 2 * t + 1));
+        const uint32_t wg[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const uint32_t w8[8] = {r8.x, r8.y, r8.z, r8.w, r9.x, r9.y, r9.z, r9.w};
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t xg = wg[ks] ^ 0x80808080u, x8 = w8[ks] ^ 0x80808080u;
+            const uint32_t a[4] = {pkv::i8x2_to_h2(xg, 0x4140), pkv::i8x2_to_h2(x8, 0x4140),
+                                   pkv::i8x2_to_h2(xg, 0x4342), pkv::i8x2_to_h2(x8, 0x4342)};
+            pkv::mma16816(s, a, this->qb[ks][0], this->qb[ks][1]);
+        }
+        const float fg = this->q_scale * pkv::lds32f(s_tile + 4 * g);
+        const float f8 = this->q_scale * pkv::lds32f(s_tile + 4 * (g + 8));
+        s[0] = g < valid ? s[0] * fg : -INFINITY;
+        s[1] = g < valid ? s[1] * fg : -INFINITY;
+        s[2] = g + 8 < valid ? s[2] * f8 : -INFINITY;
+        s[3] = g + 8 < valid ? s[3] * f8 : -INFINITY;
+        this->softmax_pv(s, v_tile, lane, scratch);
+    }
+};
+
+template <int G, int LPT, bool TC, bool KQ>
+using EngineFor = typename std::conditional<
+    KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type;
+
+template <int G, int LPT, bool TC, bool KQ>
 __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN_CTAS)
     decode_partition_kernel(const __grid_constant__ DecodeParams P) {
-    using L = SmemLayout<TC>;
-    using Engine = EngineFor<G, LPT, TC>;
+    static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
+    using L = SmemLayout<TC, KQ>;
+    using Engine = EngineFor<G, LPT, TC, KQ>;
     constexpr int kRow = L::row;
-    constexpr int kTile = L::tile;
 
     extern __shared__ __align__(1024) unsigned char smem[];
 
@@ -719,7 +790,8 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     int32_t *s_table = reinterpret_cast<int32_t *>(smem + L::table(G));
     unsigned char *scratch = smem + L::probs + warp * L::probs_per_warp(G);
     const uint32_t bar0 = pkv::smem_addr(smem + L::bars) + warp * kStages * 8;
-    const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * 2 * kTile;
+    const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * L::stage;
+    const uint32_t scale0 = pkv::smem_addr(smem + L::scales) + warp * kStages * kChunk * 4;
 
     if (TC && (pkv::smem_addr(smem) & 1023) != 0) {  // the 128-byte swizzle needs 1 KB-aligned tiles
         if (threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
@@ -742,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     const unsigned char *vc = P.v_cache;
     const void *tmap_k = &P.tmap_k;
     const void *tmap_v = &P.tmap_v;
+    const float *ksc = P.k_scale;
     const int hkv = P.num_kv_heads;
     auto issue_from = [=](int i, int64_t phys) {
         const int cidx = warp + i * kWarps;
@@ -753,16 +826,28 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
         const int st = i % kStages;
         const uint32_t bar = bar0 + 8 * st;
-        const uint32_t dst = stage0 + st * 2 * kTile;
-        if constexpr (TC) {
+        const uint32_t dst = stage0 + st * L::stage;
+        if constexpr (KQ) {
+            // One 16-row box of int8 keys, two fp16 V half-boxes and the 16 key scales (64 B).
+            if (lane == 0) {
+                const int64_t y = (phys * hkv + kvh) * bs + off;
+                pkv::mbar_arrive_expect_tx(bar, L::k_tile + 2 * kHalfTile + kChunk * 4);
+                pkv::tma_load_2d(dst, tmap_k, 0, static_cast<int>(y), bar);
+                pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, static_cast<int>(y), bar);
+                pkv::tma_load_2d(dst + L::k_tile + kHalfTile, tmap_v, 64, static_cast<int>(y), bar);
+                pkv::bulk_copy_g2s(scale0 + st * kChunk * 4, ksc + y, kChunk * 4, bar);
+            }
+            (void)byte_off;
+            (void)bytes;
+        } else if constexpr (TC) {
             // Whole 16-row boxes (a ragged tail's extra rows stay inside the block and are masked).
             if (lane == 0) {
                 const int y = static_cast<int>((phys * hkv + kvh) * bs + off);
                 pkv::mbar_arrive_expect_tx(bar, 4 * kHalfTile);
                 pkv::tma_load_2d(dst, tmap_k, 0, y, bar);
                 pkv::tma_load_2d(dst + kHalfTile, tmap_k, 64, y, bar);
-                pkv::tma_load_2d(dst + kTile, tmap_v, 0, y, bar);
-                pkv::tma_load_2d(dst + kTile + kHalfTile, tmap_v, 64, y, bar);
+                pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, y, bar);
+                pkv::tma_load_2d(dst + L::k_tile + kHalfTile, tmap_v, 64, y, bar);
             }
             (void)byte_off;
             (void)bytes;
@@ -770,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
             if (lane == 0) {
                 pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
                 pkv::bulk_copy_g2s(dst, kc + byte_off, bytes, bar);
-                pkv::bulk_copy_g2s(dst + kTile, vc + byte_off, bytes, bar);
+                pkv::bulk_copy_g2s(dst + L::k_tile, vc + byte_off, bytes, bar);
             }
         }
     };
@@ -826,12 +911,46 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     if (appends && warp == own_warp) {
         const int64_t src = (static_cast<int64_t>(b) * P.num_kv_heads + kvh) * kD + (lane & 15) * 8;
         const uint4 new_row = __ldg(reinterpret_cast<const uint4 *>((lane < 16 ? P.k_new : P.v_new) + src));
-        *reinterpret_cast<uint4 *>(s_newrow + lane * 16) = new_row;
         const int32_t id = __ldg(P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq + new_pos / bs);
-        if (id >= 0 && id < P.num_blocks) {
-            const int64_t dst = ((static_cast<int64_t>(id) * P.num_kv_heads + kvh) * bs + new_pos % bs) * kD +
-                                (lane & 15) * 8;
-            *reinterpret_cast<uint4 *>((lane < 16 ? P.k_cache_w : P.v_cache_w) + dst) = new_row;
+        const bool id_ok = id >= 0 && id < P.num_blocks;
+        const int64_t grow = (static_cast<int64_t>(id) * P.num_kv_heads + kvh) * bs + new_pos % bs;
+        if constexpr (KQ) {
+            // Lanes 0-15 quantise the K row (8 dims each; scale from a 16-lane max), 16-31 move V.
+            const uint32_t w[4] = {new_row.x, new_row.y, new_row.z, new_row.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = pkv::half2_bits_to_float2(w[e]);
+                f[2 * e] = x.x;
+                f[2 * e + 1] = x.y;
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+            for (int sh = 8; sh >= 1; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(pkv::kFullMask, amax, sh));
+            const float sc = __fdiv_rn(amax, 127.f);
+            if (lane < 16) {
+                uint32_t c[2] = {0u, 0u};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    c[e >> 2] |= (static_cast<uint32_t>(pkv::quantize_int8(f[e], sc)) & 0xffu) << (8 * (e & 3));
+                const uint2 codes = make_uint2(c[0], c[1]);
+                *reinterpret_cast<uint2 *>(s_newrow + lane * 8) = codes;
+                if (lane == 0) *reinterpret_cast<float *>(s_newrow + kD) = sc;
+                if (id_ok) {
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<unsigned char *>(P.k_cache_w) + grow * kD + lane * 8) =
+                        codes;
+                    if (lane == 0) P.k_scale_w[grow] = sc;
+                }
+            } else {
+                *reinterpret_cast<uint4 *>(s_newrow + lane * 16) = new_row;
+                if (id_ok) *reinterpret_cast<uint4 *>(P.v_cache_w + grow * kD + (lane & 15) * 8) = new_row;
+            }
+        } else {
+            *reinterpret_cast<uint4 *>(s_newrow + lane * 16) = new_row;
+            if (id_ok) *reinterpret_cast<uint4 *>((lane < 16 ? P.k_cache_w : P.v_cache_w) + grow * kD + (lane & 15) * 8) =
+                new_row;
         }
     }
 
@@ -851,8 +970,9 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         consumed = i + 1;
         const int cidx = warp + i * kWarps;
         const int valid = min(kChunk, n_tok - cidx * kChunk);
-        const uint32_t k_tile = stage0 + st * 2 * kTile;
-        const uint32_t v_tile = k_tile + kTile;
+        const uint32_t k_tile = stage0 + st * L::stage;
+        const uint32_t v_tile = k_tile + L::k_tile;
+        const uint32_t s_tile = scale0 + st * kChunk * 4;
         bool touched = false;
         if (TC && valid < kChunk) {  // the MMA reads all 16 V rows: make the unused ones finite (zero)
             for (int x = lane; x < (kChunk - valid) * 16; x += 32)
@@ -862,16 +982,28 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
             touched = true;
         }
         if (cidx == own_chunk) {  // the appended token's row: overwrite what the copy brought
-            const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
             const int nr_row = (new_pos - start) % kChunk;
-            const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"((lane < 16 ? k_tile : v_tile) + row),
-                         "r"(nr.x), "r"(nr.y), "r"(nr.z), "r"(nr.w)
-                         : "memory");
+            if (KQ && lane < 16) {
+                const uint2 nc = *reinterpret_cast<const uint2 *>(s_newrow + lane * 8);
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(k_tile + TcEngineQ<G>::swz8(nr_row, lane >> 1) +
+                                                                     (lane & 1) * 8),
+                             "r"(nc.x), "r"(nc.y)
+                             : "memory");
+                if (lane == 0)
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_tile + nr_row * 4),
+                                 "f"(*reinterpret_cast<const float *>(s_newrow + kD))
+                                 : "memory");
+            } else {
+                const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
+                const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"((lane < 16 ? k_tile : v_tile) + row),
+                             "r"(nr.x), "r"(nr.y), "r"(nr.z), "r"(nr.w)
+                             : "memory");
+            }
             touched = true;
         }
         if (touched) __syncwarp();
-        eng.chunk(k_tile, v_tile, valid, lane, scratch);
+        eng.chunk(k_tile, v_tile, s_tile, valid, lane, scratch);
         __syncwarp();
         if (i + kStages < my_chunks) {
             pkv::fence_proxy_async_smem();
@@ -1042,27 +1174,42 @@ int encode_cache_map(CUtensorMap *map, const void *base, int64_t rows) {
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int G>
+// The int8 key codes as a 2-D byte tensor [rows][128] read in 16-row x 128-byte boxes, same swizzle.
+int encode_code_map(CUtensorMap *map, const void *base, int64_t rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return PKV_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <int G, bool KQ>
 int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
-    constexpr bool TC = PKV_DECODE_TC && G >= 4;
-    auto kernel = decode_partition_kernel<G, LPT, TC>;
+    constexpr bool TC = KQ || (PKV_DECODE_TC && G >= 4);
+    auto kernel = decode_partition_kernel<G, LPT, TC, KQ>;
     DecodeParams p = p_in;
     if (TC) {
         const int64_t rows = p.num_blocks * p.num_kv_heads * p.block_size;
         if (rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // box row coordinates are signed 32-bit
-        int st = encode_cache_map(&p.tmap_k, p.k_cache, rows);
+        int st = KQ ? encode_code_map(&p.tmap_k, p.k_cache, rows) : encode_cache_map(&p.tmap_k, p.k_cache, rows);
         if (st == PKV_OK) st = encode_cache_map(&p.tmap_v, p.v_cache, rows);
         if (st != PKV_OK) return st;
     }
-    const int smem = SmemLayout<TC>::total(G, p.partition_size);
+    using L = SmemLayout<TC, KQ>;
+    const int smem = L::total(G, p.partition_size);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SmemLayout<TC>::total(G, PKV_MAX_PARTITION)) != cudaSuccess)
+                                 L::total(G, PKV_MAX_PARTITION)) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
@@ -1087,11 +1234,16 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
 }
 
 int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream, int grid_parts = 0) {
+    const bool kq = p.k_scale != nullptr;
     switch (group) {
-        case 1: return launch_partition<1>(p, num_seqs, stream, grid_parts);
-        case 2: return launch_partition<2>(p, num_seqs, stream, grid_parts);
-        case 4: return launch_partition<4>(p, num_seqs, stream, grid_parts);
-        case 8: return launch_partition<8>(p, num_seqs, stream, grid_parts);
+        case 1: return kq ? launch_partition<1, true>(p, num_seqs, stream, grid_parts)
+                          : launch_partition<1, false>(p, num_seqs, stream, grid_parts);
+        case 2: return kq ? launch_partition<2, true>(p, num_seqs, stream, grid_parts)
+                          : launch_partition<2, false>(p, num_seqs, stream, grid_parts);
+        case 4: return kq ? launch_partition<4, true>(p, num_seqs, stream, grid_parts)
+                          : launch_partition<4, false>(p, num_seqs, stream, grid_parts);
+        case 8: return kq ? launch_partition<8, true>(p, num_seqs, stream, grid_parts)
+                          : launch_partition<8, false>(p, num_seqs, stream, grid_parts);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }
@@ -1193,14 +1345,16 @@ extern "C" PKV_API int pkv_merge(void *out, const float *o_part, const float *m_
 namespace {
 
 // pkv_decode_attention, optionally appending the new token first (k_new/v_new non-null).
+// k_scale non-null: k_cache holds int8 codes with these float32 row scales.
 int decode_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                           int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, const void *k_new, const void *v_new, void *workspace,
-                          size_t workspace_bytes, pkv_stream_t stream) {
+                          size_t workspace_bytes, pkv_stream_t stream, const float *k_scale = nullptr) {
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
+    if (k_scale && !pkv_internal::aligned16(k_scale)) return PKV_ERR_INVALID_ARG;
     if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
     if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
@@ -1228,6 +1382,8 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     p.v_new = static_cast<const __half *>(v_new);
     p.k_cache_w = static_cast<__half *>(const_cast<void *>(k_cache));
     p.v_cache_w = static_cast<__half *>(const_cast<void *>(v_cache));
+    p.k_scale = k_scale;
+    p.k_scale_w = const_cast<float *>(k_scale);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
 
@@ -1278,6 +1434,32 @@ extern "C" PKV_API int pkv_decode_step(void *out, const void *q, const void *k_n
     return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
                                  workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------------ int8 key cache
+
+extern "C" PKV_API int pkv_decode_attention_int8k(void *out, const void *q, const void *k_codes, const float *k_scale,
+                                                  const void *v_cache, const int32_t *block_tables,
+                                                  const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                                  int64_t num_blocks, float scale, void *workspace,
+                                                  size_t workspace_bytes, pkv_stream_t stream) {
+    if (!k_scale) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_codes, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, nullptr, nullptr,
+                                 workspace, workspace_bytes, stream, k_scale);
+}
+
+extern "C" PKV_API int pkv_decode_step_int8k(void *out, const void *q, const void *k_new, const void *v_new,
+                                             void *k_codes, float *k_scale, void *v_cache,
+                                             const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                             int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
+                                             int block_size, int64_t num_blocks, float scale, void *workspace,
+                                             size_t workspace_bytes, pkv_stream_t stream) {
+    if (!k_new || !v_new || !k_scale) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_codes, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
+                                 workspace, workspace_bytes, stream, k_scale);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

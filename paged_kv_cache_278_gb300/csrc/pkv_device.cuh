@@ -107,6 +107,30 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t bits) {
     return __half22float2(h);
 }
 
+__device__ __forceinline__ float lds32f(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Two signed int8 values -> an exact fp16x2.  `biased` holds four int8 bytes XOR 0x80 (value + 128
+// as unsigned); `sel` picks bytes (0x4140: bytes 0 and 1, 0x4342: bytes 2 and 3).  Each picked byte
+// becomes the low mantissa byte of 0x64xx = 1024 + byte, and subtracting 1152 leaves the integer.
+__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t biased, uint32_t sel) {
+    const uint32_t h = __byte_perm(biased, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
+// Symmetric int8 code of x for the row scale s = max|k| / 127: round-half-even(x / s) in
+// [-127, 127] with IEEE float32 division; 0 when s == 0.
+__device__ __forceinline__ int quantize_int8(float x, float s) {
+    if (s == 0.f) return 0;
+    const int c = __float2int_rn(__fdiv_rn(x, s));
+    return c > 127 ? 127 : (c < -127 ? -127 : c);
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
