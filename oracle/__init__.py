@@ -112,6 +112,9 @@ class Oracle:
         lib.oracle_decode_quant_k.restype = None
         lib.oracle_decode_quant_k.argtypes = [_f64p, _u16p, _i8p, _f32p, _u16p, _i32p, _i32p] + \
             [ctypes.c_int] * 6 + [ctypes.c_double]
+        lib.oracle_decode_multi.restype = None
+        lib.oracle_decode_multi.argtypes = [_f64p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p] + \
+            [ctypes.c_int] * 6 + [ctypes.c_double]
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
         self.lib = lib
@@ -209,6 +212,24 @@ class Oracle:
                                float(scale))
         return out
 
+    def decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                     scale: float) -> np.ndarray:
+        """float64 [total_q, Hq, D]: causal attention of each request's new tokens (rows
+        query_start[b]..query_start[b+1]-1 of q) over its cache."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        t, hq, d = qb.shape
+        nb, hkv, bs, d2 = kc.shape
+        assert d2 == d and hq % hkv == 0
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        qs = np.ascontiguousarray(query_start, dtype=np.int32)
+        assert qs.shape == (bt.shape[0] + 1,) and qs[-1] == t
+        out = np.empty((t, hq, d), np.float64)
+        self.lib.oracle_decode_multi(_p(out, _f64p), _p(qb, _u16p), _p(kc, _u16p), _p(vc, _u16p), _p(bt, _i32p),
+                                     _p(cl, _i32p), _p(qs, _i32p), bt.shape[0], bt.shape[1], hq, hkv, d, bs,
+                                     float(scale))
+        return out
+
     def decode_partition(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                          partition_size: int, max_partitions: int):
         """(o [B,Hq,P,D], m [B,Hq,P], l [B,Hq,P]) float64 split-context partials."""
@@ -289,6 +310,10 @@ def copy_blocks(k_cache, v_cache, src, dst):
 
 def quantize_k_row(k_row):
     return default().quantize_k_row(k_row)
+
+
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, query_start, scale):
+    return default().decode_multi(q, k_cache, v_cache, block_tables, context_lens, query_start, scale)
 
 
 def append_quant_k(k_codes, k_scale, v_cache, slots, k_new, v_new):

@@ -312,6 +312,44 @@ void oracle_decode_quant_k(double *out, const uint16_t *q, const int8_t *k_codes
     }
 }
 
+/* Several new tokens per request (a verified draft or a prefill chunk): request b
+ * owns query rows query_start[b] .. query_start[b + 1] - 1 of q and out
+ * ([total_q][num_q_heads][head_dim]); its n_b = query_start[b + 1] - query_start[b]
+ * new tokens are already appended, so context_lens[b] counts them, and query row i
+ * sits at logical position ctx_b - n_b + i.  Causally, it attends to positions
+ * 0 .. ctx_b - n_b + i: the plain decode definition over that prefix of the
+ * request's cache.  (The pages list chunked prefill and speculative decoding as
+ * decode-side techniques over the same cache: "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 3.2.) */
+void oracle_decode_multi(double *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens, const int32_t *query_start,
+                         int num_seqs, int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, double scale)
+{
+    int group = num_q_heads / num_kv_heads;
+    for (int b = 0; b < num_seqs; ++b) {
+        int n = query_start[b + 1] - query_start[b];
+        int ctx = context_lens[b];
+        const int32_t *bt_row = block_tables + (int64_t)b * max_blocks_per_seq;
+        double *s = (double *)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+        for (int i = 0; i < n; ++i) {
+            int visible = ctx - n + i + 1;
+            int64_t t = query_start[b] + i;
+            for (int h = 0; h < num_q_heads; ++h) {
+                int kvh = h / group;
+                double *o = out + (t * num_q_heads + h) * head_dim;
+                const uint16_t *q_row = q + (t * num_q_heads + h) * head_dim;
+                double m, l;
+                scores_range(s, q_row, k_cache, bt_row, 0, visible, kvh, num_kv_heads, head_dim,
+                             block_size, scale);
+                softmax_weighted_sum(o, &m, &l, s, v_cache, bt_row, 0, visible, kvh, num_kv_heads,
+                                     head_dim, block_size);
+            }
+        }
+        free(s);
+    }
+}
+
 /* Split-context partial results.  Partition p of request b covers the
  * positions [p * partition_size, min(ctx_b, (p + 1) * partition_size)).  For
  * each such partition and q head: m = max score, l = sum exp(s - m),

@@ -244,6 +244,35 @@ def pin_decode_quant_k(orc):
     assert np.abs(got - ref).max() <= 1e-12
 
 
+def pin_decode_multi_causal(orc):
+    """Several new tokens per request: a textbook causal attention (scipy softmax over the
+    scores with every later position masked) on contiguous K/V, and row by row the single-token
+    decode with the context cut at that row's position."""
+    rng = np.random.default_rng(21)
+    hq, hkv, d, bs = 4, 2, 16, 4
+    ctxs, ns = [9, 5, 12, 3], [3, 1, 4, 3]
+    ks, vs = random_contiguous(rng, ctxs, hkv, d)
+    kpool, vpool, bt, ctx = scatter_to_pool(ks, vs, bs, rng)
+    qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    q = rng.standard_normal((qs[-1], hq, d)).astype(np.float16)
+    got = orc.decode_multi(q, kpool, vpool, bt, ctx, qs, 0.3)
+    g = hq // hkv
+    for b, (c, n) in enumerate(zip(ctxs, ns)):
+        for i in range(n):
+            t = qs[b] + i
+            pos = c - n + i
+            for h in range(hq):
+                kk = ks[b][h // g].astype(np.float64)
+                vv = vs[b][h // g].astype(np.float64)
+                sc = 0.3 * (kk @ q[t, h].astype(np.float64))
+                sc[pos + 1:] = -np.inf
+                assert np.abs(got[t, h] - softmax(sc) @ vv).max() <= 1e-12
+            cut = ctx.copy()
+            cut[b] = pos + 1
+            one = orc.decode(q[t:t + 1], kpool, vpool, bt[b:b + 1], cut[b:b + 1], 0.3)
+            assert np.abs(got[t] - one[0]).max() <= 1e-15
+
+
 def pin_slot_mapping_by_enumeration(orc):
     """Walk every block table in order, naming each pool slot by the (request, position)
     stored there; the slot mapping must be the inverse of that enumeration."""
@@ -450,6 +479,7 @@ ALL_PINS = [
     pin_quantize_properties,
     pin_append_quant_k,
     pin_decode_quant_k,
+    pin_decode_multi_causal,
     pin_slot_mapping_by_enumeration,
     pin_two_keys_golden,
     pin_textbook_contiguous,

@@ -64,9 +64,11 @@ def test_fork_then_diverge_decode_step(bs):
     pool.reserve(rows[0], 0, ctx, bs)
     for r in rows[1:]:
         pool.fork(rows[0], r, ctx, bs)
-    pairs = [pool.prepare_append(r, ctx, bs) for r in rows]
+    # the children diverge first (each copies the shared block); the parent, left as the block's
+    # only holder, then appends in place
+    pairs = [pool.prepare_append(r, ctx, bs) for r in rows[1:]] + [pool.prepare_append(rows[0], ctx, bs)]
     if ctx % bs:
-        assert all(p is not None for p in pairs[1:]) and pairs[0] is None
+        assert all(p is not None for p in pairs[:-1]) and pairs[-1] is None
     else:
         assert all(p is None for p in pairs)
     src = np.array([p[0] for p in pairs if p], np.int32)
