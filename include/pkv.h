@@ -350,6 +350,44 @@ PKV_API int pkv_decode_step_int8k(void *out, const void *q, const void *k_new, c
                                   int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
                                   pkv_stream_t stream);
 
+/* ---- several new tokens per request ----------------------------------------
+ * A verified draft (speculative decoding) or a prefill chunk: request b brings
+ * n_b = query_start[b + 1] - query_start[b] new tokens whose K/V are already in
+ * the cache (pkv_append with their slots), so context_lens[b] counts them.
+ * Query row i of the request sits at logical position ctx_b - n_b + i and
+ * attends causally to positions 0 .. ctx_b - n_b + i:
+ *   out[t][h] = softmax(scale * q[t][h] . K[0..pos]^T) V[0..pos],
+ *   t = query_start[b] + i, pos = ctx_b - n_b + i
+ * (the pages list chunked prefill and speculative decoding among the ways to
+ * run decode over the same cache: "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 3.2).  n_b = 1 for every request is pkv_decode_attention. */
+#define PKV_MAX_QUERY_LEN 1024
+
+/* Workspace bytes for pkv_decode_attention_multi (0 when no request can need
+ * a split: every table fits one 512-token partition). */
+PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int total_q, int max_query_len, int num_q_heads,
+                                               int num_kv_heads, int head_dim, int max_context);
+
+/* Causal attention of every request's new tokens over its paged cache.
+ *   q, out      : fp16 [total_q][num_q_heads][head_dim] (q 16-byte, out 8-byte aligned)
+ *   query_start : device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
+ *                 query_start[num_seqs] = total_q; every n_b <= max_query_len
+ *                 (<= PKV_MAX_QUERY_LEN) and n_b <= ctx_b.  A request with n_b = 0
+ *                 is skipped; inconsistent rows are skipped and recorded as
+ *                 PKV_DEV_BAD_CONTEXT.
+ * Other arguments as pkv_decode_attention.  One CTA serves 8 (token, head) rows
+ * of one kv head and one 512-token partition, so K/V is read by
+ * ceil(n_b * G / 8) CTAs that run back to back (L2 serves the repeats); the
+ * split's merge is fused as in pkv_decode_attention.  Workspace: zero-filled
+ * before first use, left zeroed, at least pkv_decode_multi_workspace_size bytes,
+ * 256-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       const int32_t *query_start, int num_seqs, int total_q, int max_query_len,
+                                       int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int64_t num_blocks, float scale, void *workspace,
+                                       size_t workspace_bytes, pkv_stream_t stream);
+
 /* Split-context partial attention.  Partition p of request b covers logical
  * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each
  * such partition and query head h it writes

@@ -21,7 +21,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
+from ._lib import (PKV_MAX_QUERY_LEN, PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
                    PKV_DEV_OK, PKV_DEV_PREFIX_MISMATCH, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION,
                    PkvError)
 
@@ -29,7 +29,7 @@ __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
     "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
     "decode_step", "make_step_workspace", "copy_blocks", "append_int8k", "decode_attention_int8k",
-    "decode_step_int8k", "empty_int8k_cache",
+    "decode_step_int8k", "empty_int8k_cache", "decode_attention_multi", "make_multi_workspace",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -244,6 +244,49 @@ def device_error(device=None, stream=None) -> int:
         st = _L().pkv_get_device_error(_stream(dev, stream), ctypes.byref(code))
     _lib.check(st, "pkv_get_device_error")
     return code.value
+
+
+# ---------------------------------------------------------------- several new tokens per request
+
+def make_multi_workspace(num_seqs: int, total_q: int, max_query_len: int, num_q_heads: int, num_kv_heads: int,
+                         max_context: int, device) -> torch.Tensor | None:
+    """Zero-filled workspace for decode_attention_multi (None when it needs none)."""
+    n = int(_L().pkv_decode_multi_workspace_size(num_seqs, total_q, max_query_len, num_q_heads, num_kv_heads,
+                                                 PKV_HEAD_DIM, max_context))
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_attention_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, query_start: torch.Tensor,
+                           max_query_len: int, scale: float, workspace: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Causal attention of each request's new tokens (q rows query_start[b]..query_start[b+1]-1,
+    already appended, so context_lens counts them) over its paged cache; out like q."""
+    nb, hkv, bs, d = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", torch.float16, 3, dev)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(query_start, "query_start", torch.int32, 1, dev)
+    t, hq, dq = q.shape
+    b = context_lens.shape[0]
+    if dq != d or out.shape != q.shape:
+        raise ValueError("q / out shapes disagree with the cache")
+    if block_tables.shape[0] != b or query_start.shape[0] != b + 1:
+        raise ValueError("block_tables [B, ...], context_lens [B] and query_start [B + 1] disagree")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    st = _L().pkv_decode_attention_multi(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(), b,
+                                         t, int(max_query_len), block_tables.shape[1], hq, hkv, d, bs, nb,
+                                         float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
+    _lib.check(st, "pkv_decode_attention_multi")
+    return out
 
 
 # ---------------------------------------------------------------- int8 key cache

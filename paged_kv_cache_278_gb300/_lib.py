@@ -35,6 +35,7 @@ PKV_DEV_PREFIX_MISMATCH = 5
 PKV_HEAD_DIM = 128
 PKV_DEFAULT_PARTITION = 512
 PKV_MAX_PARTITION = 4096
+PKV_MAX_QUERY_LEN = 1024
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/pkv.h declares: name -> (restype, argtypes)
@@ -59,6 +60,9 @@ SIGNATURES = {
                                                                            c_void_p]),
     "pkv_decode_step_int8k": (c_int, [c_void_p] * 9 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
                                                                       c_void_p]),
+    "pkv_decode_multi_workspace_size": (c_size_t, [c_int] * 7),
+    "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_int64, c_float, c_void_p, c_size_t,
+                                                                           c_void_p]),
     "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
     "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,

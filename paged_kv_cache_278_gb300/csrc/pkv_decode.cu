@@ -108,6 +108,10 @@ struct DecodeParams {
     const __half *v_new;
     __half *k_cache_w;        // writable views of the caches for that append
     __half *v_cache_w;
+    const int32_t *query_start;  // several new tokens per request: request b owns q/out rows
+    int total_q;                 //   query_start[b] .. query_start[b+1]-1 (null: one token per request)
+    int max_query_len;
+    int n_row_groups;            // 8-column groups of the (token, head) rows of one kv head
     const float *k_scale;     // int8 key cache: float32 scale per (block, kv head, slot); null for fp16 keys
     float *k_scale_w;         // writable view of k_scale for the fused append
     CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
@@ -141,13 +145,35 @@ struct SmemLayout {
     }
 };
 
-// Log-sum-exp merge of partial slots [0, n_total) of the G query heads of (request b, kv head
-// kvh) into fp16 out; called by every thread of one CTA (it synchronises the CTA).
+// Output rows of a CTA's G packed columns.  One token per request: the G query heads of (request,
+// kv head), consecutive rows from row0.
+struct HeadRows {
+    int64_t row0;
+    __device__ __forceinline__ int64_t row(int hh) const { return row0 + hh; }
+    __device__ __forceinline__ bool live(int) const { return true; }
+};
+// Several tokens per request: column hh of row group rg is row r = 8 rg + hh of the request's
+// n * G rows for kv head kvh, i.e. token r / G, head r % G.  Columns past the last token are
+// dead; their reads are redirected to the last token's row so every access stays in bounds.
 template <int G>
-__device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, unsigned char *smem) {
+struct TokenRows {
+    int64_t qs;
+    int n, rg, hq, kvh;
+    __device__ __forceinline__ int64_t row(int hh) const {
+        const int r = rg * 8 + hh;
+        const int i = r / G < n ? r / G : n - 1;
+        return (qs + i) * hq + kvh * G + r % G;
+    }
+    __device__ __forceinline__ bool live(int hh) const { return (rg * 8 + hh) / G < n; }
+};
+
+// Log-sum-exp merge of partial slots [0, n_total) of the G packed columns (query heads, or
+// (token, head) rows) of one CTA's kv head into fp16 out; called by every thread of one CTA
+// (it synchronises the CTA).
+template <int G, class Rows>
+__device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total, unsigned char *smem) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int Hq = P.num_q_heads;
     // Slots: (packed head, 4 consecutive dims) -> float4 loads of o; partitions are split over
     // GROUPS thread groups when there are fewer slots than threads, and loads are unrolled so a
     // thread keeps 8 rows in flight.  All weights w = l exp(m - M) of a tile are staged first.
@@ -161,7 +187,6 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
     float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
     float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
     float *s_sum = reinterpret_cast<float *>(s_acc + GROUPS * SLOTS);                     // [GROUPS][SLOTS]
-    const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
     const int grp = GROUPS > 1 ? threadIdx.x / SLOTS : 0;
     const int slot0 = GROUPS > 1 ? threadIdx.x % SLOTS : threadIdx.x;
     float4 macc[PER_THREAD];
@@ -172,7 +197,7 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
         msum[k] = 0.f;
     }
     auto o_row = [&](int hh, int d4) {
-        return reinterpret_cast<const float4 *>(P.o_part + (row0 + hh) * P.max_partitions * kD) + d4;
+        return reinterpret_cast<const float4 *>(P.o_part + rows.row(hh) * P.max_partitions * kD) + d4;
     };
     auto accumulate = [&](int k, float w, float4 v) {
         macc[k].x = fmaf(w, v.x, macc[k].x);
@@ -200,7 +225,7 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
         float *s_ll = s_wt + G * kMergeTile;
         for (int i = threadIdx.x; i < G * n_total; i += kThreads) {
             const int hh = i / n_total, pp = i - hh * n_total;
-            const int64_t prow = (row0 + hh) * P.max_partitions + pp;
+            const int64_t prow = rows.row(hh) * P.max_partitions + pp;
             s_mm[hh * kMergeTile + pp] = __ldcg(P.m_part + prow);
             s_ll[hh * kMergeTile + pp] = __ldcg(P.l_part + prow);
         }
@@ -225,7 +250,7 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
     } else {
         // Long contexts: maxima first, then tiles of weights, each tile's rows streamed.
         for (int hh = warp; hh < G; hh += kWarps) {
-            const float *m = P.m_part + (row0 + hh) * P.max_partitions;
+            const float *m = P.m_part + rows.row(hh) * P.max_partitions;
             float M = -INFINITY;
 #pragma unroll 4
             for (int pp = lane; pp < n_total; pp += 32) M = fmaxf(M, __ldcg(m + pp));
@@ -238,7 +263,7 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
             __syncthreads();  // s_max ready / previous tile consumed
             for (int i = threadIdx.x; i < G * n; i += kThreads) {
                 const int hh = i / n, pp = i - hh * n;
-                const int64_t prow = (row0 + hh) * P.max_partitions + p0 + pp;
+                const int64_t prow = rows.row(hh) * P.max_partitions + p0 + pp;
                 s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
             }
             __syncthreads();
@@ -271,13 +296,14 @@ __device__ void merge_group(const DecodeParams &P, int b, int kvh, int n_total, 
     for (int k = 0; k < PER_THREAD; ++k) {
         const int slot = slot0 + k * kThreads;
         const int hh = slot / (kD / 4), d4 = slot % (kD / 4);
+        if (!rows.live(hh)) continue;
         const float inv = 1.f / msum[k];
         __half2 lo = __floats2half2_rn(macc[k].x * inv, macc[k].y * inv);
         __half2 hi = __floats2half2_rn(macc[k].z * inv, macc[k].w * inv);
         uint2 packed;
         packed.x = *reinterpret_cast<uint32_t *>(&lo);
         packed.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(P.out + (row0 + hh) * kD + d4 * 4) = packed;
+        *reinterpret_cast<uint2 *>(P.out + rows.row(hh) * kD + d4 * 4) = packed;
     }
 }
 
@@ -350,7 +376,7 @@ struct FmaEngine {
     }
 
     __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
-                                          unsigned char *scratch) {
+                                          unsigned char *scratch, int) {
         float *s_prob = reinterpret_cast<float *>(scratch);
         // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
         float v[N];
@@ -544,15 +570,20 @@ struct TcEngine {
         reset(P);
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
-                                          unsigned char *scratch) {
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // Raw q . K of the chunk's 16 tokens (rows g, g + 8) for the lane's columns h0, h0 + 1.
+    __device__ __forceinline__ void dots(float (&s)[4], uint32_t k_tile, int lane) const {
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t a[4];
             pkv::ldsm_x4(a, k_tile + swz(lane & 15, ks * 2 + (lane >> 4)));
             pkv::mma16816(s, a, qb[ks][0], qb[ks][1]);
         }
+    }
+
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
+                                          unsigned char *scratch, int) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        dots(s, k_tile, lane);
         const int g = lane >> 2;
         s[0] = g < valid ? s[0] * q_scale : -INFINITY;
         s[1] = g < valid ? s[1] * q_scale : -INFINITY;
@@ -562,7 +593,10 @@ struct TcEngine {
     }
 
     // Online softmax of the chunk's scaled, masked log2-domain scores s (token g / g + 8, heads
-    // h0 / h0 + 1) and the P.V product into the O^T accumulators.
+    // h0 / h0 + 1) and the P.V product into the O^T accumulators.  kAnyMasked: a column may have
+    // no visible token yet (its reference max still -inf), so a masked score's weight is forced
+    // to 0 instead of exp2(-inf - -inf).
+    template <bool kAnyMasked = false>
     __device__ __forceinline__ void softmax_pv(float (&s)[4], uint32_t v_tile, int lane, unsigned char *scratch) {
         const int g = lane >> 2;
         float cm0 = fmaxf(s[0], s[2]), cm1 = fmaxf(s[1], s[3]);
@@ -588,8 +622,12 @@ struct TcEngine {
                 o[mt][3] *= a1;
             }
         }
-        const float p[4] = {exp2f(s[0] - m_ref[0]), exp2f(s[1] - m_ref[1]), exp2f(s[2] - m_ref[0]),
-                            exp2f(s[3] - m_ref[1])};
+        float p[4] = {exp2f(s[0] - m_ref[0]), exp2f(s[1] - m_ref[1]), exp2f(s[2] - m_ref[0]),
+                      exp2f(s[3] - m_ref[1])};
+        if (kAnyMasked) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = s[e] == -INFINITY ? 0.f : p[e];
+        }
         l_part[0] += p[0] + p[2];
         l_part[1] += p[1] + p[3];
         // P^T through shared memory as fp16 hi / lo: [2][8 heads][16 tokens]
@@ -681,7 +719,7 @@ struct TcEngineQ : TcEngine<G> {
     }
 
     __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t s_tile, int valid, int lane,
-                                          unsigned char *scratch) {
+                                          unsigned char *scratch, int) {
         const int g = lane >> 2, t = lane & 3;
         const uint4 r0 = pkv::lds128(k_tile + swz8(g, 2 * t)), r1 = pkv::lds128(k_tile + swz8(g, 2 * t + 1));
         const uint4 r8 = pkv::lds128(k_tile + swz8(g + 8, 2 * t)), r9 = pkv::lds128(k_tile + swz8(g + 8, 2 * t + 1));
@@ -705,27 +743,86 @@ struct TcEngineQ : TcEngine<G> {
     }
 };
 
-template <int G, int LPT, bool TC, bool KQ>
-using EngineFor = typename std::conditional<
-    KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type;
+// ---------------------------------------------------------------- several new tokens per request
+// The 8 MMA columns carry (token, head) rows r = 8 rg + c of the request's n * G rows for this kv
+// head (token r / G, head r % G), so a verified draft or a prefill chunk is the same tile as a
+// packed-GQA decode.  Each column masks the cached positions after its own token's position
+// ctx - n + token (causal); dead columns (past the last token) see nothing.
+template <int G>
+struct TcEngineM : TcEngine<8> {
+    int lim[2];  // last visible logical position of the lane's accumulator columns h0, h0 + 1
 
-template <int G, int LPT, bool TC, bool KQ>
+    __device__ __forceinline__ void init(const DecodeParams &P, int, int, int) { reset(P); }
+
+    __device__ __forceinline__ void bind(const DecodeParams &P, int kvh, int lane, int rg, int64_t qs, int n, int ctx) {
+        const int r = rg * 8 + (lane >> 2);
+        const bool live = r / G < n;
+        const __half *qrow = P.q + ((qs + (live ? r / G : 0)) * P.num_q_heads + kvh * G + r % G) * kD;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                qb[ks][j] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + (lane & 3) * 2 + j * 8)) : 0u;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int tok = (rg * 8 + (lane & 3) * 2 + j) / G;
+            lim[j] = tok < n ? ctx - n + tok : -1;
+        }
+    }
+
+    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
+                                          unsigned char *scratch, int tok0) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        dots(s, k_tile, lane);
+        const int g = lane >> 2;
+        const int p0 = tok0 + g, p8 = tok0 + g + 8;
+        s[0] = g < valid && p0 <= lim[0] ? s[0] * q_scale : -INFINITY;
+        s[1] = g < valid && p0 <= lim[1] ? s[1] * q_scale : -INFINITY;
+        s[2] = g + 8 < valid && p8 <= lim[0] ? s[2] * q_scale : -INFINITY;
+        s[3] = g + 8 < valid && p8 <= lim[1] ? s[3] * q_scale : -INFINITY;
+        softmax_pv<true>(s, v_tile, lane, scratch);
+    }
+};
+
+template <int G, int LPT, bool TC, bool KQ, bool MQ>
+using EngineFor = typename std::conditional<
+    MQ, TcEngineM<G>,
+    typename std::conditional<
+        KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type;
+
+template <int G, int LPT, bool TC, bool KQ, bool MQ>
 __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN_CTAS)
     decode_partition_kernel(const __grid_constant__ DecodeParams P) {
     static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
+    static_assert(!MQ || (TC && !KQ), "several tokens per request run on the fp16 tensor-core engine");
     using L = SmemLayout<TC, KQ>;
-    using Engine = EngineFor<G, LPT, TC, KQ>;
+    using Engine = EngineFor<G, LPT, TC, KQ, MQ>;
     constexpr int kRow = L::row;
+    constexpr int NC = MQ ? 8 : G;  // packed output columns per CTA
 
     extern __shared__ __align__(1024) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int part = blockIdx.x;
+    const int n_rg = MQ ? P.n_row_groups : 1;
+    const int part = MQ ? blockIdx.x / n_rg : blockIdx.x;
+    const int rg = MQ ? blockIdx.x - part * n_rg : 0;  // row group (fastest: groups share K/V in L2)
     const int kvh = blockIdx.y;
     const int b = blockIdx.z;
     const int Hq = P.num_q_heads;
     const int bs = P.block_size;
+    int q_len = 1;
+    int64_t qs_b = b;
+    if constexpr (MQ) {
+        qs_b = __ldg(P.query_start + b);
+        q_len = __ldg(P.query_start + b + 1) - static_cast<int>(qs_b);
+        if (q_len < 0 || q_len > P.max_query_len || qs_b < 0 || qs_b + q_len > P.total_q) {
+            if (part == 0 && kvh == 0 && rg == 0 && threadIdx.x == 0)
+                pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
+            return;
+        }
+        if (rg * 8 >= q_len * G) return;  // no live column (also q_len == 0: nothing this step)
+    }
 
     // ---------------------------------------------------------------- extent
     // The block ids of this warp's first chunks and q depend only on (b, kv head, partition):
@@ -748,6 +845,17 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         ctx = cap;
     }
     if (ctx < 0) ctx = 0;
+    if constexpr (MQ) {
+        if (ctx < q_len) {  // the new tokens must already be in the cache
+            if (part == 0 && kvh == 0 && rg == 0 && threadIdx.x == 0)
+                pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
+            return;
+        }
+        eng.bind(P, kvh, lane, rg, qs_b, q_len, ctx);
+        // keys past the group's last live token are visible to none of its columns
+        const int last_tok = min(q_len - 1, (rg * 8 + 7) / G);
+        ctx = ctx - q_len + last_tok + 1;
+    }
     const int tok_begin = P.token_offset;  // > 0 only for the suffix pass after a shared prefix
     if (tok_begin > 0 && ctx < tok_begin) {
         if (part == 0 && kvh == 0 && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
@@ -776,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     if (n_parts == 0) {  // shared-prefix pass: the whole context is the prefix, merge its chunks only
         if (part == 0 && P.counters != nullptr) {
             pkv::pdl_wait_primary();  // the prefix kernel's partials
-            merge_group<G>(P, b, kvh, P.slot_offset, smem);
+            merge_group<G>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset, smem);
         }
         return;
     }
@@ -897,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
         }
     }
 
-    static_assert(kWarps * G * (kD + 2) * 4 <= L::stage_bytes, "combine area must fit the stages");
+    static_assert(kWarps * NC * (kD + 2) * 4 <= L::stage_bytes, "combine area must fit the stages");
 
     // ---- fused append: the CTA holding the request's last position writes the new token's K/V
     // row for its kv head into the cache (lanes 0-15: K, 16-31: V of warp own_warp) and patches the
@@ -1003,7 +1111,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
             touched = true;
         }
         if (touched) __syncwarp();
-        eng.chunk(k_tile, v_tile, s_tile, valid, lane, scratch);
+        eng.chunk(k_tile, v_tile, s_tile, valid, lane, scratch, start + cidx * kChunk);
         __syncwarp();
         if (i + kStages < my_chunks) {
             pkv::fence_proxy_async_smem();
@@ -1018,26 +1126,30 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
 
     // ---- merge the 4 warps in shared memory (reusing the stage buffers)
     __syncthreads();
-    float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][G][kD]
-    float *c_m = c_acc + kWarps * G * kD;                            // [kWarps][G]
-    float *c_l = c_m + kWarps * G;                                   // [kWarps][G]
+    float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][NC][kD]
+    float *c_m = c_acc + kWarps * NC * kD;                           // [kWarps][NC]
+    float *c_l = c_m + kWarps * NC;                                  // [kWarps][NC]
     eng.finish(warp, lane, c_acc, c_m, c_l);
     __syncthreads();
+    const TokenRows<G> token_rows{qs_b, q_len, rg, Hq, kvh};
 #pragma unroll 1
-    for (int idx = threadIdx.x; idx < G * kD; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < NC * kD; idx += kThreads) {
         const int hh = idx / kD, d = idx % kD;
+        if (MQ && !token_rows.live(hh)) continue;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, c_m[w * G + hh]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, c_m[w * NC + hh]);
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float f = exp2f(c_m[w * G + hh] - M);   // 0 for warps without chunks
-            L = fmaf(c_l[w * G + hh], f, L);
-            O = fmaf(c_acc[(w * G + hh) * kD + d], f, O);
+            const float cm = c_m[w * NC + hh];
+            // 0 for warps without chunks; with causal masking a column can have seen no token at all
+            const float f = (MQ && cm == -INFINITY) ? 0.f : exp2f(cm - M);
+            L = fmaf(c_l[w * NC + hh], f, L);
+            O = fmaf(c_acc[(w * NC + hh) * kD + d], f, O);
         }
-        const int64_t row = static_cast<int64_t>(b) * Hq + kvh * G + hh;
-        const float o = O / L;
+        const int64_t row = MQ ? token_rows.row(hh) : static_cast<int64_t>(b) * Hq + kvh * G + hh;
+        const float o = (MQ && L == 0.f) ? 0.f : O / L;
         if (direct) {
             P.out[row * kD + d] = __float2half_rn(o);
         } else {
@@ -1057,12 +1169,15 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN
     // partial from L2 (ld.global.cg) after a second barrier, then returns the counter to zero.
     __shared__ int s_last;
     __syncthreads();
-    int *counter = P.counters + static_cast<int64_t>(b) * P.num_kv_heads + kvh;
+    int *counter = P.counters + (static_cast<int64_t>(b) * P.num_kv_heads + kvh) * n_rg + rg;
     if (threadIdx.x == 0) s_last = pkv::atomic_add_acq_rel_gpu(counter, 1) == n_parts - 1;
     __syncthreads();
     if (!s_last) return;
     if (P.slot_offset > 0) pkv::pdl_wait_primary();  // shared-prefix pass: the prefix kernel's partials
-    merge_group<G>(P, b, kvh, P.slot_offset + n_parts, smem);
+    if constexpr (MQ)
+        merge_group<NC>(P, token_rows, P.slot_offset + n_parts, smem);
+    else
+        merge_group<G>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset + n_parts, smem);
     if (threadIdx.x == 0) *counter = 0;
 }
 
@@ -1188,11 +1303,11 @@ int encode_code_map(CUtensorMap *map, const void *base, int64_t rows) {
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int G, bool KQ>
+template <int G, bool KQ, bool MQ>
 int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
-    constexpr bool TC = KQ || (PKV_DECODE_TC && G >= 4);
-    auto kernel = decode_partition_kernel<G, LPT, TC, KQ>;
+    constexpr bool TC = KQ || MQ || (PKV_DECODE_TC && G >= 4);
+    auto kernel = decode_partition_kernel<G, LPT, TC, KQ, MQ>;
     DecodeParams p = p_in;
     if (TC) {
         const int64_t rows = p.num_blocks * p.num_kv_heads * p.block_size;
@@ -1213,7 +1328,9 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const dim3 grid(grid_parts > 0 ? grid_parts : p.max_partitions, p.num_kv_heads, num_seqs);
+    const int64_t gx = static_cast<int64_t>(grid_parts > 0 ? grid_parts : p.max_partitions) * (MQ ? p.n_row_groups : 1);
+    if (gx > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(gx), p.num_kv_heads, num_seqs);
     if (p.slot_offset == 0) {
         kernel<<<grid, kThreads, smem, stream>>>(p);
         return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -1233,17 +1350,19 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
     return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+template <int G>
+int launch_mode(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
+    if (p.query_start) return launch_partition<G, false, true>(p, num_seqs, stream, grid_parts);
+    if (p.k_scale) return launch_partition<G, true, false>(p, num_seqs, stream, grid_parts);
+    return launch_partition<G, false, false>(p, num_seqs, stream, grid_parts);
+}
+
 int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream, int grid_parts = 0) {
-    const bool kq = p.k_scale != nullptr;
     switch (group) {
-        case 1: return kq ? launch_partition<1, true>(p, num_seqs, stream, grid_parts)
-                          : launch_partition<1, false>(p, num_seqs, stream, grid_parts);
-        case 2: return kq ? launch_partition<2, true>(p, num_seqs, stream, grid_parts)
-                          : launch_partition<2, false>(p, num_seqs, stream, grid_parts);
-        case 4: return kq ? launch_partition<4, true>(p, num_seqs, stream, grid_parts)
-                          : launch_partition<4, false>(p, num_seqs, stream, grid_parts);
-        case 8: return kq ? launch_partition<8, true>(p, num_seqs, stream, grid_parts)
-                          : launch_partition<8, false>(p, num_seqs, stream, grid_parts);
+        case 1: return launch_mode<1>(p, num_seqs, stream, grid_parts);
+        case 2: return launch_mode<2>(p, num_seqs, stream, grid_parts);
+        case 4: return launch_mode<4>(p, num_seqs, stream, grid_parts);
+        case 8: return launch_mode<8>(p, num_seqs, stream, grid_parts);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }
@@ -1460,6 +1579,81 @@ extern "C" PKV_API int pkv_decode_step_int8k(void *out, const void *q, const voi
     return decode_attention_impl(out, q, k_codes, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
                                  workspace, workspace_bytes, stream, k_scale);
+}
+
+// ------------------------------------------------------------------ several new tokens per request
+
+namespace {
+int row_groups(int max_query_len, int group) { return (max_query_len * group + 7) / 8; }
+}  // namespace
+
+extern "C" PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int total_q, int max_query_len,
+                                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                                          int max_context) {
+    if (num_seqs <= 0 || total_q <= 0 || max_query_len <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || max_context <= 0 || num_q_heads % num_kv_heads != 0)
+        return 0;
+    const size_t parts = (static_cast<size_t>(max_context) + PKV_DEFAULT_PARTITION - 1) / PKV_DEFAULT_PARTITION;
+    if (parts <= 1) return 0;
+    const size_t rows = static_cast<size_t>(total_q) * num_q_heads * parts;
+    const size_t counters =
+        static_cast<size_t>(num_seqs) * num_kv_heads * row_groups(max_query_len, num_q_heads / num_kv_heads);
+    return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float)) +
+           align256(counters * sizeof(int));
+}
+
+extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                                  const int32_t *block_tables, const int32_t *context_lens,
+                                                  const int32_t *query_start, int num_seqs, int total_q,
+                                                  int max_query_len, int max_blocks_per_seq, int num_q_heads,
+                                                  int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                                  float scale, void *workspace, size_t workspace_bytes,
+                                                  pkv_stream_t stream) {
+    int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
+    if (st != PKV_OK) return st;
+    if (!out || !pkv_internal::aligned(out, 8) || !query_start || !pkv_internal::aligned(query_start, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (total_q < 0 || max_query_len <= 0) return PKV_ERR_INVALID_ARG;
+    if (max_query_len > PKV_MAX_QUERY_LEN) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || total_q == 0) return PKV_OK;
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    const int part = PKV_DEFAULT_PARTITION;
+    const int max_parts = static_cast<int>((cap + part - 1) / part);
+    DecodeParams p{};
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const unsigned char *>(k_cache);
+    p.v_cache = static_cast<const unsigned char *>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<__half *>(out);
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.q_scale = scale * kLog2e;
+    p.partition_size = part;
+    p.max_partitions = max_parts;
+    p.direct_single = 1;
+    p.query_start = query_start;
+    p.total_q = total_q;
+    p.max_query_len = max_query_len;
+    p.n_row_groups = row_groups(max_query_len, group);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (max_parts > 1) {
+        const size_t need = pkv_decode_multi_workspace_size(num_seqs, total_q, max_query_len, num_q_heads,
+                                                            num_kv_heads, head_dim, static_cast<int>(cap));
+        if (!workspace || workspace_bytes < need || !pkv_internal::aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+        const size_t rows = static_cast<size_t>(total_q) * num_q_heads * max_parts;
+        unsigned char *ws = static_cast<unsigned char *>(workspace);
+        p.o_part = reinterpret_cast<float *>(ws);
+        p.m_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)));
+        p.l_part = reinterpret_cast<float *>(ws + align256(rows * kD * sizeof(float)) + align256(rows * sizeof(float)));
+        p.counters = reinterpret_cast<int *>(ws + counters_offset(rows));
+    }
+    return dispatch_partition(p, num_seqs, group, s);
 }
 
 // ------------------------------------------------------------------ allocation-free variant
