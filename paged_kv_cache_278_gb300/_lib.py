@@ -61,7 +61,7 @@ SIGNATURES = {
     "pkv_decode_step_int8k": (c_int, [c_void_p] * 9 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
                                                                       c_void_p]),
     "pkv_decode_multi_workspace_size": (c_size_t, [c_int] * 7),
-    "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 9 + [c_int64, c_float, c_void_p, c_size_t,
+    "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 8 + [c_int64, c_float, c_void_p, c_size_t,
                                                                            c_void_p]),
     "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),

@@ -65,6 +65,10 @@ constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 #ifndef PKV_DECODE_MIN_CTAS
 #define PKV_DECODE_MIN_CTAS 3
 #endif
+// Resident CTAs per SM the int8-key kernel is compiled for (its stages are 6 KB, not 8 KB).
+#ifndef PKV_DECODE_KQ_MIN_CTAS
+#define PKV_DECODE_KQ_MIN_CTAS 3
+#endif
 // 1: q.K and P.V use packed two-lane FMAs (fma.rn.f32x2), halving FMA issue slots.
 #ifndef PKV_DECODE_FFMA2
 #define PKV_DECODE_FFMA2 1
@@ -791,7 +795,7 @@ using EngineFor = typename std::conditional<
         KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type;
 
 template <int G, int LPT, bool TC, bool KQ, bool MQ>
-__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : PKV_DECODE_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
     decode_partition_kernel(const __grid_constant__ DecodeParams P) {
     static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
     static_assert(!MQ || (TC && !KQ), "several tokens per request run on the fp16 tensor-core engine");

@@ -39,6 +39,47 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(_lib.SIGNATURES), "the binding's signature table must match the header"
 
 
+def declared_prototypes():
+    """{name: [parameter type text, ...]} of every PKV_API function in include/."""
+    protos = {}
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        for m in re.finditer(r"PKV_API\s+([\w\s\*]+?)\b(pkv_\w+)\s*\(([^)]*)\)", text):
+            params = [x.strip() for x in m.group(3).split(",")]
+            protos[m.group(2)] = [] if params == ["void"] or params == [""] else params
+    return protos
+
+
+def _ctype_for(param: str):
+    """The ctypes type a C parameter declaration must be bound with."""
+    decl = " ".join(param.replace("*", " * ").split())
+    if "*" in decl:
+        return "pointer"
+    base = decl.rsplit(" ", 1)[0].replace("const ", "")
+    return {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "uint32_t": ctypes.c_uint32, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
+            "uint64_t": ctypes.c_uint64, "pkv_stream_t": "pointer"}[base]
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Argument count and kind of every ctypes binding against its C prototype, so a slip in the
+    table cannot shift arguments into the wrong parameters."""
+    protos = declared_prototypes()
+    assert set(protos) == set(_lib.SIGNATURES)
+    pointer_types = (ctypes.c_void_p, ctypes.c_char_p)
+    for name, params in protos.items():
+        bound = _lib.SIGNATURES[name][1]
+        assert len(bound) == len(params), (name, len(bound), len(params))
+        for decl, ct in zip(params, bound):
+            want = _ctype_for(decl)
+            if want == "pointer":
+                assert ct in pointer_types or issubclass(ct, ctypes._Pointer), (name, decl, ct)
+            else:
+                assert ct is want, (name, decl, ct)
+
+
 def test_only_api_symbols_are_visible(lib):
     # the C ABI is the only surface: hidden visibility keeps kernels and helpers private
     out = os.popen(f"nm -D --defined-only {_lib.LIB_PATH}").read()
@@ -86,6 +127,42 @@ def test_invalid_arguments_rejected_without_launch(lib):
                                     null) == _lib.PKV_ERR_INVALID_ARG
     # empty batches are a successful no-op
     assert lib.pkv_append(p, p, p, p, p, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
+
+
+def test_int8k_multi_copy_invalid_arguments(lib):
+    null = None
+    p = ctypes.c_void_p(16)
+    bad = ctypes.c_void_p(24)
+    # int8-key append / decode / step: null scale array, misaligned scales, head_dim 64
+    assert lib.pkv_append_int8k(p, null, p, p, p, p, 1, 1, 128, 16, 4, null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_append_int8k(p, p, p, p, p, p, 1, 1, 64, 16, 4, null) == _lib.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_decode_attention_int8k(p, p, p, null, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_attention_int8k(p, p, p, bad, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_int8k(p, p, null, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                     null) == _lib.PKV_ERR_INVALID_ARG
+    # several tokens per request: null query_start, query length beyond the limit, no workspace
+    assert lib.pkv_decode_attention_multi(p, p, p, p, p, p, null, 1, 4, 4, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_attention_multi(p, p, p, p, p, p, p, 1, 4, _lib.PKV_MAX_QUERY_LEN + 1, 1, 1, 1, 128, 16,
+                                          4, 1.0, null, 0, null) == _lib.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_decode_attention_multi(p, p, p, p, p, p, p, 1, 4, 4, 256, 1, 1, 128, 16, 4096, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_WORKSPACE
+    # block copy: null id arrays, head_dim not a multiple of 8
+    assert lib.pkv_copy_blocks(p, p, null, p, 1, 1, 128, 16, 4, null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(p, p, p, p, 1, 1, 12, 16, 4, null) == _lib.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_copy_blocks(p, p, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
+
+
+def test_multi_workspace_size(lib):
+    # one 512-token partition: none needed
+    assert lib.pkv_decode_multi_workspace_size(2, 10, 8, 32, 8, 128, 512) == 0
+    rows = 10 * 32 * 8
+    up = lambda x: x + (-x) % 256
+    groups = -(-8 * 4 // 8)
+    expect = up(rows * 128 * 4) + 2 * up(rows * 4) + up(2 * 8 * groups * 4)
+    assert lib.pkv_decode_multi_workspace_size(2, 10, 8, 32, 8, 128, 4096) == expect
 
 
 def test_workspace_size(lib):
