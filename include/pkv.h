@@ -170,6 +170,21 @@ PKV_API int pkv_pool_prepare_append(pkv_pool *pool, int32_t *table_row, int max_
 PKV_API int pkv_pool_free_table(pkv_pool *pool, const int32_t *table_row, int num_tokens,
                                 int block_size);
 
+/* Swap a request's blocks between two pools (device cache <-> host swap space,
+ * either direction; the pages name page-level swap in/out as a benefit of
+ * paging: "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2).  For the
+ * n = ceil(num_tokens / bs) blocks of table_row (ids in `from`): n blocks are
+ * allocated in `to`, src_ids[i] / dst_ids[i] receive the pair (old id, new id)
+ * to copy (pkv_copy_blocks_between), the old blocks are released in `from`,
+ * and table_row[i] becomes the new id.  Every block must be held by this
+ * request alone (reference count 1): a block other requests still read cannot
+ * leave.  All-or-nothing: on error nothing changes.  The copy must be enqueued
+ * before any later kernel reuses the released blocks (same stream order).
+ * Errors: INVALID_ARG (shared or unallocated block, row too short),
+ * OUT_OF_BLOCKS (`to` has fewer than n free blocks). */
+PKV_API int pkv_pool_swap(pkv_pool *from, pkv_pool *to, int32_t *table_row, int max_blocks, int num_tokens,
+                          int block_size, int32_t *src_ids, int32_t *dst_ids);
+
 /* Host slot mapping for one new token per request:
  *   slots[b] = block_tables[b][positions[b] / bs] * bs + positions[b] % bs,
  * and slots[b] = -1 when positions[b] < 0 (no token for that request).
@@ -204,6 +219,18 @@ PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping
 PKV_API int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst, int n,
                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                             pkv_stream_t stream);
+
+/* Copy whole blocks from one pool to another of the same geometry:
+ *   dst_k[dst_ids[i]] <- src_k[src_ids[i]], dst_v[dst_ids[i]] <- src_v[src_ids[i]],
+ * bit for bit (swap out / swap in).  Either pool may be host memory the GPU can
+ * address (page-locked, e.g. cudaHostAlloc or a pinned torch tensor): the copy
+ * kernel reads and writes it directly.  src_ids / dst_ids must be readable by
+ * the GPU.  Pair i is skipped, and PKV_DEV_BAD_BLOCK_ID recorded, when an id
+ * is outside its pool.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+PKV_API int pkv_copy_blocks_between(void *dst_k, void *dst_v, int64_t dst_num_blocks, const void *src_k,
+                                    const void *src_v, int64_t src_num_blocks, const int32_t *src_ids,
+                                    const int32_t *dst_ids, int n, int num_kv_heads, int head_dim,
+                                    int block_size, pkv_stream_t stream);
 
 /* Bytes of workspace pkv_decode_attention needs for contexts up to
  * max_context tokens (0 when one partition covers max_context): fp32 partials

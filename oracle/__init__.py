@@ -115,6 +115,8 @@ class Oracle:
         lib.oracle_decode_multi.restype = None
         lib.oracle_decode_multi.argtypes = [_f64p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p] + \
             [ctypes.c_int] * 6 + [ctypes.c_double]
+        lib.oracle_copy_blocks_between.restype = None
+        lib.oracle_copy_blocks_between.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, _i32p] + [ctypes.c_int] * 4
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
         self.lib = lib
@@ -160,6 +162,19 @@ class Oracle:
         ds = np.ascontiguousarray(dst, dtype=np.int32)
         self.lib.oracle_copy_blocks(_p(kc, _u16p), _p(vc, _u16p), _p(sr, _i32p), _p(ds, _i32p), sr.shape[0], hkv,
                                     d, bs)
+
+    def copy_blocks_between(self, dst_k: np.ndarray, dst_v: np.ndarray, src_k: np.ndarray, src_v: np.ndarray, src,
+                            dst) -> None:
+        """In place on dst_k / dst_v: whole blocks dst[i] <- src[i] of the source pools."""
+        nb, hkv, bs, d = src_k.shape
+        assert dst_k.shape[1:] == src_k.shape[1:] and dst_v.shape == dst_k.shape and src_v.shape == src_k.shape
+        dk, dv = _bits(dst_k), _bits(dst_v)
+        assert np.shares_memory(dk, dst_k) and np.shares_memory(dv, dst_v)
+        sk, sv = _bits(src_k), _bits(src_v)
+        sr = np.ascontiguousarray(src, dtype=np.int32)
+        ds = np.ascontiguousarray(dst, dtype=np.int32)
+        self.lib.oracle_copy_blocks_between(_p(dk, _u16p), _p(dv, _u16p), _p(sk, _u16p), _p(sv, _u16p), _p(sr, _i32p),
+                                            _p(ds, _i32p), sr.shape[0], hkv, d, bs)
 
     def quantize_k_row(self, k_row) -> tuple[np.ndarray, float]:
         """(int8 codes [D], float32 scale) of one fp16 K row."""
@@ -310,6 +325,10 @@ def copy_blocks(k_cache, v_cache, src, dst):
 
 def quantize_k_row(k_row):
     return default().quantize_k_row(k_row)
+
+
+def copy_blocks_between(dst_k, dst_v, src_k, src_v, src, dst):
+    return default().copy_blocks_between(dst_k, dst_v, src_k, src_v, src, dst)
 
 
 def decode_multi(q, k_cache, v_cache, block_tables, context_lens, query_start, scale):

@@ -146,6 +146,22 @@ void oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *src
     }
 }
 
+/* Whole blocks from one pool to another (swap out / swap in, "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 3.2: pages move in and out at page granularity): dst_k[dst[i]] <- src_k[src[i]] and the
+ * same for V, raw 16-bit patterns; both pools [blocks][num_kv_heads][block_size][head_dim]. */
+void oracle_copy_blocks_between(uint16_t *dst_k, uint16_t *dst_v, const uint16_t *src_k, const uint16_t *src_v,
+                                const int32_t *src, const int32_t *dst, int n, int num_kv_heads, int head_dim,
+                                int block_size)
+{
+    int64_t elems = (int64_t)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < n; ++i) {
+        for (int64_t e = 0; e < elems; ++e) {
+            dst_k[(int64_t)dst[i] * elems + e] = src_k[(int64_t)src[i] * elems + e];
+            dst_v[(int64_t)dst[i] * elems + e] = src_v[(int64_t)src[i] * elems + e];
+        }
+    }
+}
+
 /* scores s_p = scale * q . K[p] for p in [p0, p1) of request b, kv head j. */
 static void scores_range(double *s, const uint16_t *q_row, const uint16_t *k_cache,
                          const int32_t *bt_row, int p0, int p1, int j,

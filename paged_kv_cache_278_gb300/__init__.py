@@ -30,6 +30,7 @@ __all__ = [
     "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
     "decode_step", "make_step_workspace", "copy_blocks", "append_int8k", "decode_attention_int8k",
     "decode_step_int8k", "empty_int8k_cache", "decode_attention_multi", "make_multi_workspace",
+    "copy_blocks_between",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -391,6 +392,41 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor,
     _lib.check(st, "pkv_copy_blocks")
 
 
+def _gpu_addressable(t: torch.Tensor, name: str, device):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.is_cuda:
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+    elif not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or page-locked host memory")
+
+
+def copy_blocks_between(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor,
+                        src_ids: torch.Tensor, dst_ids: torch.Tensor, device=None, stream=None) -> None:
+    """dst_k[dst_ids[i]] <- src_k[src_ids[i]] (and V), whole blocks, bit for bit.  Pools and id arrays may
+    be CUDA tensors or pinned host tensors (the copy kernel addresses host memory directly)."""
+    dev = torch.device(device) if device is not None else next(
+        (t.device for t in (dst_k, src_k, src_ids) if t.is_cuda), torch.device("cuda", torch.cuda.current_device()))
+    for t, name in ((dst_k, "dst_k"), (dst_v, "dst_v"), (src_k, "src_k"), (src_v, "src_v")):
+        if t.dtype != torch.float16 or t.dim() != 4:
+            raise ValueError(f"{name} must be fp16 [blocks, Hkv, bs, D]")
+        _gpu_addressable(t, name, dev)
+    for t, name in ((src_ids, "src_ids"), (dst_ids, "dst_ids")):
+        if t.dtype != torch.int32 or t.dim() != 1:
+            raise ValueError(f"{name} must be int32 [n]")
+        _gpu_addressable(t, name, dev)
+    if dst_k.shape != dst_v.shape or src_k.shape != src_v.shape or dst_k.shape[1:] != src_k.shape[1:]:
+        raise ValueError("pools differ in geometry")
+    if src_ids.shape != dst_ids.shape:
+        raise ValueError("src_ids and dst_ids differ in length")
+    _, hkv, bs, d = src_k.shape
+    st = _L().pkv_copy_blocks_between(dst_k.data_ptr(), dst_v.data_ptr(), dst_k.shape[0], src_k.data_ptr(),
+                                      src_v.data_ptr(), src_k.shape[0], src_ids.data_ptr(), dst_ids.data_ptr(),
+                                      src_ids.numel(), hkv, d, bs, _stream(dev, stream))
+    _lib.check(st, "pkv_copy_blocks_between")
+
+
 def slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int) -> torch.Tensor:
     """Host slot of each request's new token: int64 [B] (CPU tensors in, CPU tensor out)."""
     bt = block_tables.to(torch.int32).contiguous().cpu()
@@ -463,6 +499,17 @@ class BlockPool:
                                           ctypes.byref(src), ctypes.byref(dst), ctypes.byref(n))
         _lib.check(st, "pkv_pool_prepare_append")
         return (src.value, dst.value) if n.value else None
+
+    def swap_to(self, other: "BlockPool", table_row: torch.Tensor, num_tokens: int, block_size: int):
+        """Move the request's blocks into `other` (swap out / in); returns (src_ids, dst_ids) int32 CPU
+        tensors of the block pairs to copy with copy_blocks_between.  table_row is rewritten."""
+        n = -(-num_tokens // block_size)
+        src = torch.empty(max(n, 1), dtype=torch.int32)
+        dst = torch.empty(max(n, 1), dtype=torch.int32)
+        st = _L().pkv_pool_swap(self._h, other._h, self._row(table_row), table_row.numel(), num_tokens, block_size,
+                                self._row(src), self._row(dst))
+        _lib.check(st, "pkv_pool_swap")
+        return src[:n], dst[:n]
 
     def free_table(self, table_row: torch.Tensor, num_tokens: int, block_size: int) -> None:
         _lib.check(_L().pkv_pool_free_table(self._h, self._row(table_row), num_tokens, block_size),

@@ -63,6 +63,9 @@ SIGNATURES = {
     "pkv_decode_multi_workspace_size": (c_size_t, [c_int] * 7),
     "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 8 + [c_int64, c_float, c_void_p, c_size_t,
                                                                            c_void_p]),
+    "pkv_pool_swap": (c_int, [c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_i32p, c_i32p]),
+    "pkv_copy_blocks_between": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
+                                        c_void_p, c_int, c_int, c_int, c_int, c_void_p]),
     "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
     "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,

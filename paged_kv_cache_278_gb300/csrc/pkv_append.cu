@@ -88,10 +88,13 @@ __global__ void __launch_bounds__(kAppendThreads)
     if (lane == 0) k_scale[dst] = s;
 }
 
-// Copy-on-write: one thread per 16-byte piece of a block (all kv heads), K then V.
+// Whole-block copies (copy-on-write within a pool, swap between a device pool and host swap
+// space): one thread per 16-byte piece of a block (all kv heads), K then V.  Plain loads and
+// stores, so either side may be page-locked host memory the GPU addresses directly.
 __global__ void __launch_bounds__(kAppendThreads)
-    copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, const int32_t *__restrict__ src,
-                       const int32_t *__restrict__ dst, int64_t pieces_per_block, int n, int64_t num_blocks) {
+    copy_blocks_kernel(uint4 *dst_k, uint4 *dst_v, int64_t dst_blocks, const uint4 *src_k, const uint4 *src_v,
+                       int64_t src_blocks, const int32_t *__restrict__ src, const int32_t *__restrict__ dst,
+                       int64_t pieces_per_block, int n) {
     int64_t idx = static_cast<int64_t>(blockIdx.x) * kAppendThreads + threadIdx.x;
     const int64_t per_tensor = pieces_per_block * n;
     const bool is_v = idx >= per_tensor;
@@ -99,13 +102,32 @@ __global__ void __launch_bounds__(kAppendThreads)
     if (idx >= per_tensor) return;
     const int pair = static_cast<int>(idx / pieces_per_block);
     const int64_t piece = idx - pair * pieces_per_block;
-    const int32_t s = __ldg(src + pair), d = __ldg(dst + pair);
-    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+    const int32_t s = src[pair], d = dst[pair];
+    if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
         if (piece == 0) pkv::record_error(&g_append_error, PKV_DEV_BAD_BLOCK_ID);
         return;
     }
-    uint4 *cache = is_v ? v_cache : k_cache;
-    cache[d * pieces_per_block + piece] = cache[s * pieces_per_block + piece];
+    (is_v ? dst_v : dst_k)[d * pieces_per_block + piece] = (is_v ? src_v : src_k)[s * pieces_per_block + piece];
+}
+
+int launch_copy_blocks(void *dst_k, void *dst_v, int64_t dst_blocks, const void *src_k, const void *src_v,
+                       int64_t src_blocks, const int32_t *src, const int32_t *dst, int n, int num_kv_heads,
+                       int head_dim, int block_size, pkv_stream_t stream) {
+    if (!dst_k || !dst_v || !src_k || !src_v || (n > 0 && (!src || !dst))) return PKV_ERR_INVALID_ARG;
+    if (n < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || dst_blocks <= 0 || src_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!pkv_internal::aligned16(dst_k) || !pkv_internal::aligned16(dst_v) || !pkv_internal::aligned16(src_k) ||
+        !pkv_internal::aligned16(src_v) || (n > 0 && (!pkv_internal::aligned(src, 4) || !pkv_internal::aligned(dst, 4))))
+        return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    const int64_t pieces = static_cast<int64_t>(num_kv_heads) * block_size * head_dim / 8;
+    const int64_t blocks = (2 * pieces * n + kAppendThreads - 1) / kAppendThreads;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    copy_blocks_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v), dst_blocks, static_cast<const uint4 *>(src_k),
+        static_cast<const uint4 *>(src_v), src_blocks, src, dst, pieces, n);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace
@@ -113,17 +135,16 @@ __global__ void __launch_bounds__(kAppendThreads)
 extern "C" PKV_API int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst, int n,
                                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                        pkv_stream_t stream) {
-    if (!k_cache || !v_cache || (n > 0 && (!src || !dst))) return PKV_ERR_INVALID_ARG;
-    if (n < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
-    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
-    if (!pkv_internal::aligned16(k_cache) || !pkv_internal::aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
-    if (n == 0) return PKV_OK;
-    const int64_t pieces = static_cast<int64_t>(num_kv_heads) * block_size * head_dim / 8;
-    const int64_t blocks = (2 * pieces * n + kAppendThreads - 1) / kAppendThreads;
-    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
-    copy_blocks_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src, dst, pieces, n, num_blocks);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_copy_blocks(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src, dst, n, num_kv_heads,
+                              head_dim, block_size, stream);
+}
+
+extern "C" PKV_API int pkv_copy_blocks_between(void *dst_k, void *dst_v, int64_t dst_num_blocks, const void *src_k,
+                                               const void *src_v, int64_t src_num_blocks, const int32_t *src_ids,
+                                               const int32_t *dst_ids, int n, int num_kv_heads, int head_dim,
+                                               int block_size, pkv_stream_t stream) {
+    return launch_copy_blocks(dst_k, dst_v, dst_num_blocks, src_k, src_v, src_num_blocks, src_ids, dst_ids, n,
+                              num_kv_heads, head_dim, block_size, stream);
 }
 
 extern "C" PKV_API int pkv_append_int8k(void *k_codes, float *k_scale, void *v_cache, const int64_t *slot_mapping,

@@ -613,7 +613,11 @@ struct TcEngine {
         top[1] = fmaxf(top[1], cm1);
         if (__any_sync(pkv::kFullMask, cm0 > m_ref[0] + kRescaleThreshold || cm1 > m_ref[1] + kRescaleThreshold)) {
             const float n0 = fmaxf(m_ref[0], cm0), n1 = fmaxf(m_ref[1], cm1);
-            const float a0 = exp2f(m_ref[0] - n0), a1 = exp2f(m_ref[1] - n1);
+            float a0 = exp2f(m_ref[0] - n0), a1 = exp2f(m_ref[1] - n1);
+            if (kAnyMasked) {  // a column still without a visible token: nothing to rescale (-inf - -inf)
+                a0 = n0 == -INFINITY ? 1.f : a0;
+                a1 = n1 == -INFINITY ? 1.f : a1;
+            }
             m_ref[0] = n0;
             m_ref[1] = n1;
             l_part[0] *= a0;

@@ -185,6 +185,31 @@ PKV_API int pkv_pool_free_table(pkv_pool *pool, const int32_t *table_row, int nu
     return pkv_pool_free(pool, static_cast<int>(n), table_row);
 }
 
+PKV_API int pkv_pool_swap(pkv_pool *from, pkv_pool *to, int32_t *table_row, int max_blocks, int num_tokens,
+                          int block_size, int32_t *src_ids, int32_t *dst_ids) {
+    if (!from || !to || from == to || !table_row || max_blocks <= 0 || num_tokens < 0 || block_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t n = (static_cast<int64_t>(num_tokens) + block_size - 1) / block_size;
+    if (n > max_blocks) return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    if (!src_ids || !dst_ids) return PKV_ERR_INVALID_ARG;
+    const int64_t nb = static_cast<int64_t>(from->refcount.size());
+    std::unordered_map<int32_t, int> seen;
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t id = table_row[i];
+        if (id < 0 || id >= nb || from->refcount[id] != 1 || ++seen[id] > 1) return PKV_ERR_INVALID_ARG;
+    }
+    const int st = pkv_pool_alloc(to, static_cast<int>(n), dst_ids);
+    if (st != PKV_OK) return st;
+    for (int64_t i = 0; i < n; ++i) {
+        src_ids[i] = table_row[i];
+        from->refcount[table_row[i]] = 0;
+        from->free_list.push_back(table_row[i]);
+        table_row[i] = dst_ids[i];
+    }
+    return PKV_OK;
+}
+
 PKV_API int pkv_slot_mapping(int64_t *slots, const int32_t *block_tables, const int32_t *positions, int num_seqs,
                              int max_blocks_per_seq, int block_size) {
     if (!slots || !block_tables || !positions || num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0)

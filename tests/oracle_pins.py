@@ -129,6 +129,20 @@ def pin_copy_blocks_golden(orc):
     assert np.array_equal(vc, np.array(g["v_cache_after"], np.float16))
 
 
+def pin_copy_blocks_between_golden(orc):
+    """The same hand-worked pool copied into a second, 2-block pool (swap out): the destination
+    receives source blocks 3 and 0 as its blocks 0 and 1; the source is left as it was."""
+    g = golden("copy_blocks_tiny.json")
+    sk = np.array(g["k_cache_before"], np.float16)
+    sv = np.array(g["v_cache_before"], np.float16)
+    dk = np.zeros((2,) + sk.shape[1:], np.float16)
+    dv = np.zeros_like(dk)
+    orc.copy_blocks_between(dk, dv, sk, sv, [3, 0], [0, 1])
+    assert np.array_equal(dk, np.array([g["k_cache_before"][3], g["k_cache_before"][0]], np.float16))
+    assert np.array_equal(dv, np.array([g["v_cache_before"][3], g["v_cache_before"][0]], np.float16))
+    assert np.array_equal(sk, np.array(g["k_cache_before"], np.float16))
+
+
 def pin_copy_on_write_keeps_attention(orc):
     """A request whose table points at a copied block must attend exactly as before the copy,
     and appending into the copy must leave the original block's readers unchanged."""
@@ -474,6 +488,7 @@ ALL_PINS = [
     pin_kv_bytes_worked_example,
     pin_append_golden,
     pin_copy_blocks_golden,
+    pin_copy_blocks_between_golden,
     pin_copy_on_write_keeps_attention,
     pin_quantize_golden,
     pin_quantize_properties,

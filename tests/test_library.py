@@ -326,3 +326,61 @@ def test_copy_on_write_flow_against_the_oracle(lib):
     after = oracle.decode(q, kpool, vpool, bt, np.array([ctx, ctx + 1], np.int32), 0.1)
     assert np.array_equal(after[0], before[0])
     assert not np.allclose(after[1], before[1])
+
+
+def test_pool_swap_out_and_in(lib):
+    dev_pool, host_pool = pkv.BlockPool(12, seed=1), pkv.BlockPool(6, seed=2)
+    row = torch.full((5,), -1, dtype=torch.int32)
+    dev_pool.reserve(row, 0, 50, 16)                        # 4 device blocks
+    before = row.clone()
+    src, dst = dev_pool.swap_to(host_pool, row, 50, 16)     # swap out
+    assert torch.equal(src, before[:4]) and torch.equal(row[:4], dst) and row[4] == -1
+    assert dev_pool.num_free() == 12 and host_pool.num_free() == 2
+    assert all(host_pool.refcount(int(i)) == 1 for i in dst)
+    back_src, back_dst = host_pool.swap_to(dev_pool, row, 50, 16)   # swap in (to fresh device blocks)
+    assert torch.equal(back_src, dst) and torch.equal(row[:4], back_dst)
+    assert dev_pool.num_free() == 8 and host_pool.num_free() == 6
+    # shared blocks cannot leave; too little room changes nothing
+    other = torch.full((5,), -1, dtype=torch.int32)
+    dev_pool.fork(row, other, 50, 16)
+    snap = row.clone()
+    with pytest.raises(pkv.PkvError) as e:
+        dev_pool.swap_to(host_pool, row, 50, 16)
+    assert e.value.status == _lib.PKV_ERR_INVALID_ARG and torch.equal(row, snap)
+    dev_pool.free_table(other, 50, 16)
+    small = pkv.BlockPool(3, seed=3)
+    with pytest.raises(pkv.PkvError) as e:
+        dev_pool.swap_to(small, row, 50, 16)
+    assert e.value.status == _lib.PKV_ERR_OUT_OF_BLOCKS and torch.equal(row, snap)
+    assert small.num_free() == 3 and dev_pool.num_free() == 8
+    assert lib.pkv_copy_blocks_between(None, None, 1, None, None, 1, None, None, 1, 1, 128, 16,
+                                       None) == _lib.PKV_ERR_INVALID_ARG
+
+
+def test_swap_round_trip_against_the_oracle(lib):
+    """Host pool logic + oracle copies: a request swapped out to a host pool and back into other
+    device blocks attends exactly as before."""
+    rng = np.random.default_rng(9)
+    hkv, hq, d, bs, ctx = 2, 4, 128, 16, 45
+    kdev = rng.standard_normal((10, hkv, bs, d)).astype(np.float16)
+    vdev = rng.standard_normal((10, hkv, bs, d)).astype(np.float16)
+    khost = np.zeros((4, hkv, bs, d), np.float16)
+    vhost = np.zeros_like(khost)
+    dev_pool, host_pool = pkv.BlockPool(10, seed=4), pkv.BlockPool(4, seed=5)
+    row = torch.full((3,), -1, dtype=torch.int32)
+    dev_pool.reserve(row, 0, ctx, bs)
+    q = rng.standard_normal((1, hq, d)).astype(np.float16)
+    ctxs = np.array([ctx], np.int32)
+    before = oracle.decode(q, kdev, vdev, row.numpy()[None], ctxs, 0.2)
+    src, dst = dev_pool.swap_to(host_pool, row, ctx, bs)
+    oracle.copy_blocks_between(khost, vhost, kdev, vdev, src.numpy(), dst.numpy())
+    kdev[src.numpy()] = np.nan                                # the freed device blocks get reused
+    vdev[src.numpy()] = np.nan
+    dev_pool.alloc(dev_pool.num_free())                        # take every free block: swap-in must wait
+    with pytest.raises(pkv.PkvError):
+        host_pool.swap_to(dev_pool, row, ctx, bs)
+    dev_pool.free(list(range(10)))
+    src2, dst2 = host_pool.swap_to(dev_pool, row, ctx, bs)
+    oracle.copy_blocks_between(kdev, vdev, khost, vhost, src2.numpy(), dst2.numpy())
+    after = oracle.decode(q, kdev, vdev, row.numpy()[None], ctxs, 0.2)
+    assert np.array_equal(before, after)

@@ -43,6 +43,8 @@ MUTANTS = {
                                "int64_t row = (blk * num_kv_heads) * block_size + off;"),
     "multi_misses_own_position": ("int visible = ctx - n + i + 1;", "int visible = ctx - n + i;"),
     "multi_row_offset": ("int64_t t = query_start[b] + i;", "int64_t t = query_start[b] + n - 1 - i;"),
+    "swap_copy_wrong_index": ("dst_k[(int64_t)dst[i] * elems + e] = src_k[(int64_t)src[i] * elems + e];",
+                              "dst_k[(int64_t)dst[i] * elems + e] = src_k[(int64_t)dst[i] * elems + e];"),
     "copy_blocks_one_head": ("int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;",
                              "int64_t per_block = (int64_t)block_size * head_dim;"),
 }

@@ -102,3 +102,49 @@ def test_fork_then_diverge_decode_step(bs):
     for r in rows:
         pool.free_table(r, ctx + 1, bs)
     assert pool.num_free() == nb
+
+
+def test_swap_out_to_pinned_host_and_back():
+    """A request's blocks go to a page-locked host pool (the copy kernel writes host memory
+    directly) and come back into other device blocks; the host pool matches the oracle's copy bit
+    for bit and the decode output over the new table is bit-identical to the one before."""
+    rng = np.random.default_rng(77)
+    hq, hkv, d, bs, nb, nh = 16, 4, 128, 16, 64, 24
+    ctxs = [300, 170]
+    kc = torch.from_numpy(rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)).cuda()
+    vc = torch.from_numpy(rng.standard_normal((nb, hkv, bs, d)).astype(np.float16)).cuda()
+    kh = torch.zeros((nh, hkv, bs, d), dtype=torch.float16).pin_memory()
+    vh = torch.zeros((nh, hkv, bs, d), dtype=torch.float16).pin_memory()
+    dev_pool, host_pool = pkv.BlockPool(nb, seed=11), pkv.BlockPool(nh, seed=12)
+    maxb = -(-max(ctxs) // bs)
+    rows = [torch.full((maxb,), -1, dtype=torch.int32) for _ in ctxs]
+    for r, c in zip(rows, ctxs):
+        dev_pool.reserve(r, 0, c, bs)
+    q = torch.from_numpy(rng.standard_normal((2, hq, d)).astype(np.float16)).cuda()
+    lens = torch.tensor(ctxs, dtype=torch.int32, device="cuda")
+    scale = d ** -0.5
+
+    def decode():
+        out = torch.empty_like(q)
+        pkv.decode_attention(out, q, kc, vc, torch.stack(rows).cuda(), lens, scale)
+        return out
+
+    before = decode()
+    host_before = (kc.cpu().numpy(), vc.cpu().numpy())
+    # swap request 0 out: ids passed in pinned host memory
+    src, dst = dev_pool.swap_to(host_pool, rows[0], ctxs[0], bs)
+    pkv.copy_blocks_between(kh, vh, kc, vc, src.pin_memory(), dst.pin_memory(), device="cuda")
+    torch.cuda.synchronize()
+    ko, vo = np.zeros(kh.shape, np.float16), np.zeros(vh.shape, np.float16)
+    oracle.copy_blocks_between(ko, vo, host_before[0], host_before[1], src.numpy(), dst.numpy())
+    assert np.array_equal(kh.numpy().view(np.uint16), ko.view(np.uint16))
+    assert np.array_equal(vh.numpy().view(np.uint16), vo.view(np.uint16))
+    # the freed device blocks are reused by someone else
+    kc[src.long().cuda()] = float("nan")
+    vc[src.long().cuda()] = float("nan")
+    # swap back in (ids on the device this time) to whatever blocks the pool hands out
+    src2, dst2 = host_pool.swap_to(dev_pool, rows[0], ctxs[0], bs)
+    pkv.copy_blocks_between(kc, vc, kh, vh, src2.cuda(), dst2.cuda())
+    after = decode()
+    assert torch.equal(before, after)
+    assert_no_device_error()
