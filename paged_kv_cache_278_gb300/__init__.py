@@ -407,7 +407,9 @@ def copy_blocks_between(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.T
     """dst_k[dst_ids[i]] <- src_k[src_ids[i]] (and V), whole blocks, bit for bit.  Pools and id arrays may
     be CUDA tensors or pinned host tensors (the copy kernel addresses host memory directly)."""
     dev = torch.device(device) if device is not None else next(
-        (t.device for t in (dst_k, src_k, src_ids) if t.is_cuda), torch.device("cuda", torch.cuda.current_device()))
+        (t.device for t in (dst_k, src_k, src_ids) if t.is_cuda), torch.device("cuda"))
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     for t, name in ((dst_k, "dst_k"), (dst_v, "dst_v"), (src_k, "src_k"), (src_v, "src_v")):
         if t.dtype != torch.float16 or t.dim() != 4:
             raise ValueError(f"{name} must be fp16 [blocks, Hkv, bs, D]")
