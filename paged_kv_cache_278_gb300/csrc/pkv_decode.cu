@@ -65,9 +65,11 @@ constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 #ifndef PKV_DECODE_MIN_CTAS
 #define PKV_DECODE_MIN_CTAS 3
 #endif
-// Resident CTAs per SM the int8-key kernel is compiled for (its stages are 6 KB, not 8 KB).
+// Resident CTAs per SM the int8-key kernel is compiled for: its stages are 6 KB, not 8 KB, so four
+// CTAs (53 KB of shared memory, 128 registers per thread) fit an SM and keep as many bytes in flight
+// as three fp16 CTAs.
 #ifndef PKV_DECODE_KQ_MIN_CTAS
-#define PKV_DECODE_KQ_MIN_CTAS 3
+#define PKV_DECODE_KQ_MIN_CTAS 4
 #endif
 // 1: q.K and P.V use packed two-lane FMAs (fma.rn.f32x2), halving FMA issue slots.
 #ifndef PKV_DECODE_FFMA2
