@@ -71,6 +71,12 @@ constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 #ifndef PKV_DECODE_KQ_MIN_CTAS
 #define PKV_DECODE_KQ_MIN_CTAS 4
 #endif
+// 1: K and V of a stage land on separate mbarriers, so a chunk's q.K starts as soon as its K has
+// arrived and the next K copy into the stage is issued before the chunk's P.V runs.  Measured 1-2.5%
+// slower on every workload (twice the barrier traffic for no gain in bytes in flight): off.
+#ifndef PKV_DECODE_SPLIT_KV
+#define PKV_DECODE_SPLIT_KV 0
+#endif
 // 1: q.K and P.V use packed two-lane FMAs (fma.rn.f32x2), halving FMA issue slots.
 #ifndef PKV_DECODE_FFMA2
 #define PKV_DECODE_FFMA2 1
@@ -82,6 +88,8 @@ constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = PKV_DECODE_STAGES;
+constexpr bool kSplitKV = PKV_DECODE_SPLIT_KV != 0;
+constexpr int kBarsPerStage = kSplitKV ? 2 : 1;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -142,7 +150,7 @@ struct SmemLayout {
     static constexpr int stage_bytes = kWarps * kStages * stage;
     static constexpr int scales = stages + stage_bytes;
     static constexpr int bars = scales + (KQ ? kWarps * kStages * kChunk * 4 : 0);
-    static constexpr int probs = bars + kWarps * kStages * 8;
+    static constexpr int probs = bars + kWarps * kStages * kBarsPerStage * 8;
     __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? 2 * 8 * kChunk * 2 : kChunk * g * 4; }
     __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
     __host__ __device__ static constexpr int table(int g) { return newrow(g) + 2 * kRowBytes; }
@@ -381,8 +389,8 @@ struct FmaEngine {
         }
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
-                                          unsigned char *scratch, int) {
+    // q . K, online softmax and the chunk's probabilities into the warp's scratch (ends synchronised).
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t, int valid, int lane, unsigned char *scratch, int) {
         float *s_prob = reinterpret_cast<float *>(scratch);
         // ---- q . K partial sums: v[h * TPL + i] over this lane's dims
         float v[N];
@@ -475,7 +483,11 @@ struct FmaEngine {
             }
         }
         __syncwarp();
+    }
 
+    // P . V of the chunk whose probabilities qk() left in scratch.
+    __device__ __forceinline__ void pv(uint32_t v_tile, int valid, int lane, unsigned char *scratch) {
+        const float *s_prob = reinterpret_cast<const float *>(scratch);
         // ---- P . V: this lane owns dims [4*lane, 4*lane+4) of every packed head
 #pragma unroll
         for (int t = 0; t < kChunk; ++t) {
@@ -586,8 +598,7 @@ struct TcEngine {
         }
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
-                                          unsigned char *scratch, int) {
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t, int valid, int lane, unsigned char *scratch, int) {
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         dots(s, k_tile, lane);
         const int g = lane >> 2;
@@ -595,15 +606,15 @@ struct TcEngine {
         s[1] = g < valid ? s[1] * q_scale : -INFINITY;
         s[2] = g + 8 < valid ? s[2] * q_scale : -INFINITY;
         s[3] = g + 8 < valid ? s[3] * q_scale : -INFINITY;
-        softmax_pv(s, v_tile, lane, scratch);
+        softmax(s, lane, scratch);
     }
 
     // Online softmax of the chunk's scaled, masked log2-domain scores s (token g / g + 8, heads
-    // h0 / h0 + 1) and the P.V product into the O^T accumulators.  kAnyMasked: a column may have
-    // no visible token yet (its reference max still -inf), so a masked score's weight is forced
-    // to 0 instead of exp2(-inf - -inf).
+    // h0 / h0 + 1); the weights go to the warp's scratch as fp16 hi / lo parts for pv() (ends
+    // synchronised).  kAnyMasked: a column may have no visible token yet (its reference max still
+    // -inf), so a masked score's weight is forced to 0 instead of exp2(-inf - -inf).
     template <bool kAnyMasked = false>
-    __device__ __forceinline__ void softmax_pv(float (&s)[4], uint32_t v_tile, int lane, unsigned char *scratch) {
+    __device__ __forceinline__ void softmax(float (&s)[4], int lane, unsigned char *scratch) {
         const int g = lane >> 2;
         float cm0 = fmaxf(s[0], s[2]), cm1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -652,6 +663,12 @@ struct TcEngine {
             pl[idx] = __float2half_rn(p[e] - __half2float(hi));
         }
         __syncwarp();
+    }
+
+    // O^T += V_tile^T . P^T with the weights softmax() left in scratch.
+    __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *scratch) {
+        const __half *ph = reinterpret_cast<const __half *>(scratch);
+        const __half *pl = ph + 8 * kChunk;
         const int n = lane >> 2, k0 = (lane & 3) * 2;
         const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + n * kChunk + k0);
         const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + n * kChunk + k0 + 8);
@@ -728,8 +745,8 @@ struct TcEngineQ : TcEngine<G> {
         this->reset(P);
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t s_tile, int valid, int lane,
-                                          unsigned char *scratch, int) {
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t s_tile, int valid, int lane, unsigned char *scratch,
+                                       int) {
         const int g = lane >> 2, t = lane & 3;
         const uint4 r0 = pkv::lds128(k_tile + swz8(g, 2 * t)), r1 = pkv::lds128(k_tile + swz8(g, 2 * t + 1));
         const uint4 r8 = pkv::lds128(k_tile + swz8(g + 8, 2 * t)), r9 = pkv::lds128(k_tile + swz8(g + 8, 2 * t + 1));
@@ -749,7 +766,7 @@ struct TcEngineQ : TcEngine<G> {
         s[1] = g < valid ? s[1] * fg : -INFINITY;
         s[2] = g + 8 < valid ? s[2] * f8 : -INFINITY;
         s[3] = g + 8 < valid ? s[3] * f8 : -INFINITY;
-        this->softmax_pv(s, v_tile, lane, scratch);
+        this->softmax(s, lane, scratch);
     }
 };
 
@@ -780,8 +797,8 @@ struct TcEngineM : TcEngine<8> {
         }
     }
 
-    __device__ __forceinline__ void chunk(uint32_t k_tile, uint32_t v_tile, uint32_t, int valid, int lane,
-                                          unsigned char *scratch, int tok0) {
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t, int valid, int lane, unsigned char *scratch,
+                                       int tok0) {
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         dots(s, k_tile, lane);
         const int g = lane >> 2;
@@ -790,7 +807,7 @@ struct TcEngineM : TcEngine<8> {
         s[1] = g < valid && p0 <= lim[1] ? s[1] * q_scale : -INFINITY;
         s[2] = g + 8 < valid && p8 <= lim[0] ? s[2] * q_scale : -INFINITY;
         s[3] = g + 8 < valid && p8 <= lim[1] ? s[3] * q_scale : -INFINITY;
-        softmax_pv<true>(s, v_tile, lane, scratch);
+        softmax<true>(s, lane, scratch);
     }
 };
 
@@ -907,7 +924,9 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
 
     int32_t *s_table = reinterpret_cast<int32_t *>(smem + L::table(G));
     unsigned char *scratch = smem + L::probs + warp * L::probs_per_warp(G);
-    const uint32_t bar0 = pkv::smem_addr(smem + L::bars) + warp * kStages * 8;
+    // per warp: the K barriers of its stages, then (split K/V) the V barriers
+    const uint32_t bar0 = pkv::smem_addr(smem + L::bars) + warp * kStages * kBarsPerStage * 8;
+    const uint32_t bar_v0 = bar0 + (kSplitKV ? 8 * kStages : 0);
     const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * L::stage;
     const uint32_t scale0 = pkv::smem_addr(smem + L::scales) + warp * kStages * kChunk * 4;
 
@@ -917,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     }
     if (lane == 0) {
 #pragma unroll
-        for (int s = 0; s < kStages; ++s) pkv::mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < kStages * kBarsPerStage; ++s) pkv::mbar_init(bar0 + 8 * s, 1);
         pkv::fence_mbar_init();
     }
     const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
@@ -934,7 +953,9 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     const void *tmap_v = &P.tmap_v;
     const float *ksc = P.k_scale;
     const int hkv = P.num_kv_heads;
-    auto issue_from = [=](int i, int64_t phys) {
+    // parts: 1 = K (with the int8 keys' scales), 2 = V, 3 = both.  Without split K/V both land on
+    // one barrier with one expect_tx for their sum.
+    auto issue_from = [=](int i, int64_t phys, int parts) {
         const int cidx = warp + i * kWarps;
         const int tok0 = start + cidx * kChunk;
         const int valid = min(kChunk, n_tok - cidx * kChunk);
@@ -943,44 +964,44 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         const int64_t byte_off = phys * block_stride + kvh * head_stride + static_cast<int64_t>(off) * kRowBytes;
         const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
         const int st = i % kStages;
-        const uint32_t bar = bar0 + 8 * st;
+        const uint32_t bar_k = bar0 + 8 * st;
+        const uint32_t bar_v = bar_v0 + 8 * st;
         const uint32_t dst = stage0 + st * L::stage;
-        if constexpr (KQ) {
-            // One 16-row box of int8 keys, two fp16 V half-boxes and the 16 key scales (64 B).
-            if (lane == 0) {
-                const int64_t y = (phys * hkv + kvh) * bs + off;
-                pkv::mbar_arrive_expect_tx(bar, L::k_tile + 2 * kHalfTile + kChunk * 4);
-                pkv::tma_load_2d(dst, tmap_k, 0, static_cast<int>(y), bar);
-                pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, static_cast<int>(y), bar);
-                pkv::tma_load_2d(dst + L::k_tile + kHalfTile, tmap_v, 64, static_cast<int>(y), bar);
-                pkv::bulk_copy_g2s(scale0 + st * kChunk * 4, ksc + y, kChunk * 4, bar);
-            }
-            (void)byte_off;
-            (void)bytes;
-        } else if constexpr (TC) {
-            // Whole 16-row boxes (a ragged tail's extra rows stay inside the block and are masked).
-            if (lane == 0) {
-                const int y = static_cast<int>((phys * hkv + kvh) * bs + off);
-                pkv::mbar_arrive_expect_tx(bar, 4 * kHalfTile);
-                pkv::tma_load_2d(dst, tmap_k, 0, y, bar);
-                pkv::tma_load_2d(dst + kHalfTile, tmap_k, 64, y, bar);
-                pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, y, bar);
-                pkv::tma_load_2d(dst + L::k_tile + kHalfTile, tmap_v, 64, y, bar);
-            }
-            (void)byte_off;
-            (void)bytes;
+        // TC: whole 16-row boxes (a ragged tail's extra rows stay inside the block and are masked)
+        const uint32_t k_bytes = KQ ? L::k_tile + kChunk * 4 : (TC ? 2 * kHalfTile : bytes);
+        const uint32_t v_bytes = TC ? 2 * kHalfTile : bytes;
+        if (lane != 0) return;
+        if (kSplitKV) {
+            if (parts & 1) pkv::mbar_arrive_expect_tx(bar_k, k_bytes);
+            if (parts & 2) pkv::mbar_arrive_expect_tx(bar_v, v_bytes);
         } else {
-            if (lane == 0) {
-                pkv::mbar_arrive_expect_tx(bar, 2 * bytes);
-                pkv::bulk_copy_g2s(dst, kc + byte_off, bytes, bar);
-                pkv::bulk_copy_g2s(dst + L::k_tile, vc + byte_off, bytes, bar);
+            pkv::mbar_arrive_expect_tx(bar_k, k_bytes + v_bytes);
+        }
+        const int64_t y = (phys * hkv + kvh) * bs + off;
+        if (parts & 1) {
+            if constexpr (KQ) {  // one 16-row box of int8 keys and the 16 key scales (64 B)
+                pkv::tma_load_2d(dst, tmap_k, 0, static_cast<int>(y), bar_k);
+                pkv::bulk_copy_g2s(scale0 + st * kChunk * 4, ksc + y, kChunk * 4, bar_k);
+            } else if constexpr (TC) {
+                pkv::tma_load_2d(dst, tmap_k, 0, static_cast<int>(y), bar_k);
+                pkv::tma_load_2d(dst + kHalfTile, tmap_k, 64, static_cast<int>(y), bar_k);
+            } else {
+                pkv::bulk_copy_g2s(dst, kc + byte_off, bytes, bar_k);
+            }
+        }
+        if (parts & 2) {
+            if constexpr (TC) {
+                pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, static_cast<int>(y), bar_v);
+                pkv::tma_load_2d(dst + L::k_tile + kHalfTile, tmap_v, 64, static_cast<int>(y), bar_v);
+            } else {
+                pkv::bulk_copy_g2s(dst + L::k_tile, vc + byte_off, bytes, bar_v);
             }
         }
     };
 
-    auto issue = [=](int i) {
+    auto issue = [=](int i, int parts) {
         const int tok0 = start + (warp + i * kWarps) * kChunk;
-        issue_from(i, s_table[tok0 / bs - lb0]);
+        issue_from(i, s_table[tok0 / bs - lb0], parts);
     };
 
     // Start-up: each warp reads the block ids of its first chunks straight from the table and
@@ -992,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         for (int k = 0; k < kStages; ++k) {
             if (k < pre) {
                 const int32_t id = __shfl_sync(pkv::kFullMask, first_ids[k], 0);
-                issue_from(k, (id < 0 || id >= P.num_blocks) ? 0 : id);  // bad ids: recorded by the table pass
+                issue_from(k, (id < 0 || id >= P.num_blocks) ? 0 : id, 3);  // bad ids: recorded by the table pass
             }
         }
     }
@@ -1075,63 +1096,105 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     __syncthreads();  // table + barrier init visible to every warp
 
 
-    int consumed = 0;
+    // Per chunk: wait for K, patch the appended token's K row, q.K and softmax, refill the K stage
+    // (split K/V), wait for V, clear a ragged tail's V rows (the MMA reads all 16), patch the V
+    // row, P.V, refill the V stage.  Without split K/V one wait covers both and one refill
+    // issues both.
+    int consumed_k = 0, consumed_v = 0;  // chunks whose K / V wait succeeded
+    int issued_k = my_chunks < kStages ? my_chunks : kStages, issued_v = issued_k;
     bool aborted = false;
+    auto landed = [&](uint32_t bar, int i) {
+        const bool ok = pkv::mbar_wait_bounded(bar, (i / kStages) & 1);
+        if (__all_sync(pkv::kFullMask, ok)) return true;  // warp-uniform decision
+        if (lane == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
+        aborted = true;
+        return false;
+    };
     for (int i = 0; i < my_chunks; ++i) {
         const int st = i % kStages;
-        const bool landed = pkv::mbar_wait_bounded(bar0 + 8 * st, (i / kStages) & 1);
-        if (!__all_sync(pkv::kFullMask, landed)) {  // warp-uniform decision
-            if (lane == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
-            aborted = true;
-            break;
-        }
-        consumed = i + 1;
+        if (!landed(bar0 + 8 * st, i)) break;
+        consumed_k = i + 1;
+        if (!kSplitKV) consumed_v = i + 1;
         const int cidx = warp + i * kWarps;
         const int valid = min(kChunk, n_tok - cidx * kChunk);
         const uint32_t k_tile = stage0 + st * L::stage;
         const uint32_t v_tile = k_tile + L::k_tile;
         const uint32_t s_tile = scale0 + st * kChunk * 4;
-        bool touched = false;
-        if (TC && valid < kChunk) {  // the MMA reads all 16 V rows: make the unused ones finite (zero)
-            for (int x = lane; x < (kChunk - valid) * 16; x += 32)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + TcEngine<4>::swz(valid + x / 16, x % 16)),
-                             "r"(0)
-                             : "memory");
-            touched = true;
-        }
-        if (cidx == own_chunk) {  // the appended token's row: overwrite what the copy brought
-            const int nr_row = (new_pos - start) % kChunk;
-            if (KQ && lane < 16) {
-                const uint2 nc = *reinterpret_cast<const uint2 *>(s_newrow + lane * 8);
-                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(k_tile + TcEngineQ<G>::swz8(nr_row, lane >> 1) +
-                                                                     (lane & 1) * 8),
-                             "r"(nc.x), "r"(nc.y)
-                             : "memory");
-                if (lane == 0)
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_tile + nr_row * 4),
-                                 "f"(*reinterpret_cast<const float *>(s_newrow + kD))
+        const bool own = cidx == own_chunk;
+        const int nr_row = (new_pos - start) % kChunk;
+        // the appended token's V row and a ragged tail's V rows, once V has landed
+        auto fix_v = [&]() {
+            bool touched = false;
+            if (TC && valid < kChunk) {
+                for (int x = lane; x < (kChunk - valid) * 16; x += 32)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + TcEngine<4>::swz(valid + x / 16, x % 16)),
+                                 "r"(0)
                                  : "memory");
-            } else {
-                const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
-                const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"((lane < 16 ? k_tile : v_tile) + row),
-                             "r"(nr.x), "r"(nr.y), "r"(nr.z), "r"(nr.w)
-                             : "memory");
+                touched = true;
+            }
+            if (own) {
+                if (lane >= 16) {
+                    const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
+                    const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(v_tile + row), "r"(nr.x), "r"(nr.y),
+                                 "r"(nr.z), "r"(nr.w)
+                                 : "memory");
+                }
+                touched = true;
+            }
+            return touched;
+        };
+        bool touched = false;
+        if (own) {  // the appended token's K row (lanes 0-15): overwrite what the copy brought
+            if (lane < 16) {
+                if (KQ) {
+                    const uint2 nc = *reinterpret_cast<const uint2 *>(s_newrow + lane * 8);
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(k_tile + TcEngineQ<G>::swz8(nr_row, lane >> 1) +
+                                                                         (lane & 1) * 8),
+                                 "r"(nc.x), "r"(nc.y)
+                                 : "memory");
+                    if (lane == 0)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_tile + nr_row * 4),
+                                     "f"(*reinterpret_cast<const float *>(s_newrow + kD))
+                                     : "memory");
+                } else {
+                    const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
+                    const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(k_tile + row), "r"(nr.x), "r"(nr.y),
+                                 "r"(nr.z), "r"(nr.w)
+                                 : "memory");
+                }
             }
             touched = true;
         }
+        if (!kSplitKV) touched |= fix_v();
         if (touched) __syncwarp();
-        eng.chunk(k_tile, v_tile, s_tile, valid, lane, scratch, start + cidx * kChunk);
+        eng.qk(k_tile, s_tile, valid, lane, scratch, start + cidx * kChunk);
+        if (kSplitKV) {
+            if (i + kStages < my_chunks) {
+                pkv::fence_proxy_async_smem();
+                issue(i + kStages, 1);
+                ++issued_k;
+            }
+            if (!landed(bar_v0 + 8 * st, i)) break;
+            consumed_v = i + 1;
+            if (fix_v()) __syncwarp();
+        }
+        eng.pv(v_tile, valid, lane, scratch);
         __syncwarp();
         if (i + kStages < my_chunks) {
             pkv::fence_proxy_async_smem();
-            issue(i + kStages);
+            issue(i + kStages, kSplitKV ? 2 : 3);
+            if (!kSplitKV) ++issued_k;
+            ++issued_v;
         }
     }
     if (aborted) {
-        // Let this warp's copies still in flight land before the buffers are reused.
-        const int issued = my_chunks < consumed + kStages ? my_chunks : consumed + kStages;
-        for (int i = consumed + 1; i < issued; ++i) pkv::mbar_wait_bounded(bar0 + 8 * (i % kStages), (i / kStages) & 1);
+        // Let this warp's copies still in flight land before the buffers are reused (bounded waits).
+        for (int i = consumed_k; i < issued_k; ++i) pkv::mbar_wait_bounded(bar0 + 8 * (i % kStages), (i / kStages) & 1);
+        if (kSplitKV)
+            for (int i = consumed_v; i < issued_v; ++i)
+                pkv::mbar_wait_bounded(bar_v0 + 8 * (i % kStages), (i / kStages) & 1);
     }
 
     // ---- merge the 4 warps in shared memory (reusing the stage buffers)
