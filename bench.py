@@ -201,7 +201,7 @@ def make_layer(workload: str, layer: int, bs: int, device, step: int = 1):
 
 
 def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tokens=0, num_seqs=None,
-                 kv="fp16"):
+                 kv="fp16", q_len=1):
     """Algorithmic bytes of one decode-attention call: K and V of every cached token read once
     (a shared prefix once), q read, out written, block-table entries and context lengths read.
     kv="int8k": a key row is head_dim int8 codes plus one float32 scale."""
@@ -209,7 +209,7 @@ def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tok
     tokens = sum(ctx) - unique_prefix_tokens * (b - 1) if unique_prefix_tokens else sum(ctx)
     k_row = head_dim + 4 if kv == "int8k" else head_dim * 2
     kv = tokens * num_kv_heads * (k_row + head_dim * 2)
-    qo = 2 * b * num_q_heads * head_dim * 2
+    qo = 2 * b * q_len * num_q_heads * head_dim * 2
     tables = sum(-(-c // bs) for c in ctx) * 4 + 4 * b
     return kv + qo + tables
 
@@ -239,7 +239,8 @@ def run_ours(args):
     cases = [make_layer(args.workload, l, bs, dev) for l in range(n_layers)]
     c0 = cases[0]
     cpu_sample = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # host copies taken before any of our kernels run
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.query_len == 1:
+        # host copies taken before any of our kernels run (the oracle baseline times single-token steps)
         cpu_sample = {k: getattr(c0, k).cpu().numpy() for k in
                       ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
     int8k = args.kv == "int8k"
@@ -258,6 +259,15 @@ def run_ours(args):
         torch.cuda.empty_cache()
     B, Hq, Hkv, D = c0.num_seqs, c0.num_q_heads, c0.num_kv_heads, c0.head_dim
     bs = c0.block_size
+    nq = args.query_len
+    if nq > 1:
+        # several new tokens per request (a draft being verified): seeded q / K / V for all of them
+        g = torch.Generator(device=dev)
+        g.manual_seed(7000 + nq)
+        for c in cases:
+            c.q = torch.randn((B * nq, Hq, D), generator=g, device=dev).half()
+            c.k_new = torch.randn((B * nq, Hkv, D), generator=g, device=dev).half()
+            c.v_new = torch.randn((B * nq, Hkv, D), generator=g, device=dev).half()
     q_all = torch.stack([c.q for c in cases])
     kn_all = torch.stack([c.k_new for c in cases])
     vn_all = torch.stack([c.v_new for c in cases])
@@ -274,18 +284,26 @@ def run_ours(args):
     else:
         ctx_steps = [c0.context_lens.cpu().tolist()]
     ctx_dev = torch.tensor(ctx_steps, dtype=torch.int32, device=dev)
+    # slots of the step's new tokens: positions ctx - nq .. ctx - 1 of every request (request-major)
     slot_dev = torch.stack([
-        pkv.slot_mapping(block_tables.cpu(), torch.tensor(c, dtype=torch.int32) - 1, bs) for c in ctx_steps]).to(dev)
+        torch.stack([pkv.slot_mapping(block_tables.cpu(), torch.tensor(c, dtype=torch.int32) - nq + i, bs)
+                     for i in range(nq)], 1).reshape(-1) for c in ctx_steps]).to(dev)
+    query_start = torch.arange(0, (B + 1) * nq, nq, dtype=torch.int32, device=dev)
     ctx_cur = ctx_dev[0].clone()
     slot_cur = slot_dev[0].clone()
     cascade = args.workload == "shared_prefix" and not args.no_cascade
     prefix_len = 1024 if cascade else 0
-    ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev)
+    ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev) if nq == 1 else \
+        pkv.make_multi_workspace(B, B * nq, nq, Hq, Hkv, max_ctx_cap, dev)
 
     def decode(l, c):
         """One layer of the step: the append is fused into the decode kernel (pkv_decode_step) unless
         --separate-append asks for the two-call path (pkv_append + attention)."""
-        if int8k:
+        if nq > 1:
+            pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
+            pkv.decode_attention_multi(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, query_start, nq,
+                                       c.scale, workspace=ws)
+        elif int8k:
             if args.separate_append:
                 pkv.append_int8k(c.k_codes, c.k_scale, c.v_cache, slot_cur, c.k_new, c.v_new)
                 pkv.decode_attention_int8k(out_all[l], c.q, c.k_codes, c.k_scale, c.v_cache, block_tables, ctx_cur,
@@ -306,12 +324,13 @@ def run_ours(args):
                             prefix_len, ws)
 
     prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
-    bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens, kv=args.kv) for c in ctx_steps]
-    logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, kv=args.kv) for c in ctx_steps]
+    bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens, kv=args.kv, q_len=nq)
+                      for c in ctx_steps]
+    logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, kv=args.kv, q_len=nq) for c in ctx_steps]
 
     # per layer: the decode kernel (append and the split's merge fused in), plus the prefix kernel with the
     # cascade, plus the append kernel on the two-call path
-    launches_per_step = n_layers * (1 + (1 if cascade else 0) + (1 if args.separate_append else 0))
+    launches_per_step = n_layers * (1 + (1 if cascade else 0) + (1 if args.separate_append or nq > 1 else 0))
 
     def step():
         for l, c in enumerate(cases):
@@ -479,11 +498,13 @@ def run_ours(args):
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
                   % (cases[0].v_cache.numel() * (3 if int8k else 4) / 1e6, bytes_job / 1e9),
             "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
-            "decode_call": ("pkv_append" + ("_int8k" if int8k else "") + " + " if args.separate_append
-                            else "pkv_decode_step" + ("_int8k" if int8k else "") + " ")
-            + ("shared prefix 1024 tokens" if cascade else ""),
+            "decode_call": (f"pkv_append + pkv_decode_attention_multi ({nq} new tokens per request, causal)"
+                            if nq > 1 else
+                            ("pkv_append" + ("_int8k" if int8k else "") + " + " if args.separate_append
+                             else "pkv_decode_step" + ("_int8k" if int8k else "") + " ")
+                            + ("shared prefix 1024 tokens" if cascade else "")),
         },
-        "tokens_per_s": round(B * world / (ms_job * 1e-3), 1),
+        "tokens_per_s": round(B * nq * world / (ms_job * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * gbs / peak, 1),
         "decode_bytes_per_step": int(bytes_job),
         "logical_bytes_per_step": int(sum(logical_bytes_per_step) / len(logical_bytes_per_step)),
@@ -680,11 +701,17 @@ def main(argv=None):
                     help="two calls per layer (pkv_append, then attention) instead of pkv_decode_step")
     ap.add_argument("--kv", choices=["fp16", "int8k"], default="fp16",
                     help="cache format: fp16 K/V, or int8 keys with float32 row scales and fp16 values")
+    ap.add_argument("--query-len", type=int, default=1,
+                    help="new tokens per request per step (>1: append them, then causal multi-token attention)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.query_len > 1 and (args.kv != "fp16" or args.workload == "shared_prefix" or args.separate_append):
+        ap.error("--query-len > 1 runs the fp16 multi-token path on mha7b, gqa8b, long_context or tiny")
+    if args.query_len > 1 and args.impl == "reference":
+        ap.error("the reference arm times single-token steps")
     if args.kv == "int8k" and args.workload == "shared_prefix" and not args.no_cascade:
         ap.error("the shared-prefix cascade reads fp16 keys; use --no-cascade with --kv int8k")
     if args.impl == "reference":

@@ -94,3 +94,28 @@ def test_multi_workspace_reuse_and_bad_rows():
                               h.context_lens.numpy()[1:], np.array([0, 2], np.int32), bad.scale)
     assert max_err(out[5:], ref) <= ATTN_TOL
     assert not out[:5].any()
+
+
+@pytest.mark.parametrize("nq", [4, 8])
+def test_multi_full_size_gqa8b_sampled(nq):
+    """The 8B-shaped GQA workload (batch 64, 2049-token contexts, block 16) with nq new tokens per
+    request, as the benchmark runs it; requests 0, 31 and 63 compared with the oracle."""
+    case = workloads.gqa8b(0, 1, 16, device="cuda")
+    b = case.num_seqs
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7000 + nq)
+    q = torch.randn((b * nq, case.num_q_heads, 128), generator=g, device="cuda").half()
+    qs = torch.arange(0, (b + 1) * nq, nq, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.make_multi_workspace(b, b * nq, nq, case.num_q_heads, case.num_kv_heads,
+                                  case.max_blocks_per_seq * 16, "cuda")
+    pkv.decode_attention_multi(out, q, case.k_cache, case.v_cache, case.block_tables, case.context_lens, qs, nq,
+                               case.scale, workspace=ws)
+    kc, vc = case.k_cache.cpu().numpy(), case.v_cache.cpu().numpy()
+    bt, cl = case.block_tables.cpu().numpy(), case.context_lens.cpu().numpy()
+    for r in (0, 31, 63):
+        ref = oracle.decode_multi(q[r * nq:(r + 1) * nq].cpu().numpy(), kc, vc, bt[r:r + 1], cl[r:r + 1],
+                                  np.array([0, nq], np.int32), case.scale)
+        assert max_err(out[r * nq:(r + 1) * nq], ref) <= ATTN_TOL, r
+    assert torch.isfinite(out.float()).all()
+    assert_no_device_error()
