@@ -470,7 +470,7 @@ def run_ours(args):
     peak, peak_src = read_peaks()
     gbs = bytes_job / (ms_job * 1e-3) / 1e9
     achieved = kernel_bytes_avg / (kernel_avg_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload + ("/int8k" if int8k else ""), bs)
+    traffic = read_traffic(args.workload + ("/int8k" if int8k else "") + (f"/q{nq}" if nq > 1 else ""), bs)
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),

@@ -33,7 +33,12 @@ namespace {
 __device__ int g_prefix_error;
 
 constexpr int kD = PKV_HEAD_DIM;       // 128
-constexpr int kChunkTok = 64;          // prefix tokens per CTA
+#ifndef PKV_PREFIX_CHUNK
+#define PKV_PREFIX_CHUNK 64
+#endif
+constexpr int kChunkTok = PKV_PREFIX_CHUNK;  // prefix tokens per CTA (a multiple of 16)
+constexpr int kNT = kChunkTok / 8;           // 8-token MMA n-tiles of a chunk
+static_assert(kChunkTok % 16 == 0 && kChunkTok >= 16, "chunk of whole 16-token k-steps");
 constexpr int kWarps = 8;              // 16 query rows per warp
 constexpr int kRows = kWarps * 16;     // query rows per CTA
 constexpr int kThreads = kWarps * 32;
@@ -146,15 +151,15 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     if (row0 + warp * 16 >= rows) return;  // no barrier follows
 
     // ---- S = Q K^T for this warp's 16 rows x 64 tokens (8 n-tiles), K = 128 dims (8 k-steps)
-    float s[8][4];
+    float s[kNT][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
         uint32_t a[4];
         ldmatrix_x4(a, sQ + (warp * 16 + (lane & 15)) * kPad + ks * 16 + (lane >> 4) * 8);
 #pragma unroll
-        for (int nt = 0; nt < 8; nt += 2) {
+        for (int nt = 0; nt < kNT; nt += 2) {
             uint32_t bfr[4];
             ldmatrix_x4(bfr, sK + (nt * 8 + (lane & 7) + (lane >> 4) * 8) * kPad + ks * 16 + ((lane >> 3) & 1) * 8);
             mma16816(s[nt], a, bfr[0], bfr[1]);
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     // ---- exact softmax over the chunk for rows g = lane/4 (regs 0,1) and g + 8 (regs 2,3)
     float m_lo = -INFINITY, m_hi = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int col = nt * 8 + (lane & 3) * 2 + (e & 1);
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     }
     float l_lo = 0.f, l_hi = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
         s[nt][0] = exp2f(s[nt][0] - m_lo);
         s[nt][1] = exp2f(s[nt][1] - m_lo);
         s[nt][2] = exp2f(s[nt][2] - m_hi);
