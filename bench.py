@@ -296,23 +296,27 @@ def run_ours(args):
     ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev) if nq == 1 else \
         pkv.make_multi_workspace(B, B * nq, nq, Hq, Hkv, max_ctx_cap, dev)
 
-    def decode(l, c):
+    def decode(l, c, attention_only=False):
         """One layer of the step: the append is fused into the decode kernel (pkv_decode_step) unless
-        --separate-append asks for the two-call path (pkv_append + attention)."""
+        --separate-append asks for the two-call path (pkv_append + attention).  attention_only skips a
+        separate append launch (the kernel-only timing region)."""
         if nq > 1:
-            pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
+            if not attention_only:
+                pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
             pkv.decode_attention_multi(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, query_start, nq,
                                        c.scale, workspace=ws)
         elif int8k:
             if args.separate_append:
-                pkv.append_int8k(c.k_codes, c.k_scale, c.v_cache, slot_cur, c.k_new, c.v_new)
+                if not attention_only:
+                    pkv.append_int8k(c.k_codes, c.k_scale, c.v_cache, slot_cur, c.k_new, c.v_new)
                 pkv.decode_attention_int8k(out_all[l], c.q, c.k_codes, c.k_scale, c.v_cache, block_tables, ctx_cur,
                                            c.scale, workspace=ws)
             else:
                 pkv.decode_step_int8k(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_cache,
                                       block_tables, ctx_cur, c.scale, workspace=ws)
         elif args.separate_append:
-            pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
+            if not attention_only:
+                pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
             if cascade:
                 pkv.decode_attention_shared_prefix(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur,
                                                    c.scale, prefix_len, ws)
@@ -336,6 +340,10 @@ def run_ours(args):
         for l, c in enumerate(cases):
             decode(l, c)
 
+    def attention_only():
+        for l, c in enumerate(cases):
+            decode(l, c, attention_only=True)
+
     def set_step(i):
         j = i % steps_cycle
         if steps_cycle > 1:
@@ -350,11 +358,14 @@ def run_ours(args):
             set_step(i)
             step()
     torch.cuda.synchronize(dev)
-    graph = None
+    graph = kernel_graph = None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             step()
+        kernel_graph = torch.cuda.CUDAGraph()  # the attention launches alone (no separate append)
+        with torch.cuda.graph(kernel_graph, stream=stream):
+            attention_only()
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 set_step(i)
@@ -397,7 +408,8 @@ def run_ours(args):
 
     # ---- timed region 2: the dominant kernel alone.  A pkv_decode_step call is exactly one launch of
     # the decode kernel (the append and the split's log-sum-exp merge run inside it; the cascade adds
-    # its small prefix kernel); per step the layers' launches run back to back between one pair of
+    # its small prefix kernel); a separate append launch is left out here.  Per step the layers'
+    # launches are replayed back to back from a CUDA graph (no host launch gaps) between one pair of
     # CUDA events on the launching stream: average launch duration = event interval / launches.
     kt_steps = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kt_steps)]
@@ -409,8 +421,10 @@ def run_ours(args):
             j = set_step(i)
             a, b = ev[i]
             a.record(stream)
-            for l, c in enumerate(cases):
-                decode(l, c)
+            if kernel_graph is not None:
+                kernel_graph.replay()
+            else:
+                attention_only()
             b.record(stream)
             kernel_bytes += bytes_per_step[j % len(bytes_per_step)]
     barrier()
@@ -509,7 +523,10 @@ def run_ours(args):
         "decode_bytes_per_step": int(bytes_job),
         "logical_bytes_per_step": int(sum(logical_bytes_per_step) / len(logical_bytes_per_step)),
         "roofline": {
-            "kernel": "decode_partition_kernel (packed-GQA paged decode, 512-token partitions, fused LSE merge)",
+            "kernel": "decode_partition_kernel (packed-GQA paged decode, 512-token partitions, fused LSE merge)"
+                      + (" + prefix_kernel (timed together)" if cascade else ""),
+            "timing": "CUDA events around graph replays of the layers' attention launches"
+                      if kernel_graph is not None else "CUDA events around eager attention launches",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

@@ -280,7 +280,7 @@ PKV_API size_t pkv_shared_prefix_workspace_size(int num_seqs, int num_q_heads, i
  * result equals pkv_decode_attention on the same arguments, but the prefix's
  * K/V is read once per kv head for the whole batch instead of once per
  * request: a first kernel scores every request's query rows against the
- * prefix in 64-token chunks (tensor-core MMA over the B x G rows of each kv
+ * prefix in 128-token chunks (tensor-core MMA over the B x G rows of each kv
  * head), a second runs the split decode over each request's suffix (tokens
  * from prefix_len on) and merges prefix chunks and suffix partitions by
  * log-sum-exp.
