@@ -1792,6 +1792,10 @@ extern "C" PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, co
 
 namespace pkv_internal {
 
+int encode_fp16_cache_map(void *map, const void *base, int64_t rows) {
+    return encode_cache_map(static_cast<CUtensorMap *>(map), base, rows);
+}
+
 int check_decode_args(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads,
                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks) {

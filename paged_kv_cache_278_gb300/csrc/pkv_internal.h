@@ -17,6 +17,10 @@ int prefix_take_error(int *code);
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// A cache tensor [rows][128] fp16 as a tensor map (CUtensorMap, passed as void*) for 2-D tensor
+// copies of 16-row x 64-dim boxes in the 128-byte swizzle.  PKV_OK or PKV_ERR_CUDA.
+int encode_fp16_cache_map(void *map, const void *base, int64_t rows);
+
 // Host-side argument checks shared by every decode entry point (PKV_OK or an error status).
 int check_decode_args(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads,

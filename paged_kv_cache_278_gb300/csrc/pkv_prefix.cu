@@ -17,6 +17,7 @@
 //   2. The ordinary split decode kernel over each request's private suffix (tokens from
 //      prefix_len on), writing slots n_chunks.. and merging all slots by log-sum-exp in the
 //      same kernel (last partition of each request to finish).
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -65,6 +66,7 @@ struct PrefixParams {
     int max_partitions;
     int64_t num_blocks;
     float q_scale;  // scale * log2(e)
+    CUtensorMap tmap_k;  // tensor-memory kernel: the K cache as [NB*Hkv*bs][128] fp16, 16 x 64 boxes, 128B swizzle
 };
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) { pkv::ldsm_x4(r, pkv::smem_addr(p)); }
@@ -252,6 +254,240 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) 
     }
 }
 
+// ---------------------------------------------------------------- tcgen05 / tensor-memory variant
+// The same chunk computation as prefix_kernel on the 5th-generation tensor cores: one thread
+// issues tcgen05.mma with both operands described in shared memory (K-major, 128-byte swizzle)
+// and the fp32 accumulators in tensor memory, so the four warps hold no accumulator registers.
+//   S[128 rows x 128 tokens] = Q[128 x 128 dims] K^T          8 MMAs (M 128, N 128, K 16), TMEM cols 0-127
+//   exact chunk softmax: thread = row = TMEM lane, S read back with tcgen05.ld, P = hi + lo fp16
+//   O[128 rows x 128 dims] = P_hi V + P_lo V                   16 MMAs (K = tokens), TMEM cols 128-255
+// K arrives by tensor copies (16 x 64 boxes, 128-byte swizzle) straight into the B-operand tile;
+// Q rows and the transposed V chunk (the PV B operand is V^T, K-major) are written by the threads
+// in the same swizzle.  Tensor memory is allocated and freed by warp 0 on every path.
+#ifndef PKV_PREFIX_TCGEN05
+#define PKV_PREFIX_TCGEN05 0
+#endif
+namespace tc5 {
+constexpr int kTok = 128;                 // prefix tokens per CTA: N of Q K^T, K of P V
+constexpr int kRowsT = 128;               // query rows per CTA: M, one tensor-memory lane each
+constexpr int kThreadsT = 128;            // one thread per query row
+constexpr int kAtom = 128 * 128;          // one 64-element K slab of a 128-row operand tile (bytes)
+constexpr int kTile = 2 * kAtom;          // 128 rows x 128 K fp16
+// Q | K | V^T | P_hi | P_lo | barriers, TMEM slot; the rest of the 227 KB a CTA may hold is left
+// unused, so that the operand tiles sit well inside the allocation.
+constexpr int kSmem = 227 * 1024;
+static_assert(5 * kTile + 64 <= kSmem, "tiles and barriers");
+constexpr uint32_t kTmemCols = 256;       // S in columns 0-127, O in 128-255
+}  // namespace tc5
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+// Byte offset of 16-byte chunk c (0..15 along K) of row r in a K-major 128-row operand tile.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+    return (c >> 3) * tc5::kAtom + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(tc5::kThreadsT, 1) prefix_kernel_tmem(const __grid_constant__ PrefixParams P) {
+    extern __shared__ __align__(1024) unsigned char smem_tc[];
+    unsigned char *smem = smem_tc;
+    pkv::pdl_launch_dependents();  // the suffix pass may start streaming right away
+    const uint32_t base = pkv::smem_addr(smem);
+    if ((base & 1023) != 0) {  // the swizzled operand tiles need 1 KB alignment (before any allocation)
+        if (threadIdx.x == 0) pkv::record_error(&g_prefix_error, PKV_DEV_WAIT_TIMEOUT);
+        return;
+    }
+    const uint32_t sQ = base, sK = base + tc5::kTile, sVt = base + 2 * tc5::kTile;
+    const uint32_t sPh = base + 3 * tc5::kTile, sPl = base + 4 * tc5::kTile;
+    const uint32_t tma_bar = base + 5 * tc5::kTile, mma_bar = tma_bar + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 5 * tc5::kTile + 16);
+    int *s_ok = reinterpret_cast<int *>(smem + 5 * tc5::kTile + 20);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chunk = blockIdx.x, kvh = blockIdx.y, rtile = blockIdx.z;
+    const int Hq = P.num_q_heads, Hkv = P.num_kv_heads, G = Hq / Hkv, bs = P.block_size;
+    const int rows = P.num_seqs * G;
+    const int row0 = rtile * tc5::kRowsT;
+    const int tok0 = chunk * tc5::kTok;
+    const int ntok = min(tc5::kTok, P.prefix_len - tok0);  // a multiple of 16: the prefix is whole blocks
+
+    if (tid == 0) {
+        pkv::mbar_init(tma_bar, 1);
+        pkv::mbar_init(mma_bar, 1);
+        pkv::fence_mbar_init();
+    }
+    if (warp == 0) pkv::tmem_alloc(pkv::smem_addr(tmem_slot), tc5::kTmemCols);
+    pkv::tmem_fence_before_sync();
+    __syncthreads();
+    pkv::tmem_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_s = tmem, t_o = tmem + 128;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
+
+    // K chunk by tensor copies: per 16-token group two 16 x 64 boxes into the two K slabs.
+    if (tid == 0) {
+        const int groups = ntok / 16;
+        pkv::mbar_arrive_expect_tx(tma_bar, groups * 2 * 2048);
+        for (int g = 0; g < groups; ++g) {
+            const int tok = tok0 + 16 * g;
+            int32_t id = __ldg(P.block_tables + tok / bs);
+            if (id < 0 || id >= P.num_blocks) {
+                pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
+                id = 0;
+            }
+            const int y = static_cast<int>((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs);
+            pkv::tma_load_2d(sK + g * 2048, &P.tmap_k, 0, y, tma_bar);
+            pkv::tma_load_2d(sK + tc5::kAtom + g * 2048, &P.tmap_k, 64, y, tma_bar);
+        }
+    }
+    // Q: thread r writes its query row (zero past the last row).
+    {
+        const int gr = row0 + tid;
+        const uint4 *qrow = nullptr;
+        if (gr < rows)
+            qrow = reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(gr / G) * Hq + kvh * G + gr % G) * kD);
+        uint4 qv[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) qv[c] = qrow ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) sts128(sQ + tile_off(tid, c), qv[c]);
+    }
+    // V^T: thread t moves token t's V row into column t of the 128 dim-rows (zero past the prefix).
+    {
+        const int t = tid;
+        const uint4 *vrow = nullptr;
+        if (t < ntok) {
+            const int tok = tok0 + t;
+            int32_t id = __ldg(P.block_tables + tok / bs);
+            if (id < 0 || id >= P.num_blocks) id = 0;  // recorded by the K copies
+            vrow = reinterpret_cast<const uint4 *>(P.v_cache + ((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs) * kD);
+        }
+        uint4 vv[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) vv[c] = vrow ? __ldg(vrow + c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t col = (t >> 6) * tc5::kAtom + (t & 7) * 2;  // slab of the token, byte in the 16-B chunk
+        const int c8 = (t & 63) >> 3;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint32_t w[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int d = c * 8 + e;
+                sts16(sVt + col + d * 128 + ((c8 ^ (d & 7)) << 4), static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+            }
+        }
+    }
+    pkv::fence_proxy_async_smem();  // the threads' tile writes, visible to the tensor core
+    __syncthreads();
+
+    constexpr uint32_t kIdesc = pkv::umma_idesc_f16_f32(128, 128);
+    if (tid == 0) {
+        const bool landed = pkv::mbar_wait_bounded(tma_bar, 0);
+        if (landed) {
+            pkv::tmem_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * tc5::kAtom + (ks & 3) * 32;
+                pkv::umma_f16(t_s, pkv::umma_desc_k_sw128(sQ + off), pkv::umma_desc_k_sw128(sK + off), kIdesc, ks > 0);
+            }
+            pkv::umma_commit(mma_bar);
+        } else {
+            pkv::record_error(&g_prefix_error, PKV_DEV_WAIT_TIMEOUT);
+        }
+        *s_ok = landed ? 1 : 0;
+    }
+    __syncthreads();
+    bool ok = *s_ok != 0 && pkv::mbar_wait_bounded(mma_bar, 0);
+    ok = __syncthreads_and(ok);
+    pkv::tmem_fence_after_sync();
+
+    float m = -INFINITY, l = 0.f;
+    if (ok) {
+        // exact softmax of this thread's row over the chunk (log2 domain), P = hi + lo into the A tiles
+        uint32_t r[32];
+#pragma unroll
+        for (int c0 = 0; c0 < tc5::kTok; c0 += 32) {
+            pkv::tmem_ld32(t_s + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                m = fmaxf(m, c0 + j < ntok ? __uint_as_float(r[j]) * P.q_scale : -INFINITY);
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < tc5::kTok; c0 += 32) {
+            pkv::tmem_ld32(t_s + lane_base + c0, r);
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float p0 = c0 + j < ntok ? exp2f(__uint_as_float(r[j]) * P.q_scale - m) : 0.f;
+                const float p1 = c0 + j + 1 < ntok ? exp2f(__uint_as_float(r[j + 1]) * P.q_scale - m) : 0.f;
+                l += p0 + p1;
+                const __half2 h = __floats2half2_rn(p0, p1);
+                const float2 hf = __half22float2(h);
+                hi[j / 2] = *reinterpret_cast<const uint32_t *>(&h);
+                lo[j / 2] = pack_half2(p0 - hf.x, p1 - hf.y);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t off = tile_off(tid, (c0 >> 3) + k);
+                sts128(sPh + off, make_uint4(hi[4 * k], hi[4 * k + 1], hi[4 * k + 2], hi[4 * k + 3]));
+                sts128(sPl + off, make_uint4(lo[4 * k], lo[4 * k + 1], lo[4 * k + 2], lo[4 * k + 3]));
+            }
+        }
+    }
+    pkv::fence_proxy_async_smem();
+    pkv::tmem_fence_before_sync();
+    __syncthreads();
+    if (ok && tid == 0) {
+        pkv::tmem_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * tc5::kAtom + (ks & 3) * 32;
+            pkv::umma_f16(t_o, pkv::umma_desc_k_sw128(sPh + off), pkv::umma_desc_k_sw128(sVt + off), kIdesc, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * tc5::kAtom + (ks & 3) * 32;
+            pkv::umma_f16(t_o, pkv::umma_desc_k_sw128(sPl + off), pkv::umma_desc_k_sw128(sVt + off), kIdesc, true);
+        }
+        pkv::umma_commit(mma_bar);
+    }
+    if (ok) {
+        ok = pkv::mbar_wait_bounded(mma_bar, 1);
+        if (!ok && (tid & 31) == 0) pkv::record_error(&g_prefix_error, PKV_DEV_WAIT_TIMEOUT);
+    }
+    ok = __syncthreads_and(ok);
+    pkv::tmem_fence_after_sync();
+    if (ok) {
+        // partial slot `chunk` of this thread's row: normalised o, m in natural-log units, l
+        const int gr = row0 + tid;
+        const int64_t prow =
+            gr < rows ? (static_cast<int64_t>(gr / G) * Hq + kvh * G + gr % G) * P.max_partitions + chunk : 0;
+        const float inv = 1.f / l;
+        uint32_t r[32];
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+            pkv::tmem_ld32(t_o + lane_base + c0, r);
+            if (gr < rows) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(P.o_part + prow * kD + c0 + j) =
+                        make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
+                                    __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+            }
+        }
+        if (gr < rows) {
+            P.m_part[prow] = m * kLn2;
+            P.l_part[prow] = l;
+        }
+    }
+    pkv::tmem_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) pkv::tmem_dealloc(tmem, tc5::kTmemCols);
+}
+
 constexpr int kMinSuffixPartition = 64;
 // The suffix partition is halved (from 512) until the suffix grid offers this many CTAs per
 // resident CTA slot.
@@ -362,15 +598,30 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev & 63);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+#if PKV_PREFIX_TCGEN05
+    static_assert(kChunkTok == tc5::kTok && kRows == tc5::kRowsT, "partial slots are 128-token chunks of 128 rows");
+    const int64_t cache_rows = num_blocks * num_kv_heads * block_size;
+    if (cache_rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    if (pkv_internal::encode_fp16_cache_map(&p.tmap_k, k_cache, cache_rows) != PKV_OK) return PKV_ERR_CUDA;
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(prefix_kernel_tmem, cudaFuncAttributeMaxDynamicSharedMemorySize, tc5::kSmem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const dim3 grid(L.n_pre, num_kv_heads, (rows + tc5::kRowsT - 1) / tc5::kRowsT);
+    prefix_kernel_tmem<<<grid, tc5::kThreadsT, tc5::kSmem, s>>>(p);
+#else
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         if (cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess)
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(L.n_pre, num_kv_heads, (rows + kRows - 1) / kRows);
     prefix_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+#endif
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
 
     pkv_internal::SplitPass a{};
