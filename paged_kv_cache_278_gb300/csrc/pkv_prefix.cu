@@ -273,10 +273,9 @@ constexpr int kRowsT = 128;               // query rows per CTA: M, one tensor-m
 constexpr int kThreadsT = 128;            // one thread per query row
 constexpr int kAtom = 128 * 128;          // one 64-element K slab of a 128-row operand tile (bytes)
 constexpr int kTile = 2 * kAtom;          // 128 rows x 128 K fp16
-// Q | K | V^T | P_hi | P_lo | barriers, TMEM slot; the rest of the 227 KB a CTA may hold is left
-// unused, so that the operand tiles sit well inside the allocation.
-constexpr int kSmem = 227 * 1024;
-static_assert(5 * kTile + 64 <= kSmem, "tiles and barriers");
+// Q | K | V^T | barriers, TMEM slot.  P_hi and P_lo reuse the Q and K tiles once S is complete, so
+// a prefix CTA (96 KB) leaves room on its SM for a suffix-pass CTA started early.
+constexpr int kSmem = 3 * kTile + 64;
 constexpr uint32_t kTmemCols = 256;       // S in columns 0-127, O in 128-255
 }  // namespace tc5
 
@@ -302,10 +301,10 @@ __global__ void __launch_bounds__(tc5::kThreadsT, 1) prefix_kernel_tmem(const __
         return;
     }
     const uint32_t sQ = base, sK = base + tc5::kTile, sVt = base + 2 * tc5::kTile;
-    const uint32_t sPh = base + 3 * tc5::kTile, sPl = base + 4 * tc5::kTile;
-    const uint32_t tma_bar = base + 5 * tc5::kTile, mma_bar = tma_bar + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 5 * tc5::kTile + 16);
-    int *s_ok = reinterpret_cast<int *>(smem + 5 * tc5::kTile + 20);
+    const uint32_t sPh = sQ, sPl = sK;  // written only after the Q K^T MMAs have completed
+    const uint32_t tma_bar = base + 3 * tc5::kTile, mma_bar = tma_bar + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 3 * tc5::kTile + 16);
+    int *s_ok = reinterpret_cast<int *>(smem + 3 * tc5::kTile + 20);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int chunk = blockIdx.x, kvh = blockIdx.y, rtile = blockIdx.z;
     const int Hq = P.num_q_heads, Hkv = P.num_kv_heads, G = Hq / Hkv, bs = P.block_size;
