@@ -6,7 +6,7 @@
 
 A step is the whole hot path over one batch: for each of the 32 layers, pkv_append writes the
 new token's K/V into its slot and pkv_decode_attention attends over every cached token
-(split into 512-token partitions + log-sum-exp merge where a context needs it).  The default
+(split into 1024-token partitions, 512 for the long-context workload, + log-sum-exp merge where a context needs it).  The default
 workload is the 7B-shaped MHA decode: batch 16, 32 layers, 32 q = 32 kv heads, head_dim 128,
 block_size 16, context lengths uniform in [200, 4000] per request (seeded), fp16 K/V ~ N(0, 1),
 physical blocks a seeded permutation of the pool.  Each layer has its own 554 MB cache, so
@@ -293,7 +293,10 @@ def run_ours(args):
     slot_cur = slot_dev[0].clone()
     cascade = args.workload == "shared_prefix" and not args.no_cascade
     prefix_len = 1024 if cascade else 0
-    ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev) if nq == 1 else \
+    # the long-context workload is defined with 512-token split partitions; the others take the library's
+    # default (PKV_DEFAULT_PARTITION)
+    part = 512 if args.workload == "long_context" and nq == 1 and not int8k and not args.separate_append else 0
+    ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev, partition_size=part) if nq == 1 else \
         pkv.make_multi_workspace(B, B * nq, nq, Hq, Hkv, max_ctx_cap, dev)
 
     def decode(l, c, attention_only=False):
@@ -325,7 +328,7 @@ def run_ours(args):
                                      workspace=ws)
         else:
             pkv.decode_step(out_all[l], c.q, c.k_new, c.v_new, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
-                            prefix_len, ws)
+                            prefix_len, ws, partition_size=part)
 
     prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
     bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens, kv=args.kv, q_len=nq)
@@ -507,7 +510,7 @@ def run_ours(args):
             "num_kv_heads": Hkv,
             "head_dim": D,
             "block_size": bs,
-            "partition_size": pkv.PKV_DEFAULT_PARTITION,
+            "partition_size": part or pkv.PKV_DEFAULT_PARTITION,
             "kv_cache": "int8 keys + float32 scale per (token, kv head), fp16 values" if int8k else "fp16 K and V",
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
                   % (cases[0].v_cache.numel() * (3 if int8k else 4) / 1e6, bytes_job / 1e9),
@@ -523,7 +526,8 @@ def run_ours(args):
         "decode_bytes_per_step": int(bytes_job),
         "logical_bytes_per_step": int(sum(logical_bytes_per_step) / len(logical_bytes_per_step)),
         "roofline": {
-            "kernel": "decode_partition_kernel (packed-GQA paged decode, 512-token partitions, fused LSE merge)"
+            "kernel": f"decode_partition_kernel (packed-GQA paged decode, {part or pkv.PKV_DEFAULT_PARTITION}-token "
+                      "partitions, fused LSE merge)"
                       + (" + prefix_kernel (timed together)" if cascade else ""),
             "timing": "CUDA events around graph replays of the layers' attention launches"
                       if kernel_graph is not None else "CUDA events around eager attention launches",

@@ -84,7 +84,7 @@ extern "C" {
 
 /* Defaults and limits of the decode kernels. */
 #define PKV_HEAD_DIM 128             /* the only head_dim the decode kernels take */
-#define PKV_DEFAULT_PARTITION 512    /* split-context partition used by pkv_decode_attention */
+#define PKV_DEFAULT_PARTITION 1024   /* split-context partition used by pkv_decode_attention */
 #define PKV_MAX_PARTITION 4096       /* largest partition_size accepted */
 #define PKV_MIN_BLOCK_SIZE 16        /* block_size must be a multiple of 16 ... */
 #define PKV_MAX_BLOCK_SIZE 256       /* ... and at most 256 */
@@ -391,7 +391,7 @@ PKV_API int pkv_decode_step_int8k(void *out, const void *q, const void *k_new, c
 #define PKV_MAX_QUERY_LEN 1024
 
 /* Workspace bytes for pkv_decode_attention_multi (0 when no request can need
- * a split: every table fits one 512-token partition). */
+ * a split: every table fits one PKV_DEFAULT_PARTITION-token partition). */
 PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int total_q, int max_query_len, int num_q_heads,
                                                int num_kv_heads, int head_dim, int max_context);
 
@@ -403,7 +403,7 @@ PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int total_q, int ma
  *                 is skipped; inconsistent rows are skipped and recorded as
  *                 PKV_DEV_BAD_CONTEXT.
  * Other arguments as pkv_decode_attention.  One CTA serves 8 (token, head) rows
- * of one kv head and one 512-token partition, so K/V is read by
+ * of one kv head and one PKV_DEFAULT_PARTITION-token partition, so K/V is read by
  * ceil(n_b * G / 8) CTAs that run back to back (L2 serves the repeats); the
  * split's merge is fused as in pkv_decode_attention.  Workspace: zero-filled
  * before first use, left zeroed, at least pkv_decode_multi_workspace_size bytes,
@@ -414,6 +414,19 @@ PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_c
                                        int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
                                        int block_size, int64_t num_blocks, float scale, void *workspace,
                                        size_t workspace_bytes, pkv_stream_t stream);
+
+/* pkv_decode_step (prefix_len 0) with the split-context partition chosen by the
+ * caller instead of PKV_DEFAULT_PARTITION: a multiple of 16 in
+ * [16, PKV_MAX_PARTITION]; 0 selects the default.  Smaller partitions give more
+ * CTAs per request (short batches, very long contexts), larger ones amortise
+ * each CTA's start-up.  Workspace: pkv_decode_workspace_size(..., max_context,
+ * partition_size).  Other arguments, results and errors as pkv_decode_step. */
+PKV_API int pkv_decode_step_partition(void *out, const void *q, const void *k_new, const void *v_new,
+                                      void *k_cache, void *v_cache, const int32_t *block_tables,
+                                      const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, float scale, int partition_size, void *workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream);
 
 /* Split-context partial attention.  Partition p of request b covers logical
  * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each

@@ -165,9 +165,12 @@ def decode_attention_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: 
 
 
 def make_step_workspace(num_seqs: int, num_q_heads: int, max_context: int, prefix_len: int = 0,
-                        device=None) -> torch.Tensor | None:
-    """Zero-filled workspace for decode_step (None when it needs none)."""
-    n = int(_L().pkv_decode_step_workspace_size(num_seqs, num_q_heads, PKV_HEAD_DIM, max_context, prefix_len))
+                        device=None, partition_size: int = 0) -> torch.Tensor | None:
+    """Zero-filled workspace for decode_step (None when it needs none); partition_size as decode_step's."""
+    if partition_size and not prefix_len:
+        n = decode_workspace_size(num_seqs, num_q_heads, max_context, partition_size)
+    else:
+        n = int(_L().pkv_decode_step_workspace_size(num_seqs, num_q_heads, PKV_HEAD_DIM, max_context, prefix_len))
     if n == 0:
         return None
     return torch.zeros(n, dtype=torch.uint8, device=device)
@@ -176,9 +179,10 @@ def make_step_workspace(num_seqs: int, num_q_heads: int, max_context: int, prefi
 def decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                 context_lens: torch.Tensor, scale: float, prefix_len: int = 0,
-                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                workspace: torch.Tensor | None = None, stream=None, partition_size: int = 0) -> torch.Tensor:
     """One decode step: write each request's new token [B, Hkv, D] at position context_lens - 1,
-    then out = softmax(scale q K^T) V over the whole context (append fused into the decode kernel)."""
+    then out = softmax(scale q K^T) V over the whole context (append fused into the decode kernel).
+    partition_size > 0 (prefix_len 0 only) overrides the split-context partition."""
     nb, hkv, bs, d, b, hq, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
     _need(out, "out", torch.float16, 3, dev)
     _need(k_new, "k_new", torch.float16, 3, dev)
@@ -191,6 +195,15 @@ def decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: 
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, 1, dev)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    if partition_size:
+        if prefix_len:
+            raise ValueError("partition_size applies to steps without a shared prefix")
+        st = _L().pkv_decode_step_partition(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                            k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                            context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb,
+                                            float(scale), int(partition_size), ws_ptr, ws_bytes, _stream(dev, stream))
+        _lib.check(st, "pkv_decode_step_partition")
+        return out
     st = _L().pkv_decode_step(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
                               v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), b,
                               block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), int(prefix_len), ws_ptr,

@@ -33,7 +33,7 @@ PKV_DEV_WAIT_TIMEOUT = 4
 PKV_DEV_PREFIX_MISMATCH = 5
 
 PKV_HEAD_DIM = 128
-PKV_DEFAULT_PARTITION = 512
+PKV_DEFAULT_PARTITION = 1024
 PKV_MAX_PARTITION = 4096
 PKV_MAX_QUERY_LEN = 1024
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -60,6 +60,8 @@ SIGNATURES = {
                                                                            c_void_p]),
     "pkv_decode_step_int8k": (c_int, [c_void_p] * 9 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
                                                                       c_void_p]),
+    "pkv_decode_step_partition": (c_int, [c_void_p] * 8 + [c_int] * 6 + [c_int64, c_float, c_int, c_void_p, c_size_t,
+                                                                         c_void_p]),
     "pkv_decode_multi_workspace_size": (c_size_t, [c_int] * 7),
     "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 8 + [c_int64, c_float, c_void_p, c_size_t,
                                                                            c_void_p]),

@@ -1548,7 +1548,8 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                           int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, const void *k_new, const void *v_new, void *workspace,
-                          size_t workspace_bytes, pkv_stream_t stream, const float *k_scale = nullptr) {
+                          size_t workspace_bytes, pkv_stream_t stream, const float *k_scale = nullptr,
+                          int partition_size = PKV_DEFAULT_PARTITION) {
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
@@ -1556,9 +1557,11 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
     if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
+    if (partition_size < kChunk || partition_size > PKV_MAX_PARTITION || partition_size % kChunk != 0)
+        return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
-    const int part = PKV_DEFAULT_PARTITION;
+    const int part = partition_size;
     const int max_parts = static_cast<int>((cap + part - 1) / part);
     DecodeParams p{};
     p.q = static_cast<const __half *>(q);
@@ -1632,6 +1635,19 @@ extern "C" PKV_API int pkv_decode_step(void *out, const void *q, const void *k_n
     return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
                                  workspace, workspace_bytes, stream);
+}
+
+extern "C" PKV_API int pkv_decode_step_partition(void *out, const void *q, const void *k_new, const void *v_new,
+                                                 void *k_cache, void *v_cache, const int32_t *block_tables,
+                                                 const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                                 int64_t num_blocks, float scale, int partition_size,
+                                                 void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    if (!k_new || !v_new || partition_size < 0) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
+                                 workspace, workspace_bytes, stream, nullptr,
+                                 partition_size > 0 ? partition_size : PKV_DEFAULT_PARTITION);
 }
 
 // ------------------------------------------------------------------ int8 key cache

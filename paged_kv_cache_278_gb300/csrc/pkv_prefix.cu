@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(tc5::kThreadsT, 1) prefix_kernel_tmem(const __
 }
 
 constexpr int kMinSuffixPartition = 64;
+constexpr int kMaxSuffixPartition = 512;
 // The suffix partition is halved (from 512) until the suffix grid offers this many CTAs per
 // resident CTA slot.
 #ifndef PKV_SUFFIX_WAVES
@@ -559,7 +560,7 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     // PKV_SUFFIX_WAVES CTAs per resident CTA slot (3 per SM), so short private suffixes still fill
     // the GPU.
     int dev_sm = 0;
-    int suffix_part = PKV_DEFAULT_PARTITION;
+    int suffix_part = kMaxSuffixPartition;
     {
         int d = 0;
         if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&dev_sm, cudaDevAttrMultiProcessorCount, d) !=

@@ -1,5 +1,5 @@
 """Decode attention on the GPU against the float64 oracle, element by element, at sizes that
-span several 16-token tiles, several 512-token partitions and ragged tails."""
+span several 16-token tiles, several split partitions and ragged tails."""
 import numpy as np
 import pytest
 import torch
@@ -39,7 +39,7 @@ def test_ragged_batch(group, bs):
 
 @pytest.mark.parametrize("group", [1, 4])
 def test_single_pass_only(group):
-    # every table fits one 512-token partition: no workspace, one kernel
+    # every table fits one partition: no workspace, one kernel
     case = workloads.random_case(77 + group, [1, 7, 16, 33, 255, 256, 500], 4 * group, 4, block_size=16)
     assert case.max_blocks_per_seq * 16 <= pkv.PKV_DEFAULT_PARTITION
     h = host_inputs(case)
@@ -156,7 +156,7 @@ def test_workspace_reuse_leaves_counters_zero():
         out = gpu_step(case.to("cuda"), workspace=ws)
         assert max_err(out, ref) <= ATTN_TOL
         torch.cuda.synchronize()
-        rows = 4 * 16 * -(-first.max_blocks_per_seq * 16 // 512)
+        rows = 4 * 16 * -(-first.max_blocks_per_seq * 16 // pkv.PKV_DEFAULT_PARTITION)
         up = lambda x: x + (-x) % 256
         counters = ws[up(rows * 128 * 4) + 2 * up(rows * 4):].view(torch.int32)
         assert int(counters.abs().sum()) == 0
@@ -166,5 +166,27 @@ def test_workspace_reuse_leaves_counters_zero():
 def test_context_beyond_one_merge_tile():
     # 270,000 tokens = 528 partitions of 512: the fused merge takes its tiled branch
     case = workloads.random_case(31, [270000, 700], 2, 1, block_size=128)
-    err, _, _ = run_parity(case)
-    assert err <= ATTN_TOL, err
+    h = host_inputs(case)
+    ref = oracle_step(h, case)
+    dev = case.to("cuda")
+    out = torch.empty_like(dev.q)
+    ws = pkv.make_step_workspace(2, 2, case.max_blocks_per_seq * 128, device="cuda", partition_size=512)
+    pkv.decode_step(out, dev.q, dev.k_new, dev.v_new, dev.k_cache, dev.v_cache, dev.block_tables, dev.context_lens,
+                    case.scale, workspace=ws, partition_size=512)
+    assert max_err(out, ref) <= ATTN_TOL
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("part", [16, 256, 512, 1536, 4096])
+def test_step_with_explicit_partition(part):
+    # the fused step at other partition sizes, down to one 16-token chunk per CTA
+    case = workloads.random_case(32 + part, [5000, 1, 2049, 333, 4097], 16, 4, block_size=16, extra_blocks=5)
+    h = host_inputs(case)
+    ref = oracle_step(h, case)
+    dev = case.to("cuda")
+    out = torch.empty_like(dev.q)
+    ws = pkv.make_step_workspace(5, 16, case.max_blocks_per_seq * 16, device="cuda", partition_size=part)
+    pkv.decode_step(out, dev.q, dev.k_new, dev.v_new, dev.k_cache, dev.v_cache, dev.block_tables, dev.context_lens,
+                    case.scale, workspace=ws, partition_size=part)
+    assert max_err(out, ref) <= ATTN_TOL
+    assert_no_device_error()

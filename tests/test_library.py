@@ -156,13 +156,14 @@ def test_int8k_multi_copy_invalid_arguments(lib):
 
 
 def test_multi_workspace_size(lib):
-    # one 512-token partition: none needed
-    assert lib.pkv_decode_multi_workspace_size(2, 10, 8, 32, 8, 128, 512) == 0
-    rows = 10 * 32 * 8
+    # one default partition: none needed
+    part = _lib.PKV_DEFAULT_PARTITION
+    assert lib.pkv_decode_multi_workspace_size(2, 10, 8, 32, 8, 128, part) == 0
+    rows = 10 * 32 * (8192 // part)
     up = lambda x: x + (-x) % 256
     groups = -(-8 * 4 // 8)
     expect = up(rows * 128 * 4) + 2 * up(rows * 4) + up(2 * 8 * groups * 4)
-    assert lib.pkv_decode_multi_workspace_size(2, 10, 8, 32, 8, 128, 4096) == expect
+    assert lib.pkv_decode_multi_workspace_size(2, 10, 8, 32, 8, 128, 8192) == expect
 
 
 def test_workspace_size(lib):

@@ -1,5 +1,5 @@
 """The five workload shapes at full size, in the launch configuration the benchmark times
-(pkv.append + pkv.decode_attention with the default 512-token split), against the oracle on
+(pkv.append + pkv.decode_attention with the default split), against the oracle on
 every request and head of the sampled layers / steps."""
 import numpy as np
 import pytest

@@ -62,10 +62,11 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 
 def test_noalloc_refuses_requests_beyond_its_scratch():
     lib = _lib.load()
-    # 16 requests x 32 heads x 64 partitions of 512 tokens need more than 16 MiB of partials.
+    # 16 requests x 32 heads x 64 default partitions need more than 16 MiB of partials.
     # Every buffer is allocated at the size the call names (contexts are 0), so nothing could
     # be read out of bounds even if the call were not refused.
-    b, hq, hkv, maxb = 16, 32, 32, 2048
+    b, hq, hkv = 16, 32, 32
+    maxb = 64 * pkv.PKV_DEFAULT_PARTITION // 16
     assert pkv.decode_workspace_size(b, hq, maxb * 16) > _lib.PKV_NOALLOC_SCRATCH_BYTES
     c = workloads.random_case(903, [0] * b, hq, hkv, block_size=16, extra_blocks=4).to("cuda")
     c.block_tables = torch.zeros((b, maxb), dtype=torch.int32, device="cuda")
