@@ -131,7 +131,8 @@ struct DecodeParams {
     const int32_t *query_start;  // several new tokens per request: request b owns q/out rows
     int total_q;                 //   query_start[b] .. query_start[b+1]-1 (null: one token per request)
     int max_query_len;
-    int n_row_groups;            // 8-column groups of the (token, head) rows of one kv head
+    int n_row_groups;            // groups of 8 x mq_tiles (token, head) rows of one kv head
+    int mq_tiles;                // 8-column MMA tiles per CTA for several tokens per request (1 or 2)
     const float *k_scale;     // int8 key cache: float32 scale per (block, kv head, slot); null for fp16 keys
     float *k_scale_w;         // writable view of k_scale for the fused append
     CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
@@ -146,7 +147,7 @@ constexpr int kMergeTile = 512;  // partitions whose weights the fused merge sta
 // KQ (int8 keys): the K tile is one 2 KB box of 16 int8 rows in the same swizzle, and each stage
 // also holds the chunk's 16 float32 key scales.
 constexpr int kHalfTile = kChunk * 128;
-template <bool TC, bool KQ = false>
+template <bool TC, bool KQ = false, int NT = 1>
 struct SmemLayout {
     static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
@@ -157,7 +158,7 @@ struct SmemLayout {
     static constexpr int scales = stages + stage_bytes;
     static constexpr int bars = scales + (KQ ? kWarps * kStages * kChunk * 4 : 0);
     static constexpr int probs = bars + kWarps * kStages * kBarsPerStage * 8;
-    __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? 2 * 8 * kChunk * 2 : kChunk * g * 4; }
+    __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? NT * 2 * 8 * kChunk * 2 : kChunk * g * 4; }
     __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
     __host__ __device__ static constexpr int table(int g) { return newrow(g) + 2 * kRowBytes; }
     __host__ __device__ static constexpr int total(int g, int partition_size) {
@@ -172,19 +173,19 @@ struct HeadRows {
     __device__ __forceinline__ int64_t row(int hh) const { return row0 + hh; }
     __device__ __forceinline__ bool live(int) const { return true; }
 };
-// Several tokens per request: column hh of row group rg is row r = 8 rg + hh of the request's
+// Several tokens per request: column hh of row group rg is row r = NC rg + hh of the request's
 // n * G rows for kv head kvh, i.e. token r / G, head r % G.  Columns past the last token are
 // dead; their reads are redirected to the last token's row so every access stays in bounds.
-template <int G>
+template <int G, int NC = 8>
 struct TokenRows {
     int64_t qs;
     int n, rg, hq, kvh;
     __device__ __forceinline__ int64_t row(int hh) const {
-        const int r = rg * 8 + hh;
+        const int r = rg * NC + hh;
         const int i = r / G < n ? r / G : n - 1;
         return (qs + i) * hq + kvh * G + r % G;
     }
-    __device__ __forceinline__ bool live(int hh) const { return (rg * 8 + hh) / G < n; }
+    __device__ __forceinline__ bool live(int hh) const { return (rg * NC + hh) / G < n; }
 };
 
 // Log-sum-exp merge of partial slots [0, n_total) of the G packed columns (query heads, or
@@ -201,10 +202,11 @@ __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total
     constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
     constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
     static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
-    static_assert(2 * G * kMergeTile * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout<true, true>::stage_bytes,
+    constexpr int TILE = G > 8 ? kMergeTile / 2 : kMergeTile;  // partitions staged at a time
+    static_assert(2 * G * TILE * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout<true, true>::stage_bytes,
                   "merge staging must fit the stages");
-    float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][kMergeTile]
-    float *s_max = s_wt + 2 * G * kMergeTile;                        // [G]
+    float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][TILE]
+    float *s_max = s_wt + 2 * G * TILE;                        // [G]
     float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
     float *s_sum = reinterpret_cast<float *>(s_acc + GROUPS * SLOTS);                     // [GROUPS][SLOTS]
     const int grp = GROUPS > 1 ? threadIdx.x / SLOTS : 0;
@@ -226,7 +228,7 @@ __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total
         macc[k].w = fmaf(w, v.w, macc[k].w);
         msum[k] += w;
     };
-    if (n_total <= kMergeTile) {
+    if (n_total <= TILE) {
         // Fast path, about one L2 round trip: issue this thread's first PRE partial rows, stage
         // every (m, l) of the group in shared memory meanwhile, then weight the rows in registers.
         constexpr int PRE = 8;
@@ -242,20 +244,20 @@ __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total
             }
         }
         float *s_mm = s_wt;
-        float *s_ll = s_wt + G * kMergeTile;
+        float *s_ll = s_wt + G * TILE;
         for (int i = threadIdx.x; i < G * n_total; i += kThreads) {
             const int hh = i / n_total, pp = i - hh * n_total;
             const int64_t prow = rows.row(hh) * P.max_partitions + pp;
-            s_mm[hh * kMergeTile + pp] = __ldcg(P.m_part + prow);
-            s_ll[hh * kMergeTile + pp] = __ldcg(P.l_part + prow);
+            s_mm[hh * TILE + pp] = __ldcg(P.m_part + prow);
+            s_ll[hh * TILE + pp] = __ldcg(P.l_part + prow);
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < PER_THREAD; ++k) {
             const int slot = slot0 + k * kThreads;
             const int hh = slot / (kD / 4);
-            const float *mm = s_mm + hh * kMergeTile;
-            const float *ll = s_ll + hh * kMergeTile;
+            const float *mm = s_mm + hh * TILE;
+            const float *ll = s_ll + hh * TILE;
             float M = -INFINITY;
             for (int pp = 0; pp < n_total; ++pp) M = fmaxf(M, mm[pp]);
 #pragma unroll
@@ -278,13 +280,13 @@ __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total
             for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(pkv::kFullMask, M, sh));
             if (lane == 0) s_max[hh] = M;
         }
-        for (int p0 = 0; p0 < n_total; p0 += kMergeTile) {
-            const int n = min(kMergeTile, n_total - p0);
+        for (int p0 = 0; p0 < n_total; p0 += TILE) {
+            const int n = min(TILE, n_total - p0);
             __syncthreads();  // s_max ready / previous tile consumed
             for (int i = threadIdx.x; i < G * n; i += kThreads) {
                 const int hh = i / n, pp = i - hh * n;
                 const int64_t prow = rows.row(hh) * P.max_partitions + p0 + pp;
-                s_wt[hh * kMergeTile + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
+                s_wt[hh * TILE + pp] = __ldcg(P.l_part + prow) * expf(__ldcg(P.m_part + prow) - s_max[hh]);
             }
             __syncthreads();
 #pragma unroll
@@ -292,7 +294,7 @@ __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total
                 const int slot = slot0 + k * kThreads;
                 const int hh = slot / (kD / 4);
                 const float4 *o = o_row(hh, slot % (kD / 4)) + static_cast<int64_t>(p0) * (kD / 4);
-                const float *w = s_wt + hh * kMergeTile;
+                const float *w = s_wt + hh * TILE;
 #pragma unroll 8
                 for (int pp = grp; pp < n; pp += GROUPS) accumulate(k, w[pp], __ldcg(o + static_cast<int64_t>(pp) * (kD / 4)));
             }
@@ -689,7 +691,9 @@ struct TcEngine {
         }
     }
 
-    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+    // Columns go to slots c0 .. c0 + G - 1 of the combine area's nc columns per warp.
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l, int nc = G,
+                                           int c0 = 0) {
         float l[2] = {l_part[0], l_part[1]};
 #pragma unroll
         for (int sh = 4; sh <= 16; sh <<= 1) {
@@ -711,14 +715,14 @@ struct TcEngine {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int h = h0 + (e & 1);
-                if (h < G) c_acc[(warp * G + h) * kD + mt * 16 + g + (e >> 1) * 8] = o[mt][e] * f[e & 1];
+                if (h < G) c_acc[(warp * nc + c0 + h) * kD + mt * 16 + g + (e >> 1) * 8] = o[mt][e] * f[e & 1];
             }
         if (g == 0) {
 #pragma unroll
             for (int j = 0; j < 2; ++j)
                 if (h0 + j < G) {
-                    c_m[warp * G + h0 + j] = m[j];
-                    c_l[warp * G + h0 + j] = l[j];
+                    c_m[warp * nc + c0 + h0 + j] = m[j];
+                    c_l[warp * nc + c0 + h0 + j] = l[j];
                 }
         }
     }
@@ -787,8 +791,10 @@ struct TcEngineM : TcEngine<8> {
 
     __device__ __forceinline__ void init(const DecodeParams &P, int, int, int) { reset(P); }
 
-    __device__ __forceinline__ void bind(const DecodeParams &P, int kvh, int lane, int rg, int64_t qs, int n, int ctx) {
-        const int r = rg * 8 + (lane >> 2);
+    // Columns c0 .. c0 + 7 of row group rg, whose groups are nc rows wide.
+    __device__ __forceinline__ void bind(const DecodeParams &P, int kvh, int lane, int rg, int64_t qs, int n, int ctx,
+                                         int nc = 8, int c0 = 0) {
+        const int r = rg * nc + c0 + (lane >> 2);
         const bool live = r / G < n;
         const __half *qrow = P.q + ((qs + (live ? r / G : 0)) * P.num_q_heads + kvh * G + r % G) * kD;
 #pragma unroll
@@ -798,7 +804,7 @@ struct TcEngineM : TcEngine<8> {
                 qb[ks][j] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + (lane & 3) * 2 + j * 8)) : 0u;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int tok = (rg * 8 + (lane & 3) * 2 + j) / G;
+            const int tok = (rg * nc + c0 + (lane & 3) * 2 + j) / G;
             lim[j] = tok < n ? ctx - n + tok : -1;
         }
     }
@@ -817,21 +823,56 @@ struct TcEngineM : TcEngine<8> {
     }
 };
 
-template <int G, int LPT, bool TC, bool KQ, bool MQ>
-using EngineFor = typename std::conditional<
-    MQ, TcEngineM<G>,
-    typename std::conditional<
-        KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type;
+// Two column tiles (16 (token, head) rows) per CTA: each chunk's K/V tile, staged once, feeds two
+// independent 8-column engines, so a request with up to 16 rows per kv head is one stream of the
+// cache instead of two.
+template <int G>
+struct TcEngineM2 {
+    TcEngineM<G> e[2];
+    static constexpr int kScratch = 2 * 8 * kChunk * 2;  // one engine's P^T buffers
 
-template <int G, int LPT, bool TC, bool KQ, bool MQ>
-__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
+    __device__ __forceinline__ void init(const DecodeParams &P, int b, int kvh, int lane) {
+        e[0].init(P, b, kvh, lane);
+        e[1].init(P, b, kvh, lane);
+    }
+    __device__ __forceinline__ void bind(const DecodeParams &P, int kvh, int lane, int rg, int64_t qs, int n, int ctx) {
+        e[0].bind(P, kvh, lane, rg, qs, n, ctx, 16, 0);
+        e[1].bind(P, kvh, lane, rg, qs, n, ctx, 16, 8);
+    }
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t s_tile, int valid, int lane, unsigned char *scratch,
+                                       int tok0) {
+        e[0].qk(k_tile, s_tile, valid, lane, scratch, tok0);
+        e[1].qk(k_tile, s_tile, valid, lane, scratch + kScratch, tok0);
+    }
+    __device__ __forceinline__ void pv(uint32_t v_tile, int valid, int lane, unsigned char *scratch) {
+        e[0].pv(v_tile, valid, lane, scratch);
+        e[1].pv(v_tile, valid, lane, scratch + kScratch);
+    }
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+        e[0].finish(warp, lane, c_acc, c_m, c_l, 16, 0);
+        e[1].finish(warp, lane, c_acc, c_m, c_l, 16, 8);
+    }
+};
+
+template <int G, int LPT, bool TC, bool KQ, int MQ>
+using EngineFor = typename std::conditional<
+    MQ == 2, TcEngineM2<G>,
+    typename std::conditional<MQ == 1, TcEngineM<G>,
+    typename std::conditional<
+        KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type>::type;
+
+// MQ: 0 one token per request; 1 or 2 several tokens per request, with that many 8-column tiles.
+template <int G, int LPT, bool TC, bool KQ, int MQ>
+__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
+                                                ? 2
+                                                : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
     decode_partition_kernel(const __grid_constant__ DecodeParams P) {
     static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
     static_assert(!MQ || (TC && !KQ), "several tokens per request run on the fp16 tensor-core engine");
-    using L = SmemLayout<TC, KQ>;
+    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1>;
     using Engine = EngineFor<G, LPT, TC, KQ, MQ>;
     constexpr int kRow = L::row;
-    constexpr int NC = MQ ? 8 : G;  // packed output columns per CTA
+    constexpr int NC = MQ ? 8 * MQ : G;  // packed output columns per CTA
 
     extern __shared__ __align__(1024) unsigned char smem[];
 
@@ -854,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                 pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
             return;
         }
-        if (rg * 8 >= q_len * G) return;  // no live column (also q_len == 0: nothing this step)
+        if (rg * NC >= q_len * G) return;  // no live column (also q_len == 0: nothing this step)
     }
 
     // ---------------------------------------------------------------- extent
@@ -886,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         }
         eng.bind(P, kvh, lane, rg, qs_b, q_len, ctx);
         // keys past the group's last live token are visible to none of its columns
-        const int last_tok = min(q_len - 1, (rg * 8 + 7) / G);
+        const int last_tok = min(q_len - 1, (rg * NC + NC - 1) / G);
         ctx = ctx - q_len + last_tok + 1;
     }
     const int tok_begin = P.token_offset;  // > 0 only for the suffix pass after a shared prefix
@@ -1210,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     float *c_l = c_m + kWarps * NC;                                  // [kWarps][NC]
     eng.finish(warp, lane, c_acc, c_m, c_l);
     __syncthreads();
-    const TokenRows<G> token_rows{qs_b, q_len, rg, Hq, kvh};
+    const TokenRows<G, NC> token_rows{qs_b, q_len, rg, Hq, kvh};
 #pragma unroll 1
     for (int idx = threadIdx.x; idx < NC * kD; idx += kThreads) {
         const int hh = idx / kD, d = idx % kD;
@@ -1382,7 +1423,7 @@ int encode_code_map(CUtensorMap *map, const void *base, int64_t rows) {
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int G, bool KQ, bool MQ>
+template <int G, bool KQ, int MQ>
 int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
     constexpr bool TC = KQ || MQ || (PKV_DECODE_TC && G >= PKV_DECODE_TC_MIN_GROUP);
@@ -1395,7 +1436,7 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
         if (st == PKV_OK) st = encode_cache_map(&p.tmap_v, p.v_cache, rows);
         if (st != PKV_OK) return st;
     }
-    using L = SmemLayout<TC, KQ>;
+    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1>;
     const int smem = L::total(G, p.partition_size);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -1431,9 +1472,11 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
 
 template <int G>
 int launch_mode(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
-    if (p.query_start) return launch_partition<G, false, true>(p, num_seqs, stream, grid_parts);
-    if (p.k_scale) return launch_partition<G, true, false>(p, num_seqs, stream, grid_parts);
-    return launch_partition<G, false, false>(p, num_seqs, stream, grid_parts);
+    if (p.query_start)
+        return p.mq_tiles == 2 ? launch_partition<G, false, 2>(p, num_seqs, stream, grid_parts)
+                               : launch_partition<G, false, 1>(p, num_seqs, stream, grid_parts);
+    if (p.k_scale) return launch_partition<G, true, 0>(p, num_seqs, stream, grid_parts);
+    return launch_partition<G, false, 0>(p, num_seqs, stream, grid_parts);
 }
 
 int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream, int grid_parts = 0) {
@@ -1679,7 +1722,12 @@ extern "C" PKV_API int pkv_decode_step_int8k(void *out, const void *q, const voi
 // ------------------------------------------------------------------ several new tokens per request
 
 namespace {
-int row_groups(int max_query_len, int group) { return (max_query_len * group + 7) / 8; }
+// 8-column tiles per CTA: two once a request brings more than 8 (token, head) rows per kv head.
+int mq_tiles(int max_query_len, int group) { return max_query_len * group > 8 ? 2 : 1; }
+int row_groups(int max_query_len, int group) {
+    const int nc = 8 * mq_tiles(max_query_len, group);
+    return (max_query_len * group + nc - 1) / nc;
+}
 }  // namespace
 
 extern "C" PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int total_q, int max_query_len,
@@ -1736,6 +1784,7 @@ extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, cons
     p.total_q = total_q;
     p.max_query_len = max_query_len;
     p.n_row_groups = row_groups(max_query_len, group);
+    p.mq_tiles = mq_tiles(max_query_len, group);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts > 1) {
         const size_t need = pkv_decode_multi_workspace_size(num_seqs, total_q, max_query_len, num_q_heads,

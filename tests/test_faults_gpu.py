@@ -64,12 +64,13 @@ def test_context_is_usable_after_recorded_errors():
 def test_host_side_argument_errors():
     case = fresh(5)
     out = torch.empty_like(case.q)
-    with pytest.raises(pkv.PkvError) as e:   # split needed, no workspace
-        big = torch.zeros((3, 64), dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:   # split needed (tables of two default partitions), no workspace
+        nblk = 2 * pkv.PKV_DEFAULT_PARTITION // 16
+        big = torch.zeros((3, nblk), dtype=torch.int32, device="cuda")
         pkv.decode_attention(out, case.q, case.k_cache, case.v_cache, big, case.context_lens, case.scale)
     assert e.value.status == -5
     with pytest.raises(pkv.PkvError):        # workspace one byte short
-        need = pkv.decode_workspace_size(3, 8, 64 * 16)
+        need = pkv.decode_workspace_size(3, 8, nblk * 16)
         ws = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
         pkv.decode_attention(out, case.q, case.k_cache, case.v_cache, big, case.context_lens, case.scale,
                              workspace=ws)
