@@ -39,6 +39,12 @@ constexpr int kD = PKV_HEAD_DIM;       // 128
 #ifndef PKV_PREFIX_CHUNK
 #define PKV_PREFIX_CHUNK 128
 #endif
+// Registers per thread of the prefix kernel: at 168 (no spills), one 8-warp prefix CTA and one
+// 4-warp suffix-pass CTA fit an SM's register file together, so the suffix pass streams on the
+// prefix kernel's SMs too.
+#ifndef PKV_PREFIX_MAXNREG
+#define PKV_PREFIX_MAXNREG 168
+#endif
 constexpr int kChunkTok = PKV_PREFIX_CHUNK;  // prefix tokens per CTA (a multiple of 16)
 constexpr int kNT = kChunkTok / 8;           // 8-token MMA n-tiles of a chunk
 static_assert(kChunkTok % 16 == 0 && kChunkTok >= 16, "chunk of whole 16-token k-steps");
@@ -83,7 +89,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // Grid (prefix chunks, kv heads, ceil(B*G / 128)); 8 warps, each owning 16 query rows.
-__global__ void __launch_bounds__(kThreads) prefix_kernel(const PrefixParams P) {
+__global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams P) {  // launched with kThreads threads
     extern __shared__ __align__(128) unsigned char smem[];
     __half *sK = reinterpret_cast<__half *>(smem);      // [kChunkTok][kPad]
     __half *sV = sK + kChunkTok * kPad;                   // [kChunkTok][kPad]
@@ -614,8 +620,12 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     prefix_kernel_tmem<<<grid, tc5::kThreadsT, tc5::kSmem, s>>>(p);
 #else
     if (!(configured.load(std::memory_order_acquire) & bit)) {
+        // The whole shared memory as carveout: an SM running a prefix CTA (104 KB) then still has room
+        // for a suffix-pass CTA, which otherwise could not share the SM's smaller configuration.
         if (cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
