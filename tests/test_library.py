@@ -155,6 +155,17 @@ def test_int8k_multi_copy_invalid_arguments(lib):
     assert lib.pkv_copy_blocks(p, p, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
 
 
+def test_step_partition_arguments(lib):
+    null = None
+    p = ctypes.c_void_p(16)
+    args = lambda part: (p, p, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, part, null, 0, null)
+    assert lib.pkv_decode_step_partition(*args(-16)) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_partition(*args(24)) == _lib.PKV_ERR_UNSUPPORTED       # not a multiple of 16
+    assert lib.pkv_decode_step_partition(*args(_lib.PKV_MAX_PARTITION + 16)) == _lib.PKV_ERR_UNSUPPORTED
+    no_new = (p, p, null, p) + args(512)[4:]
+    assert lib.pkv_decode_step_partition(*no_new) == _lib.PKV_ERR_INVALID_ARG
+
+
 def test_multi_workspace_size(lib):
     # one default partition: none needed
     part = _lib.PKV_DEFAULT_PARTITION
