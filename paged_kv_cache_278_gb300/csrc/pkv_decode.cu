@@ -8,32 +8,31 @@
 //     out[b][h] = softmax(scale * q[b][h] . K_b^T) . V_b
 //
 // How (GB300 design; the pages only give the operation):
-//   * One CTA owns one (request b, kv head, partition of the context).  All
-//     g = Hq/Hkv query heads that read that kv head are packed into the CTA,
-//     so every K/V byte is fetched from HBM exactly once per step.
-//   * The partition is cut into 16-token chunks.  A chunk never straddles a
-//     block (block_size is a multiple of 16), so its K rows (16 x 256 B) and V
-//     rows are each ONE contiguous 4 KiB run in the [block][kv head][slot][dim]
-//     layout, fetched by a single 1-D bulk copy (the TMA engine) into shared
-//     memory and counted on an mbarrier.
-//   * Each of the 4 warps streams its own chunks (w, w+4, w+8, ...) through a
-//     private 3-stage ring: no block-wide barrier inside the main loop, and up
-//     to 3 x 8 KiB in flight per warp, 2 CTAs per SM.
-//   * q . K: LPT lanes share a token row (each lane holds 128/LPT dims of q in
-//     fp32 registers, pre-multiplied by scale*log2(e)); partial dot products
-//     are combined with a reduce-scatter of warp shuffles, after which each
-//     lane holds finished scores for a fixed (token, head) subset.
-//   * Online softmax in fp32 with lazy rescaling: the reference max is only
-//     raised (and the accumulators rescaled) when a score exceeds it by more
-//     than 2^8, so most chunks skip the rescale; the true max is tracked on
-//     the side and everything is re-referenced to it once at the end.  Probabilities go through a
-//     small per-warp shared buffer to the P.V stage, where each lane owns 4
-//     output dims of every packed head and walks the chunk's tokens.
-//   * At the end the 4 warps' (m, l, acc) are merged in shared memory; the CTA
-//     writes either the fp16 output (request fits one partition) or fp32
-//     partials (m, l, normalised o) for the log-sum-exp merge kernel.
-//   * Indices read from memory are checked (block ids, context length) and
-//     clamped; problems are recorded in the device error word.
+//   * One CTA owns one (request b, kv head, partition of the context; 1024 tokens by default).
+//     All g = Hq/Hkv query heads that read that kv head are packed into the CTA, so every K/V
+//     byte is fetched from HBM exactly once per step.
+//   * The partition is cut into 16-token chunks; a chunk never straddles a block (block_size is
+//     a multiple of 16).  Its K and V rows arrive by 2-D tensor copies (TMA: 16-row x 64-dim
+//     boxes of the cache viewed as [rows][128], 128-byte swizzle) into shared memory, counted on
+//     an mbarrier with a bounded wait.
+//   * Each of the 4 warps streams its own chunks (w, w+4, w+8, ...) through a private 2-stage
+//     ring: no block-wide barrier inside the main loop; 3 CTAs per SM.
+//   * q . K and P . V run on the tensor cores (mma.m16n8k16, fp32 accumulation): the packed
+//     heads are the 8 MMA columns, K comes from the swizzled tile by ldmatrix, P is split into
+//     fp16 hi + lo parts.  Variants of the same engine serve int8 keys (codes converted to exact
+//     fp16 integers in registers, row scales applied to the finished dot products) and several
+//     new tokens per request ((token, head) rows as the columns, causal masks per column).  A
+//     CUDA-core engine (packed fp32x2 FMAs) remains behind PKV_DECODE_TC_MIN_GROUP.
+//   * Online softmax in fp32 with lazy rescaling: the reference max is only raised (and the
+//     accumulators rescaled) when a score exceeds it by more than 2^8; the true max is tracked
+//     on the side and everything is re-referenced to it once at the end.
+//   * The new token's K/V (decode step) is written by the CTA that owns its position and
+//     patched into the staged tile.  At the end the 4 warps' (m, l, acc) are merged in shared
+//     memory; the CTA writes the fp16 output when the request fits one partition, else fp32
+//     partials, and the last partition CTA of a (request, kv head) to finish merges them by
+//     log-sum-exp in the same launch.
+//   * Indices read from memory are checked (block ids, context length) and clamped; problems
+//     are recorded in the device error word.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
