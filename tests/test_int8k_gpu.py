@@ -133,3 +133,32 @@ def test_decode_int8k_block_relabel_bit_identical():
     case2.block_tables = torch.from_numpy(np.where(bt >= 0, relabel[np.clip(bt, 0, None)], -1).astype(np.int32))
     out2 = run_decode(case2, c2, s2, v2)
     assert torch.equal(out1, out2)
+
+
+def test_int8k_full_size_mha7b_sampled():
+    """The 7B-shaped workload as the benchmark runs it with int8 keys: every pool row quantised by
+    the library's append kernel (codes and scales bit-exact against the oracle's quantiser), then
+    one fused decode step; requests 0, 7 and 15 compared with the oracle."""
+    case = workloads.mha7b(0, device="cuda")
+    nb, hkv, bs, d = case.k_cache.shape
+    kc, ks, vc = pkv.empty_int8k_cache(nb, hkv, bs, "cuda")
+    vc.copy_(case.v_cache)
+    rows_k = case.k_cache.permute(0, 2, 1, 3).reshape(nb * bs, hkv, d).contiguous()
+    rows_v = case.v_cache.permute(0, 2, 1, 3).reshape(nb * bs, hkv, d).contiguous()
+    pkv.append_int8k(kc, ks, vc, torch.arange(nb * bs, device="cuda"), rows_k, rows_v)
+    codes, scales, v = quantised_pool(case)
+    assert np.array_equal(kc.cpu().numpy(), codes)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), scales.view(np.uint32))
+    h = case.to("cpu")
+    bt, ctx = h.block_tables.numpy(), h.context_lens.numpy()
+    co, so, vo = codes.copy(), scales.copy(), v.copy()
+    slots = oracle.slot_mapping(bt, h.positions.numpy(), bs)
+    oracle.append_quant_k(co, so, vo, slots, h.k_new.numpy(), h.v_new.numpy())
+    out = torch.empty_like(case.q)
+    ws = pkv.make_workspace(case.num_seqs, case.num_q_heads, case.max_blocks_per_seq * bs, "cuda")
+    pkv.decode_step_int8k(out, case.q, case.k_new, case.v_new, kc, ks, vc, case.block_tables, case.context_lens,
+                          case.scale, workspace=ws)
+    for r in (0, 7, 15):
+        ref = oracle.decode_quant_k(h.q.numpy()[r:r + 1], co, so, vo, bt[r:r + 1], ctx[r:r + 1], case.scale)
+        assert max_err(out[r:r + 1], ref) <= ATTN_TOL, r
+    assert_no_device_error()
