@@ -117,6 +117,11 @@ class Oracle:
             [ctypes.c_int] * 6 + [ctypes.c_double]
         lib.oracle_copy_blocks_between.restype = None
         lib.oracle_copy_blocks_between.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, _i32p] + [ctypes.c_int] * 4
+        lib.oracle_append_quant_kv.restype = None
+        lib.oracle_append_quant_kv.argtypes = [_i8p, _f32p, _i8p, _f32p, _i64p, _u16p, _u16p] + [ctypes.c_int] * 4
+        lib.oracle_decode_quant_kv.restype = None
+        lib.oracle_decode_quant_kv.argtypes = [_f64p, _u16p, _i8p, _f32p, _i8p, _f32p, _i32p, _i32p] + \
+            [ctypes.c_int] * 6 + [ctypes.c_double]
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
         self.lib = lib
@@ -211,6 +216,37 @@ class Oracle:
         out = np.empty((b, hq, d), np.float64)
         self.lib.oracle_decode_quant_k(_p(out, _f64p), _p(qb, _u16p), _p(kc, _i8p), _p(ks, _f32p), _p(vc, _u16p),
                                        _p(bt, _i32p), _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs, float(scale))
+        return out
+
+    def append_quant_kv(self, k_codes, k_scale, v_codes, v_scale, slots, k_new, v_new) -> None:
+        """In place on the int8 K + V cache: codes int8 [NB,Hkv,bs,D], scales float32 [NB,Hkv,bs]."""
+        nb, hkv, bs, d = k_codes.shape
+        for a, dt in ((k_codes, np.int8), (v_codes, np.int8), (k_scale, np.float32), (v_scale, np.float32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        assert v_codes.shape == k_codes.shape and k_scale.shape == (nb, hkv, bs) and v_scale.shape == k_scale.shape
+        kn, vn = _bits(k_new), _bits(v_new)
+        sl = np.ascontiguousarray(slots, dtype=np.int64)
+        assert kn.shape == (sl.shape[0], hkv, d) and vn.shape == kn.shape
+        self.lib.oracle_append_quant_kv(_p(k_codes, _i8p), _p(k_scale, _f32p), _p(v_codes, _i8p), _p(v_scale, _f32p),
+                                        _p(sl, _i64p), _p(kn, _u16p), _p(vn, _u16p), sl.shape[0], hkv, d, bs)
+
+    def decode_quant_kv(self, q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens,
+                        scale: float) -> np.ndarray:
+        """float64 [B, Hq, D] decode over the int8 K + V cache (both dequantised exactly)."""
+        qb = _bits(q)
+        kc = np.ascontiguousarray(k_codes, dtype=np.int8)
+        vc = np.ascontiguousarray(v_codes, dtype=np.int8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        b, hq, d = qb.shape
+        nb, hkv, bs, d2 = kc.shape
+        assert d2 == d and hq % hkv == 0 and vc.shape == kc.shape and ks.shape == vs.shape == (nb, hkv, bs)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty((b, hq, d), np.float64)
+        self.lib.oracle_decode_quant_kv(_p(out, _f64p), _p(qb, _u16p), _p(kc, _i8p), _p(ks, _f32p), _p(vc, _i8p),
+                                        _p(vs, _f32p), _p(bt, _i32p), _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs,
+                                        float(scale))
         return out
 
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
@@ -329,6 +365,14 @@ def quantize_k_row(k_row):
 
 def copy_blocks_between(dst_k, dst_v, src_k, src_v, src, dst):
     return default().copy_blocks_between(dst_k, dst_v, src_k, src_v, src, dst)
+
+
+def append_quant_kv(k_codes, k_scale, v_codes, v_scale, slots, k_new, v_new):
+    return default().append_quant_kv(k_codes, k_scale, v_codes, v_scale, slots, k_new, v_new)
+
+
+def decode_quant_kv(q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, scale):
+    return default().decode_quant_kv(q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, scale)
 
 
 def decode_multi(q, k_cache, v_cache, block_tables, context_lens, query_start, scale):

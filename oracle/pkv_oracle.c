@@ -44,6 +44,7 @@
  *     code_d = round-half-even(k_d / s), both in float32, so that the integer
  *     decision is taken in the precision the kernels use; an all-zero row has
  *     s = 0 and zero codes.  Attention then uses k_d = code_d * s exactly.
+ *     The optional int8 K + V cache quantises value rows by the same scheme.
  *
  * fp16 values are carried as raw uint16 bit patterns and decoded to double by
  * the IEEE-754 binary16 definition (sign, 5-bit exponent with bias 15, 10-bit
@@ -361,6 +362,74 @@ void oracle_decode_multi(double *out, const uint16_t *q, const uint16_t *k_cache
                 softmax_weighted_sum(o, &m, &l, s, v_cache, bt_row, 0, visible, kvh, num_kv_heads,
                                      head_dim, block_size);
             }
+        }
+        free(s);
+    }
+}
+
+/* Append into the int8 K + V cache: both rows quantised by oracle_quantize_k_row
+ * (the same symmetric per-row scheme for values), codes and scales stored at the
+ * slot.  Layouts as oracle_append_quant_k, with v_codes / v_scale like the keys'. */
+void oracle_append_quant_kv(int8_t *k_codes, float *k_scale, int8_t *v_codes, float *v_scale,
+                            const int64_t *slot_mapping, const uint16_t *k_new, const uint16_t *v_new,
+                            int num_tokens, int num_kv_heads, int head_dim, int block_size)
+{
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t blk = slot / block_size;
+        int off = (int)(slot % block_size);
+        for (int j = 0; j < num_kv_heads; ++j) {
+            int64_t row = blk * num_kv_heads * block_size + (int64_t)j * block_size + off;
+            int64_t src = ((int64_t)t * num_kv_heads + j) * head_dim;
+            oracle_quantize_k_row(k_codes + row * head_dim, k_scale + row, k_new + src, head_dim);
+            oracle_quantize_k_row(v_codes + row * head_dim, v_scale + row, v_new + src, head_dim);
+        }
+    }
+}
+
+/* Decode attention over the int8 K + V cache: keys and values dequantised,
+ * code * scale (float64), then the plain definition.  Same shapes and rules as
+ * oracle_decode. */
+void oracle_decode_quant_kv(double *out, const uint16_t *q, const int8_t *k_codes, const float *k_scale,
+                            const int8_t *v_codes, const float *v_scale, const int32_t *block_tables,
+                            const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size, double scale)
+{
+    int group = num_q_heads / num_kv_heads;
+    for (int b = 0; b < num_seqs; ++b) {
+        int ctx = context_lens[b];
+        const int32_t *bt_row = block_tables + (int64_t)b * max_blocks_per_seq;
+        double *s = (double *)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+        for (int h = 0; h < num_q_heads; ++h) {
+            int head_kv = h / group;
+            double *o = out + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            if (ctx <= 0)
+                continue;
+            const uint16_t *q_row = q + ((int64_t)b * num_q_heads + h) * head_dim;
+            double m = -INFINITY;
+            for (int p = 0; p < ctx; ++p) {
+                int64_t row = ((int64_t)bt_row[p / block_size] * num_kv_heads + head_kv) * block_size + p % block_size;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += oracle_half_to_double(q_row[d]) * ((double)k_scale[row] * k_codes[row * head_dim + d]);
+                s[p] = scale * dot;
+                if (s[p] > m)
+                    m = s[p];
+            }
+            double l = 0.0;
+            for (int p = 0; p < ctx; ++p) {
+                int64_t row = ((int64_t)bt_row[p / block_size] * num_kv_heads + head_kv) * block_size + p % block_size;
+                double w = exp(s[p] - m);
+                l = l + w;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] += w * ((double)v_codes[row * head_dim + d] * v_scale[row]);
+            }
+            for (int d = 0; d < head_dim; ++d)
+                o[d] /= l;
         }
         free(s);
     }

@@ -258,6 +258,53 @@ def pin_decode_quant_k(orc):
     assert np.abs(got - ref).max() <= 1e-12
 
 
+def pin_quant_kv(orc):
+    """int8 K + V: the append stores the quantiser's codes and scales for both rows; with scales
+    that are powers of two the decode equals the fp16 decode of the exact dequantised cache, and
+    with the values' codes and scales it equals the int8-key decode over those dequantised values."""
+    rng = np.random.default_rng(31)
+    nb, hkv, bs, d = 6, 2, 4, 16
+    kc = np.zeros((nb, hkv, bs, d), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((nb, hkv, bs), np.float32)
+    vs = np.zeros_like(ks)
+    slots = np.array([3, 22, -1, 9], np.int64)
+    kn = rng.standard_normal((4, hkv, d)).astype(np.float16)
+    vn = rng.standard_normal((4, hkv, d)).astype(np.float16)
+    orc.append_quant_kv(kc, ks, vc, vs, slots, kn, vn)
+    for ti, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        for j in range(hkv):
+            c, sc = orc.quantize_k_row(vn[ti, j])
+            assert np.array_equal(vc[sl // bs, j, sl % bs], c) and vs[sl // bs, j, sl % bs] == sc
+            c, sc = orc.quantize_k_row(kn[ti, j])
+            assert np.array_equal(kc[sl // bs, j, sl % bs], c) and ks[sl // bs, j, sl % bs] == sc
+    hq, ctxs = 4, [7, 0, 16, 1]
+    nb = 20
+    kc = rng.integers(-127, 128, size=(nb, hkv, bs, d)).astype(np.int8)
+    vc = rng.integers(-127, 128, size=(nb, hkv, bs, d)).astype(np.int8)
+    ks = (2.0 ** rng.integers(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    vs = (2.0 ** rng.integers(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    bt = rng.permutation(nb)[:16].reshape(4, 4).astype(np.int32)
+    q = rng.standard_normal((4, hq, d)).astype(np.float16)
+    ctx = np.array(ctxs, np.int32)
+    k16 = (kc.astype(np.float64) * ks[..., None]).astype(np.float16)
+    v16 = (vc.astype(np.float64) * vs[..., None]).astype(np.float16)
+    got = orc.decode_quant_kv(q, kc, ks, vc, vs, bt, ctx, 0.3)
+    assert np.abs(got - orc.decode(q, k16, v16, bt, ctx, 0.3)).max() <= 1e-15
+    vs = rng.uniform(1e-3, 5e-2, size=(nb, hkv, bs)).astype(np.float32)
+    vdq = vc.astype(np.float64) * vs[..., None].astype(np.float64)
+    got = orc.decode_quant_kv(q, kc, ks, vc, vs, bt, ctx, 0.3)
+    ks_rows = [[kc[bt[b, p // bs], :, p % bs].astype(np.float64) * ks[bt[b, p // bs], :, p % bs][:, None]
+                for p in range(c)] for b, c in enumerate(ctxs)]
+    kk = [np.stack(r, 1) if r else np.zeros((hkv, 0, d)) for r in ks_rows]
+    vv = [np.stack([vdq[bt[b, p // bs], :, p % bs] for p in range(c)], 1) if c else np.zeros((hkv, 0, d))
+          for b, c in enumerate(ctxs)]
+    ref = textbook_attention(q, kk, vv, 0.3)
+    assert np.abs(got - ref).max() <= 1e-12
+
+
 def pin_decode_multi_causal(orc):
     """Several new tokens per request: a textbook causal attention (scipy softmax over the
     scores with every later position masked) on contiguous K/V, and row by row the single-token
@@ -495,6 +542,7 @@ ALL_PINS = [
     pin_append_quant_k,
     pin_decode_quant_k,
     pin_decode_multi_causal,
+    pin_quant_kv,
     pin_slot_mapping_by_enumeration,
     pin_two_keys_golden,
     pin_textbook_contiguous,

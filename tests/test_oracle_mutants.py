@@ -45,6 +45,10 @@ MUTANTS = {
     "multi_row_offset": ("int64_t t = query_start[b] + i;", "int64_t t = query_start[b] + n - 1 - i;"),
     "swap_copy_wrong_index": ("dst_k[(int64_t)dst[i] * elems + e] = src_k[(int64_t)src[i] * elems + e];",
                               "dst_k[(int64_t)dst[i] * elems + e] = src_k[(int64_t)dst[i] * elems + e];"),
+    "quant_kv_drops_v_scale": ("o[d] += w * ((double)v_codes[row * head_dim + d] * v_scale[row]);",
+                               "o[d] += w * ((double)v_codes[row * head_dim + d]);"),
+    "quant_kv_v_from_k": ("oracle_quantize_k_row(v_codes + row * head_dim, v_scale + row, v_new + src, head_dim);",
+                          "oracle_quantize_k_row(v_codes + row * head_dim, v_scale + row, k_new + src, head_dim);"),
     "copy_blocks_one_head": ("int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;",
                              "int64_t per_block = (int64_t)block_size * head_dim;"),
 }
