@@ -204,11 +204,12 @@ def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tok
                  kv="fp16", q_len=1):
     """Algorithmic bytes of one decode-attention call: K and V of every cached token read once
     (a shared prefix once), q read, out written, block-table entries and context lengths read.
-    kv="int8k": a key row is head_dim int8 codes plus one float32 scale."""
+    kv="int8k": a key row is head_dim int8 codes plus one float32 scale; kv="int8kv": value rows too."""
     b = len(ctx) if num_seqs is None else num_seqs
     tokens = sum(ctx) - unique_prefix_tokens * (b - 1) if unique_prefix_tokens else sum(ctx)
-    k_row = head_dim + 4 if kv == "int8k" else head_dim * 2
-    kv = tokens * num_kv_heads * (k_row + head_dim * 2)
+    k_row = head_dim + 4 if kv in ("int8k", "int8kv") else head_dim * 2
+    v_row = head_dim + 4 if kv == "int8kv" else head_dim * 2
+    kv = tokens * num_kv_heads * (k_row + v_row)
     qo = 2 * b * q_len * num_q_heads * head_dim * 2
     tables = sum(-(-c // bs) for c in ctx) * 4 + 4 * b
     return kv + qo + tables
@@ -244,6 +245,21 @@ def run_ours(args):
         cpu_sample = {k: getattr(c0, k).cpu().numpy() for k in
                       ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
     int8k = args.kv == "int8k"
+    int8kv = args.kv == "int8kv"
+    if int8kv:
+        # int8 K + V cache per layer: every pool row of the generated fp16 keys and values quantised by the
+        # library's own append kernel (set-up, outside the timed regions)
+        for c in cases:
+            nb_, hkv_, bs_, d_ = c.k_cache.shape
+            c.k_codes, c.k_scale, c.v_codes, c.v_scale = pkv.empty_int8kv_cache(nb_, hkv_, bs_, dev)
+            rows_k = c.k_cache.permute(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_).contiguous()
+            rows_v = c.v_cache.permute(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_).contiguous()
+            pkv.append_int8kv(c.k_codes, c.k_scale, c.v_codes, c.v_scale, torch.arange(nb_ * bs_, device=dev), rows_k,
+                              rows_v)
+            del rows_k, rows_v
+            c.k_cache = c.v_cache = None
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
     if int8k:
         # int8-key cache per layer: every pool row of the generated fp16 keys quantised by the library's own
         # append kernel (set-up, outside the timed regions); V stays as generated
@@ -295,7 +311,8 @@ def run_ours(args):
     prefix_len = 1024 if cascade else 0
     # the long-context workload is defined with 512-token split partitions; the others take the library's
     # default (PKV_DEFAULT_PARTITION)
-    part = 512 if args.workload == "long_context" and nq == 1 and not int8k and not args.separate_append else 0
+    part = 512 if (args.workload == "long_context" and nq == 1 and args.kv == "fp16"
+                   and not args.separate_append) else 0
     ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev, partition_size=part) if nq == 1 else \
         pkv.make_multi_workspace(B, B * nq, nq, Hq, Hkv, max_ctx_cap, dev)
 
@@ -308,6 +325,15 @@ def run_ours(args):
                 pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
             pkv.decode_attention_multi(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, query_start, nq,
                                        c.scale, workspace=ws)
+        elif int8kv:
+            if args.separate_append:
+                if not attention_only:
+                    pkv.append_int8kv(c.k_codes, c.k_scale, c.v_codes, c.v_scale, slot_cur, c.k_new, c.v_new)
+                pkv.decode_attention_int8kv(out_all[l], c.q, c.k_codes, c.k_scale, c.v_codes, c.v_scale, block_tables,
+                                            ctx_cur, c.scale, workspace=ws)
+            else:
+                pkv.decode_step_int8kv(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_codes, c.v_scale,
+                                       block_tables, ctx_cur, c.scale, workspace=ws)
         elif int8k:
             if args.separate_append:
                 if not attention_only:
@@ -487,7 +513,11 @@ def run_ours(args):
     peak, peak_src = read_peaks()
     gbs = bytes_job / (ms_job * 1e-3) / 1e9
     achieved = kernel_bytes_avg / (kernel_avg_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload + ("/int8k" if int8k else "") + (f"/q{nq}" if nq > 1 else ""), bs)
+    traffic = read_traffic(args.workload + ("" if args.kv == "fp16" else "/" + args.kv) + (f"/q{nq}" if nq > 1 else ""),
+                           bs)
+    layer_cache_bytes = (cases[0].k_codes.numel() * (2 if int8kv else 1) + cases[0].k_scale.numel() * 4
+                         * (2 if int8kv else 1) + (0 if int8kv else cases[0].v_cache.numel() * 2)
+                         if args.kv != "fp16" else cases[0].v_cache.numel() * 4)
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -499,7 +529,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "i8 keys (f32 row scales), f16 values" if int8k else "f16",
+        "dtype": KV_DTYPE[args.kv],
         "accumulate": "f32",
         "data": "synthetic (seeded N(0,1) fp16 K/V/q, seeded block permutation)",
         "config": {
@@ -511,14 +541,14 @@ def run_ours(args):
             "head_dim": D,
             "block_size": bs,
             "partition_size": part or pkv.PKV_DEFAULT_PARTITION,
-            "kv_cache": "int8 keys + float32 scale per (token, kv head), fp16 values" if int8k else "fp16 K and V",
+            "kv_cache": KV_TEXT[args.kv],
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
-                  % (cases[0].v_cache.numel() * (3 if int8k else 4) / 1e6, bytes_job / 1e9),
+                  % (layer_cache_bytes / 1e6, bytes_job / 1e9),
             "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
             "decode_call": (f"pkv_append + pkv_decode_attention_multi ({nq} new tokens per request, causal)"
                             if nq > 1 else
-                            ("pkv_append" + ("_int8k" if int8k else "") + " + " if args.separate_append
-                             else "pkv_decode_step" + ("_int8k" if int8k else "") + " ")
+                            ("pkv_append" + KV_SUFFIX[args.kv] + " + " if args.separate_append
+                             else "pkv_decode_step" + KV_SUFFIX[args.kv] + " ")
                             + ("shared prefix 1024 tokens" if cascade else "")),
         },
         "tokens_per_s": round(B * nq * world / (ms_job * 1e-3), 1),
@@ -564,6 +594,27 @@ def run_ours(args):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
+KV_DTYPE = {"fp16": "f16", "int8k": "i8 keys (f32 row scales), f16 values",
+            "int8kv": "i8 keys and values (f32 row scales)"}
+KV_TEXT = {"fp16": "fp16 K and V", "int8k": "int8 keys + float32 scale per (token, kv head), fp16 values",
+           "int8kv": "int8 keys and values, each + float32 scale per (token, kv head)"}
+KV_SUFFIX = {"fp16": "", "int8k": "_int8k", "int8kv": "_int8kv"}
+
+
+def oracle_int8kv_pool(h):
+    """Host int8 K + V pool (k_codes, k_scale, v_codes, v_scale) of the sample's fp16 rows, quantised
+    by the oracle."""
+    import numpy as np
+
+    import oracle
+    nb, hkv, bs, d = h["k_cache"].shape
+    pool = (np.zeros((nb, hkv, bs, d), np.int8), np.zeros((nb, hkv, bs), np.float32),
+            np.zeros((nb, hkv, bs, d), np.int8), np.zeros((nb, hkv, bs), np.float32))
+    rows = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    oracle.append_quant_kv(*pool, np.arange(nb * bs, dtype=np.int64), rows(h["k_cache"]), rows(h["v_cache"]))
+    return pool
+
+
 def oracle_int8k_pool(h):
     """Host int8-key pool (codes, scales) of the sample's fp16 keys, quantised by the oracle."""
     import numpy as np
@@ -588,7 +639,13 @@ def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None, kv="
     ctx = h["context_lens"].tolist()
     b = len(ctx)
     slots = oracle.slot_mapping(h["block_tables"], h["positions"], bs)
-    if kv == "int8k":
+    if kv == "int8kv":
+        pool = oracle_int8kv_pool(h)
+        t0 = time.perf_counter()
+        oracle.append_quant_kv(*pool, slots, h["k_new"], h["v_new"])
+        decode_one = lambda sl: oracle.decode_quant_kv(h["q"][sl], *pool, h["block_tables"][sl],
+                                                       h["context_lens"][sl], case.scale)
+    elif kv == "int8k":
         codes, scales = oracle_int8k_pool(h)
         t0 = time.perf_counter()
         oracle.append_quant_k(codes, scales, h["v_cache"], slots, h["k_new"], h["v_new"])
@@ -660,7 +717,13 @@ def run_reference(args):
     sl = slice(0, n_req)
     slots = oracle.slot_mapping(h["block_tables"][sl], h["positions"][sl], bs)
 
-    if args.kv == "int8k":
+    if args.kv == "int8kv":
+        pool = oracle_int8kv_pool(h)
+
+        def one():
+            oracle.append_quant_kv(*pool, slots, h["k_new"][sl], h["v_new"][sl])
+            oracle.decode_quant_kv(h["q"][sl], *pool, h["block_tables"][sl], h["context_lens"][sl], case.scale)
+    elif args.kv == "int8k":
         codes, scales = oracle_int8k_pool(h)
 
         def one():
@@ -698,8 +761,7 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) fp16 K/V/q, seeded block permutation)",
         "config": {"workload": WORKLOAD_TEXT[args.workload].format(bs=bs), "block_size": bs,
-                   "kv_cache": "int8 keys + float32 scale per (token, kv head), fp16 values" if args.kv == "int8k"
-                   else "fp16 K and V"},
+                   "kv_cache": KV_TEXT[args.kv]},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -720,8 +782,9 @@ def main(argv=None):
     ap.add_argument("--no-cascade", action="store_true", help="shared_prefix: plain decode instead of the cascade")
     ap.add_argument("--separate-append", action="store_true",
                     help="two calls per layer (pkv_append, then attention) instead of pkv_decode_step")
-    ap.add_argument("--kv", choices=["fp16", "int8k"], default="fp16",
-                    help="cache format: fp16 K/V, or int8 keys with float32 row scales and fp16 values")
+    ap.add_argument("--kv", choices=["fp16", "int8k", "int8kv"], default="fp16",
+                    help="cache format: fp16 K/V; int8 keys with float32 row scales and fp16 values; "
+                         "or int8 keys and values, each with float32 row scales")
     ap.add_argument("--query-len", type=int, default=1,
                     help="new tokens per request per step (>1: append them, then causal multi-token attention)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -733,8 +796,8 @@ def main(argv=None):
         ap.error("--query-len > 1 runs the fp16 multi-token path on mha7b, gqa8b, long_context or tiny")
     if args.query_len > 1 and args.impl == "reference":
         ap.error("the reference arm times single-token steps")
-    if args.kv == "int8k" and args.workload == "shared_prefix" and not args.no_cascade:
-        ap.error("the shared-prefix cascade reads fp16 keys; use --no-cascade with --kv int8k")
+    if args.kv != "fp16" and args.workload == "shared_prefix" and not args.no_cascade:
+        ap.error("the shared-prefix cascade reads fp16 K/V; use --no-cascade with an int8 cache")
     if args.impl == "reference":
         run_reference(args)
     else:

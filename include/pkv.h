@@ -377,6 +377,41 @@ PKV_API int pkv_decode_step_int8k(void *out, const void *q, const void *k_new, c
                                   int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
                                   pkv_stream_t stream);
 
+/* ---- int8 keys and values (optional) --------------------------------------
+ * Values quantised by the same per-row scheme as the keys: int8 codes
+ * v_codes [num_blocks][num_kv_heads][block_size][128] and float32 v_scale
+ * [num_blocks][num_kv_heads][block_size]; attention uses v_d = code_d * scale.
+ * 128 + 4 + 128 + 4 bytes per cached token and kv head instead of 512.  The
+ * pages advise keeping values in high precision (quality on long generations,
+ * "推理优化这件事，为什么值得反复复盘", sec. 4.4): this is the option for callers
+ * that accept that trade; the int8-key cache above is the default form. */
+
+/* Append into the int8 K + V cache: both rows quantised at each slot.  Rules and
+ * errors as pkv_append_int8k. */
+PKV_API int pkv_append_int8kv(void *k_codes, float *k_scale, void *v_codes, float *v_scale,
+                              const int64_t *slot_mapping, const void *k_new, const void *v_new, int num_tokens,
+                              int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                              pkv_stream_t stream);
+
+/* pkv_decode_attention over the int8 K + V cache (keys and values dequantised).
+ * Scales 16-byte aligned.  Workspace and errors as pkv_decode_attention_int8k. */
+PKV_API int pkv_decode_attention_int8kv(void *out, const void *q, const void *k_codes, const float *k_scale,
+                                        const void *v_codes, const float *v_scale, const int32_t *block_tables,
+                                        const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                        int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                        pkv_stream_t stream);
+
+/* pkv_decode_step over the int8 K + V cache: the new token's key and value rows
+ * are quantised and written by the decode kernel, then attended.  Same as
+ * pkv_append_int8kv at positions ctx - 1 followed by pkv_decode_attention_int8kv. */
+PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const void *k_new, const void *v_new, void *k_codes,
+                                   float *k_scale, void *v_codes, float *v_scale, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream);
+
 /* ---- several new tokens per request ----------------------------------------
  * A verified draft (speculative decoding) or a prefill chunk: request b brings
  * n_b = query_start[b + 1] - query_start[b] new tokens whose K/V are already in

@@ -54,11 +54,28 @@ __global__ void __launch_bounds__(kAppendThreads)
 // scale max|k| / 127 comes from a warp max; codes are round-half-even(k / scale) in float32.
 constexpr int kRowsPerAppendBlock = kAppendThreads / 32;
 
+// The row's codes (4 per lane, little-endian: dim 4i in byte 0) and scale max|x| / 127.
+__device__ __forceinline__ uint32_t quantize_row_part(uint2 raw, float &scale) {
+    const float2 x01 = pkv::half2_bits_to_float2(raw.x);
+    const float2 x23 = pkv::half2_bits_to_float2(raw.y);
+    float amax = fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(pkv::kFullMask, amax, sh));
+    const float s = __fdiv_rn(amax, 127.f);
+    scale = s;
+    return (static_cast<uint32_t>(pkv::quantize_int8(x01.x, s)) & 0xffu) |
+           ((static_cast<uint32_t>(pkv::quantize_int8(x01.y, s)) & 0xffu) << 8) |
+           ((static_cast<uint32_t>(pkv::quantize_int8(x23.x, s)) & 0xffu) << 16) |
+           (static_cast<uint32_t>(pkv::quantize_int8(x23.y, s)) << 24);
+}
+
+// QV: the value rows are quantised too (v_out holds int8 codes, v_scale their scales).
+template <bool QV>
 __global__ void __launch_bounds__(kAppendThreads)
-    append_int8k_kernel(uint32_t *__restrict__ k_codes, float *__restrict__ k_scale, uint2 *__restrict__ v_cache,
-                        const int64_t *__restrict__ slot_mapping, const uint2 *__restrict__ k_new,
-                        const uint2 *__restrict__ v_new, int64_t rows, int num_kv_heads, int block_size,
-                        int64_t num_slots) {
+    append_int8k_kernel(uint32_t *__restrict__ k_codes, float *__restrict__ k_scale, void *__restrict__ v_out,
+                        float *__restrict__ v_scale, const int64_t *__restrict__ slot_mapping,
+                        const uint2 *__restrict__ k_new, const uint2 *__restrict__ v_new, int64_t rows,
+                        int num_kv_heads, int block_size, int64_t num_slots) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerAppendBlock + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;  // warp-uniform
@@ -72,18 +89,17 @@ __global__ void __launch_bounds__(kAppendThreads)
     }
     const int64_t block = slot / block_size;
     const int64_t dst = (block * num_kv_heads + head) * block_size + (slot - block * block_size);
-    v_cache[dst * 32 + lane] = __ldg(v_new + row * 32 + lane);
-    const uint2 raw = __ldg(k_new + row * 32 + lane);
-    const float2 k01 = pkv::half2_bits_to_float2(raw.x);
-    const float2 k23 = pkv::half2_bits_to_float2(raw.y);
-    float amax = fmaxf(fmaxf(fabsf(k01.x), fabsf(k01.y)), fmaxf(fabsf(k23.x), fabsf(k23.y)));
-#pragma unroll
-    for (int sh = 16; sh >= 1; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(pkv::kFullMask, amax, sh));
-    const float s = __fdiv_rn(amax, 127.f);
-    const uint32_t packed = (static_cast<uint32_t>(pkv::quantize_int8(k01.x, s)) & 0xffu) |
-                            ((static_cast<uint32_t>(pkv::quantize_int8(k01.y, s)) & 0xffu) << 8) |
-                            ((static_cast<uint32_t>(pkv::quantize_int8(k23.x, s)) & 0xffu) << 16) |
-                            (static_cast<uint32_t>(pkv::quantize_int8(k23.y, s)) << 24);
+    const uint2 v_raw = __ldg(v_new + row * 32 + lane);
+    if constexpr (QV) {
+        float vs;
+        const uint32_t vc = quantize_row_part(v_raw, vs);
+        static_cast<uint32_t *>(v_out)[dst * 32 + lane] = vc;
+        if (lane == 0) v_scale[dst] = vs;
+    } else {
+        static_cast<uint2 *>(v_out)[dst * 32 + lane] = v_raw;
+    }
+    float s;
+    const uint32_t packed = quantize_row_part(__ldg(k_new + row * 32 + lane), s);
     k_codes[dst * 32 + lane] = packed;
     if (lane == 0) k_scale[dst] = s;
 }
@@ -162,10 +178,34 @@ extern "C" PKV_API int pkv_append_int8k(void *k_codes, float *k_scale, void *v_c
     const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads;
     const int64_t blocks = (rows + kRowsPerAppendBlock - 1) / kRowsPerAppendBlock;
     if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
-    append_int8k_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint32_t *>(k_codes), k_scale, static_cast<uint2 *>(v_cache), slot_mapping,
-        static_cast<const uint2 *>(k_new), static_cast<const uint2 *>(v_new), rows, num_kv_heads, block_size,
-        num_blocks * block_size);
+    append_int8k_kernel<false><<<static_cast<unsigned>(blocks), kAppendThreads, 0,
+                                 reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint32_t *>(k_codes), k_scale, v_cache, nullptr, slot_mapping, static_cast<const uint2 *>(k_new),
+        static_cast<const uint2 *>(v_new), rows, num_kv_heads, block_size, num_blocks * block_size);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" PKV_API int pkv_append_int8kv(void *k_codes, float *k_scale, void *v_codes, float *v_scale,
+                                         const int64_t *slot_mapping, const void *k_new, const void *v_new,
+                                         int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                                         int64_t num_blocks, pkv_stream_t stream) {
+    if (!k_codes || !k_scale || !v_codes || !v_scale || (num_tokens > 0 && (!slot_mapping || !k_new || !v_new)))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != PKV_HEAD_DIM) return PKV_ERR_UNSUPPORTED;
+    if (!pkv_internal::aligned16(k_codes) || !pkv_internal::aligned(k_scale, 4) || !pkv_internal::aligned16(v_codes) ||
+        !pkv_internal::aligned(v_scale, 4) ||
+        (num_tokens > 0 && (!pkv_internal::aligned(slot_mapping, 8) || !pkv_internal::aligned(k_new, 8) ||
+                            !pkv_internal::aligned(v_new, 8))))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads;
+    const int64_t blocks = (rows + kRowsPerAppendBlock - 1) / kRowsPerAppendBlock;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    append_int8k_kernel<true><<<static_cast<unsigned>(blocks), kAppendThreads, 0,
+                                reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint32_t *>(k_codes), k_scale, v_codes, v_scale, slot_mapping, static_cast<const uint2 *>(k_new),
+        static_cast<const uint2 *>(v_new), rows, num_kv_heads, block_size, num_blocks * block_size);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

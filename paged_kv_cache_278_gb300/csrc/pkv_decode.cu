@@ -134,6 +134,8 @@ struct DecodeParams {
     int mq_tiles;                // 8-column MMA tiles per CTA for several tokens per request (1 or 2)
     const float *k_scale;     // int8 key cache: float32 scale per (block, kv head, slot); null for fp16 keys
     float *k_scale_w;         // writable view of k_scale for the fused append
+    const float *v_scale;     // int8 values too: float32 scale per (block, kv head, slot); null for fp16 values
+    float *v_scale_w;
     CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
     CUtensorMap tmap_v;       //   16 x 64 boxes, 128-byte swizzle (int8 keys: 16 x 128-byte boxes)
 };
@@ -146,16 +148,19 @@ constexpr int kMergeTile = 512;  // partitions whose weights the fused merge sta
 // KQ (int8 keys): the K tile is one 2 KB box of 16 int8 rows in the same swizzle, and each stage
 // also holds the chunk's 16 float32 key scales.
 constexpr int kHalfTile = kChunk * 128;
-template <bool TC, bool KQ = false, int NT = 1>
+// KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values.
+template <bool TC, int KQ = 0, int NT = 1>
 struct SmemLayout {
     static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
     static constexpr int k_tile = KQ ? kChunk * kD : tile;
-    static constexpr int stage = k_tile + tile;
+    static constexpr int v_tile = KQ == 2 ? kChunk * kD : tile;
+    static constexpr int stage = k_tile + v_tile;
+    static constexpr int scale_stride = KQ == 2 ? 2 * kChunk * 4 : kChunk * 4;  // K scales (| V scales) per stage
     static constexpr int stages = 0;
     static constexpr int stage_bytes = kWarps * kStages * stage;
     static constexpr int scales = stages + stage_bytes;
-    static constexpr int bars = scales + (KQ ? kWarps * kStages * kChunk * 4 : 0);
+    static constexpr int bars = scales + (KQ ? kWarps * kStages * scale_stride : 0);
     static constexpr int probs = bars + kWarps * kStages * kBarsPerStage * 8;
     __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? NT * 2 * 8 * kChunk * 2 : kChunk * g * 4; }
     __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
@@ -190,7 +195,8 @@ struct TokenRows {
 // Log-sum-exp merge of partial slots [0, n_total) of the G packed columns (query heads, or
 // (token, head) rows) of one CTA's kv head into fp16 out; called by every thread of one CTA
 // (it synchronises the CTA).
-template <int G, class Rows>
+// STAGE_BYTES: the caller's shared memory available for the staging (its stage buffers).
+template <int G, int STAGE_BYTES, class Rows>
 __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total, unsigned char *smem) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -201,9 +207,12 @@ __device__ void merge_group(const DecodeParams &P, const Rows &rows, int n_total
     constexpr int GROUPS = SLOTS >= kThreads ? 1 : kThreads / SLOTS;
     constexpr int PER_THREAD = SLOTS >= kThreads ? SLOTS / kThreads : 1;
     static_assert(SLOTS % kThreads == 0 || kThreads % SLOTS == 0, "slot split");
-    constexpr int TILE = G > 8 ? kMergeTile / 2 : kMergeTile;  // partitions staged at a time
-    static_assert(2 * G * TILE * 4 + G * 4 + 16 + GROUPS * SLOTS * 20 <= SmemLayout<true, true>::stage_bytes,
-                  "merge staging must fit the stages");
+    // partitions staged at a time: the largest of 512, 256, 128 whose staging fits
+    constexpr int kFixed = G * 4 + 16 + GROUPS * SLOTS * 20;
+    constexpr int TILE = 2 * G * kMergeTile * 4 + kFixed <= STAGE_BYTES         ? kMergeTile
+                         : 2 * G * (kMergeTile / 2) * 4 + kFixed <= STAGE_BYTES ? kMergeTile / 2
+                                                                                 : kMergeTile / 4;
+    static_assert(2 * G * TILE * 4 + kFixed <= STAGE_BYTES, "merge staging must fit the stages");
     float *s_wt = reinterpret_cast<float *>(smem);                  // [2][G][TILE]
     float *s_max = s_wt + 2 * G * TILE;                        // [G]
     float4 *s_acc = reinterpret_cast<float4 *>(s_max + G + 4 - (G % 4 == 0 ? 4 : G % 4));  // [GROUPS][SLOTS]
@@ -630,8 +639,12 @@ struct TcEngine {
     // h0 / h0 + 1); the weights go to the warp's scratch as fp16 hi / lo parts for pv() (ends
     // synchronised).  kAnyMasked: a column may have no visible token yet (its reference max still
     // -inf), so a masked score's weight is forced to 0 instead of exp2(-inf - -inf).
-    template <bool kAnyMasked = false>
-    __device__ __forceinline__ void softmax(float (&s)[4], int lane, unsigned char *scratch) {
+    // kVScale: the weights stored for P.V are multiplied by the chunk's value row scales (float32 at
+    // vs_tile, one per token); l keeps the unscaled weights.  The reference max then follows the
+    // running max exactly (no lazy margin), so a weight is at most 1 and weight x scale at most
+    // 65504 / 127: it cannot overflow fp16.
+    template <bool kAnyMasked = false, bool kVScale = false>
+    __device__ __forceinline__ void softmax(float (&s)[4], int lane, unsigned char *scratch, uint32_t vs_tile = 0) {
         const int g = lane >> 2;
         float cm0 = fmaxf(s[0], s[2]), cm1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -641,7 +654,8 @@ struct TcEngine {
         }
         top[0] = fmaxf(top[0], cm0);
         top[1] = fmaxf(top[1], cm1);
-        if (__any_sync(pkv::kFullMask, cm0 > m_ref[0] + kRescaleThreshold || cm1 > m_ref[1] + kRescaleThreshold)) {
+        constexpr float kMargin = kVScale ? 0.f : kRescaleThreshold;
+        if (__any_sync(pkv::kFullMask, cm0 > m_ref[0] + kMargin || cm1 > m_ref[1] + kMargin)) {
             const float n0 = fmaxf(m_ref[0], cm0), n1 = fmaxf(m_ref[1], cm1);
             float a0 = exp2f(m_ref[0] - n0), a1 = exp2f(m_ref[1] - n1);
             if (kAnyMasked) {  // a column still without a visible token: nothing to rescale (-inf - -inf)
@@ -668,6 +682,11 @@ struct TcEngine {
         }
         l_part[0] += p[0] + p[2];
         l_part[1] += p[1] + p[3];
+        if (kVScale) {
+            const float vg = pkv::lds32f(vs_tile + 4 * g), v8 = pkv::lds32f(vs_tile + 4 * (g + 8));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = p[e] == 0.f ? 0.f : p[e] * (e < 2 ? vg : v8);  // masked rows: 0
+        }
         // P^T through shared memory as fp16 hi / lo: [2][8 heads][16 tokens]
         __half *ph = reinterpret_cast<__half *>(scratch);
         __half *pl = ph + 8 * kChunk;
@@ -700,7 +719,10 @@ struct TcEngine {
         }
     }
 
-    // Columns go to slots c0 .. c0 + G - 1 of the combine area's nc columns per warp.
+    // Columns go to slots c0 .. c0 + G - 1 of the combine area's nc columns per warp.  kPermDims:
+    // the accumulator rows are dims in the int8-value order (row g of m-tile mt = dim 16 g + 2 mt,
+    // row g + 8 = dim 16 g + 2 mt + 1).
+    template <bool kPermDims = false>
     __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l, int nc = G,
                                            int c0 = 0) {
         float l[2] = {l_part[0], l_part[1]};
@@ -724,7 +746,8 @@ struct TcEngine {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int h = h0 + (e & 1);
-                if (h < G) c_acc[(warp * nc + c0 + h) * kD + mt * 16 + g + (e >> 1) * 8] = o[mt][e] * f[e & 1];
+                const int dim = kPermDims ? 16 * g + 2 * mt + (e >> 1) : mt * 16 + g + (e >> 1) * 8;
+                if (h < G) c_acc[(warp * nc + c0 + h) * kD + dim] = o[mt][e] * f[e & 1];
             }
         if (g == 0) {
 #pragma unroll
@@ -766,12 +789,20 @@ struct TcEngineQ : TcEngine<G> {
 
     __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t s_tile, int valid, int lane, unsigned char *scratch,
                                        int) {
+        float s[4];
+        int8_scores(s, k_tile, s_tile, valid, lane);
+        this->softmax(s, lane, scratch);
+    }
+
+    // Scaled, masked log2-domain scores of the chunk from the int8 keys and their row scales.
+    __device__ __forceinline__ void int8_scores(float (&s)[4], uint32_t k_tile, uint32_t s_tile, int valid,
+                                                int lane) const {
         const int g = lane >> 2, t = lane & 3;
         const uint4 r0 = pkv::lds128(k_tile + swz8(g, 2 * t)), r1 = pkv::lds128(k_tile + swz8(g, 2 * t + 1));
         const uint4 r8 = pkv::lds128(k_tile + swz8(g + 8, 2 * t)), r9 = pkv::lds128(k_tile + swz8(g + 8, 2 * t + 1));
         const uint32_t wg[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         const uint32_t w8[8] = {r8.x, r8.y, r8.z, r8.w, r9.x, r9.y, r9.z, r9.w};
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        s[0] = s[1] = s[2] = s[3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             const uint32_t xg = wg[ks] ^ 0x80808080u, x8 = w8[ks] ^ 0x80808080u;
@@ -785,7 +816,55 @@ struct TcEngineQ : TcEngine<G> {
         s[1] = g < valid ? s[1] * fg : -INFINITY;
         s[2] = g + 8 < valid ? s[2] * f8 : -INFINITY;
         s[3] = g + 8 < valid ? s[3] * f8 : -INFINITY;
-        this->softmax(s, lane, scratch);
+    }
+};
+
+// ---------------------------------------------------------------- int8 keys and values
+// TcEngineQ's q.K, with the value rows int8 too.  Each value row's scale multiplies its token's
+// weight in P (l keeps the unscaled weights).  For O^T += V^T P^T the MMA's M dimension (dims)
+// may be permuted freely as long as the output is written back in order: row g of m-tile mt
+// stands for dim 16 g + 2 mt and row g + 8 for dim 16 g + 2 mt + 1, so a lane (g = lane / 4)
+// needs dims [16 g, 16 g + 16) of its four token rows (2t, 2t+1, 2t+8, 2t+9): four conflict-free
+// 16-byte loads per chunk from the swizzled int8 tile, paired across tokens with a byte
+// permute and converted to exact fp16 integers as for the keys.
+template <int G>
+struct TcEngineQV : TcEngineQ<G> {
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t s_tile, int valid, int lane, unsigned char *scratch,
+                                       int) {
+        float s[4];
+        this->int8_scores(s, k_tile, s_tile, valid, lane);
+        this->template softmax<false, true>(s, lane, scratch, s_tile + kChunk * 4);
+    }
+
+    __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *scratch) {
+        const __half *ph = reinterpret_cast<const __half *>(scratch);
+        const __half *pl = ph + 8 * kChunk;
+        const int g = lane >> 2, t = lane & 3, k0 = t * 2;
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0);
+        const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0 + 8);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0);
+        const uint32_t bl1 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0 + 8);
+        const uint4 r0 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t, g));
+        const uint4 r1 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 1, g));
+        const uint4 r8 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 8, g));
+        const uint4 r9 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 9, g));
+        const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+        const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w}, w9[4] = {r9.x, r9.y, r9.z, r9.w};
+#pragma unroll
+        for (int mt = 0; mt < kD / 16; ++mt) {
+            // bytes 2mt, 2mt+1 (dims 16g + 2mt, +1) of the two token rows, interleaved token-wise
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t xa = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel) ^ 0x80808080u;
+            const uint32_t xb = __byte_perm(w8[mt >> 1], w9[mt >> 1], sel) ^ 0x80808080u;
+            const uint32_t a[4] = {pkv::i8x2_to_h2(xa, 0x4140), pkv::i8x2_to_h2(xa, 0x4342),
+                                   pkv::i8x2_to_h2(xb, 0x4140), pkv::i8x2_to_h2(xb, 0x4342)};
+            pkv::mma16816(this->o[mt], a, bh0, bh1);
+            pkv::mma16816(this->o[mt], a, bl0, bl1);
+        }
+    }
+
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+        TcEngine<G>::template finish<true>(warp, lane, c_acc, c_m, c_l);
     }
 };
 
@@ -863,15 +942,18 @@ struct TcEngineM2 {
     }
 };
 
-template <int G, int LPT, bool TC, bool KQ, int MQ>
+template <int G, int LPT, bool TC, int KQ, int MQ>
 using EngineFor = typename std::conditional<
     MQ == 2, TcEngineM2<G>,
     typename std::conditional<MQ == 1, TcEngineM<G>,
     typename std::conditional<
-        KQ, TcEngineQ<G>, typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type>::type;
+        KQ == 2, TcEngineQV<G>,
+        typename std::conditional<
+            KQ == 1, TcEngineQ<G>,
+            typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type>::type>::type;
 
 // MQ: 0 one token per request; 1 or 2 several tokens per request, with that many 8-column tiles.
-template <int G, int LPT, bool TC, bool KQ, int MQ>
+template <int G, int LPT, bool TC, int KQ, int MQ>
 __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
                                                 ? 2
                                                 : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
@@ -967,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
     if (n_parts == 0) {  // shared-prefix pass: the whole context is the prefix, merge its chunks only
         if (part == 0 && P.counters != nullptr) {
             pkv::pdl_wait_primary();  // the prefix kernel's partials
-            merge_group<G>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset, smem);
+            merge_group<G, L::stage_bytes>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset, smem);
         }
         return;
     }
@@ -984,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
     const uint32_t bar0 = pkv::smem_addr(smem + L::bars) + warp * kStages * kBarsPerStage * 8;
     const uint32_t bar_v0 = bar0 + (kSplitKV ? 8 * kStages : 0);
     const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * L::stage;
-    const uint32_t scale0 = pkv::smem_addr(smem + L::scales) + warp * kStages * kChunk * 4;
+    const uint32_t scale0 = pkv::smem_addr(smem + L::scales) + warp * kStages * L::scale_stride;
 
     if (TC && (pkv::smem_addr(smem) & 1023) != 0) {  // the 128-byte swizzle needs 1 KB-aligned tiles
         if (threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
@@ -1008,6 +1090,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
     const void *tmap_k = &P.tmap_k;
     const void *tmap_v = &P.tmap_v;
     const float *ksc = P.k_scale;
+    const float *vsc = P.v_scale;
     const int hkv = P.num_kv_heads;
     // parts: 1 = K (with the int8 keys' scales), 2 = V, 3 = both.  Without split K/V both land on
     // one barrier with one expect_tx for their sum.
@@ -1025,7 +1108,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
         const uint32_t dst = stage0 + st * L::stage;
         // TC: whole 16-row boxes (a ragged tail's extra rows stay inside the block and are masked)
         const uint32_t k_bytes = KQ ? L::k_tile + kChunk * 4 : (TC ? 2 * kHalfTile : bytes);
-        const uint32_t v_bytes = TC ? 2 * kHalfTile : bytes;
+        const uint32_t v_bytes = KQ == 2 ? L::v_tile + kChunk * 4 : (TC ? 2 * kHalfTile : bytes);
         if (lane != 0) return;
         if (kSplitKV) {
             if (parts & 1) pkv::mbar_arrive_expect_tx(bar_k, k_bytes);
@@ -1037,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
         if (parts & 1) {
             if constexpr (KQ) {  // one 16-row box of int8 keys and the 16 key scales (64 B)
                 pkv::tma_load_2d(dst, tmap_k, 0, static_cast<int>(y), bar_k);
-                pkv::bulk_copy_g2s(scale0 + st * kChunk * 4, ksc + y, kChunk * 4, bar_k);
+                pkv::bulk_copy_g2s(scale0 + st * L::scale_stride, ksc + y, kChunk * 4, bar_k);
             } else if constexpr (TC) {
                 pkv::tma_load_2d(dst, tmap_k, 0, static_cast<int>(y), bar_k);
                 pkv::tma_load_2d(dst + kHalfTile, tmap_k, 64, static_cast<int>(y), bar_k);
@@ -1046,7 +1129,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
             }
         }
         if (parts & 2) {
-            if constexpr (TC) {
+            if constexpr (KQ == 2) {  // one 16-row box of int8 values and their 16 scales
+                pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, static_cast<int>(y), bar_v);
+                pkv::bulk_copy_g2s(scale0 + st * L::scale_stride + kChunk * 4, vsc + y, kChunk * 4, bar_v);
+            } else if constexpr (TC) {
                 pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, static_cast<int>(y), bar_v);
                 pkv::tma_load_2d(dst + L::k_tile + kHalfTile, tmap_v, 64, static_cast<int>(y), bar_v);
             } else {
@@ -1138,6 +1224,20 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
                         codes;
                     if (lane == 0) P.k_scale_w[grow] = sc;
                 }
+            } else if (KQ == 2) {  // lanes 16-31 quantise the V row the same way
+                const int l16 = lane & 15;
+                uint32_t c[2] = {0u, 0u};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    c[e >> 2] |= (static_cast<uint32_t>(pkv::quantize_int8(f[e], sc)) & 0xffu) << (8 * (e & 3));
+                const uint2 codes = make_uint2(c[0], c[1]);
+                *reinterpret_cast<uint2 *>(s_newrow + 2 * kD + l16 * 8) = codes;
+                if (l16 == 0) *reinterpret_cast<float *>(s_newrow + 3 * kD) = sc;
+                if (id_ok) {
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<unsigned char *>(P.v_cache_w) + grow * kD + l16 * 8) =
+                        codes;
+                    if (l16 == 0) P.v_scale_w[grow] = sc;
+                }
             } else {
                 *reinterpret_cast<uint4 *>(s_newrow + lane * 16) = new_row;
                 if (id_ok) *reinterpret_cast<uint4 *>(P.v_cache_w + grow * kD + (lane & 15) * 8) = new_row;
@@ -1175,13 +1275,15 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
         const int valid = min(kChunk, n_tok - cidx * kChunk);
         const uint32_t k_tile = stage0 + st * L::stage;
         const uint32_t v_tile = k_tile + L::k_tile;
-        const uint32_t s_tile = scale0 + st * kChunk * 4;
+        const uint32_t s_tile = scale0 + st * L::scale_stride;
         const bool own = cidx == own_chunk;
         const int nr_row = (new_pos - start) % kChunk;
         // the appended token's V row and a ragged tail's V rows, once V has landed
         auto fix_v = [&]() {
             bool touched = false;
-            if (TC && valid < kChunk) {
+            // (int8 values need no clearing: codes are finite and the scaled weights of the unused
+            // rows are forced to zero)
+            if (TC && KQ != 2 && valid < kChunk) {
                 for (int x = lane; x < (kChunk - valid) * 16; x += 32)
                     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + TcEngine<4>::swz(valid + x / 16, x % 16)),
                                  "r"(0)
@@ -1189,7 +1291,18 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
                 touched = true;
             }
             if (own) {
-                if (lane >= 16) {
+                if (KQ == 2 && lane >= 16) {  // int8 value row (8 bytes a lane) and its scale
+                    const int l16 = lane & 15;
+                    const uint2 nc = *reinterpret_cast<const uint2 *>(s_newrow + 2 * kD + l16 * 8);
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(v_tile + TcEngineQ<G>::swz8(nr_row, l16 >> 1) +
+                                                                     (l16 & 1) * 8),
+                                 "r"(nc.x), "r"(nc.y)
+                                 : "memory");
+                    if (l16 == 0)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_tile + kChunk * 4 + nr_row * 4),
+                                     "f"(*reinterpret_cast<const float *>(s_newrow + 3 * kD))
+                                     : "memory");
+                } else if (KQ != 2 && lane >= 16) {
                     const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
                     const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(v_tile + row), "r"(nr.x), "r"(nr.y),
@@ -1304,9 +1417,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
     if (!s_last) return;
     if (P.slot_offset > 0) pkv::pdl_wait_primary();  // shared-prefix pass: the prefix kernel's partials
     if constexpr (MQ)
-        merge_group<NC>(P, token_rows, P.slot_offset + n_parts, smem);
+        merge_group<NC, L::stage_bytes>(P, token_rows, P.slot_offset + n_parts, smem);
     else
-        merge_group<G>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset + n_parts, smem);
+        merge_group<G, L::stage_bytes>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset + n_parts,
+                                       smem);
     if (threadIdx.x == 0) *counter = 0;
 }
 
@@ -1432,7 +1546,7 @@ int encode_code_map(CUtensorMap *map, const void *base, int64_t rows) {
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int G, bool KQ, int MQ>
+template <int G, int KQ, int MQ>
 int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
     constexpr bool TC = KQ || MQ || (PKV_DECODE_TC && G >= PKV_DECODE_TC_MIN_GROUP);
@@ -1442,7 +1556,8 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
         const int64_t rows = p.num_blocks * p.num_kv_heads * p.block_size;
         if (rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // box row coordinates are signed 32-bit
         int st = KQ ? encode_code_map(&p.tmap_k, p.k_cache, rows) : encode_cache_map(&p.tmap_k, p.k_cache, rows);
-        if (st == PKV_OK) st = encode_cache_map(&p.tmap_v, p.v_cache, rows);
+        if (st == PKV_OK)
+            st = KQ == 2 ? encode_code_map(&p.tmap_v, p.v_cache, rows) : encode_cache_map(&p.tmap_v, p.v_cache, rows);
         if (st != PKV_OK) return st;
     }
     using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1>;
@@ -1482,10 +1597,11 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
 template <int G>
 int launch_mode(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
     if (p.query_start)
-        return p.mq_tiles == 2 ? launch_partition<G, false, 2>(p, num_seqs, stream, grid_parts)
-                               : launch_partition<G, false, 1>(p, num_seqs, stream, grid_parts);
-    if (p.k_scale) return launch_partition<G, true, 0>(p, num_seqs, stream, grid_parts);
-    return launch_partition<G, false, 0>(p, num_seqs, stream, grid_parts);
+        return p.mq_tiles == 2 ? launch_partition<G, 0, 2>(p, num_seqs, stream, grid_parts)
+                               : launch_partition<G, 0, 1>(p, num_seqs, stream, grid_parts);
+    if (p.k_scale && p.v_scale) return launch_partition<G, 2, 0>(p, num_seqs, stream, grid_parts);
+    if (p.k_scale) return launch_partition<G, 1, 0>(p, num_seqs, stream, grid_parts);
+    return launch_partition<G, 0, 0>(p, num_seqs, stream, grid_parts);
 }
 
 int dispatch_partition(const DecodeParams &p, int num_seqs, int group, cudaStream_t stream, int grid_parts = 0) {
@@ -1601,11 +1717,12 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
                           int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, const void *k_new, const void *v_new, void *workspace,
                           size_t workspace_bytes, pkv_stream_t stream, const float *k_scale = nullptr,
-                          int partition_size = PKV_DEFAULT_PARTITION) {
+                          int partition_size = PKV_DEFAULT_PARTITION, const float *v_scale = nullptr) {
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
     if (k_scale && !pkv_internal::aligned16(k_scale)) return PKV_ERR_INVALID_ARG;
+    if (v_scale && (!k_scale || !pkv_internal::aligned16(v_scale))) return PKV_ERR_INVALID_ARG;
     if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
     if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
@@ -1637,6 +1754,8 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     p.v_cache_w = static_cast<__half *>(const_cast<void *>(v_cache));
     p.k_scale = k_scale;
     p.k_scale_w = const_cast<float *>(k_scale);
+    p.v_scale = v_scale;
+    p.v_scale_w = const_cast<float *>(v_scale);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
 
@@ -1807,6 +1926,33 @@ extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, cons
         p.counters = reinterpret_cast<int *>(ws + counters_offset(rows));
     }
     return dispatch_partition(p, num_seqs, group, s);
+}
+
+// ------------------------------------------------------------------ int8 keys and values
+
+extern "C" PKV_API int pkv_decode_attention_int8kv(void *out, const void *q, const void *k_codes,
+                                                   const float *k_scale, const void *v_codes, const float *v_scale,
+                                                   const int32_t *block_tables, const int32_t *context_lens,
+                                                   int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                                                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                                   float scale, void *workspace, size_t workspace_bytes,
+                                                   pkv_stream_t stream) {
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_codes, v_codes, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, nullptr, nullptr,
+                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale);
+}
+
+extern "C" PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const void *k_new, const void *v_new,
+                                              void *k_codes, float *k_scale, void *v_codes, float *v_scale,
+                                              const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                              int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                                              int head_dim, int block_size, int64_t num_blocks, float scale,
+                                              void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    if (!k_new || !v_new || !k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_codes, v_codes, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
+                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

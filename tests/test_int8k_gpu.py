@@ -52,7 +52,7 @@ def test_append_int8k_bit_exact():
     kn = rng.standard_normal((t, hkv, d)).astype(np.float16)
     kn[0, 0] = 0                                                       # zero row: scale 0
     kn[1, 1] = np.tile(np.array([63.5, -63.5, 0.25, 0.75, -1.25, 10, 0.5, 1.5], np.float16), 16)  # ties
-    kn[2, 2] = (rng.standard_normal(d) * 3e4).astype(np.float16)       # large
+    kn[2, 2] = np.clip(rng.standard_normal(d) * 3e4, -65504, 65504).astype(np.float16)  # large
     kn[3, 3] = (rng.standard_normal(d) * 1e-6).astype(np.float16)      # fp16 subnormals
     kn[4, :] = (rng.standard_normal((hkv, d)) * 10.0 ** rng.uniform(-4, 4, (hkv, 1))).astype(np.float16)
     vn = rng.standard_normal((t, hkv, d)).astype(np.float16)

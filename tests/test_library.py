@@ -142,6 +142,18 @@ def test_int8k_multi_copy_invalid_arguments(lib):
                                           null) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_decode_step_int8k(p, p, null, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
                                      null) == _lib.PKV_ERR_INVALID_ARG
+    # int8 keys and values: null value scales, misaligned value scales, null value codes, head_dim 64
+    assert lib.pkv_append_int8kv(p, p, p, null, p, p, p, 1, 1, 128, 16, 4, null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_append_int8kv(p, p, p, p, p, p, p, 1, 1, 64, 16, 4, null) == _lib.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_decode_attention_int8kv(p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                           null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_attention_int8kv(p, p, p, p, p, bad, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                           null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_attention_int8kv(p, p, p, p, null, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                           null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_int8kv(p, p, p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                      null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_append_int8kv(p, p, p, p, null, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
     # several tokens per request: null query_start, query length beyond the limit, no workspace
     assert lib.pkv_decode_attention_multi(p, p, p, p, p, p, null, 1, 4, 4, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
                                           null) == _lib.PKV_ERR_INVALID_ARG
