@@ -1046,10 +1046,19 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
         }
         return;
     }
+    // Suffix pass whose merge is a separate launch: this CTA alone waits for the prefix kernel once
+    // its own work is done, so the pass cannot complete before the prefix kernel (evaluated where
+    // used, so nothing stays live through the main loop; the pass reads fp16 K/V, one token per request).
+    auto waits_for_prefix = [&P]() {
+        return KQ == 0 && MQ == 0 && P.slot_offset > 0 && P.counters == nullptr && blockIdx.x == 0 &&
+               blockIdx.y == 0 && blockIdx.z == 0;
+    };
     if (n_parts == 0) {  // shared-prefix pass: the whole context is the prefix, merge its chunks only
         if (part == 0 && P.counters != nullptr) {
             pkv::pdl_wait_primary();  // the prefix kernel's partials
             merge_group<G, L::stage_bytes>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset, smem);
+        } else if (waits_for_prefix()) {
+            pkv::pdl_wait_primary();
         }
         return;
     }
@@ -1403,7 +1412,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
             }
         }
     }
-    if (direct || P.counters == nullptr) return;
+    if (direct || P.counters == nullptr) {
+        if (waits_for_prefix()) pkv::pdl_wait_primary();
+        return;
+    }
 
     // ---- fused log-sum-exp merge: the last partition CTA of (b, kv head) to finish merges them all.
     // The CTA's partial writes are ordered before one acquire-release increment of the counter by
@@ -1422,6 +1434,24 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
         merge_group<G, L::stage_bytes>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset + n_parts,
                                        smem);
     if (threadIdx.x == 0) *counter = 0;
+}
+
+// The shared-prefix merge as its own launch: one CTA per (kv head, request) runs the fused merge
+// (same code, same result) over the prefix chunks and the suffix partitions, after waiting
+// (griddepcontrol.wait) for the suffix pass, which completes only after the prefix kernel.
+constexpr int kMergeStageBytes = 24 * 1024;
+template <int G>
+__global__ void __launch_bounds__(kThreads) merge_groups_kernel(const __grid_constant__ DecodeParams P) {
+    __shared__ __align__(16) unsigned char smem[kMergeStageBytes];
+    pkv::pdl_wait_primary();
+    const int kvh = blockIdx.x, b = blockIdx.y;
+    // the suffix pass's partition count for this request (same clamps)
+    const int cap = P.max_blocks_per_seq * P.block_size;
+    int ctx = __ldg(P.context_lens + b);
+    ctx = max(min(ctx, cap), P.token_offset);
+    const int n_parts = (ctx - P.token_offset + P.partition_size - 1) / P.partition_size;
+    merge_group<G, kMergeStageBytes>(P, HeadRows{static_cast<int64_t>(b) * P.num_q_heads + kvh * G},
+                                     P.slot_offset + n_parts, smem);
 }
 
 // One CTA per (q head, request); thread d owns output dim d.  Partitions are taken in tiles
@@ -2050,8 +2080,30 @@ int launch_split_pass(const SplitPass &a, void *stream) {
     p.v_new = static_cast<const __half *>(a.v_new);
     p.k_cache_w = static_cast<__half *>(const_cast<void *>(a.k_cache));
     p.v_cache_w = static_cast<__half *>(const_cast<void *>(a.v_cache));
-    return dispatch_partition(p, a.num_seqs, a.num_q_heads / a.num_kv_heads, reinterpret_cast<cudaStream_t>(stream),
-                              a.grid_partitions);
+    if (a.separate_merge) p.counters = nullptr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int group = a.num_q_heads / a.num_kv_heads;
+    const int st = dispatch_partition(p, a.num_seqs, group, s, a.grid_partitions);
+    if (st != PKV_OK || !a.separate_merge) return st;
+    // the merge as a programmatic dependent of the pass: launched as the pass's CTAs drain
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.num_kv_heads, a.num_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (group) {
+        case 1: e = cudaLaunchKernelEx(&cfg, merge_groups_kernel<1>, p); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, merge_groups_kernel<2>, p); break;
+        case 4: e = cudaLaunchKernelEx(&cfg, merge_groups_kernel<4>, p); break;
+        case 8: e = cudaLaunchKernelEx(&cfg, merge_groups_kernel<8>, p); break;
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int decode_take_error(int *code) {

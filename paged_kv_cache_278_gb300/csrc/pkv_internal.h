@@ -28,7 +28,8 @@ int check_decode_args(const void *q, const void *k_cache, const void *v_cache, c
 
 // One split pass of the decode kernel writing partial slots [slot_offset, slot_offset + parts)
 // for the tokens from token_offset on, with the log-sum-exp merge of slots
-// [0, slot_offset + parts) fused in (counters must be zero; they are left zero).
+// [0, slot_offset + parts) fused in (counters must be zero; they are left zero), or, with
+// separate_merge, done by a merge kernel launched after the pass (counters unused).
 struct SplitPass {
     void *out;
     const void *q, *k_cache, *v_cache;
@@ -40,6 +41,7 @@ struct SplitPass {
     float *o_part, *m_part, *l_part;
     int *counters;
     const void *k_new, *v_new;  // non-null: fused append of the new token (caches are written)
+    bool separate_merge;
 };
 int launch_split_pass(const SplitPass &a, void *stream);
 

@@ -45,6 +45,13 @@ constexpr int kD = PKV_HEAD_DIM;       // 128
 #ifndef PKV_PREFIX_MAXNREG
 #define PKV_PREFIX_MAXNREG 168
 #endif
+// 1: the suffix pass writes its partials and exits; a merge kernel launched after it (one CTA per
+// request and kv head) folds the prefix chunks and the suffix partitions.  0: the last suffix CTA
+// of each (request, kv head) merges, waiting for the prefix kernel first, which holds a CTA slot
+// while the prefix kernel runs (4 % slower on the shared-prefix step).
+#ifndef PKV_PREFIX_SEPARATE_MERGE
+#define PKV_PREFIX_SEPARATE_MERGE 1
+#endif
 constexpr int kChunkTok = PKV_PREFIX_CHUNK;  // prefix tokens per CTA (a multiple of 16)
 constexpr int kNT = kChunkTok / 8;           // 8-token MMA n-tiles of a chunk
 static_assert(kChunkTok % 16 == 0 && kChunkTok >= 16, "chunk of whole 16-token k-steps");
@@ -659,6 +666,7 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     a.counters = reinterpret_cast<int *>(ws + L.counter_off);
     a.k_new = k_new;
     a.v_new = v_new;
+    a.separate_merge = PKV_PREFIX_SEPARATE_MERGE != 0;
     return pkv_internal::launch_split_pass(a, stream);
 }
 

@@ -97,3 +97,41 @@ def test_prefix_mismatch_is_recorded():
     with pytest.raises(pkv.PkvError):   # prefix length not a multiple of the block size
         pkv.decode_attention_shared_prefix(out, case.q, case.k_cache, case.v_cache, case.block_tables,
                                            case.context_lens, case.scale, 40, ws)
+
+
+def run_no_append(case, prefix_len):
+    """decode_attention_shared_prefix over the cache as generated (no new token), twice."""
+    h = host_inputs(case)
+    ref = oracle.decode(h["q"], h["k_cache"], h["v_cache"], h["block_tables"], h["context_lens"], case.scale)
+    dev = case.to("cuda")
+    ws = pkv.make_shared_prefix_workspace(case.num_seqs, case.num_q_heads, case.max_blocks_per_seq * case.block_size,
+                                          prefix_len, "cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.empty_like(dev.q)
+        pkv.decode_attention_shared_prefix(out, dev.q, dev.k_cache, dev.v_cache, dev.block_tables, dev.context_lens,
+                                           case.scale, prefix_len, ws)
+        outs.append(out)
+    return max_err(outs[0], ref), outs
+
+
+@pytest.mark.parametrize("group,hkv", [(1, 4), (4, 2), (8, 1)])
+def test_prefix_only_requests_merged_by_the_prefix_kernel(group, hkv):
+    # every context is exactly the prefix: no suffix partition exists, so the prefix kernel's
+    # last chunk CTA completes every request's count and merges it
+    case = with_prefix(200 + group, 512, [0] * 6, group * hkv, hkv)
+    err, outs = run_no_append(case, 512)
+    assert err <= ATTN_TOL, err
+    assert torch.equal(outs[0], outs[1])
+    assert_no_device_error()
+
+
+def test_mixed_prefix_only_and_long_suffixes_two_row_tiles():
+    # 160 requests x 1 q head per kv head (two 128-row tiles); every other request has no suffix,
+    # the others up to 1000 tokens: merges fall to both kernels, results repeat bit for bit
+    suffixes = [0 if i % 2 == 0 else 100 + 37 * i % 900 for i in range(160)]
+    case = with_prefix(210, 256, suffixes, 4, 4)
+    err, outs = run_no_append(case, 256)
+    assert err <= ATTN_TOL, err
+    assert torch.equal(outs[0], outs[1])
+    assert_no_device_error()
