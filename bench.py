@@ -540,7 +540,8 @@ def run_ours(args):
             "num_kv_heads": Hkv,
             "head_dim": D,
             "block_size": bs,
-            "partition_size": part or pkv.PKV_DEFAULT_PARTITION,
+            "partition_size": ("prefix: 128-token chunks; suffix: picked per call (64-512 tokens)" if cascade
+                               else part or pkv.PKV_DEFAULT_PARTITION),
             "kv_cache": KV_TEXT[args.kv],
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
                   % (layer_cache_bytes / 1e6, bytes_job / 1e9),
