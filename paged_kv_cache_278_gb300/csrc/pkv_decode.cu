@@ -90,6 +90,13 @@ constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 #ifndef PKV_DECODE_TC_MIN_GROUP
 #define PKV_DECODE_TC_MIN_GROUP 1
 #endif
+// Independent accumulator chains of a chunk's q.K MMAs on the fp16 tensor-core engines (the
+// k-steps are dealt round-robin and the chains added at the end; 1 = one dependent chain of 8
+// MMAs).  2 measured 0.2-1 % faster on every fp16 workload (most on the 16-column multi-token
+// engine), 4 no better than 2.
+#ifndef PKV_QK_CHAINS
+#define PKV_QK_CHAINS 2
+#endif
 constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = PKV_DECODE_STAGES;
@@ -614,14 +621,21 @@ struct TcEngine {
         reset(P);
     }
 
-    // Raw q . K of the chunk's 16 tokens (rows g, g + 8) for the lane's columns h0, h0 + 1.
+    // Raw q . K of the chunk's 16 tokens (rows g, g + 8) for the lane's columns h0, h0 + 1
+    // (PKV_QK_CHAINS independent accumulator chains over the k-steps, added at the end).
     __device__ __forceinline__ void dots(float (&s)[4], uint32_t k_tile, int lane) const {
+        float chain[PKV_QK_CHAINS > 1 ? PKV_QK_CHAINS - 1 : 1][4] = {};
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t a[4];
             pkv::ldsm_x4(a, k_tile + swz(lane & 15, ks * 2 + (lane >> 4)));
-            pkv::mma16816(s, a, qb[ks][0], qb[ks][1]);
+            float(&acc)[4] = ks % PKV_QK_CHAINS == 0 ? s : chain[ks % PKV_QK_CHAINS - 1];
+            pkv::mma16816(acc, a, qb[ks][0], qb[ks][1]);
         }
+#pragma unroll
+        for (int c = 0; c < PKV_QK_CHAINS - 1; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[e] += chain[c][e];
     }
 
     __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t, int valid, int lane, unsigned char *scratch, int) {
@@ -803,6 +817,8 @@ struct TcEngineQ : TcEngine<G> {
         const uint32_t wg[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         const uint32_t w8[8] = {r8.x, r8.y, r8.z, r8.w, r9.x, r9.y, r9.z, r9.w};
         s[0] = s[1] = s[2] = s[3] = 0.f;
+        // one accumulator chain: two measured 0.2-0.9 % slower here (the conversions between the
+        // MMAs already hide their latency)
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             const uint32_t xg = wg[ks] ^ 0x80808080u, x8 = w8[ks] ^ 0x80808080u;
