@@ -361,9 +361,9 @@ def run_ours(args):
                       for c in ctx_steps]
     logical_bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, kv=args.kv, q_len=nq) for c in ctx_steps]
 
-    # per layer: the decode kernel (append and the split's merge fused in), plus the prefix kernel with the
-    # cascade, plus the append kernel on the two-call path
-    launches_per_step = n_layers * (1 + (1 if cascade else 0) + (1 if args.separate_append or nq > 1 else 0))
+    # per layer: the decode kernel (append and the split's merge fused in), plus the prefix kernel and the
+    # merge kernel with the cascade, plus the append kernel on the two-call path
+    launches_per_step = n_layers * (1 + (2 if cascade else 0) + (1 if args.separate_append or nq > 1 else 0))
 
     def step():
         for l, c in enumerate(cases):
@@ -437,7 +437,7 @@ def run_ours(args):
 
     # ---- timed region 2: the dominant kernel alone.  A pkv_decode_step call is exactly one launch of
     # the decode kernel (the append and the split's log-sum-exp merge run inside it; the cascade adds
-    # its small prefix kernel); a separate append launch is left out here.  Per step the layers'
+    # its prefix kernel and its merge kernel); a separate append launch is left out here.  Per step the layers'
     # launches are replayed back to back from a CUDA graph (no host launch gaps) between one pair of
     # CUDA events on the launching stream: average launch duration = event interval / launches.
     kt_steps = args.steps
@@ -559,7 +559,7 @@ def run_ours(args):
         "roofline": {
             "kernel": f"decode_partition_kernel (packed-GQA paged decode, {part or pkv.PKV_DEFAULT_PARTITION}-token "
                       "partitions, fused LSE merge)"
-                      + (" + prefix_kernel (timed together)" if cascade else ""),
+                      + (" + prefix_kernel + merge_groups_kernel (timed together)" if cascade else ""),
             "timing": "CUDA events around graph replays of the layers' attention launches"
                       if kernel_graph is not None else "CUDA events around eager attention launches",
             "bound": "hbm",

@@ -267,7 +267,7 @@ PKV_API int pkv_decode_attention(void *out, const void *q, const void *k_cache,
                                  void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* Bytes of workspace pkv_decode_attention_shared_prefix needs: fp32 partials for
- * ceil(prefix_len / 64) prefix chunks plus up to ceil((max_context - prefix_len) / 64)
+ * ceil(prefix_len / 128) prefix chunks plus up to ceil((max_context - prefix_len) / 64)
  * suffix partitions per (request, q head) (the call picks the suffix partition,
  * 64..512 tokens, from the grid it gives), then one int counter per
  * (request, q head).  0 for invalid arguments. */
@@ -282,8 +282,9 @@ PKV_API size_t pkv_shared_prefix_workspace_size(int num_seqs, int num_q_heads, i
  * request: a first kernel scores every request's query rows against the
  * prefix in 128-token chunks (tensor-core MMA over the B x G rows of each kv
  * head), a second runs the split decode over each request's suffix (tokens
- * from prefix_len on) and merges prefix chunks and suffix partitions by
- * log-sum-exp.
+ * from prefix_len on) and a third merges each request's prefix chunks and
+ * suffix partitions by log-sum-exp (the three launched back to back on
+ * `stream`, the later two as programmatic dependents).
  * Requirements (besides those of pkv_decode_attention): prefix_len > 0 and a
  * multiple of block_size; context_lens[b] >= prefix_len; row b of
  * block_tables starts with the same prefix_len / block_size ids as row 0
@@ -323,7 +324,7 @@ PKV_API size_t pkv_decode_step_workspace_size(int num_seqs, int num_q_heads, int
  * pkv_decode_attention_shared_prefix (the new token must lie past the prefix).
  * The append is fused into the decode kernel: the CTA that owns a request's
  * last position writes the row to the cache and uses it directly, so a step
- * is one kernel launch (two with a shared prefix).  Workspace rules as for the
+ * is one kernel launch (three with a shared prefix).  Workspace rules as for the
  * matching attention call.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 PKV_API int pkv_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
                             void *k_cache, void *v_cache, const int32_t *block_tables,
