@@ -85,9 +85,12 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(workload: str = "") -> str:
+    """Hash of the kernel sources a workload's timed launches come from (the shared-prefix step
+    also runs the prefix kernel)."""
     h = hashlib.sha256()
-    for name in ("pkv_decode.cu", "pkv_device.cuh"):
+    names = ["pkv_decode.cu", "pkv_device.cuh"] + (["pkv_prefix.cu"] if workload.startswith("shared_prefix") else [])
+    for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_278_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -99,7 +102,7 @@ def read_traffic(workload: str, bs: int):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(workload)
     with open(path, encoding="utf-8") as f:
         for line in f:
             if line.startswith("#") or not line.strip():
@@ -585,7 +588,7 @@ def run_ours(args):
         },
         "gpu_launches": launches_per_step * args.steps + (2 * args.steps if steps_cycle > 1 else 0),
         "clocks": clocks.summary(windows),
-        "kernel_source": kernel_source_hash(),
+        "kernel_source": kernel_source_hash(args.workload if cascade else ""),
         "gpu": torch.cuda.get_device_name(dev),
     }
     if cpu_sample is not None:

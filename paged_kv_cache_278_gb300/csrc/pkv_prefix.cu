@@ -55,7 +55,11 @@ constexpr int kD = PKV_HEAD_DIM;       // 128
 constexpr int kChunkTok = PKV_PREFIX_CHUNK;  // prefix tokens per CTA (a multiple of 16)
 constexpr int kNT = kChunkTok / 8;           // 8-token MMA n-tiles of a chunk
 static_assert(kChunkTok % 16 == 0 && kChunkTok >= 16, "chunk of whole 16-token k-steps");
-constexpr int kWarps = 8;              // 16 query rows per warp
+// Warps per prefix CTA (16 query rows each, so 16 x warps rows per row tile).
+#ifndef PKV_PREFIX_WARPS
+#define PKV_PREFIX_WARPS 8
+#endif
+constexpr int kWarps = PKV_PREFIX_WARPS;  // 16 query rows per warp
 constexpr int kRows = kWarps * 16;     // query rows per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kPad = kD + 8;           // halves per shared-memory row: 272 B keeps ldmatrix conflict-free
@@ -95,7 +99,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Grid (prefix chunks, kv heads, ceil(B*G / 128)); 8 warps, each owning 16 query rows.
+__device__ __forceinline__ void cp_async16(const void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(pkv::smem_addr(smem_dst)), "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Grid (prefix chunks, kv heads, ceil(B*G / kRows)); kWarps warps, each owning 16 query rows.
 __global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams P) {  // launched with kThreads threads
     extern __shared__ __align__(128) unsigned char smem[];
     __half *sK = reinterpret_cast<__half *>(smem);      // [kChunkTok][kPad]
@@ -110,60 +120,47 @@ __global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams
     const int tok0 = chunk * kChunkTok;
     const int ntok = min(kChunkTok, P.prefix_len - tok0);
 
-    // K/V chunk (zero rows past the prefix) and the CTA's query rows, 16 bytes per access.  All
-    // loads of a thread are issued before any store so they overlap (about two L2/HBM round
-    // trips in all: block ids, then rows).
-    constexpr int KV_PER_THREAD = kChunkTok * (kD / 8) / kThreads;
-    constexpr int Q_PER_THREAD = kRows * (kD / 8) / kThreads;        // 8
-    static_assert(KV_PER_THREAD * kThreads == kChunkTok * (kD / 8) && Q_PER_THREAD * kThreads == kRows * (kD / 8),
-                  "load split");
-    uint4 qv[Q_PER_THREAD];
-#pragma unroll
-    for (int k = 0; k < Q_PER_THREAD; ++k) {
-        const int i = threadIdx.x + k * kThreads;
+    // K/V chunk (zero rows past the prefix) and the CTA's query rows (zero rows past the last),
+    // 16-byte asynchronous copies straight into shared memory: the block ids of the chunk first
+    // (one round trip), then every row piece (a second).
+    __shared__ int32_t s_ids[kChunkTok / 16];
+    const int blk0 = tok0 / bs, nblk = (tok0 + ntok - 1) / bs - blk0 + 1;  // at most kChunkTok / 16
+    if (static_cast<int>(threadIdx.x) < nblk) {
+        int32_t id = __ldg(P.block_tables + blk0 + threadIdx.x);
+        if (id < 0 || id >= P.num_blocks) {
+            pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
+            id = 0;
+        }
+        s_ids[threadIdx.x] = id;
+    }
+    for (int i = threadIdx.x; i < kRows * (kD / 8); i += kThreads) {
         const int r = i / (kD / 8), piece = i % (kD / 8);
         const int gr = row0 + r;
-        qv[k] = make_uint4(0, 0, 0, 0);
+        __half *dst = sQ + r * kPad + piece * 8;
         if (gr < rows) {
             const int b = gr / G, hh = gr % G;
-            qv[k] = __ldg(reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD) +
-                          piece);
+            cp_async16(dst, P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD + piece * 8);
+        } else {
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
         }
     }
-    int64_t src[KV_PER_THREAD];
-#pragma unroll
-    for (int k = 0; k < KV_PER_THREAD; ++k) {
-        const int i = threadIdx.x + k * kThreads;
+    __syncthreads();  // s_ids
+    for (int i = threadIdx.x; i < kChunkTok * (kD / 8); i += kThreads) {
         const int t = i / (kD / 8), piece = i % (kD / 8);
-        src[k] = -1;
+        __half *dk = sK + t * kPad + piece * 8;
+        __half *dv = sV + t * kPad + piece * 8;
         if (t < ntok) {
             const int tok = tok0 + t;
-            int32_t id = __ldg(P.block_tables + tok / bs);
-            if (id < 0 || id >= P.num_blocks) {
-                pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
-                id = 0;
-            }
-            src[k] = ((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs) * kD + piece * 8;
+            const int64_t src = ((static_cast<int64_t>(s_ids[tok / bs - blk0]) * Hkv + kvh) * bs + tok % bs) * kD +
+                                piece * 8;
+            cp_async16(dk, P.k_cache + src);
+            cp_async16(dv, P.v_cache + src);
+        } else {
+            *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
         }
     }
-    uint4 kv[KV_PER_THREAD], vv[KV_PER_THREAD];
-#pragma unroll
-    for (int k = 0; k < KV_PER_THREAD; ++k) {
-        kv[k] = src[k] >= 0 ? __ldg(reinterpret_cast<const uint4 *>(P.k_cache + src[k])) : make_uint4(0, 0, 0, 0);
-        vv[k] = src[k] >= 0 ? __ldg(reinterpret_cast<const uint4 *>(P.v_cache + src[k])) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int k = 0; k < Q_PER_THREAD; ++k) {
-        const int i = threadIdx.x + k * kThreads;
-        *reinterpret_cast<uint4 *>(sQ + (i / (kD / 8)) * kPad + (i % (kD / 8)) * 8) = qv[k];
-    }
-#pragma unroll
-    for (int k = 0; k < KV_PER_THREAD; ++k) {
-        const int i = threadIdx.x + k * kThreads;
-        const int t = i / (kD / 8), piece = i % (kD / 8);
-        *reinterpret_cast<uint4 *>(sK + t * kPad + piece * 8) = kv[k];
-        *reinterpret_cast<uint4 *>(sV + t * kPad + piece * 8) = vv[k];
-    }
+    cp_async_wait_all();
     __syncthreads();
     if (row0 + warp * 16 >= rows) return;  // no barrier follows
 
