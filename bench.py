@@ -85,14 +85,23 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed (string literals of the kernel
+    sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(workload: str = "") -> str:
-    """Hash of the kernel sources a workload's timed launches come from (the shared-prefix step
-    also runs the prefix kernel)."""
+    """Hash of the code (comments and layout ignored) of the kernel sources a workload's timed
+    launches come from (the shared-prefix step also runs the prefix kernel)."""
     h = hashlib.sha256()
     names = ["pkv_decode.cu", "pkv_device.cuh"] + (["pkv_prefix.cu"] if workload.startswith("shared_prefix") else [])
     for name in names:
-        with open(os.path.join(ROOT, "paged_kv_cache_278_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_278_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -20,9 +20,10 @@
 //   * q . K and P . V run on the tensor cores (mma.m16n8k16, fp32 accumulation): the packed
 //     heads are the 8 MMA columns, K comes from the swizzled tile by ldmatrix, P is split into
 //     fp16 hi + lo parts.  Variants of the same engine serve int8 keys (codes converted to exact
-//     fp16 integers in registers, row scales applied to the finished dot products) and several
-//     new tokens per request ((token, head) rows as the columns, causal masks per column).  A
-//     CUDA-core engine (packed fp32x2 FMAs) remains behind PKV_DECODE_TC_MIN_GROUP.
+//     fp16 integers in registers, row scales applied to the finished dot products), int8 keys
+//     and values (value scales folded into the weights) and several new tokens per request
+//     ((token, head) rows as the columns, causal masks per column).  A CUDA-core engine (packed
+//     fp32x2 FMAs) remains behind PKV_DECODE_TC_MIN_GROUP.
 //   * Online softmax in fp32 with lazy rescaling: the reference max is only raised (and the
 //     accumulators rescaled) when a score exceeds it by more than 2^8; the true max is tracked
 //     on the side and everything is re-referenced to it once at the end.
@@ -30,7 +31,7 @@
 //     patched into the staged tile.  At the end the 4 warps' (m, l, acc) are merged in shared
 //     memory; the CTA writes the fp16 output when the request fits one partition, else fp32
 //     partials, and the last partition CTA of a (request, kv head) to finish merges them by
-//     log-sum-exp in the same launch.
+//     log-sum-exp in the same launch (after a shared prefix, by default a separate merge launch).
 //   * Indices read from memory are checked (block ids, context length) and clamped; problems
 //     are recorded in the device error word.
 #include <cuda.h>

@@ -4,7 +4,7 @@
 // ("推理优化这件事，为什么值得反复复盘", sec. 4.2: a shared-prefix cache lets many requests use
 // one copy of the prompt's KV; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2: pages
 // shared across requests with the same prompt).  Attention over such a batch is computed in
-// two passes that together equal softmax(scale q K^T) V over each full context:
+// two passes and a merge that together equal softmax(scale q K^T) V over each full context:
 //
 //   1. prefix_kernel: for every kv head and every 128-token chunk of the shared prefix, the
 //      scores of ALL requests' query rows that read this kv head (B x G rows) against the
@@ -15,8 +15,11 @@
 //      m16n8k16 MMAs, fp16 operands with fp32 accumulation; P is split into fp16 hi + lo
 //      parts for the P.V product so the weights keep ~22 bits.
 //   2. The ordinary split decode kernel over each request's private suffix (tokens from
-//      prefix_len on), writing slots n_chunks.. and merging all slots by log-sum-exp in the
-//      same kernel (last partition of each request to finish).
+//      prefix_len on), writing slots n_chunks.., launched as a programmatic dependent so it
+//      streams while the prefix kernel runs.
+//   3. A merge launch (one CTA per request and kv head) folding all slots by log-sum-exp
+//      (PKV_PREFIX_SEPARATE_MERGE; else the suffix pass's last partition merges after waiting
+//      for the prefix kernel).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
