@@ -57,3 +57,12 @@ def test_decode_bytes_model():
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_kernel_hash_ignores_comments_not_code():
+    src = """// header\n__global__ void k(int *p) { /* note */ p[0] = 1; }  // trailing\n"""
+    same = """// another header\n__global__ void k(int *p) {\n    p[0] = 1;\n}\n"""
+    changed = """__global__ void k(int *p) { p[0] = 2; }\n"""
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(changed)
+
