@@ -66,3 +66,28 @@ def test_kernel_hash_ignores_comments_not_code():
     assert bench._code_only(src) == bench._code_only(same)
     assert bench._code_only(src) != bench._code_only(changed)
 
+
+
+def test_decode_bytes_model_by_hand():
+    # two requests (ctx 20 and 33), Hkv 2, Hq 4, D 128, bs 16
+    ctx, hkv, hq, d, bs = [20, 33], 2, 4, 128, 16
+    kv_row = d * 2                                   # one fp16 K or V row
+    tables = (2 + 3) * 4 + 4 * 2                     # ceil(20/16) + ceil(33/16) ids, context lengths
+    qo = 2 * 2 * hq * d * 2                          # q in, out back
+    fp16 = 53 * hkv * 2 * kv_row + qo + tables
+    assert bench.decode_bytes(ctx, hkv, hq, d, bs) == fp16
+    # int8 keys: a key row is 128 codes + a float32 scale; values stay fp16
+    assert bench.decode_bytes(ctx, hkv, hq, d, bs, kv="int8k") == 53 * hkv * ((d + 4) + kv_row) + qo + tables
+    # int8 keys and values
+    assert bench.decode_bytes(ctx, hkv, hq, d, bs, kv="int8kv") == 53 * hkv * 2 * (d + 4) + qo + tables
+    # several new tokens per request: q and out counted per token
+    assert bench.decode_bytes(ctx, hkv, hq, d, bs, q_len=3) == fp16 + 2 * qo
+    # a shared 16-token prefix counted once: unique tokens = 20 + 33 - 16
+    assert bench.decode_bytes(ctx, hkv, hq, d, bs, unique_prefix_tokens=16) == fp16 - 16 * hkv * 2 * kv_row
+
+
+def test_decode_bytes_of_the_mha7b_workload():
+    # the 7B-shaped workload's algorithmic bytes per layer, as the results quote them (480.89 MB)
+    import workloads
+    ctx, nb, bt = workloads.mha7b_structure()
+    assert abs(bench.decode_bytes(ctx, 32, 32, 128, 16) / 1e6 - 480.89) < 0.01
