@@ -91,3 +91,18 @@ def test_decode_bytes_of_the_mha7b_workload():
     import workloads
     ctx, nb, bt = workloads.mha7b_structure()
     assert abs(bench.decode_bytes(ctx, 32, 32, 128, 16) / 1e6 - 480.89) < 0.01
+
+
+@pytest.mark.parametrize("argv", [
+    ["--warmup", "2"],                                                   # fewer than 3 warm-up steps
+    ["--workload", "shared_prefix", "--kv", "int8k"],                    # the cascade reads fp16 K/V
+    ["--workload", "shared_prefix", "--kv", "int8kv"],
+    ["--query-len", "4", "--kv", "int8k"],                               # several tokens: fp16 path only
+    ["--query-len", "4", "--workload", "shared_prefix"],
+    ["--query-len", "2", "--impl", "reference"],                         # the reference arm times single tokens
+    ["--kv", "fp8"],                                                     # not a cache format
+])
+def test_bench_refuses_unsupported_combinations(argv):
+    with pytest.raises(SystemExit) as e:
+        bench.main(argv)
+    assert e.value.code == 2
