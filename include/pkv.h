@@ -36,7 +36,9 @@
  *   * Pointers named *_cache, q, out, k_new, v_new, o_part, m_part, l_part,
  *     block_tables, context_lens, slot_mapping and workspace are DEVICE
  *     pointers owned by the caller.  The library never allocates, frees or
- *     retains device memory and keeps no pointer after a call returns.
+ *     retains device memory (its only device memory is the static scratch
+ *     array of pkv_decode_attention_noalloc, part of the loaded module) and
+ *     keeps no pointer after a call returns.
  *   * Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream): they validate arguments on the host, enqueue
  *     kernels and return without synchronising.  A call that returns an
@@ -498,8 +500,8 @@ PKV_API int pkv_merge(void *out, const float *o_part, const float *m_part, const
 /* Size of the library's built-in scratch array used by pkv_decode_attention_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
 
-/* Allocation-free form of pkv_decode_attention.  The paper has no counterpart:
- * this call exists for callers that cannot allocate device memory.
+/* Allocation-free form of pkv_decode_attention.  The pages describe no
+ * counterpart: this call exists for callers that cannot allocate device memory.
  *
  * Who needs it: code running while a stream is captured into a CUDA graph in
  * global capture mode (cudaMalloc synchronises the device, which that mode
