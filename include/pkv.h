@@ -440,10 +440,11 @@ PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int total_q, int ma
  *                 (<= PKV_MAX_QUERY_LEN) and n_b <= ctx_b.  A request with n_b = 0
  *                 is skipped; inconsistent rows are skipped and recorded as
  *                 PKV_DEV_BAD_CONTEXT.
- * Other arguments as pkv_decode_attention.  One CTA serves 8 (token, head) rows
- * of one kv head and one PKV_DEFAULT_PARTITION-token partition, so K/V is read by
- * ceil(n_b * G / 8) CTAs that run back to back (L2 serves the repeats); the
- * split's merge is fused as in pkv_decode_attention.  Workspace: zero-filled
+ * Other arguments as pkv_decode_attention.  One CTA serves C (token, head) rows
+ * of one kv head and one PKV_DEFAULT_PARTITION-token partition, C = 8 when
+ * max_query_len * G <= 8 and 16 otherwise, so K/V is read by ceil(n_b * G / C)
+ * CTAs that run back to back (L2 serves the repeats); the split's merge is
+ * fused as in pkv_decode_attention.  Workspace: zero-filled
  * before first use, left zeroed, at least pkv_decode_multi_workspace_size bytes,
  * 256-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_cache, const void *v_cache,
