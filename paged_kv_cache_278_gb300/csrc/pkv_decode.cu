@@ -1094,16 +1094,17 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
     const uint32_t stage0 = pkv::smem_addr(smem + L::stages) + warp * kStages * L::stage;
     const uint32_t scale0 = pkv::smem_addr(smem + L::scales) + warp * kStages * L::scale_stride;
 
-    if (TC && (pkv::smem_addr(smem) & 1023) != 0) {  // the 128-byte swizzle needs 1 KB-aligned tiles
-        if (threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
-        return;
-    }
+    // The 128-byte swizzle needs 1 KB-aligned tiles.  A CTA whose shared memory is not so aligned
+    // stages none of its tokens (the error is recorded) but still writes its result and takes part
+    // in the split's completion counter, so the merge runs and the counter returns to zero.
+    const bool smem_ok = !TC || (pkv::smem_addr(smem) & 1023) == 0;
+    if (!smem_ok && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_SMEM_MISALIGNED);
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages * kBarsPerStage; ++s) pkv::mbar_init(bar0 + 8 * s, 1);
         pkv::fence_mbar_init();
     }
-    const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
+    const int my_chunks = smem_ok && n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
     const int64_t head_stride = static_cast<int64_t>(bs) * kRowBytes;
     const int64_t block_stride = head_stride * P.num_kv_heads;
 
@@ -1142,6 +1143,11 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
         } else {
             pkv::mbar_arrive_expect_tx(bar_k, k_bytes + v_bytes);
         }
+#if PKV_WAIT_TEST
+        // Test build only: the grid's first CTA arms warp 0's first stage for its bytes but issues
+        // no copy, so that wait can only run out (nothing is in flight for the stage).
+        if (i == 0 && warp == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) return;
+#endif
         const int64_t y = (phys * hkv + kvh) * bs + off;
         if (parts & 1) {
             if constexpr (KQ) {  // one 16-row box of int8 keys and the 16 key scales (64 B)
@@ -2004,11 +2010,13 @@ extern "C" PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const vo
 
 // ------------------------------------------------------------------ allocation-free variant
 //
-// For callers that cannot allocate device memory (global-mode stream capture, hosted plugins
-// that only receive input/output pointers, allocator-free serving loops): the split partials
-// go to this file-scope array instead of a caller workspace.  On the host the symbol names a
-// stand-in, not device memory, so it is never passed to a kernel directly; its device address
-// is looked up once per device with cudaGetSymbolAddress while that device is current.
+// For callers that cannot allocate device memory (plugins hosted by a runtime that owns all
+// device memory and hands them only input/output pointers; serving loops that forbid allocator
+// calls, and the device synchronisation cudaMalloc implies, once they are running): the split
+// partials go to this file-scope array instead of a caller workspace.  On the host the symbol
+// names a stand-in, not device memory, so it is never passed to a kernel directly; its device
+// address is looked up once per device with cudaGetSymbolAddress while that device is current
+// and kept for the life of the process (a cudaDeviceReset of that device invalidates it).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -2023,12 +2031,17 @@ extern "C" PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, co
                                                     int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
                                                     int head_dim, int block_size, int64_t num_blocks, float scale,
                                                     pkv_stream_t stream) {
-    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
-    if (cap > 0 && cap <= 0x7fffffffLL) {
-        const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, static_cast<int>(cap),
-                                                      PKV_DEFAULT_PARTITION);
-        if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
-    }
+    // Every argument is checked before any CUDA call, so a refused call enqueues nothing (in
+    // particular no clear of the counters at an offset computed from bad sizes).
+    int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
+    if (st != PKV_OK) return st;
+    if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;  // <= 2^31 - 1 (checked)
+    const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, static_cast<int>(cap),
+                                                  PKV_DEFAULT_PARTITION);
+    if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
@@ -2044,8 +2057,8 @@ extern "C" PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, co
     }
     // The split's completion counters must start at zero; every call leaves them zero, but the
     // array is shared by all calls, so clear them here rather than trust an earlier call.
-    const int max_parts = cap > 0 ? static_cast<int>((cap + PKV_DEFAULT_PARTITION - 1) / PKV_DEFAULT_PARTITION) : 0;
-    if (max_parts > 1 && num_seqs > 0 && num_q_heads > 0 && head_dim == kD) {
+    const int max_parts = static_cast<int>((cap + PKV_DEFAULT_PARTITION - 1) / PKV_DEFAULT_PARTITION);
+    if (max_parts > 1) {  // need (checked above) covers this counter region
         const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
         if (cudaMemsetAsync(static_cast<unsigned char *>(scratch) + counters_offset(rows), 0,
                             static_cast<size_t>(num_seqs) * num_q_heads * sizeof(int),

@@ -167,6 +167,28 @@ def test_int8k_multi_copy_invalid_arguments(lib):
     assert lib.pkv_copy_blocks(p, p, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
 
 
+def test_noalloc_validates_before_any_cuda_call(lib):
+    """The allocation-free entry refuses bad or oversize requests before its first CUDA call (on
+    this GPU-less machine any CUDA call would fail with CUDA, so each status below also shows
+    that none was made)."""
+    null = None
+    p = ctypes.c_void_p(16)
+    call = lambda maxb, bs, hq=1, hkv=1, b=1, hd=128, out=p: lib.pkv_decode_attention_noalloc(
+        out, p, p, p, p, p, b, maxb, hq, hkv, hd, bs, 4, 1.0, null)
+    # table capacity max_blocks_per_seq * block_size beyond 2^31 - 1 tokens
+    assert call(2 ** 31 // 16, 16) == _lib.PKV_ERR_INVALID_ARG
+    assert call(2 ** 30, 256) == _lib.PKV_ERR_INVALID_ARG
+    # valid shape whose split needs more than the static scratch: 16 x 32 heads x 64 partitions
+    assert lib.pkv_decode_workspace_size(16, 32, 128, 64 * 1024, 1024) > _lib.PKV_NOALLOC_SCRATCH_BYTES
+    assert call(64 * 1024 // 16, 16, hq=32, hkv=32, b=16) == _lib.PKV_ERR_WORKSPACE
+    # the other argument rules of pkv_decode_attention
+    assert call(4, 16, out=null) == _lib.PKV_ERR_INVALID_ARG
+    assert call(4, 16, out=ctypes.c_void_p(20)) == _lib.PKV_ERR_INVALID_ARG
+    assert call(4, 16, hd=64) == _lib.PKV_ERR_UNSUPPORTED
+    assert call(4, 16, hq=6, hkv=4) == _lib.PKV_ERR_INVALID_ARG
+    assert call(4, 16, b=0) == _lib.PKV_OK
+
+
 def test_step_partition_arguments(lib):
     null = None
     p = ctypes.c_void_p(16)

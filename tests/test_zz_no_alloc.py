@@ -1,23 +1,26 @@
 """The allocation-free decode entry point, called through the C ABI.
 
-pkv_decode_attention_noalloc serves callers that cannot allocate device memory: code running
-under a global-mode stream capture (cudaMalloc synchronises the device, which that mode
-forbids), plugins whose host runtime owns all device memory and passes them only input and
-output pointers, and serving loops that ban allocator calls after start-up.  It keeps the split
-partials in the library's own static device array instead of a caller workspace.
+pkv_decode_attention_noalloc serves callers that cannot allocate device memory: plugins whose
+host runtime owns all device memory and passes them only input and output pointers, and serving
+loops that ban allocator calls (and the device synchronisation cudaMalloc implies) once they are
+running.  It keeps the split partials in the library's own static device array instead of a
+caller workspace.
 
-Its output must match the workspace entry point's (pkv_decode_attention) within the attention
-tolerance every other GPU test uses, on two calls in a row with different inputs (the array
-keeps the previous call's contents), and an oversize request must be refused before launch.
-This file is collected last, so a stop-at-first-failure run has already run every other test.
+Its output must match the float64 oracle and the workspace entry point's (pkv_decode_attention)
+within the attention tolerance every other GPU test uses, on two calls in a row with different
+inputs and shapes (the array keeps the previous call's contents; the first call's split fills
+most of the array), and an oversize request must be refused before launch.  This file is
+collected last, so a stop-at-first-failure run has already run every other test.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_278_gb300 as pkv
 import workloads
+from gpu_util import host_inputs, max_err
 from paged_kv_cache_278_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
@@ -41,20 +44,26 @@ def _with_workspace(c):
     return out
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls():
     lib = _lib.load()
     cases = [
-        # ragged batch that needs the split (contexts up to 5000 tokens), GQA-4
-        workloads.random_case(901, [5000, 1, 0, 700, 2049, 513], 32, 8, block_size=16).to("cuda"),
+        # ragged GQA-4 batch whose split needs 8 x 32 x 118 partial rows: 15.7 MB of the 16 MiB array
+        workloads.random_case(901, [120000, 1, 0, 700, 2049, 513, 3000, 40], 32, 8, block_size=16),
         # a different shape on the second call: MHA, block 64, long contexts
-        workloads.random_case(902, [3000, 6100, 40], 16, 16, block_size=64).to("cuda"),
+        workloads.random_case(902, [3000, 6100, 40], 16, 16, block_size=64),
     ]
-    for c in cases:
+    need = pkv.decode_workspace_size(8, 32, cases[0].max_blocks_per_seq * 16)
+    assert 0.9 * _lib.PKV_NOALLOC_SCRATCH_BYTES < need <= _lib.PKV_NOALLOC_SCRATCH_BYTES
+    for host_case in cases:
+        h = host_inputs(host_case)
+        expect = oracle.decode(h["q"], h["k_cache"], h["v_cache"], h["block_tables"], h["context_lens"],
+                               host_case.scale)
+        c = host_case.to("cuda")
         ref = _with_workspace(c)
         out = torch.full_like(c.q, float("nan"))
         assert _noalloc(lib, out, c) == _lib.PKV_OK
         torch.cuda.synchronize()
-        assert torch.isfinite(out.float()).all()
+        assert max_err(out, expect) <= ATTN_TOL
         err = (out.float() - ref.float()).abs().max().item()
         assert err <= ATTN_TOL, err
     assert pkv.device_error() == pkv.PKV_DEV_OK
