@@ -83,6 +83,7 @@ extern "C" {
 #define PKV_DEV_BAD_SLOT 3       /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEV_WAIT_TIMEOUT 4   /* an asynchronous copy did not complete in time */
 #define PKV_DEV_PREFIX_MISMATCH 5 /* a block table does not start with the shared prefix's blocks */
+#define PKV_DEV_SMEM_MISALIGNED 6 /* dynamic shared memory not 1024-byte aligned (the CTA skipped its tokens) */
 
 /* Defaults and limits of the decode kernels. */
 #define PKV_HEAD_DIM 128             /* the only head_dim the decode kernels take */
@@ -94,10 +95,12 @@ extern "C" {
 typedef struct CUstream_st *pkv_stream_t; /* == cudaStream_t */
 typedef struct pkv_pool pkv_pool;         /* opaque host object */
 
-/* Human-readable name of a PKV_* status code (static storage, never NULL). */
+/* Human-readable name of a PKV_* status code (static storage, never NULL).
+ * Library plumbing; the pages describe no counterpart. */
 PKV_API const char *pkv_status_string(int status);
 
-/* Library version as 10000*major + 100*minor + patch. */
+/* Library version as 10000*major + 100*minor + patch.  Library plumbing; the
+ * pages describe no counterpart. */
 PKV_API int pkv_version(void);
 
 /* ================================================================ host pool
@@ -108,9 +111,12 @@ PKV_API int pkv_version(void);
  * All pool calls are host-only and synchronous.
  */
 
-/* Create a pool of num_blocks (1 .. 2^31-1) free blocks.  The free list is a
- * permutation of 0..num_blocks-1 drawn from `seed` (splitmix64 + Fisher-Yates),
- * so consecutive allocations scatter over the pool.  *out receives the pool;
+/* Create a pool of num_blocks (1 .. 2^31-1) free blocks (the preallocated
+ * block pool of the pages' paged cache, sec. 4.2 of the page above).  The free
+ * list is a permutation of 0..num_blocks-1 drawn from `seed` (splitmix64 +
+ * Fisher-Yates), so consecutive allocations scatter over the pool, as the pages
+ * say history K/V ends up ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2:
+ * random addresses).  *out receives the pool;
  * release it with pkv_pool_destroy.  Errors: INVALID_ARG. */
 PKV_API int pkv_pool_create(int64_t num_blocks, uint64_t seed, pkv_pool **out);
 
@@ -122,7 +128,8 @@ PKV_API void pkv_pool_destroy(pkv_pool *pool);
  * allocated and ids is untouched). */
 PKV_API int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *ids);
 
-/* Add one reference to each of n allocated blocks (prefix sharing).  All ids
+/* Add one reference to each of n allocated blocks (prefix sharing, sec. 4.2 of
+ * the page above).  All ids
  * are checked before any count changes.  Errors: INVALID_ARG (an id that is
  * out of range or not allocated). */
 PKV_API int pkv_pool_share(pkv_pool *pool, int n, const int32_t *ids);
@@ -147,7 +154,8 @@ PKV_API int pkv_pool_refcount(const pkv_pool *pool, int32_t id);
 PKV_API int pkv_pool_reserve(pkv_pool *pool, int32_t *table_row, int max_blocks,
                              int cur_tokens, int new_tokens, int block_size);
 
-/* Fork: a new request starts as a copy of the first num_tokens tokens of another.
+/* Fork: a new request starts as a copy of the first num_tokens tokens of another
+ * (a shared prefix, sec. 4.2 of the page above).
  * dst_row[0 .. ceil(num_tokens/bs)) receives the same block ids as src_row and
  * every one of those blocks gains a reference (shared, not copied).  Errors:
  * INVALID_ARG (an id not allocated, or more blocks than max_blocks). */
@@ -155,7 +163,8 @@ PKV_API int pkv_pool_fork(pkv_pool *pool, const int32_t *src_row, int32_t *dst_r
                           int num_tokens, int block_size);
 
 /* Make position `cur_tokens` of a request writable before its token is
- * appended.  If the position starts a new block, one block is allocated and
+ * appended (copy-on-write: this library's reading of how a block shared as a
+ * prefix, sec. 4.2 of the page above, stays unchanged for its other readers).  If the position starts a new block, one block is allocated and
  * written to table_row.  If it falls inside a block that other requests also
  * reference (reference count > 1), that block is copied on write: a fresh
  * block replaces it in table_row, the old block loses this request's
@@ -187,7 +196,9 @@ PKV_API int pkv_pool_free_table(pkv_pool *pool, const int32_t *table_row, int nu
 PKV_API int pkv_pool_swap(pkv_pool *from, pkv_pool *to, int32_t *table_row, int max_blocks, int num_tokens,
                           int block_size, int32_t *src_ids, int32_t *dst_ids);
 
-/* Host slot mapping for one new token per request:
+/* Host slot mapping for one new token per request: the page-table lookup from a
+ * logical position to its physical slot ("为什么“推理优化”不是锦上添花", sec. 3.2,
+ * scheme 1: fixed-size pages found through a page table):
  *   slots[b] = block_tables[b][positions[b] / bs] * bs + positions[b] % bs,
  * and slots[b] = -1 when positions[b] < 0 (no token for that request).
  * block_tables, positions and slots are HOST pointers.  Errors: INVALID_ARG
@@ -197,7 +208,11 @@ PKV_API int pkv_slot_mapping(int64_t *slots, const int32_t *block_tables, const 
 
 /* ================================================================ device calls */
 
-/* In-place append of one decode step's new K/V into the cache.
+/* In-place append of one decode step's new K/V into the cache: the new token's
+ * entries are written into the preallocated cache at their slots, no tensor is
+ * rebuilt or reallocated ("为什么“推理优化”不是锦上添花", sec. 3.1: write the new
+ * K/V into a preallocated cache; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 4.3: in-place append instead of torch.cat).
  *   k_cache, v_cache : fp16 [num_blocks][num_kv_heads][block_size][head_dim], 16-byte aligned
  *   slot_mapping     : int64 [num_tokens]; token t goes to slot slot_mapping[t];
  *                      a negative slot skips the token (padding)
@@ -211,7 +226,11 @@ PKV_API int pkv_append(void *k_cache, void *v_cache, const int64_t *slot_mapping
                        const void *k_new, const void *v_new, int num_tokens, int num_kv_heads,
                        int head_dim, int block_size, int64_t num_blocks, pkv_stream_t stream);
 
-/* Copy whole blocks (every kv head, every slot) of both caches:
+/* Copy whole blocks (every kv head, every slot) of both caches -- the device
+ * half of copy-on-write for blocks shared between requests
+ * ("推理优化这件事，为什么值得反复复盘", sec. 4.2 shares prefix blocks; the copy of
+ * a shared block before a write into it is this library's reading of that
+ * sharing):
  *   k_cache[dst[i]] <- k_cache[src[i]], v_cache[dst[i]] <- v_cache[src[i]], i < n,
  * bit for bit (copy-on-write of a shared block).  src and dst are DEVICE int32
  * arrays; a destination must not appear twice nor also be a source.  Ids
@@ -222,7 +241,9 @@ PKV_API int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, co
                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                             pkv_stream_t stream);
 
-/* Copy whole blocks from one pool to another of the same geometry:
+/* Copy whole blocks from one pool to another of the same geometry -- the
+ * device half of swapping a request's pages out of and back into the cache
+ * ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2: page-level swap):
  *   dst_k[dst_ids[i]] <- src_k[src_ids[i]], dst_v[dst_ids[i]] <- src_v[src_ids[i]],
  * bit for bit (swap out / swap in).  Either pool may be host memory the GPU can
  * address (page-locked, e.g. cudaHostAlloc or a pinned torch tensor): the copy
@@ -237,11 +258,18 @@ PKV_API int pkv_copy_blocks_between(void *dst_k, void *dst_v, int64_t dst_num_bl
 /* Bytes of workspace pkv_decode_attention needs for contexts up to
  * max_context tokens (0 when one partition covers max_context): fp32 partials
  * for every (request, q head, partition) followed by one int completion
- * counter per (request, q head). */
+ * counter per (request, q head).  Source: the pages attend over a request's
+ * whole context in one pass and do not split it; the split into partitions
+ * and their log-sum-exp merge (see pkv_decode_partition) is this library's
+ * design for long contexts, exact because softmax over a union of token
+ * ranges is the l-weighted merge of the softmaxes over the ranges. */
 PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                          int max_context, int partition_size);
 
-/* One decode step of attention for every request and query head:
+/* One decode step of attention for every request and query head: read every
+ * cached K of the request, score it against q, normalise with softmax and take
+ * the weighted sum of V ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.2),
+ * with K/V gathered through the request's page table (same page, sec. 3.2):
  *   out[b][h][:] = softmax(scale * q[b][h] . K_b^T) . V_b
  * over the context_lens[b] cached tokens of request b, K_b/V_b gathered
  * through block_tables (kv head h / (num_q_heads / num_kv_heads)).
@@ -306,7 +334,8 @@ PKV_API int pkv_decode_attention_shared_prefix(void *out, const void *q, const v
 
 /* Workspace for pkv_decode_step: pkv_decode_workspace_size(..., max_context,
  * PKV_DEFAULT_PARTITION) when prefix_len is 0, else
- * pkv_shared_prefix_workspace_size(..., prefix_len). */
+ * pkv_shared_prefix_workspace_size(..., prefix_len).  Source: the split and its
+ * merge are this library's (see pkv_decode_workspace_size), not the pages'. */
 PKV_API size_t pkv_decode_step_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                               int max_context, int prefix_len);
 
@@ -455,7 +484,9 @@ PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_c
                                        size_t workspace_bytes, pkv_stream_t stream);
 
 /* pkv_decode_step (prefix_len 0) with the split-context partition chosen by the
- * caller instead of PKV_DEFAULT_PARTITION: a multiple of 16 in
+ * caller instead of PKV_DEFAULT_PARTITION (the split and its log-sum-exp merge
+ * are this library's design, exact by the softmax identity noted at
+ * pkv_decode_workspace_size; the pages do not split a context): a multiple of 16 in
  * [16, PKV_MAX_PARTITION]; 0 selects the default.  Smaller partitions give more
  * CTAs per request (short batches, very long contexts), larger ones amortise
  * each CTA's start-up.  Workspace: pkv_decode_workspace_size(..., max_context,
@@ -467,7 +498,11 @@ PKV_API int pkv_decode_step_partition(void *out, const void *q, const void *k_ne
                                       int64_t num_blocks, float scale, int partition_size, void *workspace,
                                       size_t workspace_bytes, pkv_stream_t stream);
 
-/* Split-context partial attention.  Partition p of request b covers logical
+/* Split-context partial attention.  Source: not the pages, which attend over a
+ * whole context in one pass; this is one half of the library's split for long
+ * contexts, defined so that pkv_merge of these partials equals the one-pass
+ * softmax exactly in real arithmetic (softmax over a union of token ranges is
+ * the merge below of per-range statistics).  Partition p of request b covers logical
  * tokens [p * partition_size, min(ctx_b, (p + 1) * partition_size)); for each
  * such partition and query head h it writes
  *   m_part[b][h][p]      = max score (natural-log units, scale applied)
@@ -489,7 +524,9 @@ PKV_API int pkv_decode_partition(float *o_part, float *m_part, float *l_part, co
                                  int64_t num_blocks, float scale, int partition_size,
                                  int max_partitions, pkv_stream_t stream);
 
-/* Log-sum-exp merge of the partials of pkv_decode_partition:
+/* Log-sum-exp merge of the partials of pkv_decode_partition (the other half of
+ * the library's split; the pages do not define it: it is the softmax identity
+ * that rebuilds the one-pass result from per-range max, sum and average):
  *   M = max_p m_p,  w_p = l_p * exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p
  * over the ceil(ctx_b / partition_size) partitions of each request, rounded
  * to fp16 (round to nearest even); an empty request gets a zero row.
@@ -504,21 +541,22 @@ PKV_API int pkv_merge(void *out, const float *o_part, const float *m_part, const
 /* Allocation-free form of pkv_decode_attention.  The pages describe no
  * counterpart: this call exists for callers that cannot allocate device memory.
  *
- * Who needs it: code running while a stream is captured into a CUDA graph in
- * global capture mode (cudaMalloc synchronises the device, which that mode
- * forbids); plugins hosted by another runtime that owns all device memory and
- * hands them only input and output pointers; latency-bound serving loops that
- * ban allocator calls after start-up.  None of them can supply the split
- * workspace pkv_decode_attention asks for.
+ * Who needs it: plugins hosted by another runtime that owns all device memory
+ * and hands them only input and output pointers; latency-bound serving loops
+ * that ban allocator calls (and the device-wide synchronisation cudaMalloc
+ * implies) once they are running.  Neither can supply the split workspace
+ * pkv_decode_attention asks for.
  *
  * Same arguments, semantics and results as pkv_decode_attention, minus the
  * workspace: the split partials live in a file-scope static __device__ array
  * of PKV_NOALLOC_SCRATCH_BYTES bytes inside libpkv.so.  Every GPU on which the
  * library's kernels are loaded holds that array until the process exits.  The
  * first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture begins.  Nothing here calls cudaMalloc, cudaFree or any allocating
- * routine.
+ * device current) and caches it for the life of the process; make that first
+ * call before any stream capture begins.  A cudaDeviceReset of the device
+ * invalidates the cached address: do not call this entry on a device after
+ * resetting it.  Nothing here calls cudaMalloc, cudaFree or any allocating
+ * routine.  Every argument is checked before any CUDA call.
  *
  * Limit and sharing: a call whose split needs more than
  * PKV_NOALLOC_SCRATCH_BYTES (pkv_decode_workspace_size with max_context =
@@ -540,7 +578,8 @@ PKV_API int pkv_decode_attention_noalloc(void *out, const void *q, const void *k
                                          float scale, pkv_stream_t stream);
 
 /* Synchronise `stream`, then report (in *code) and clear the device error
- * word of the current device: PKV_DEV_OK when no kernel recorded an index
+ * word of the current device (library plumbing for failure detection; the pages
+ * describe no counterpart): PKV_DEV_OK when no kernel recorded an index
  * problem since the last call.  Returns PKV_OK, or CUDA when a runtime call
  * fails.  This is the only library call that synchronises. */
 PKV_API int pkv_get_device_error(pkv_stream_t stream, int *code);

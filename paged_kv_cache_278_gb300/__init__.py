@@ -22,7 +22,7 @@ import torch
 
 from . import _lib
 from ._lib import (PKV_MAX_QUERY_LEN, PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
-                   PKV_DEV_OK, PKV_DEV_PREFIX_MISMATCH, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION,
+                   PKV_DEV_OK, PKV_DEV_PREFIX_MISMATCH, PKV_DEV_SMEM_MISALIGNED, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION,
                    PkvError)
 
 __all__ = [
@@ -34,6 +34,7 @@ __all__ = [
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
+    "PKV_DEV_SMEM_MISALIGNED",
 ]
 
 

@@ -31,6 +31,7 @@ PKV_DEV_BAD_CONTEXT = 2
 PKV_DEV_BAD_SLOT = 3
 PKV_DEV_WAIT_TIMEOUT = 4
 PKV_DEV_PREFIX_MISMATCH = 5
+PKV_DEV_SMEM_MISALIGNED = 6
 
 PKV_HEAD_DIM = 128
 PKV_DEFAULT_PARTITION = 1024
@@ -106,14 +107,15 @@ class PkvError(RuntimeError):
         super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
 
 
-_lib = None
+_loaded: dict = {}
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libpkv.so once; raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load libpkv.so (or another build of the same sources at `path`) once per path, with the
+    argument and result types of every declared call; raises if it has not been built."""
+    lib = _loaded.get(path)
+    if lib is not None:
+        return lib
     if not os.path.exists(path):
         raise ImportError(f"libpkv.so is not built ({path}); run `python -m paged_kv_cache_278_gb300.build`")
     lib = ctypes.CDLL(path)
@@ -121,7 +123,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    _loaded[path] = lib
     return lib
 
 

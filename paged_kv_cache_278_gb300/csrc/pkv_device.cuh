@@ -13,7 +13,12 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 // A wait on an mbarrier gives up after this many nanoseconds of %globaltimer,
 // records PKV_DEV_WAIT_TIMEOUT and lets the kernel finish instead of hanging.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// PKV_WAIT_TEST (a separate test build of the library, never the product) makes
+// one wait of the decode kernel run out on purpose and shortens the limit to 1 ms.
+#ifndef PKV_WAIT_TEST
+#define PKV_WAIT_TEST 0
+#endif
+constexpr uint64_t kWaitLimitNs = PKV_WAIT_TEST ? 1000000ull : 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
