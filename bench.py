@@ -1,16 +1,18 @@
 #!/usr/bin/env python
 """Benchmark: one decode step (append + paged decode attention, every layer) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha7b] [--block-size 16]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gqa8b] [--block-size 16]
     python bench.py --impl reference ...      # the float64 CPU oracle on the host cores
 
-A step is the whole hot path over one batch: for each of the 32 layers, pkv_append writes the
-new token's K/V into its slot and pkv_decode_attention attends over every cached token
-(split into 1024-token partitions, 512 for the long-context workload, + log-sum-exp merge where a context needs it).  The default
-workload is the 7B-shaped MHA decode: batch 16, 32 layers, 32 q = 32 kv heads, head_dim 128,
-block_size 16, context lengths uniform in [200, 4000] per request (seeded), fp16 K/V ~ N(0, 1),
-physical blocks a seeded permutation of the pool.  Each layer has its own 554 MB cache, so
-every step streams ~17.7 GB: far larger than L2, no flush needed.
+A step is the whole hot path over one batch: for each of the 32 layers, the new token's K/V is
+written into its slot and decode attention runs over every cached token (split into 1024-token
+partitions, 512 for the long-context workload, + log-sum-exp merge where a context needs it).
+The default workload is the largest single-GPU configuration, the 8B-shaped GQA decode: batch
+64, 32 layers, 32 q / 8 kv heads, head_dim 128, block_size 16, 2048 prefilled tokens per
+request and 128 consecutive decode steps (step t appends position 2047 + t; timed steps cycle
+through them), fp16 K/V ~ N(0, 1), physical blocks a seeded permutation of the pool.  Each
+layer has its own ~570 MB cache, so every step streams ~17 GB: far larger than L2, no flush
+needed.  --workload mha7b | shared_prefix | long_context | tiny select the other shapes.
 
 Printed (rank 0, one JSON line): decode-attention HBM GB/s over the whole step (value), the
 step time, tokens/s, the dominant kernel's roofline (algorithmic bytes / its CUDA-event time,
@@ -843,7 +845,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="mha7b")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="gqa8b")
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--layers", type=int, default=0, help="layers per step (default 32; fewer only for profiling)")
     ap.add_argument("--no-graph", action="store_true")
