@@ -100,7 +100,8 @@ def kernel_source_hash(workload: str = "") -> str:
     """Hash of the code (comments and layout ignored) of the kernel sources a workload's timed
     launches come from (the shared-prefix step also runs the prefix kernel)."""
     h = hashlib.sha256()
-    names = ["pkv_decode.cu", "pkv_device.cuh"] + (["pkv_prefix.cu"] if workload.startswith("shared_prefix") else [])
+    names = ["pkv_decode.cu", "pkv_engine.cuh", "pkv_device.cuh"] + \
+        (["pkv_prefix.cu"] if workload.startswith("shared_prefix") else [])
     for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_278_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(_code_only(f.read()).encode())
