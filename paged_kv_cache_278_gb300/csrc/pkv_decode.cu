@@ -59,14 +59,19 @@ __device__ int g_decode_error;
 namespace {
 
 // MQ: 0 one token per request; 1 or 2 several tokens per request, with that many 8-column tiles.
+// Copy stages per warp of a kernel variant.
+template <int MQ>
+constexpr int stages_of() {
+    return MQ == 2 ? PKV_DECODE_MQ2_STAGES : kStages;
+}
+
 template <int G, int LPT, bool TC, int KQ, int MQ>
-__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) || MQ == 2
-                                                ? 2
-                                                : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
+__global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
     decode_partition_kernel(const __grid_constant__ DecodeParams P) {
     static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
     static_assert(!MQ || (TC && !KQ), "several tokens per request run on the fp16 tensor-core engine");
-    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1>;
+    constexpr int kStages = stages_of<MQ>();  // this variant's ring depth
+    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, kStages>;
     using Engine = EngineFor<G, LPT, TC, KQ, MQ>;
     constexpr int kRow = L::row;
     constexpr int NC = MQ ? 8 * MQ : G;  // packed output columns per CTA
@@ -702,7 +707,7 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
             st = KQ == 2 ? encode_code_map(&p.tmap_v, p.v_cache, rows) : encode_cache_map(&p.tmap_v, p.v_cache, rows);
         if (st != PKV_OK) return st;
     }
-    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1>;
+    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, stages_of<MQ>()>;
     const int smem = L::total(G, p.partition_size);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;

@@ -38,6 +38,10 @@ constexpr int kRowBytes = kD * 2;       // one fp16 K or V row
 #ifndef PKV_DECODE_KQ_MIN_CTAS
 #define PKV_DECODE_KQ_MIN_CTAS 4
 #endif
+// Copy stages per warp of the 16-column multi-token kernel (it runs at 2 CTAs per SM).
+#ifndef PKV_DECODE_MQ2_STAGES
+#define PKV_DECODE_MQ2_STAGES 2
+#endif
 // 1: K and V of a stage land on separate mbarriers, so a chunk's q.K starts as soon as its K has
 // arrived and the next K copy into the stage is issued before the chunk's P.V runs.  Measured 1-2.5%
 // slower on every workload (twice the barrier traffic for no gain in bytes in flight): off.
@@ -124,7 +128,7 @@ constexpr int kMergeTile = 512;  // partitions whose weights the fused merge sta
 // also holds the chunk's 16 float32 key scales.
 constexpr int kHalfTile = kChunk * 128;
 // KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values.
-template <bool TC, int KQ = 0, int NT = 1>
+template <bool TC, int KQ = 0, int NT = 1, int NS = kStages>
 struct SmemLayout {
     static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
@@ -133,10 +137,10 @@ struct SmemLayout {
     static constexpr int stage = k_tile + v_tile;
     static constexpr int scale_stride = KQ == 2 ? 2 * kChunk * 4 : kChunk * 4;  // K scales (| V scales) per stage
     static constexpr int stages = 0;
-    static constexpr int stage_bytes = kWarps * kStages * stage;
+    static constexpr int stage_bytes = kWarps * NS * stage;
     static constexpr int scales = stages + stage_bytes;
-    static constexpr int bars = scales + (KQ ? kWarps * kStages * scale_stride : 0);
-    static constexpr int probs = bars + kWarps * kStages * kBarsPerStage * 8;
+    static constexpr int bars = scales + (KQ ? kWarps * NS * scale_stride : 0);
+    static constexpr int probs = bars + kWarps * NS * kBarsPerStage * 8;
     __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? NT * 2 * 8 * kChunk * 2 : kChunk * g * 4; }
     __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
     __host__ __device__ static constexpr int table(int g) { return newrow(g) + 2 * kRowBytes; }
@@ -926,9 +930,157 @@ struct TcEngineM2 {
     }
 };
 
+// Sixteen (token, head) rows of one kv head as the M dimension of the MMAs (several tokens per
+// request, more than 8 rows per kv head): per 16-token chunk
+//   S[16 rows x 16 tok] = Q[16 x 128] . K^T     2 n-tiles x 8 k-steps of mma.m16n8k16, K by ldmatrix
+//   O[16 rows x 128]   += P[16 x 16] . V         16 n-tiles x 2 (P = hi + lo), V by ldmatrix.trans
+// with fp32 accumulation.  Q stays in registers as A fragments, and P goes from the S accumulators
+// straight into A fragments (no shared-memory round trip), so one engine holds what two 8-column
+// engines held and the kernel fits three CTAs per SM.  Lane l owns rows g = l / 4 and g + 8 for the
+// online softmax; each row masks the cached positions after its own token's (causal).
+template <int G>
+struct TcEngineR16 {
+    uint32_t qa[kD / 16][4];  // Q A-fragments of the 8 k-steps
+    float o[kD / 8][4];       // O: n-tile j = dims 8j .. 8j + 7: (row g, dims 8j + 2t, +1), (row g + 8, same)
+    uint32_t ph[4], pl[4];    // the chunk's P as A fragments, fp16 hi and lo parts
+    float m_ref[2], top[2], l_part[2];  // rows g, g + 8 (log2 units; l_part this lane's share)
+    int lim[2];                         // last visible logical position of rows g, g + 8 (-1: dead row)
+    float q_scale;
+
+    __device__ __forceinline__ void init(const DecodeParams &P, int, int, int) {
+#pragma unroll
+        for (int j = 0; j < kD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        m_ref[0] = m_ref[1] = top[0] = top[1] = -INFINITY;
+        l_part[0] = l_part[1] = 0.f;
+        q_scale = P.q_scale;
+    }
+
+    // Rows rg * 16 .. rg * 16 + 15 of the request's n * G rows for kv head kvh (row r = token r / G,
+    // head r % G); rows past the last token are dead (zero q, nothing visible).
+    __device__ __forceinline__ void bind(const DecodeParams &P, int kvh, int lane, int rg, int64_t qs, int n, int ctx) {
+        const int g = lane >> 2, t = lane & 3;
+        const __half *qrow[2];
+        bool live[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = rg * 16 + g + 8 * i;
+            live[i] = r / G < n;
+            qrow[i] = P.q + ((qs + (live[i] ? r / G : 0)) * P.num_q_heads + kvh * G + r % G) * kD;
+            lim[i] = live[i] ? ctx - n + r / G : -1;
+        }
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = k & 1, d = ks * 16 + 2 * t + (k >> 1) * 8;
+                qa[ks][k] = live[i] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[i] + d)) : 0u;
+            }
+    }
+
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t, int valid, int lane, unsigned char *, int tok0) {
+        const int t = lane & 3;
+        float s[2][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t b[4];
+            pkv::ldsm_x4(b, k_tile + TcEngine<8>::swz((lane & 7) + ((lane >> 4) << 3), 2 * ks + ((lane >> 3) & 1)));
+            pkv::mma16816(s[0], qa[ks], b[0], b[1]);
+            pkv::mma16816(s[1], qa[ks], b[2], b[3]);
+        }
+        // mask (past the chunk's tokens, or after the row's own position) and scale
+        float cm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tk = 8 * j + 2 * t + (e & 1), i = e >> 1;
+                s[j][e] = tk < valid && tok0 + tk <= lim[i] ? s[j][e] * q_scale : -INFINITY;
+                cm[i] = fmaxf(cm[i], s[j][e]);
+            }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            cm[i] = fmaxf(cm[i], __shfl_xor_sync(pkv::kFullMask, cm[i], 1));
+            cm[i] = fmaxf(cm[i], __shfl_xor_sync(pkv::kFullMask, cm[i], 2));
+            top[i] = fmaxf(top[i], cm[i]);
+        }
+        // online softmax with the lazy 2^8 margin; a row with nothing visible yet keeps weight 0
+        if (__any_sync(pkv::kFullMask, cm[0] > m_ref[0] + kRescaleThreshold || cm[1] > m_ref[1] + kRescaleThreshold)) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float mn = fmaxf(m_ref[i], cm[i]);
+                const float a = mn == -INFINITY ? 1.f : exp2f(m_ref[i] - mn);
+                m_ref[i] = mn;
+                l_part[i] *= a;
+#pragma unroll
+                for (int j = 0; j < kD / 8; ++j) {
+                    o[j][2 * i] *= a;
+                    o[j][2 * i + 1] *= a;
+                }
+            }
+        }
+        float p[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = e >> 1;
+                p[j][e] = s[j][e] == -INFINITY ? 0.f : exp2f(s[j][e] - m_ref[i]);
+                l_part[i] += p[j][e];
+            }
+        // A fragments of P (rows g / g + 8 x tokens 2t, 2t + 1 / + 8), hi + lo parts
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = k >> 1, e = (k & 1) * 2;  // a0 (j 0, row g), a1 (j 0, row g + 8), a2 (j 1, g), a3 (j 1, g + 8)
+            const __half2 hi = __floats2half2_rn(p[j][e], p[j][e + 1]);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(p[j][e] - hf.x, p[j][e + 1] - hf.y);
+            ph[k] = *reinterpret_cast<const uint32_t *>(&hi);
+            pl[k] = *reinterpret_cast<const uint32_t *>(&lo);
+        }
+    }
+
+    __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *) {
+#pragma unroll
+        for (int j2 = 0; j2 < kD / 16; ++j2) {
+            uint32_t b[4];
+            pkv::ldsm_x4_trans(b, v_tile + TcEngine<8>::swz((lane & 7) + ((lane >> 3) & 1) * 8, 2 * j2 + (lane >> 4)));
+            pkv::mma16816(o[2 * j2], ph, b[0], b[1]);
+            pkv::mma16816(o[2 * j2 + 1], ph, b[2], b[3]);
+            pkv::mma16816(o[2 * j2], pl, b[0], b[1]);
+            pkv::mma16816(o[2 * j2 + 1], pl, b[2], b[3]);
+        }
+    }
+
+    // Rows g and g + 8 into the combine area's 16 columns per warp, re-referenced to the true max.
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float l = l_part[i];
+            l += __shfl_xor_sync(pkv::kFullMask, l, 1);
+            l += __shfl_xor_sync(pkv::kFullMask, l, 2);
+            float m = m_ref[i], f = 1.f;
+            if (top[i] > -INFINITY) {  // m_ref <= top < m_ref + 2^8
+                f = exp2f(m_ref[i] - top[i]);
+                l *= f;
+                m = top[i];
+            }
+            const int row = g + 8 * i;
+            float *acc = c_acc + (warp * 16 + row) * kD + 2 * t;
+#pragma unroll
+            for (int j = 0; j < kD / 8; ++j)
+                *reinterpret_cast<float2 *>(acc + 8 * j) = make_float2(o[j][2 * i] * f, o[j][2 * i + 1] * f);
+            if (t == 0) {
+                c_m[warp * 16 + row] = m;
+                c_l[warp * 16 + row] = l;
+            }
+        }
+    }
+};
+
 template <int G, int LPT, bool TC, int KQ, int MQ>
 using EngineFor = typename std::conditional<
-    MQ == 2, TcEngineM2<G>,
+    MQ == 2, TcEngineR16<G>,
     typename std::conditional<MQ == 1, TcEngineM<G>,
     typename std::conditional<
         KQ == 2, TcEngineQV<G>,
