@@ -899,37 +899,6 @@ struct TcEngineM : TcEngine<8> {
     }
 };
 
-// Two column tiles (16 (token, head) rows) per CTA: each chunk's K/V tile, staged once, feeds two
-// independent 8-column engines, so a request with up to 16 rows per kv head is one stream of the
-// cache instead of two.
-template <int G>
-struct TcEngineM2 {
-    TcEngineM<G> e[2];
-    static constexpr int kScratch = 2 * 8 * kChunk * 2;  // one engine's P^T buffers
-
-    __device__ __forceinline__ void init(const DecodeParams &P, int b, int kvh, int lane) {
-        e[0].init(P, b, kvh, lane);
-        e[1].init(P, b, kvh, lane);
-    }
-    __device__ __forceinline__ void bind(const DecodeParams &P, int kvh, int lane, int rg, int64_t qs, int n, int ctx) {
-        e[0].bind(P, kvh, lane, rg, qs, n, ctx, 16, 0);
-        e[1].bind(P, kvh, lane, rg, qs, n, ctx, 16, 8);
-    }
-    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t s_tile, int valid, int lane, unsigned char *scratch,
-                                       int tok0) {
-        e[0].qk(k_tile, s_tile, valid, lane, scratch, tok0);
-        e[1].qk(k_tile, s_tile, valid, lane, scratch + kScratch, tok0);
-    }
-    __device__ __forceinline__ void pv(uint32_t v_tile, int valid, int lane, unsigned char *scratch) {
-        e[0].pv(v_tile, valid, lane, scratch);
-        e[1].pv(v_tile, valid, lane, scratch + kScratch);
-    }
-    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
-        e[0].finish(warp, lane, c_acc, c_m, c_l, 16, 0);
-        e[1].finish(warp, lane, c_acc, c_m, c_l, 16, 8);
-    }
-};
-
 // Sixteen (token, head) rows of one kv head as the M dimension of the MMAs (several tokens per
 // request, more than 8 rows per kv head): per 16-token chunk
 //   S[16 rows x 16 tok] = Q[16 x 128] . K^T     2 n-tiles x 8 k-steps of mma.m16n8k16, K by ldmatrix
