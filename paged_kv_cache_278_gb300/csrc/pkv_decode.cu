@@ -22,7 +22,8 @@
 //     fp16 hi + lo parts.  Variants of the same engine serve int8 keys (codes converted to exact
 //     fp16 integers in registers, row scales applied to the finished dot products), int8 keys
 //     and values (value scales folded into the weights) and several new tokens per request
-//     ((token, head) rows as the columns, causal masks per column).  A CUDA-core engine (packed
+//     ((token, head) rows as the 8 columns, or for more than 8 rows per kv head 16 rows as the MMA's
+//     M dimension with P kept in registers; causal masks per row).  A CUDA-core engine (packed
 //     fp32x2 FMAs) remains behind PKV_DECODE_TC_MIN_GROUP.
 //   * Online softmax in fp32 with lazy rescaling: the reference max is only raised (and the
 //     accumulators rescaled) when a score exceeds it by more than 2^8; the true max is tracked
