@@ -1171,6 +1171,21 @@ int encode_fp16_cache_map(void *map, const void *base, int64_t rows) {
     return encode_cache_map(static_cast<CUtensorMap *>(map), base, rows);
 }
 
+int encode_q_map(void *map, const void *q, int num_seqs, int num_q_heads, int group) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn || group <= 0 || 128 % group != 0) return PKV_ERR_CUDA;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_q_heads),
+                                static_cast<cuuint64_t>(num_seqs)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes),
+                                   static_cast<cuuint64_t>(num_q_heads) * kRowBytes};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = fn(static_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q),
+                          dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int check_decode_args(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq, int num_q_heads,
                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks) {

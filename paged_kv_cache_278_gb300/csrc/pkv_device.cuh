@@ -93,6 +93,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tensor_map
         : "memory");
 }
 
+// 3-D tensor-map copy of one box into shared memory, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tensor_map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(tensor_map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -196,7 +205,18 @@ __device__ __forceinline__ uint64_t umma_desc_k_sw128(uint32_t smem_addr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-// Instruction descriptor of kind::f16 with fp16 A and B (both K-major), fp32 accumulation, M x N.
+// Shared-memory matrix descriptor of an MN-major operand tile in the 128-byte swizzle: 64 elements of
+// the M/N dimension per 128-byte row, rows along K, 8-row groups `sbo` bytes apart (stride byte
+// offset) and 64-wide M/N slabs `lbo` bytes apart (leading byte offset), descriptor version 1,
+// layout 2.  The start must lie on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of kind::f16 with fp16 A and B (both K-major), fp32 accumulation, M x N;
+// bit 16 set makes B MN-major.
 __host__ __device__ constexpr uint32_t umma_idesc_f16_f32(int m, int n) {
     return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }

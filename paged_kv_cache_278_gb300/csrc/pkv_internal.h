@@ -20,6 +20,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // A cache tensor [rows][128] fp16 as a tensor map (CUtensorMap, passed as void*) for 2-D tensor
 // copies of 16-row x 64-dim boxes in the 128-byte swizzle.  PKV_OK or PKV_ERR_CUDA.
 int encode_fp16_cache_map(void *map, const void *base, int64_t rows);
+// q [num_seqs][num_q_heads][128] fp16 as a 3-D tensor map read in (64 dims, group heads, 128 / group
+// requests) boxes in the 128-byte swizzle: 128 query rows of one kv head.  PKV_OK or PKV_ERR_CUDA.
+int encode_q_map(void *map, const void *q, int num_seqs, int num_q_heads, int group);
 
 // Host-side argument checks shared by every decode entry point (PKV_OK or an error status).
 int check_decode_args(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,

@@ -86,7 +86,9 @@ struct PrefixParams {
     int max_partitions;
     int64_t num_blocks;
     float q_scale;  // scale * log2(e)
-    CUtensorMap tmap_k;  // tensor-memory kernel: the K cache as [NB*Hkv*bs][128] fp16, 16 x 64 boxes, 128B swizzle
+    CUtensorMap tmap_k;  // tensor-memory kernel: the K and V caches as [NB*Hkv*bs][128] fp16, 16 x 64 boxes,
+    CUtensorMap tmap_v;  //   128-byte swizzle
+    CUtensorMap tmap_q;  // tensor-memory kernel: q as [B][Hq][128] fp16, (64, G, 128 / G) boxes, 128-byte swizzle
 };
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) { pkv::ldsm_x4(r, pkv::smem_addr(p)); }
@@ -269,32 +271,39 @@ __global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams
 
 // ---------------------------------------------------------------- tcgen05 / tensor-memory variant
 // The same chunk computation as prefix_kernel on the 5th-generation tensor cores: one thread
-// issues tcgen05.mma with both operands described in shared memory (K-major, 128-byte swizzle)
-// and the fp32 accumulators in tensor memory, so the four warps hold no accumulator registers.
+// issues tcgen05.mma with both operands described in shared memory (128-byte swizzle) and the fp32
+// accumulators in tensor memory, so the eight warps hold no accumulator registers.
 //   S[128 rows x 128 tokens] = Q[128 x 128 dims] K^T          8 MMAs (M 128, N 128, K 16), TMEM cols 0-127
-//   exact chunk softmax: thread = row = TMEM lane, S read back with tcgen05.ld, P = hi + lo fp16
+//   exact chunk softmax: two threads per row (64 columns each, TMEM lanes of their warp), S read
+//   back with tcgen05.ld, the row's max and sum exchanged in shared memory, P = hi + lo fp16
 //   O[128 rows x 128 dims] = P_hi V + P_lo V                   16 MMAs (K = tokens), TMEM cols 128-255
-// K arrives by tensor copies (16 x 64 boxes, 128-byte swizzle) straight into the B-operand tile;
-// Q rows and the transposed V chunk (the PV B operand is V^T, K-major) are written by the threads
-// in the same swizzle.  Tensor memory is allocated and freed by warp 0 on every path.
+// Q (a 3-D tensor map over q: 128 / G requests x the G heads of one kv head), K and V arrive by
+// tensor copies straight into their operand tiles, all issued by one thread before anything else;
+// V enters the P.V product as it arrived (tokens x dims), an MN-major B operand.  O leaves through
+// the free tiles so every global store writes a whole 512-byte row.  Tensor memory is allocated and
+// freed by warp 0 on every path.  Measured on the shared-prefix step: the MMAs take 0.4 us of a
+// CTA's ~7-10 us (the per-row softmax and epilogue phases dominate), and the step is 6 % slower
+// than with the mma.sync tile, so the mma.sync tile is the default; this form is built and checked
+// against the oracle by its own GPU test.
 #ifndef PKV_PREFIX_TCGEN05
 #define PKV_PREFIX_TCGEN05 0
+#endif
+// 1: the prefix CTAs release the suffix pass only once their tensor copies are queued.
+#ifndef PKV_PREFIX_LATE_TRIGGER
+#define PKV_PREFIX_LATE_TRIGGER 0
 #endif
 namespace tc5 {
 constexpr int kTok = 128;                 // prefix tokens per CTA: N of Q K^T, K of P V
 constexpr int kRowsT = 128;               // query rows per CTA: M, one tensor-memory lane each
-constexpr int kThreadsT = 128;            // one thread per query row
+constexpr int kThreadsT = 256;            // two threads per query row (64 columns each)
 constexpr int kAtom = 128 * 128;          // one 64-element K slab of a 128-row operand tile (bytes)
 constexpr int kTile = 2 * kAtom;          // 128 rows x 128 K fp16
 // Q | K | V^T | barriers, TMEM slot.  P_hi and P_lo reuse the Q and K tiles once S is complete, so
 // a prefix CTA (96 KB) leaves room on its SM for a suffix-pass CTA started early.
-constexpr int kSmem = 3 * kTile + 64;
+constexpr int kSmem = 3 * kTile + 64 + 2 * 2 * 128 * 4;  // + the row halves' (max, sum) exchange
 constexpr uint32_t kTmemCols = 256;       // S in columns 0-127, O in 128-255
 }  // namespace tc5
 
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -307,93 +316,76 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 __global__ void __launch_bounds__(tc5::kThreadsT, 1) prefix_kernel_tmem(const __grid_constant__ PrefixParams P) {
     extern __shared__ __align__(1024) unsigned char smem_tc[];
     unsigned char *smem = smem_tc;
+#if !PKV_PREFIX_LATE_TRIGGER
     pkv::pdl_launch_dependents();  // the suffix pass may start streaming right away
+#endif
     const uint32_t base = pkv::smem_addr(smem);
     if ((base & 1023) != 0) {  // the swizzled operand tiles need 1 KB alignment (before any allocation)
-        if (threadIdx.x == 0) pkv::record_error(&g_prefix_error, PKV_DEV_WAIT_TIMEOUT);
+        if (threadIdx.x == 0) pkv::record_error(&g_prefix_error, PKV_DEV_SMEM_MISALIGNED);
+#if PKV_PREFIX_LATE_TRIGGER
+        pkv::pdl_launch_dependents();
+#endif
         return;
     }
-    const uint32_t sQ = base, sK = base + tc5::kTile, sVt = base + 2 * tc5::kTile;
+    const uint32_t sQ = base, sK = base + tc5::kTile, sV = base + 2 * tc5::kTile;
     const uint32_t sPh = sQ, sPl = sK;  // written only after the Q K^T MMAs have completed
     const uint32_t tma_bar = base + 3 * tc5::kTile, mma_bar = tma_bar + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 3 * tc5::kTile + 16);
     int *s_ok = reinterpret_cast<int *>(smem + 3 * tc5::kTile + 20);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    float *s_max = reinterpret_cast<float *>(smem + 3 * tc5::kTile + 64);  // [2 halves][128 rows]
+    float *s_sum = s_max + 2 * 128;                                        // [2 halves][128 rows]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its rows) and columns 64 (w / 4) .. + 63.
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane;
     const int chunk = blockIdx.x, kvh = blockIdx.y, rtile = blockIdx.z;
     const int Hq = P.num_q_heads, Hkv = P.num_kv_heads, G = Hq / Hkv, bs = P.block_size;
     const int rows = P.num_seqs * G;
     const int row0 = rtile * tc5::kRowsT;
     const int tok0 = chunk * tc5::kTok;
     const int ntok = min(tc5::kTok, P.prefix_len - tok0);  // a multiple of 16: the prefix is whole blocks
+    const int groups = ntok / 16;
 
+    // Every operand by tensor copies on one barrier, issued before anything else: the CTA's 128 query
+    // rows (the 3-D q map: 128 / G requests x the G heads of kv head kvh; rows past the batch read as
+    // zeros), and per 16-token group of the chunk two 16 x 64 boxes of K and two of V into the slabs.
     if (tid == 0) {
         pkv::mbar_init(tma_bar, 1);
         pkv::mbar_init(mma_bar, 1);
         pkv::fence_mbar_init();
+        pkv::mbar_arrive_expect_tx(tma_bar, 2 * tc5::kAtom + groups * 4 * 2048);
+        const int rq = tc5::kRowsT / G;
+        pkv::tma_load_3d(sQ, &P.tmap_q, 0, kvh * G, rtile * rq, tma_bar);
+        pkv::tma_load_3d(sQ + tc5::kAtom, &P.tmap_q, 64, kvh * G, rtile * rq, tma_bar);
+        int32_t ids[tc5::kTok / 16];
+#pragma unroll
+        for (int g = 0; g < tc5::kTok / 16; ++g) ids[g] = g < groups ? __ldg(P.block_tables + (tok0 + 16 * g) / bs) : 0;
+#pragma unroll
+        for (int g = 0; g < tc5::kTok / 16; ++g) {
+            if (g >= groups) break;
+            int32_t id = ids[g];
+            if (id < 0 || id >= P.num_blocks) {
+                pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
+                id = 0;
+            }
+            const int tok = tok0 + 16 * g;
+            const int y = static_cast<int>((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs);
+            pkv::tma_load_2d(sK + g * 2048, &P.tmap_k, 0, y, tma_bar);
+            pkv::tma_load_2d(sK + tc5::kAtom + g * 2048, &P.tmap_k, 64, y, tma_bar);
+            pkv::tma_load_2d(sV + g * 2048, &P.tmap_v, 0, y, tma_bar);
+            pkv::tma_load_2d(sV + tc5::kAtom + g * 2048, &P.tmap_v, 64, y, tma_bar);
+        }
     }
     if (warp == 0) pkv::tmem_alloc(pkv::smem_addr(tmem_slot), tc5::kTmemCols);
     pkv::tmem_fence_before_sync();
     __syncthreads();
     pkv::tmem_fence_after_sync();
+#if PKV_PREFIX_LATE_TRIGGER
+    pkv::pdl_launch_dependents();  // the prefix's loads are queued first; the suffix pass may start now
+#endif
     const uint32_t tmem = *tmem_slot;
     const uint32_t t_s = tmem, t_o = tmem + 128;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
-
-    // K chunk by tensor copies: per 16-token group two 16 x 64 boxes into the two K slabs.
-    if (tid == 0) {
-        const int groups = ntok / 16;
-        pkv::mbar_arrive_expect_tx(tma_bar, groups * 2 * 2048);
-        for (int g = 0; g < groups; ++g) {
-            const int tok = tok0 + 16 * g;
-            int32_t id = __ldg(P.block_tables + tok / bs);
-            if (id < 0 || id >= P.num_blocks) {
-                pkv::record_error(&g_prefix_error, PKV_DEV_BAD_BLOCK_ID);
-                id = 0;
-            }
-            const int y = static_cast<int>((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs);
-            pkv::tma_load_2d(sK + g * 2048, &P.tmap_k, 0, y, tma_bar);
-            pkv::tma_load_2d(sK + tc5::kAtom + g * 2048, &P.tmap_k, 64, y, tma_bar);
-        }
-    }
-    // Q: thread r writes its query row (zero past the last row).
-    {
-        const int gr = row0 + tid;
-        const uint4 *qrow = nullptr;
-        if (gr < rows)
-            qrow = reinterpret_cast<const uint4 *>(P.q + (static_cast<int64_t>(gr / G) * Hq + kvh * G + gr % G) * kD);
-        uint4 qv[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) qv[c] = qrow ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) sts128(sQ + tile_off(tid, c), qv[c]);
-    }
-    // V^T: thread t moves token t's V row into column t of the 128 dim-rows (zero past the prefix).
-    {
-        const int t = tid;
-        const uint4 *vrow = nullptr;
-        if (t < ntok) {
-            const int tok = tok0 + t;
-            int32_t id = __ldg(P.block_tables + tok / bs);
-            if (id < 0 || id >= P.num_blocks) id = 0;  // recorded by the K copies
-            vrow = reinterpret_cast<const uint4 *>(P.v_cache + ((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs) * kD);
-        }
-        uint4 vv[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) vv[c] = vrow ? __ldg(vrow + c) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t col = (t >> 6) * tc5::kAtom + (t & 7) * 2;  // slab of the token, byte in the 16-B chunk
-        const int c8 = (t & 63) >> 3;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint32_t w[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int d = c * 8 + e;
-                sts16(sVt + col + d * 128 + ((c8 ^ (d & 7)) << 4), static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-            }
-        }
-    }
-    pkv::fence_proxy_async_smem();  // the threads' tile writes, visible to the tensor core
-    __syncthreads();
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;  // this warp's TMEM lanes
 
     constexpr uint32_t kIdesc = pkv::umma_idesc_f16_f32(128, 128);
     if (tid == 0) {
@@ -416,83 +408,108 @@ __global__ void __launch_bounds__(tc5::kThreadsT, 1) prefix_kernel_tmem(const __
     ok = __syncthreads_and(ok);
     pkv::tmem_fence_after_sync();
 
+    // ---- exact softmax of each row over the chunk (log2 domain): this thread's 64 columns, the row's
+    // max and sum exchanged with the thread holding the other half; P = hi + lo into the A tiles.
     float m = -INFINITY, l = 0.f;
+    const int c_begin = 64 * half;
+    uint32_t r[2][32];
     if (ok) {
-        // exact softmax of this thread's row over the chunk (log2 domain), P = hi + lo into the A tiles
-        uint32_t r[32];
+        pkv::tmem_ld32(t_s + lane_base + c_begin, r[0]);
+        pkv::tmem_ld32(t_s + lane_base + c_begin + 32, r[1]);
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c0 = 0; c0 < tc5::kTok; c0 += 32) {
-            pkv::tmem_ld32(t_s + lane_base + c0, r);
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                m = fmaxf(m, c0 + j < ntok ? __uint_as_float(r[j]) * P.q_scale : -INFINITY);
-        }
+                mx[j & 3] = fmaxf(mx[j & 3], c_begin + 32 * h + j < ntok ? __uint_as_float(r[h][j]) * P.q_scale : -INFINITY);
+        s_max[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    }
+    __syncthreads();
+    if (ok) {
+        m = fmaxf(s_max[row], s_max[128 + row]);
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c0 = 0; c0 < tc5::kTok; c0 += 32) {
-            pkv::tmem_ld32(t_s + lane_base + c0, r);
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const float p0 = c0 + j < ntok ? exp2f(__uint_as_float(r[j]) * P.q_scale - m) : 0.f;
-                const float p1 = c0 + j + 1 < ntok ? exp2f(__uint_as_float(r[j + 1]) * P.q_scale - m) : 0.f;
-                l += p0 + p1;
-                const __half2 h = __floats2half2_rn(p0, p1);
-                const float2 hf = __half22float2(h);
-                hi[j / 2] = *reinterpret_cast<const uint32_t *>(&h);
-                lo[j / 2] = pack_half2(p0 - hf.x, p1 - hf.y);
-            }
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint32_t off = tile_off(tid, (c0 >> 3) + k);
-                sts128(sPh + off, make_uint4(hi[4 * k], hi[4 * k + 1], hi[4 * k + 2], hi[4 * k + 3]));
-                sts128(sPl + off, make_uint4(lo[4 * k], lo[4 * k + 1], lo[4 * k + 2], lo[4 * k + 3]));
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    const int c = c_begin + 32 * h + 8 * k + j;
+                    const float p0 = c < ntok ? exp2f(__uint_as_float(r[h][8 * k + j]) * P.q_scale - m) : 0.f;
+                    const float p1 = c + 1 < ntok ? exp2f(__uint_as_float(r[h][8 * k + j + 1]) * P.q_scale - m) : 0.f;
+                    sum[j >> 1] += p0 + p1;
+                    const __half2 hh = __floats2half2_rn(p0, p1);
+                    const float2 hf = __half22float2(hh);
+                    hi[j / 2] = *reinterpret_cast<const uint32_t *>(&hh);
+                    lo[j / 2] = pack_half2(p0 - hf.x, p1 - hf.y);
+                }
+                const uint32_t off = tile_off(row, (c_begin >> 3) + 4 * h + k);
+                sts128(sPh + off, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+                sts128(sPl + off, make_uint4(lo[0], lo[1], lo[2], lo[3]));
             }
-        }
+        s_sum[half * 128 + row] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     }
     pkv::fence_proxy_async_smem();
     pkv::tmem_fence_before_sync();
     __syncthreads();
+    if (ok) l = s_sum[row] + s_sum[128 + row];
     if (ok && tid == 0) {
         pkv::tmem_fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+        // O = P V with V as it arrived (tokens x dims): the B operand MN-major, 16 tokens (two 8-row
+        // groups, 1 KB apart) per K step, the dims' two 64-wide slabs one slab apart
+        constexpr uint32_t kIdescPV = kIdesc | (1u << 16);
+        for (int ks = 0; ks < groups; ++ks) {
             const uint32_t off = (ks >> 2) * tc5::kAtom + (ks & 3) * 32;
-            pkv::umma_f16(t_o, pkv::umma_desc_k_sw128(sPh + off), pkv::umma_desc_k_sw128(sVt + off), kIdesc, ks > 0);
+            const uint64_t vdesc = pkv::umma_desc_mn_sw128(sV + ks * 2048, tc5::kAtom, 1024);
+            pkv::umma_f16(t_o, pkv::umma_desc_k_sw128(sPh + off), vdesc, kIdescPV, ks > 0);
         }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < groups; ++ks) {
             const uint32_t off = (ks >> 2) * tc5::kAtom + (ks & 3) * 32;
-            pkv::umma_f16(t_o, pkv::umma_desc_k_sw128(sPl + off), pkv::umma_desc_k_sw128(sVt + off), kIdesc, true);
+            const uint64_t vdesc = pkv::umma_desc_mn_sw128(sV + ks * 2048, tc5::kAtom, 1024);
+            pkv::umma_f16(t_o, pkv::umma_desc_k_sw128(sPl + off), vdesc, kIdescPV, true);
         }
         pkv::umma_commit(mma_bar);
     }
     if (ok) {
         ok = pkv::mbar_wait_bounded(mma_bar, 1);
-        if (!ok && (tid & 31) == 0) pkv::record_error(&g_prefix_error, PKV_DEV_WAIT_TIMEOUT);
+        if (!ok && lane == 0) pkv::record_error(&g_prefix_error, PKV_DEV_WAIT_TIMEOUT);
     }
     ok = __syncthreads_and(ok);
     pkv::tmem_fence_after_sync();
     if (ok) {
-        // partial slot `chunk` of this thread's row: normalised o, m in natural-log units, l
-        const int gr = row0 + tid;
-        const int64_t prow =
-            gr < rows ? (static_cast<int64_t>(gr / G) * Hq + kvh * G + gr % G) * P.max_partitions + chunk : 0;
+        // partial slot `chunk` of every row: normalised o, m in natural-log units, l.  Each thread's 64
+        // dims go through the free operand tiles (rows padded to 528 B), then every store instruction
+        // writes one 512-byte row of o_part contiguously.
+        constexpr int kRowPad = kD * 4 + 16;
         const float inv = 1.f / l;
-        uint32_t r[32];
+        pkv::tmem_ld32(t_o + lane_base + c_begin, r[0]);
+        pkv::tmem_ld32(t_o + lane_base + c_begin + 32, r[1]);
 #pragma unroll
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-            pkv::tmem_ld32(t_o + lane_base + c0, r);
-            if (gr < rows) {
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(P.o_part + prow * kD + c0 + j) =
-                        make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
-                                    __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-            }
-        }
-        if (gr < rows) {
+            for (int j = 0; j < 32; j += 4)
+                sts128(base + row * kRowPad + (c_begin + 32 * h + j) * 4,
+                       make_uint4(__float_as_uint(__uint_as_float(r[h][j]) * inv),
+                                  __float_as_uint(__uint_as_float(r[h][j + 1]) * inv),
+                                  __float_as_uint(__uint_as_float(r[h][j + 2]) * inv),
+                                  __float_as_uint(__uint_as_float(r[h][j + 3]) * inv)));
+        const int gr = row0 + row;
+        if (half == 0 && gr < rows) {
+            const int64_t prow = (static_cast<int64_t>(gr / G) * Hq + kvh * G + gr % G) * P.max_partitions + chunk;
             P.m_part[prow] = m * kLn2;
             P.l_part[prow] = l;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+#pragma unroll 1
+        for (int i = warp; i < tc5::kRowsT; i += tc5::kThreadsT / 32) {
+            const int gri = row0 + i;
+            if (gri >= rows) break;
+            const int64_t prow = (static_cast<int64_t>(gri / G) * Hq + kvh * G + gri % G) * P.max_partitions + chunk;
+            const uint4 v = pkv::lds128(base + i * (kD * 4 + 16) + lane * 16);
+            *reinterpret_cast<uint4 *>(P.o_part + prow * kD + lane * 4) = v;
         }
     }
     pkv::tmem_fence_before_sync();
@@ -616,7 +633,10 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     static_assert(kChunkTok == tc5::kTok && kRows == tc5::kRowsT, "partial slots are 128-token chunks of 128 rows");
     const int64_t cache_rows = num_blocks * num_kv_heads * block_size;
     if (cache_rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
-    if (pkv_internal::encode_fp16_cache_map(&p.tmap_k, k_cache, cache_rows) != PKV_OK) return PKV_ERR_CUDA;
+    if (pkv_internal::encode_fp16_cache_map(&p.tmap_k, k_cache, cache_rows) != PKV_OK ||
+        pkv_internal::encode_fp16_cache_map(&p.tmap_v, v_cache, cache_rows) != PKV_OK ||
+        pkv_internal::encode_q_map(&p.tmap_q, q, num_seqs, num_q_heads, num_q_heads / num_kv_heads) != PKV_OK)
+        return PKV_ERR_CUDA;
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         if (cudaFuncSetAttribute(prefix_kernel_tmem, cudaFuncAttributeMaxDynamicSharedMemorySize, tc5::kSmem) !=
             cudaSuccess)
