@@ -328,6 +328,8 @@ def run_ours(args):
     # default (PKV_DEFAULT_PARTITION)
     part = 512 if (args.workload == "long_context" and nq == 1 and args.kv == "fp16"
                    and not args.separate_append) else 0
+    if args.partition:
+        part = args.partition
     ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev, partition_size=part) if nq == 1 else \
         pkv.make_multi_workspace(B, B * nq, nq, Hq, Hkv, max_ctx_cap, dev)
 
@@ -858,6 +860,8 @@ def main(argv=None):
                          "or int8 keys and values, each with float32 row scales")
     ap.add_argument("--query-len", type=int, default=1,
                     help="new tokens per request per step (>1: append them, then causal multi-token attention)")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="split-context partition in tokens for the fused fp16 step (0: the workload's default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)
@@ -865,6 +869,10 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.query_len > 1 and (args.kv != "fp16" or args.workload == "shared_prefix" or args.separate_append):
         ap.error("--query-len > 1 runs the fp16 multi-token path on mha7b, gqa8b, long_context or tiny")
+    if args.partition and (args.partition % 16 or not 16 <= args.partition <= 4096 or args.kv != "fp16"
+                           or args.query_len > 1 or args.separate_append
+                           or (args.workload == "shared_prefix" and not args.no_cascade)):
+        ap.error("--partition (a multiple of 16 in [16, 4096]) applies to the fused fp16 single-token step")
     if args.query_len > 1 and args.impl == "reference":
         ap.error("the reference arm times single-token steps")
     if args.kv != "fp16" and args.workload == "shared_prefix" and not args.no_cascade:
