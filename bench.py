@@ -333,6 +333,10 @@ def run_ours(args):
     ws = pkv.make_step_workspace(B, Hq, max_ctx_cap, prefix_len, dev, partition_size=part) if nq == 1 else \
         pkv.make_multi_workspace(B, B * nq, nq, Hq, Hkv, max_ctx_cap, dev)
 
+    # Each layer's step reads its own caches, which the kernel before it (the previous layer's step)
+    # never writes, so every step call may stream its cache history while that kernel drains.
+    overlap = not args.no_overlap
+
     def decode(l, c, attention_only=False):
         """One layer of the step: the append is fused into the decode kernel (pkv_decode_step) unless
         --separate-append asks for the two-call path (pkv_append + attention).  attention_only skips a
@@ -350,7 +354,7 @@ def run_ours(args):
                                             ctx_cur, c.scale, workspace=ws)
             else:
                 pkv.decode_step_int8kv(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_codes, c.v_scale,
-                                       block_tables, ctx_cur, c.scale, workspace=ws)
+                                       block_tables, ctx_cur, c.scale, workspace=ws, overlap=overlap)
         elif int8k:
             if args.separate_append:
                 if not attention_only:
@@ -359,7 +363,7 @@ def run_ours(args):
                                            c.scale, workspace=ws)
             else:
                 pkv.decode_step_int8k(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_cache,
-                                      block_tables, ctx_cur, c.scale, workspace=ws)
+                                      block_tables, ctx_cur, c.scale, workspace=ws, overlap=overlap)
         elif args.separate_append:
             if not attention_only:
                 pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
@@ -371,7 +375,7 @@ def run_ours(args):
                                      workspace=ws)
         else:
             pkv.decode_step(out_all[l], c.q, c.k_new, c.v_new, c.k_cache, c.v_cache, block_tables, ctx_cur, c.scale,
-                            prefix_len, ws, partition_size=part)
+                            prefix_len, ws, partition_size=part, overlap=overlap)
 
     prefix_tokens = 1024 if args.workload == "shared_prefix" else 0
     bytes_per_step = [n_layers * decode_bytes(c, Hkv, Hq, D, bs, prefix_tokens, kv=args.kv, q_len=nq)
@@ -621,7 +625,9 @@ def run_ours(args):
                             if nq > 1 else
                             ("pkv_append" + KV_SUFFIX[args.kv] + " + " if args.separate_append
                              else "pkv_decode_step" + KV_SUFFIX[args.kv] + " ")
-                            + ("shared prefix 1024 tokens" if cascade else "")),
+                            + ("shared prefix 1024 tokens" if cascade else "")
+                            + (" with PKV_STEP_OVERLAP (each layer streams its cache history while the previous "
+                               "layer's kernel drains)" if overlap and nq == 1 and not args.separate_append else "")),
         },
         "tokens_per_s": round(B * nq * world / (ms_job * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * gbs / peak, 1),
@@ -862,6 +868,8 @@ def main(argv=None):
                     help="new tokens per request per step (>1: append them, then causal multi-token attention)")
     ap.add_argument("--partition", type=int, default=0,
                     help="split-context partition in tokens for the fused fp16 step (0: the workload's default)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="step calls without PKV_STEP_OVERLAP (no layer streams its cache before the previous drains)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)

@@ -92,6 +92,23 @@ extern "C" {
 #define PKV_MIN_BLOCK_SIZE 16        /* block_size must be a multiple of 16 ... */
 #define PKV_MAX_BLOCK_SIZE 256       /* ... and at most 256 */
 
+/* Flags of the pkv_decode_step* calls.
+ * PKV_STEP_OVERLAP: the call's kernels may start reading this call's block
+ * tables, context lengths and cached K/V rows (every position before each
+ * request's new token; with prefix_len > 0 the shared prefix) while the kernel
+ * issued just before them on `stream` is still running; q, k_new, v_new, the
+ * workspace and out are touched only after that kernel has completed, and the
+ * call's own kernels let the next kernel on the stream start the same way.  Set
+ * it only when that preceding kernel writes neither this call's caches nor its
+ * tables or context lengths: e.g. the previous layer's step (another cache) or
+ * the projection that produced q, k_new and v_new.  Not for two steps in a row
+ * on the same cache, where the second reads the row the first appended.
+ * Source: the library's scheduling (programmatic dependent launch), not the
+ * pages; results are identical with and without it.  Without the flag every
+ * kernel still launches as a programmatic dependent but reads nothing before
+ * the preceding kernel completes. */
+#define PKV_STEP_OVERLAP 1u
+
 typedef struct CUstream_st *pkv_stream_t; /* == cudaStream_t */
 typedef struct pkv_pool pkv_pool;         /* opaque host object */
 
@@ -356,13 +373,14 @@ PKV_API size_t pkv_decode_step_workspace_size(int num_seqs, int num_q_heads, int
  * The append is fused into the decode kernel: the CTA that owns a request's
  * last position writes the row to the cache and uses it directly, so a step
  * is one kernel launch (three with a shared prefix).  Workspace rules as for the
- * matching attention call.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+ * matching attention call.  flags: 0 or PKV_STEP_OVERLAP (other bits are
+ * INVALID_ARG).  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 PKV_API int pkv_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
                             void *k_cache, void *v_cache, const int32_t *block_tables,
                             const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                             int64_t num_blocks, float scale, int prefix_len, void *workspace,
-                            size_t workspace_bytes, pkv_stream_t stream);
+                            size_t workspace_bytes, unsigned flags, pkv_stream_t stream);
 
 /* ---- int8 key cache ------------------------------------------------------
  * Keys stored as int8 codes with one float32 scale per (block, kv head, slot);
@@ -401,13 +419,14 @@ PKV_API int pkv_decode_attention_int8k(void *out, const void *q, const void *k_c
  * written (codes and scale) with its value by the decode kernel itself, then
  * attended.  Same as pkv_append_int8k at positions ctx - 1 followed by
  * pkv_decode_attention_int8k.  No shared-prefix form.  Workspace as
- * pkv_decode_attention_int8k.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+ * pkv_decode_attention_int8k.  flags as pkv_decode_step.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 PKV_API int pkv_decode_step_int8k(void *out, const void *q, const void *k_new, const void *v_new, void *k_codes,
                                   float *k_scale, void *v_cache, const int32_t *block_tables,
                                   const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                   int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
-                                  pkv_stream_t stream);
+                                  unsigned flags, pkv_stream_t stream);
 
 /* ---- int8 keys and values (optional) --------------------------------------
  * Values quantised by the same per-row scheme as the keys: int8 codes
@@ -436,13 +455,14 @@ PKV_API int pkv_decode_attention_int8kv(void *out, const void *q, const void *k_
 
 /* pkv_decode_step over the int8 K + V cache: the new token's key and value rows
  * are quantised and written by the decode kernel, then attended.  Same as
- * pkv_append_int8kv at positions ctx - 1 followed by pkv_decode_attention_int8kv. */
+ * pkv_append_int8kv at positions ctx - 1 followed by pkv_decode_attention_int8kv.
+ * flags as pkv_decode_step. */
 PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const void *k_new, const void *v_new, void *k_codes,
                                    float *k_scale, void *v_codes, float *v_scale, const int32_t *block_tables,
                                    const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                    int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
-                                   pkv_stream_t stream);
+                                   unsigned flags, pkv_stream_t stream);
 
 /* ---- several new tokens per request ----------------------------------------
  * A verified draft (speculative decoding) or a prefill chunk: request b brings
@@ -496,7 +516,7 @@ PKV_API int pkv_decode_step_partition(void *out, const void *q, const void *k_ne
                                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, float scale, int partition_size, void *workspace,
-                                      size_t workspace_bytes, pkv_stream_t stream);
+                                      size_t workspace_bytes, unsigned flags, pkv_stream_t stream);
 
 /* Split-context partial attention.  Source: not the pages, which attend over a
  * whole context in one pass; this is one half of the library's split for long

@@ -23,7 +23,7 @@ import torch
 from . import _lib
 from ._lib import (PKV_MAX_QUERY_LEN, PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
                    PKV_DEV_OK, PKV_DEV_PREFIX_MISMATCH, PKV_DEV_SMEM_MISALIGNED, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION,
-                   PkvError)
+                   PKV_STEP_OVERLAP, PkvError)
 
 __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
@@ -34,7 +34,7 @@ __all__ = [
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
-    "PKV_DEV_SMEM_MISALIGNED",
+    "PKV_DEV_SMEM_MISALIGNED", "PKV_STEP_OVERLAP",
 ]
 
 
@@ -50,6 +50,10 @@ def _stream(device: torch.device, stream):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _flags(overlap: bool) -> int:
+    return _lib.PKV_STEP_OVERLAP if overlap else 0
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim: int, device=None):
@@ -180,10 +184,14 @@ def make_step_workspace(num_seqs: int, num_q_heads: int, max_context: int, prefi
 def decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                 context_lens: torch.Tensor, scale: float, prefix_len: int = 0,
-                workspace: torch.Tensor | None = None, stream=None, partition_size: int = 0) -> torch.Tensor:
+                workspace: torch.Tensor | None = None, stream=None, partition_size: int = 0,
+                overlap: bool = False) -> torch.Tensor:
     """One decode step: write each request's new token [B, Hkv, D] at position context_lens - 1,
     then out = softmax(scale q K^T) V over the whole context (append fused into the decode kernel).
-    partition_size > 0 (prefix_len 0 only) overrides the split-context partition."""
+    partition_size > 0 (prefix_len 0 only) overrides the split-context partition.  overlap=True
+    passes PKV_STEP_OVERLAP: the step's kernels start streaming the cache history while the
+    previous kernel on the stream drains, which that kernel must not write (another layer's step
+    is fine; the previous step on the same cache is not)."""
     nb, hkv, bs, d, b, hq, dev = _decode_inputs(q, k_cache, v_cache, block_tables, context_lens)
     _need(out, "out", torch.float16, 3, dev)
     _need(k_new, "k_new", torch.float16, 3, dev)
@@ -202,13 +210,14 @@ def decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: 
         st = _L().pkv_decode_step_partition(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
                                             k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
                                             context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb,
-                                            float(scale), int(partition_size), ws_ptr, ws_bytes, _stream(dev, stream))
+                                            float(scale), int(partition_size), ws_ptr, ws_bytes, _flags(overlap),
+                                            _stream(dev, stream))
         _lib.check(st, "pkv_decode_step_partition")
         return out
     st = _L().pkv_decode_step(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
                               v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), b,
                               block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), int(prefix_len), ws_ptr,
-                              ws_bytes, _stream(dev, stream))
+                              ws_bytes, _flags(overlap), _stream(dev, stream))
     _lib.check(st, "pkv_decode_step")
     return out
 
@@ -376,8 +385,9 @@ def decode_attention_int8k(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Te
 def decode_step_int8k(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       k_codes: torch.Tensor, k_scale: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                       context_lens: torch.Tensor, scale: float, workspace: torch.Tensor | None = None,
-                      stream=None) -> torch.Tensor:
-    """decode_step over the int8-key cache: quantise + write the new token at ctx - 1, then attend."""
+                      stream=None, overlap: bool = False) -> torch.Tensor:
+    """decode_step over the int8-key cache: quantise + write the new token at ctx - 1, then attend.
+    overlap as decode_step's."""
     nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes = _int8k_decode_inputs(q, k_codes, k_scale, v_cache, block_tables,
                                                                         context_lens, out, workspace)
     _need(k_new, "k_new", torch.float16, 3, dev)
@@ -387,7 +397,7 @@ def decode_step_int8k(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v
     st = _L().pkv_decode_step_int8k(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
                                     k_codes.data_ptr(), k_scale.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
                                     context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb, float(scale),
-                                    ws_ptr, ws_bytes, _stream(dev, stream))
+                                    ws_ptr, ws_bytes, _flags(overlap), _stream(dev, stream))
     _lib.check(st, "pkv_decode_step_int8k")
     return out
 
@@ -461,8 +471,8 @@ def decode_attention_int8kv(out, q, k_codes, k_scale, v_codes, v_scale, block_ta
 
 
 def decode_step_int8kv(out, q, k_new, v_new, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens,
-                       scale: float, workspace=None, stream=None) -> torch.Tensor:
-    """decode_step over the int8 K + V cache."""
+                       scale: float, workspace=None, stream=None, overlap: bool = False) -> torch.Tensor:
+    """decode_step over the int8 K + V cache; overlap as decode_step's."""
     nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes = _int8kv_inputs(q, k_codes, k_scale, v_codes, v_scale, block_tables,
                                                                   context_lens, out, workspace)
     _need(k_new, "k_new", torch.float16, 3, dev)
@@ -472,7 +482,7 @@ def decode_step_int8kv(out, q, k_new, v_new, k_codes, k_scale, v_codes, v_scale,
     st = _L().pkv_decode_step_int8kv(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
                                      k_codes.data_ptr(), k_scale.data_ptr(), v_codes.data_ptr(), v_scale.data_ptr(),
                                      block_tables.data_ptr(), context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv,
-                                     d, bs, nb, float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
+                                     d, bs, nb, float(scale), ws_ptr, ws_bytes, _flags(overlap), _stream(dev, stream))
     _lib.check(st, "pkv_decode_step_int8kv")
     return out
 

@@ -11,8 +11,8 @@ import os
 
 from .build import LIB_PATH
 
-c_int, c_int64, c_size_t, c_float, c_void_p, c_uint64 = (
-    ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p, ctypes.c_uint64)
+c_int, c_int64, c_size_t, c_float, c_void_p, c_uint64, c_uint = (
+    ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint)
 c_i32p = ctypes.POINTER(ctypes.c_int32)
 c_i64p = ctypes.POINTER(ctypes.c_int64)
 
@@ -36,6 +36,7 @@ PKV_DEV_SMEM_MISALIGNED = 6
 PKV_HEAD_DIM = 128
 PKV_DEFAULT_PARTITION = 1024
 PKV_MAX_PARTITION = 4096
+PKV_STEP_OVERLAP = 1
 PKV_MAX_QUERY_LEN = 1024
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -60,9 +61,9 @@ SIGNATURES = {
     "pkv_decode_attention_int8k": (c_int, [c_void_p] * 7 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
                                                                            c_void_p]),
     "pkv_decode_step_int8k": (c_int, [c_void_p] * 9 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
-                                                                      c_void_p]),
+                                                                      c_uint, c_void_p]),
     "pkv_decode_step_partition": (c_int, [c_void_p] * 8 + [c_int] * 6 + [c_int64, c_float, c_int, c_void_p, c_size_t,
-                                                                         c_void_p]),
+                                                                         c_uint, c_void_p]),
     "pkv_decode_multi_workspace_size": (c_size_t, [c_int] * 7),
     "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 8 + [c_int64, c_float, c_void_p, c_size_t,
                                                                            c_void_p]),
@@ -73,7 +74,7 @@ SIGNATURES = {
     "pkv_decode_attention_int8kv": (c_int, [c_void_p] * 8 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
                                                                             c_void_p]),
     "pkv_decode_step_int8kv": (c_int, [c_void_p] * 10 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
-                                                                        c_void_p]),
+                                                                        c_uint, c_void_p]),
     "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
     "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
@@ -91,7 +92,7 @@ SIGNATURES = {
     "pkv_decode_step_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "pkv_decode_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float, c_int, c_void_p,
-                                c_size_t, c_void_p]),
+                                c_size_t, c_uint, c_void_p]),
     "pkv_decode_partition": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_float,
                                      c_int, c_int, c_void_p]),

@@ -79,6 +79,23 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
 
     extern __shared__ __align__(1024) unsigned char smem[];
 
+    // Launched as a programmatic dependent of the kernel before it on the stream.  The suffix pass
+    // after a shared-prefix kernel reads nothing that kernel writes until its merge.  Otherwise the
+    // CTA reads nothing before the preceding kernel has completed, except with `overlap`, where it
+    // first stages its cache history (tables, context lengths, K/V tiles: what the caller states the
+    // preceding kernel does not write) and waits just before it touches q, the new token's rows or
+    // any output.  Once past that point, the kernel after this one may start launching: it too
+    // touches nothing written here before this grid completes.
+    const bool suffix_pass = P.slot_offset > 0;
+    const bool overlap = MQ == 0 && P.overlap != 0;  // several tokens per request: never
+    const bool late_q = overlap && !suffix_pass;       // q read after the wait
+    auto wait_preceding = [suffix_pass]() {
+        if (suffix_pass) return;
+        pkv::pdl_wait_primary();
+        pkv::pdl_launch_dependents();
+    };
+    if (!overlap) wait_preceding();
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_rg = MQ ? P.n_row_groups : 1;
@@ -115,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                            : 0;
     }
     Engine eng;
-    eng.init(P, b, kvh, lane);
+    if (!late_q) eng.init(P, b, kvh, lane);
     int ctx = __ldg(P.context_lens + b);
     if (ctx > cap) {
         if (part == 0 && kvh == 0 && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
@@ -143,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
 
     if (ctx == 0) {  // empty request: zero output (or an empty partial)
         if (part != 0) return;
+        if (overlap) wait_preceding();
         for (int i = threadIdx.x; i < G * kD; i += kThreads) {
             const int hq = kvh * G + i / kD, d = i % kD;
             const int64_t row = static_cast<int64_t>(b) * Hq + hq;
@@ -306,6 +324,11 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     }
 
     static_assert(kWarps * NC * (kD + 2) * 4 <= L::stage_bytes, "combine area must fit the stages");
+
+    if (late_q) {  // the history is in flight: now q and the new rows of the preceding kernel
+        wait_preceding();
+        eng.init(P, b, kvh, lane);
+    }
 
     // ---- fused append: the CTA holding the request's last position writes the new token's K/V
     // row for its kv head into the cache (lanes 0-15: K, 16-31: V of warp own_warp) and patches the
@@ -562,6 +585,7 @@ template <int G>
 __global__ void __launch_bounds__(kThreads) merge_groups_kernel(const __grid_constant__ DecodeParams P) {
     __shared__ __align__(16) unsigned char smem[kMergeStageBytes];
     pkv::pdl_wait_primary();
+    pkv::pdl_launch_dependents();  // the next step's first kernel touches nothing written here early
     const int kvh = blockIdx.x, b = blockIdx.y;
     // the suffix pass's partition count for this request (same clamps)
     const int cap = P.max_blocks_per_seq * P.block_size;
@@ -723,12 +747,9 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
     const int64_t gx = static_cast<int64_t>(grid_parts > 0 ? grid_parts : p.max_partitions) * (MQ ? p.n_row_groups : 1);
     if (gx > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
     const dim3 grid(static_cast<unsigned>(gx), p.num_kv_heads, num_seqs);
-    if (p.slot_offset == 0) {
-        kernel<<<grid, kThreads, smem, stream>>>(p);
-        return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
-    }
-    // Suffix pass after the shared-prefix kernel: launched as a programmatic dependent so it
-    // streams the suffixes while the prefix kernel runs; only its merges wait for the prefix.
+    // Always a programmatic dependent of the preceding kernel: its CTAs may become resident while
+    // that kernel drains (the kernel waits, see above).  The suffix pass after the shared-prefix
+    // kernel streams the suffixes while the prefix kernel runs; only its merges wait for the prefix.
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -865,7 +886,9 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
                           int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, const void *k_new, const void *v_new, void *workspace,
                           size_t workspace_bytes, pkv_stream_t stream, const float *k_scale = nullptr,
-                          int partition_size = PKV_DEFAULT_PARTITION, const float *v_scale = nullptr) {
+                          int partition_size = PKV_DEFAULT_PARTITION, const float *v_scale = nullptr,
+                          unsigned flags = 0) {
+    if (flags & ~PKV_STEP_OVERLAP) return PKV_ERR_INVALID_ARG;
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
@@ -904,6 +927,7 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     p.k_scale_w = const_cast<float *>(k_scale);
     p.v_scale = v_scale;
     p.v_scale_w = const_cast<float *>(v_scale);
+    p.overlap = (flags & PKV_STEP_OVERLAP) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
 
@@ -943,17 +967,17 @@ extern "C" PKV_API int pkv_decode_step(void *out, const void *q, const void *k_n
                                        const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
                                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                        int64_t num_blocks, float scale, int prefix_len, void *workspace,
-                                       size_t workspace_bytes, pkv_stream_t stream) {
-    if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+                                       size_t workspace_bytes, unsigned flags, pkv_stream_t stream) {
+    if (!k_new || !v_new || (flags & ~PKV_STEP_OVERLAP)) return PKV_ERR_INVALID_ARG;
     if (prefix_len > 0)
         return pkv_internal::shared_prefix_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                                   max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
                                                   num_blocks, scale, prefix_len, k_new, v_new, workspace,
-                                                  workspace_bytes, stream);
+                                                  workspace_bytes, stream, (flags & PKV_STEP_OVERLAP) != 0);
     if (prefix_len < 0) return PKV_ERR_INVALID_ARG;
     return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
-                                 workspace, workspace_bytes, stream);
+                                 workspace, workspace_bytes, stream, nullptr, PKV_DEFAULT_PARTITION, nullptr, flags);
 }
 
 extern "C" PKV_API int pkv_decode_step_partition(void *out, const void *q, const void *k_new, const void *v_new,
@@ -961,12 +985,13 @@ extern "C" PKV_API int pkv_decode_step_partition(void *out, const void *q, const
                                                  const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
                                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                                  int64_t num_blocks, float scale, int partition_size,
-                                                 void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+                                                 void *workspace, size_t workspace_bytes, unsigned flags,
+                                                 pkv_stream_t stream) {
     if (!k_new || !v_new || partition_size < 0) return PKV_ERR_INVALID_ARG;
     return decode_attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
                                  workspace, workspace_bytes, stream, nullptr,
-                                 partition_size > 0 ? partition_size : PKV_DEFAULT_PARTITION);
+                                 partition_size > 0 ? partition_size : PKV_DEFAULT_PARTITION, nullptr, flags);
 }
 
 // ------------------------------------------------------------------ int8 key cache
@@ -988,11 +1013,11 @@ extern "C" PKV_API int pkv_decode_step_int8k(void *out, const void *q, const voi
                                              const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                                              int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
                                              int block_size, int64_t num_blocks, float scale, void *workspace,
-                                             size_t workspace_bytes, pkv_stream_t stream) {
+                                             size_t workspace_bytes, unsigned flags, pkv_stream_t stream) {
     if (!k_new || !v_new || !k_scale) return PKV_ERR_INVALID_ARG;
     return decode_attention_impl(out, q, k_codes, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
-                                 workspace, workspace_bytes, stream, k_scale);
+                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, nullptr, flags);
 }
 
 // ------------------------------------------------------------------ several new tokens per request
@@ -1096,11 +1121,12 @@ extern "C" PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const vo
                                               const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                                               int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
                                               int head_dim, int block_size, int64_t num_blocks, float scale,
-                                              void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+                                              void *workspace, size_t workspace_bytes, unsigned flags,
+                                              pkv_stream_t stream) {
     if (!k_new || !v_new || !k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
     return decode_attention_impl(out, q, k_codes, v_codes, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
-                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale);
+                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale, flags);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

@@ -115,6 +115,7 @@ struct DecodeParams {
     float *k_scale_w;         // writable view of k_scale for the fused append
     const float *v_scale;     // int8 values too: float32 scale per (block, kv head, slot); null for fp16 values
     float *v_scale_w;
+    int overlap;              // 1: stream the cache history before the preceding kernel completes
     CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
     CUtensorMap tmap_v;       //   16 x 64 boxes, 128-byte swizzle (int8 keys: 16 x 128-byte boxes)
 };

@@ -53,6 +53,6 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                          int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int64_t num_blocks, float scale, int prefix_len, const void *k_new, const void *v_new,
-                         void *workspace, size_t workspace_bytes, void *stream);
+                         void *workspace, size_t workspace_bytes, void *stream, bool overlap = false);
 
 }  // namespace pkv_internal

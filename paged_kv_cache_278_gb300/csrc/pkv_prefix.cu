@@ -86,6 +86,7 @@ struct PrefixParams {
     int max_partitions;
     int64_t num_blocks;
     float q_scale;  // scale * log2(e)
+    int overlap;    // 1: stage the prefix's K/V before the preceding kernel completes
     CUtensorMap tmap_k;  // tensor-memory kernel: the K and V caches as [NB*Hkv*bs][128] fp16, 16 x 64 boxes,
     CUtensorMap tmap_v;  //   128-byte swizzle
     CUtensorMap tmap_q;  // tensor-memory kernel: q as [B][Hq][128] fp16, (64, G, 128 / G) boxes, 128-byte swizzle
@@ -116,7 +117,15 @@ __global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams
     __half *sK = reinterpret_cast<__half *>(smem);      // [kChunkTok][kPad]
     __half *sV = sK + kChunkTok * kPad;                   // [kChunkTok][kPad]
     __half *sQ = sV + kChunkTok * kPad;                   // [kRows][kPad]
-    pkv::pdl_launch_dependents();  // the suffix pass may start streaming right away
+    // A programmatic dependent of the kernel before it on the stream: nothing is read before that
+    // kernel completes, except with `overlap`, where the prefix's block ids and K/V (which the
+    // caller states that kernel does not write) are staged first.  Past the wait the suffix pass
+    // may launch and stream the suffixes alongside.
+    auto wait_preceding = []() {
+        pkv::pdl_wait_primary();
+        pkv::pdl_launch_dependents();
+    };
+    if (!P.overlap) wait_preceding();
     const int chunk = blockIdx.x, kvh = blockIdx.y, rtile = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hq = P.num_q_heads, Hkv = P.num_kv_heads, G = Hq / Hkv, bs = P.block_size;
@@ -138,17 +147,20 @@ __global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams
         }
         s_ids[threadIdx.x] = id;
     }
-    for (int i = threadIdx.x; i < kRows * (kD / 8); i += kThreads) {
-        const int r = i / (kD / 8), piece = i % (kD / 8);
-        const int gr = row0 + r;
-        __half *dst = sQ + r * kPad + piece * 8;
-        if (gr < rows) {
-            const int b = gr / G, hh = gr % G;
-            cp_async16(dst, P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD + piece * 8);
-        } else {
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    auto stage_q = [&]() {
+        for (int i = threadIdx.x; i < kRows * (kD / 8); i += kThreads) {
+            const int r = i / (kD / 8), piece = i % (kD / 8);
+            const int gr = row0 + r;
+            __half *dst = sQ + r * kPad + piece * 8;
+            if (gr < rows) {
+                const int b = gr / G, hh = gr % G;
+                cp_async16(dst, P.q + (static_cast<int64_t>(b) * Hq + kvh * G + hh) * kD + piece * 8);
+            } else {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+            }
         }
-    }
+    };
+    if (!P.overlap) stage_q();
     __syncthreads();  // s_ids
     for (int i = threadIdx.x; i < kChunkTok * (kD / 8); i += kThreads) {
         const int t = i / (kD / 8), piece = i % (kD / 8);
@@ -164,6 +176,10 @@ __global__ void __maxnreg__(PKV_PREFIX_MAXNREG) prefix_kernel(const PrefixParams
             *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
         }
+    }
+    if (P.overlap) {  // the prefix is in flight: now q, written by the preceding kernel
+        wait_preceding();
+        stage_q();
     }
     cp_async_wait_all();
     __syncthreads();
@@ -572,7 +588,7 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                          int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int64_t num_blocks, float scale, int prefix_len, const void *k_new, const void *v_new,
-                         void *workspace, size_t workspace_bytes, void *stream) {
+                         void *workspace, size_t workspace_bytes, void *stream, bool overlap) {
     int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
@@ -656,8 +672,18 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
             return PKV_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const dim3 grid(L.n_pre, num_kv_heads, (rows + kRows - 1) / kRows);
-    prefix_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    p.overlap = overlap ? 1 : 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(L.n_pre, num_kv_heads, (rows + kRows - 1) / kRows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, prefix_kernel, p) != cudaSuccess) return PKV_ERR_CUDA;
 #endif
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
 

@@ -60,7 +60,7 @@ def _ctype_for(param: str):
         return "pointer"
     base = decl.rsplit(" ", 1)[0].replace("const ", "")
     return {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "uint32_t": ctypes.c_uint32, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
-            "uint64_t": ctypes.c_uint64, "pkv_stream_t": "pointer"}[base]
+            "uint64_t": ctypes.c_uint64, "unsigned": ctypes.c_uint, "pkv_stream_t": "pointer"}[base]
 
 
 def test_binding_signatures_match_the_header(lib):
@@ -140,7 +140,7 @@ def test_int8k_multi_copy_invalid_arguments(lib):
                                           null) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_decode_attention_int8k(p, p, p, bad, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
                                           null) == _lib.PKV_ERR_INVALID_ARG
-    assert lib.pkv_decode_step_int8k(p, p, null, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+    assert lib.pkv_decode_step_int8k(p, p, null, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 0,
                                      null) == _lib.PKV_ERR_INVALID_ARG
     # int8 keys and values: null value scales, misaligned value scales, null value codes, head_dim 64
     assert lib.pkv_append_int8kv(p, p, p, null, p, p, p, 1, 1, 128, 16, 4, null) == _lib.PKV_ERR_INVALID_ARG
@@ -151,7 +151,7 @@ def test_int8k_multi_copy_invalid_arguments(lib):
                                            null) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_decode_attention_int8kv(p, p, p, p, null, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
                                            null) == _lib.PKV_ERR_INVALID_ARG
-    assert lib.pkv_decode_step_int8kv(p, p, p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+    assert lib.pkv_decode_step_int8kv(p, p, p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 0,
                                       null) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_append_int8kv(p, p, p, p, null, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
     # several tokens per request: null query_start, query length beyond the limit, no workspace
@@ -192,12 +192,31 @@ def test_noalloc_validates_before_any_cuda_call(lib):
 def test_step_partition_arguments(lib):
     null = None
     p = ctypes.c_void_p(16)
-    args = lambda part: (p, p, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, part, null, 0, null)
+    args = lambda part, flags=0: (p, p, p, p, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, part, null, 0, flags, null)
     assert lib.pkv_decode_step_partition(*args(-16)) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_decode_step_partition(*args(24)) == _lib.PKV_ERR_UNSUPPORTED       # not a multiple of 16
     assert lib.pkv_decode_step_partition(*args(_lib.PKV_MAX_PARTITION + 16)) == _lib.PKV_ERR_UNSUPPORTED
     no_new = (p, p, null, p) + args(512)[4:]
     assert lib.pkv_decode_step_partition(*no_new) == _lib.PKV_ERR_INVALID_ARG
+    # flags: bits other than PKV_STEP_OVERLAP are refused before any CUDA call
+    assert lib.pkv_decode_step_partition(*args(512, 2)) == _lib.PKV_ERR_INVALID_ARG
+
+
+def test_step_flags(lib):
+    null = None
+    p = ctypes.c_void_p(16)
+    step = lambda flags, prefix=0, b=1: lib.pkv_decode_step(p, p, p, p, p, p, p, p, b, 4, 1, 1, 128, 16, 4, 1.0,
+                                                            prefix, null, 0, flags, null)
+    assert step(4) == _lib.PKV_ERR_INVALID_ARG
+    assert step(0x80000000) == _lib.PKV_ERR_INVALID_ARG
+    assert step(4, prefix=16) == _lib.PKV_ERR_INVALID_ARG
+    # a valid flag on an empty batch: nothing to launch
+    assert step(_lib.PKV_STEP_OVERLAP, b=0) == _lib.PKV_OK
+    assert step(0, b=0) == _lib.PKV_OK
+    assert lib.pkv_decode_step_int8k(p, p, p, p, p, p, p, p, p, 0, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 8,
+                                     null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_int8kv(p, p, p, p, p, p, p, p, p, p, 0, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 8,
+                                      null) == _lib.PKV_ERR_INVALID_ARG
 
 
 def test_multi_workspace_size(lib):
