@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         }
     }
 
-    static_assert(kWarps * NC * (kD + 2) * 4 <= L::stage_bytes, "combine area must fit the stages");
+    static_assert((kWarps * NC * (kD + 3) + 2 * NC) * 4 <= L::stage_bytes, "combine area must fit the stages");
 
     if (late_q) {  // the history is in flight: now q and the new rows of the preceding kernel
         wait_preceding();
@@ -521,25 +521,40 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][NC][kD]
     float *c_m = c_acc + kWarps * NC * kD;                           // [kWarps][NC]
     float *c_l = c_m + kWarps * NC;                                  // [kWarps][NC]
+    float *c_f = c_l + kWarps * NC;                                  // [kWarps][NC] weight of each warp
+    float *c_row = c_f + kWarps * NC;                                // [2][NC] row max, row sum
     eng.finish(warp, lane, c_acc, c_m, c_l);
     __syncthreads();
-    const TokenRows<G, NC> token_rows{qs_b, q_len, rg, Hq, kvh};
-#pragma unroll 1
-    for (int idx = threadIdx.x; idx < NC * kD; idx += kThreads) {
-        const int hh = idx / kD, d = idx % kD;
-        if (MQ && !token_rows.live(hh)) continue;
+    // Per row, once: the max over the warps, each warp's weight 2^(m_w - M) (0 for a warp without
+    // chunks; with causal masking a column can have seen no token at all) and the weighted sum of l.
+    // The element pass below then has no dependent chain longer than the four warps' FMAs, so its
+    // iterations overlap (one row after another, it cost ~0.35 us per row).
+    if (threadIdx.x < NC) {
+        const int hh = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, c_m[w * NC + hh]);
-        float L = 0.f, O = 0.f;
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float cm = c_m[w * NC + hh];
-            // 0 for warps without chunks; with causal masking a column can have seen no token at all
             const float f = (MQ && cm == -INFINITY) ? 0.f : exp2f(cm - M);
+            c_f[w * NC + hh] = f;
             L = fmaf(c_l[w * NC + hh], f, L);
-            O = fmaf(c_acc[(w * NC + hh) * kD + d], f, O);
         }
+        c_row[hh] = M;
+        c_row[NC + hh] = L;
+    }
+    __syncthreads();
+    const TokenRows<G, NC> token_rows{qs_b, q_len, rg, Hq, kvh};
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < NC * kD; idx += kThreads) {
+        const int hh = idx / kD, d = idx % kD;
+        if (MQ && !token_rows.live(hh)) continue;
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) O = fmaf(c_acc[(w * NC + hh) * kD + d], c_f[w * NC + hh], O);
+        const float L = c_row[NC + hh];
         const int64_t row = MQ ? token_rows.row(hh) : static_cast<int64_t>(b) * Hq + kvh * G + hh;
         const float o = (MQ && L == 0.f) ? 0.f : O / L;
         if (direct) {
@@ -548,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
             const int64_t prow = row * P.max_partitions + P.slot_offset + part;
             P.o_part[prow * kD + d] = o;
             if (d == 0) {
-                P.m_part[prow] = M * kLn2;
+                P.m_part[prow] = c_row[hh] * kLn2;
                 P.l_part[prow] = L;
             }
         }

@@ -255,6 +255,15 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
     return old;
 }
 
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz.f32: one instruction;
+// subnormal results flush to zero).  For softmax weights in [0, 1] whose products are split into
+// fp16 hi + lo parts; the attention results it feeds are checked against the float64 oracle.
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start launching now, and
 // (in that kernel) wait until the preceding grid has completed and its writes are visible.
 // Both are no-ops when the launch carries no programmatic dependency.

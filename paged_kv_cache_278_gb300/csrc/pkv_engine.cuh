@@ -994,7 +994,7 @@ struct TcEngineR16 {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int i = e >> 1;
-                p[j][e] = s[j][e] == -INFINITY ? 0.f : exp2f(s[j][e] - m_ref[i]);
+                p[j][e] = s[j][e] == -INFINITY ? 0.f : pkv::exp2_approx(s[j][e] - m_ref[i]);
                 l_part[i] += p[j][e];
             }
         // A fragments of P (rows g / g + 8 x tokens 2t, 2t + 1 / + 8), hi + lo parts
