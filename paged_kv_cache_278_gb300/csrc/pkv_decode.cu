@@ -232,13 +232,17 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     const float *ksc = P.k_scale;
     const float *vsc = P.v_scale;
     const int hkv = P.num_kv_heads;
+    // Logical block of a token: a shift for power-of-two block sizes (a uniform branch), so the
+    // per-chunk copy issue carries no integer division.
+    const int bs_shift = (bs & (bs - 1)) == 0 ? __ffs(bs) - 1 : -1;
+    auto block_of = [bs, bs_shift](int tok) { return bs_shift >= 0 ? tok >> bs_shift : tok / bs; };
     // parts: 1 = K (with the int8 keys' scales), 2 = V, 3 = both.  Without split K/V both land on
     // one barrier with one expect_tx for their sum.
     auto issue_from = [=](int i, int64_t phys, int parts) {
         const int cidx = warp + i * kWarps;
         const int tok0 = start + cidx * kChunk;
         const int valid = min(kChunk, n_tok - cidx * kChunk);
-        const int lb = tok0 / bs;
+        const int lb = block_of(tok0);
         const int off = tok0 - lb * bs;
         const int64_t byte_off = phys * block_stride + kvh * head_stride + static_cast<int64_t>(off) * kRowBytes;
         const uint32_t bytes = static_cast<uint32_t>(valid) * kRowBytes;
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
 
     auto issue = [=](int i, int parts) {
         const int tok0 = start + (warp + i * kWarps) * kChunk;
-        issue_from(i, s_table[tok0 / bs - lb0], parts);
+        issue_from(i, s_table[block_of(tok0) - lb0], parts);
     };
 
     // Start-up: each warp reads the block ids of its first chunks straight from the table and
@@ -547,21 +551,36 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     }
     __syncthreads();
     const TokenRows<G, NC> token_rows{qs_b, q_len, rg, Hq, kvh};
-#pragma unroll 4
-    for (int idx = threadIdx.x; idx < NC * kD; idx += kThreads) {
-        const int hh = idx / kD, d = idx % kD;
+    // Four consecutive dims per thread and iteration (16-byte shared loads and global stores):
+    // with the SM's other CTAs streaming, the pass's cost is its instruction count.
+    constexpr int kQuads = kD / 4;
+    constexpr int kUnroll = MQ ? 1 : 4;  // the 16-row engine's kernel has no registers to spare
+#pragma unroll kUnroll
+    for (int idx = threadIdx.x; idx < NC * kQuads; idx += kThreads) {
+        const int hh = idx / kQuads, d = 4 * (idx % kQuads);
         if (MQ && !token_rows.live(hh)) continue;
-        float O = 0.f;
+        float O[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) O = fmaf(c_acc[(w * NC + hh) * kD + d], c_f[w * NC + hh], O);
+        for (int w = 0; w < kWarps; ++w) {
+            const float4 a = *reinterpret_cast<const float4 *>(c_acc + (w * NC + hh) * kD + d);
+            const float f = c_f[w * NC + hh];
+            O[0] = fmaf(a.x, f, O[0]);
+            O[1] = fmaf(a.y, f, O[1]);
+            O[2] = fmaf(a.z, f, O[2]);
+            O[3] = fmaf(a.w, f, O[3]);
+        }
         const float L = c_row[NC + hh];
         const int64_t row = MQ ? token_rows.row(hh) : static_cast<int64_t>(b) * Hq + kvh * G + hh;
-        const float o = (MQ && L == 0.f) ? 0.f : O / L;
+        float o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = (MQ && L == 0.f) ? 0.f : O[k] / L;
         if (direct) {
-            P.out[row * kD + d] = __float2half_rn(o);
+            const __half2 lo = __floats2half2_rn(o[0], o[1]), hi = __floats2half2_rn(o[2], o[3]);
+            *reinterpret_cast<uint2 *>(P.out + row * kD + d) =
+                make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
         } else {
             const int64_t prow = row * P.max_partitions + P.slot_offset + part;
-            P.o_part[prow * kD + d] = o;
+            *reinterpret_cast<float4 *>(P.o_part + prow * kD + d) = make_float4(o[0], o[1], o[2], o[3]);
             if (d == 0) {
                 P.m_part[prow] = c_row[hh] * kLn2;
                 P.l_part[prow] = L;

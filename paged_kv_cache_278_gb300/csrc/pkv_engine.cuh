@@ -957,14 +957,16 @@ struct TcEngineR16 {
             pkv::mma16816(s[0], qa[ks], b[0], b[1]);
             pkv::mma16816(s[1], qa[ks], b[2], b[3]);
         }
-        // mask (past the chunk's tokens, or after the row's own position) and scale
+        // mask (past the chunk's tokens, or after the row's own position) and scale: token
+        // 8j + 2t + c of the chunk is visible to row i iff 8j + c <= cut[i]
         float cm[2] = {-INFINITY, -INFINITY};
+        const int cut[2] = {min(valid - 1, lim[0] - tok0) - 2 * t, min(valid - 1, lim[1] - tok0) - 2 * t};
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int tk = 8 * j + 2 * t + (e & 1), i = e >> 1;
-                s[j][e] = tk < valid && tok0 + tk <= lim[i] ? s[j][e] * q_scale : -INFINITY;
+                const int i = e >> 1;
+                s[j][e] = 8 * j + (e & 1) <= cut[i] ? s[j][e] * q_scale : -INFINITY;
                 cm[i] = fmaxf(cm[i], s[j][e]);
             }
 #pragma unroll
@@ -988,13 +990,16 @@ struct TcEngineR16 {
                 }
             }
         }
+        // 2^(-inf) = 0 for masked tokens; a row that has seen nothing yet (reference max still
+        // -inf) has only masked tokens, so it subtracts 0 instead
+        const float m_use[2] = {m_ref[0] == -INFINITY ? 0.f : m_ref[0], m_ref[1] == -INFINITY ? 0.f : m_ref[1]};
         float p[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int i = e >> 1;
-                p[j][e] = s[j][e] == -INFINITY ? 0.f : pkv::exp2_approx(s[j][e] - m_ref[i]);
+                p[j][e] = pkv::exp2_approx(s[j][e] - m_use[i]);
                 l_part[i] += p[j][e];
             }
         // A fragments of P (rows g / g + 8 x tokens 2t, 2t + 1 / + 8), hi + lo parts
