@@ -342,10 +342,14 @@ def run_ours(args):
         --separate-append asks for the two-call path (pkv_append + attention).  attention_only skips a
         separate append launch (the kernel-only timing region)."""
         if nq > 1:
-            if not attention_only:
-                pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
-            pkv.decode_attention_multi(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, query_start, nq,
-                                       c.scale, workspace=ws)
+            if args.separate_append:
+                if not attention_only:
+                    pkv.append(c.k_cache, c.v_cache, slot_cur, c.k_new, c.v_new)
+                pkv.decode_attention_multi(out_all[l], c.q, c.k_cache, c.v_cache, block_tables, ctx_cur, query_start,
+                                           nq, c.scale, workspace=ws)
+            else:
+                pkv.decode_step_multi(out_all[l], c.q, c.k_new, c.v_new, c.k_cache, c.v_cache, block_tables, ctx_cur,
+                                      query_start, nq, c.scale, workspace=ws, overlap=overlap)
         elif int8kv:
             if args.separate_append:
                 if not attention_only:
@@ -384,7 +388,7 @@ def run_ours(args):
 
     # per layer: the decode kernel (append and the split's merge fused in), plus the prefix kernel and the
     # merge kernel with the cascade, plus the append kernel on the two-call path
-    launches_per_step = n_layers * (1 + (2 if cascade else 0) + (1 if args.separate_append or nq > 1 else 0))
+    launches_per_step = n_layers * (1 + (2 if cascade else 0) + (1 if args.separate_append else 0))
 
     def step():
         for l, c in enumerate(cases):
@@ -621,13 +625,15 @@ def run_ours(args):
             "l2": "inputs larger than L2: every layer has its own cache (%.0f MB), %.1f GB streamed per step"
                   % (layer_cache_bytes / 1e6, bytes_job / 1e9),
             "timing": "CUDA-graph replay of the whole step" if graph is not None else "eager launches",
-            "decode_call": (f"pkv_append + pkv_decode_attention_multi ({nq} new tokens per request, causal)"
-                            if nq > 1 else
+            "decode_call": ((f"pkv_append + pkv_decode_attention_multi ({nq} new tokens per request, causal)"
+                             if args.separate_append else
+                             f"pkv_decode_step_multi ({nq} new tokens per request appended and attended causally"
+                             f" in one launch)") if nq > 1 else
                             ("pkv_append" + KV_SUFFIX[args.kv] + " + " if args.separate_append
                              else "pkv_decode_step" + KV_SUFFIX[args.kv] + " ")
                             + ("shared prefix 1024 tokens" if cascade else "")
                             + (" with PKV_STEP_OVERLAP (each layer streams its cache history while the previous "
-                               "layer's kernel drains)" if overlap and nq == 1 and not args.separate_append else "")),
+                               "layer's kernel drains)" if overlap and not args.separate_append else "")),
         },
         "tokens_per_s": round(B * nq * world / (ms_job * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * gbs / peak, 1),
@@ -875,8 +881,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.query_len > 1 and (args.kv != "fp16" or args.workload == "shared_prefix" or args.separate_append):
+    if args.query_len > 1 and (args.kv != "fp16" or args.workload == "shared_prefix"):
         ap.error("--query-len > 1 runs the fp16 multi-token path on mha7b, gqa8b, long_context or tiny")
+    if args.query_len > 16 and not args.separate_append:
+        ap.error("the one-launch several-token step takes up to 16 new tokens; use --separate-append beyond")
     if args.partition and (args.partition % 16 or not 16 <= args.partition <= 4096 or args.kv != "fp16"
                            or args.query_len > 1 or args.separate_append
                            or (args.workload == "shared_prefix" and not args.no_cascade)):

@@ -503,6 +503,33 @@ PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_c
                                        int block_size, int64_t num_blocks, float scale, void *workspace,
                                        size_t workspace_bytes, pkv_stream_t stream);
 
+/* Largest max_query_len of pkv_decode_step_multi (the new rows a CTA patches are
+ * staged in its shared memory). */
+#define PKV_MAX_STEP_QUERY_LEN 16
+
+/* One several-token step in one launch: append each request's new tokens in
+ * place, then attend causally over its cache (the append of pkv_decode_step,
+ * "为什么“推理优化”不是锦上添花", sec. 3.1, applied to a verified draft or a
+ * prefill chunk, "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 3.2).
+ *   k_new, v_new : fp16 [total_q][num_kv_heads][head_dim], 16-byte aligned; row
+ *                  query_start[b] + i goes to logical position ctx_b - n_b + i of
+ *                  request b (its slot in block_tables[b]; an invalid block id skips
+ *                  the write and is recorded as PKV_DEV_BAD_BLOCK_ID)
+ *   k_cache, v_cache : written (the new rows) and read.
+ * Same result as pkv_append at those positions followed by
+ * pkv_decode_attention_multi; max_query_len <= PKV_MAX_STEP_QUERY_LEN (else
+ * UNSUPPORTED).  Every CTA whose token range holds new positions patches their
+ * rows into its shared-memory tiles; the CTA of the request's last row group
+ * also writes them to the cache.  flags: 0 or PKV_STEP_OVERLAP (as
+ * pkv_decode_step; the query starts count among what the preceding kernel must
+ * not write).  Other arguments, workspace and errors as pkv_decode_attention_multi. */
+PKV_API int pkv_decode_step_multi(void *out, const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                  void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                                  const int32_t *query_start, int num_seqs, int total_q, int max_query_len,
+                                  int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int64_t num_blocks, float scale, void *workspace,
+                                  size_t workspace_bytes, unsigned flags, pkv_stream_t stream);
+
 /* pkv_decode_step (prefix_len 0) with the split-context partition chosen by the
  * caller instead of PKV_DEFAULT_PARTITION (the split and its log-sum-exp merge
  * are this library's design, exact by the softmax identity noted at

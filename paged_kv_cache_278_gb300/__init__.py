@@ -23,18 +23,18 @@ import torch
 from . import _lib
 from ._lib import (PKV_MAX_QUERY_LEN, PKV_DEFAULT_PARTITION, PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT, PKV_DEV_BAD_SLOT,
                    PKV_DEV_OK, PKV_DEV_PREFIX_MISMATCH, PKV_DEV_SMEM_MISALIGNED, PKV_DEV_WAIT_TIMEOUT, PKV_HEAD_DIM, PKV_MAX_PARTITION,
-                   PKV_STEP_OVERLAP, PkvError)
+                   PKV_STEP_OVERLAP, PKV_MAX_STEP_QUERY_LEN, PkvError)
 
 __all__ = [
     "append", "decode_attention", "decode_partition", "merge", "decode_workspace_size", "make_workspace",
     "decode_attention_shared_prefix", "make_shared_prefix_workspace", "PKV_DEV_PREFIX_MISMATCH",
     "decode_step", "make_step_workspace", "copy_blocks", "append_int8k", "decode_attention_int8k",
-    "decode_step_int8k", "empty_int8k_cache", "decode_attention_multi", "make_multi_workspace",
+    "decode_step_int8k", "empty_int8k_cache", "decode_attention_multi", "decode_step_multi", "make_multi_workspace",
     "copy_blocks_between", "empty_int8kv_cache", "append_int8kv", "decode_attention_int8kv", "decode_step_int8kv",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
-    "PKV_DEV_SMEM_MISALIGNED", "PKV_STEP_OVERLAP",
+    "PKV_DEV_SMEM_MISALIGNED", "PKV_STEP_OVERLAP", "PKV_MAX_STEP_QUERY_LEN",
 ]
 
 
@@ -310,6 +310,44 @@ def decode_attention_multi(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
                                          t, int(max_query_len), block_tables.shape[1], hq, hkv, d, bs, nb,
                                          float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
     _lib.check(st, "pkv_decode_attention_multi")
+    return out
+
+
+def decode_step_multi(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, query_start: torch.Tensor, max_query_len: int, scale: float,
+                      workspace: torch.Tensor | None = None, stream=None, overlap: bool = False) -> torch.Tensor:
+    """One several-token step: write request b's new tokens (k_new/v_new rows query_start[b]..,
+    [total_q, Hkv, D]) at positions context_lens[b] - n_b .., then the causal attention of
+    decode_attention_multi, in one launch; max_query_len <= PKV_MAX_STEP_QUERY_LEN.  overlap as
+    decode_step's."""
+    nb, hkv, bs, d = _cache_shape(k_cache, v_cache)
+    dev = k_cache.device
+    _need(q, "q", torch.float16, 3, dev)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(query_start, "query_start", torch.int32, 1, dev)
+    t, hq, dq = q.shape
+    b = context_lens.shape[0]
+    if dq != d or out.shape != q.shape:
+        raise ValueError("q / out shapes disagree with the cache")
+    if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
+    if block_tables.shape[0] != b or query_start.shape[0] != b + 1:
+        raise ValueError("block_tables [B, ...], context_lens [B] and query_start [B + 1] disagree")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    st = _L().pkv_decode_step_multi(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                    k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                    context_lens.data_ptr(), query_start.data_ptr(), b, t, int(max_query_len),
+                                    block_tables.shape[1], hq, hkv, d, bs, nb, float(scale), ws_ptr, ws_bytes,
+                                    _flags(overlap), _stream(dev, stream))
+    _lib.check(st, "pkv_decode_step_multi")
     return out
 
 

@@ -38,6 +38,7 @@ PKV_DEFAULT_PARTITION = 1024
 PKV_MAX_PARTITION = 4096
 PKV_STEP_OVERLAP = 1
 PKV_MAX_QUERY_LEN = 1024
+PKV_MAX_STEP_QUERY_LEN = 16
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # every symbol include/pkv.h declares: name -> (restype, argtypes)
@@ -67,6 +68,8 @@ SIGNATURES = {
     "pkv_decode_multi_workspace_size": (c_size_t, [c_int] * 7),
     "pkv_decode_attention_multi": (c_int, [c_void_p] * 7 + [c_int] * 8 + [c_int64, c_float, c_void_p, c_size_t,
                                                                            c_void_p]),
+    "pkv_decode_step_multi": (c_int, [c_void_p] * 9 + [c_int] * 8 + [c_int64, c_float, c_void_p, c_size_t, c_uint,
+                                                                      c_void_p]),
     "pkv_pool_swap": (c_int, [c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_i32p, c_i32p]),
     "pkv_copy_blocks_between": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
                                         c_void_p, c_int, c_int, c_int, c_int, c_void_p]),

@@ -65,6 +65,12 @@ template <int MQ>
 constexpr int stages_of() {
     return MQ == 2 ? PKV_DECODE_MQ2_STAGES : kStages;
 }
+// New token rows a CTA of a fused step stages: one; up to 8 with one 8-column tile (then
+// n_b * G <= 8); up to PKV_MAX_STEP_QUERY_LEN with 16 rows.  (Each CTA keeps 3 per SM.)
+template <int MQ>
+constexpr int new_rows_of() {
+    return MQ == 2 ? PKV_MAX_STEP_QUERY_LEN : (MQ ? 8 : 1);
+}
 
 template <int G, int LPT, bool TC, int KQ, int MQ>
 __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
     static_assert(!MQ || (TC && !KQ), "several tokens per request run on the fp16 tensor-core engine");
     constexpr int kStages = stages_of<MQ>();  // this variant's ring depth
-    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, kStages>;
+    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, kStages, new_rows_of<MQ>()>;
     using Engine = EngineFor<G, LPT, TC, KQ, MQ>;
     constexpr int kRow = L::row;
     constexpr int NC = MQ ? 8 * MQ : G;  // packed output columns per CTA
@@ -87,8 +93,8 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     // any output.  Once past that point, the kernel after this one may start launching: it too
     // touches nothing written here before this grid completes.
     const bool suffix_pass = P.slot_offset > 0;
-    const bool overlap = MQ == 0 && P.overlap != 0;  // several tokens per request: never
-    const bool late_q = overlap && !suffix_pass;       // q read after the wait
+    const bool overlap = P.overlap != 0;          // set by the step calls only
+    const bool late_q = overlap && !suffix_pass;  // q read after the wait
     auto wait_preceding = [suffix_pass]() {
         if (suffix_pass) return;
         pkv::pdl_wait_primary();
@@ -139,13 +145,14 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         ctx = cap;
     }
     if (ctx < 0) ctx = 0;
+    const int ctx_full = ctx;  // several tokens: before the row group's cut below
     if constexpr (MQ) {
         if (ctx < q_len) {  // the new tokens must already be in the cache
             if (part == 0 && kvh == 0 && rg == 0 && threadIdx.x == 0)
                 pkv::record_error(&g_decode_error, PKV_DEV_BAD_CONTEXT);
             return;
         }
-        eng.bind(P, kvh, lane, rg, qs_b, q_len, ctx);
+        if (!late_q) eng.bind(P, kvh, lane, rg, qs_b, q_len, ctx);
         // keys past the group's last live token are visible to none of its columns
         const int last_tok = min(q_len - 1, (rg * NC + NC - 1) / G);
         ctx = ctx - q_len + last_tok + 1;
@@ -332,6 +339,37 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     if (late_q) {  // the history is in flight: now q and the new rows of the preceding kernel
         wait_preceding();
         eng.init(P, b, kvh, lane);
+        if constexpr (MQ) eng.bind(P, kvh, lane, rg, qs_b, q_len, ctx_full);
+    }
+
+    // ---- fused append of several new tokens per request (pkv_decode_step_multi): positions
+    // ctx_full - q_len .. ctx_full - 1 take rows query_start[b] .. of k_new / v_new.  Every CTA
+    // whose token range holds some of them stages those rows in shared memory and patches them
+    // into its tiles once the chunks have landed (whatever the copies brought); the CTA of the
+    // request's last row group, whose range runs to ctx_full, also writes them to the cache.
+    int new_lo = 0, new_hi = 0;
+    unsigned char *s_new = smem + L::newrow(G);  // [rows][K row | V row] of the new tokens
+    if constexpr (MQ) {
+        if (P.k_new != nullptr) {
+            new_lo = max(start, ctx_full - q_len);
+            new_hi = min(start + n_tok, ctx_full);
+            const bool writer = rg == (q_len * G - 1) / NC;
+            const int64_t t0 = qs_b - (ctx_full - q_len);  // k_new row of position p: t0 + p
+            for (int idx = threadIdx.x; idx < (new_hi - new_lo) * 32; idx += kThreads) {
+                const int p = new_lo + (idx >> 5), piece = idx & 31;
+                const int64_t src = ((t0 + p) * P.num_kv_heads + kvh) * kD + (piece & 15) * 8;
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>((piece < 16 ? P.k_new : P.v_new) + src));
+                *reinterpret_cast<uint4 *>(s_new + (p - new_lo) * 2 * kRowBytes + piece * 16) = v;
+                if (writer) {
+                    const int32_t id = __ldg(P.block_tables + static_cast<int64_t>(b) * P.max_blocks_per_seq + p / bs);
+                    if (id >= 0 && id < P.num_blocks) {  // bad ids: recorded by the table pass
+                        const int64_t grow = (static_cast<int64_t>(id) * P.num_kv_heads + kvh) * bs + p % bs;
+                        *reinterpret_cast<uint4 *>((piece < 16 ? P.k_cache_w : P.v_cache_w) + grow * kD +
+                                                   (piece & 15) * 8) = v;
+                    }
+                }
+            }
+        }
     }
 
     // ---- fused append: the CTA holding the request's last position writes the new token's K/V
@@ -339,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     // row in its shared-memory tile once the chunk has landed, so the attention sees the new token
     // whatever the order of the global write and the bulk copy.
     const int new_pos = ctx - 1;
-    const bool appends = P.k_new != nullptr && part == n_parts - 1;
+    const bool appends = !MQ && P.k_new != nullptr && part == n_parts - 1;
     const int own_chunk = appends ? (new_pos - start) / kChunk : -1;
     const int own_warp = own_chunk % kWarps;
     unsigned char *s_newrow = smem + L::newrow(G);  // [K row | V row] of the new token
@@ -432,6 +470,19 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         const uint32_t s_tile = scale0 + st * L::scale_stride;
         const bool own = cidx == own_chunk;
         const int nr_row = (new_pos - start) % kChunk;
+        // several-token step: rows [r0, r1) of this chunk are new tokens staged in s_new
+        const int tok0c = start + cidx * kChunk;
+        const int r0 = max(new_lo - tok0c, 0), r1 = min(new_hi - tok0c, kChunk);
+        auto patch_new = [&](uint32_t tile, int half) {
+            for (int x = lane; x < (r1 - r0) * 16; x += 32) {
+                const int r = r0 + (x >> 4), pc = x & 15;
+                const uint4 nr =
+                    *reinterpret_cast<const uint4 *>(s_new + (tok0c + r - new_lo) * 2 * kRowBytes + half * kRowBytes + pc * 16);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(tile + TcEngine<4>::swz(r, pc)), "r"(nr.x),
+                             "r"(nr.y), "r"(nr.z), "r"(nr.w)
+                             : "memory");
+            }
+        };
         // the appended token's V row and a ragged tail's V rows, once V has landed
         auto fix_v = [&]() {
             bool touched = false;
@@ -465,6 +516,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                 }
                 touched = true;
             }
+            if (MQ && r1 > r0) {
+                patch_new(v_tile, 1);
+                touched = true;
+            }
             return touched;
         };
         bool touched = false;
@@ -488,6 +543,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                                  : "memory");
                 }
             }
+            touched = true;
+        }
+        if (MQ && r1 > r0) {  // the new tokens' K rows
+            patch_new(k_tile, 0);
             touched = true;
         }
         if (!kSplitKV) touched |= fix_v();
@@ -766,7 +825,10 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
             st = KQ == 2 ? encode_code_map(&p.tmap_v, p.v_cache, rows) : encode_cache_map(&p.tmap_v, p.v_cache, rows);
         if (st != PKV_OK) return st;
     }
-    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, stages_of<MQ>()>;
+    using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, stages_of<MQ>(), new_rows_of<MQ>()>;
+    // three fp16 tensor-core CTAs per SM at the default partition (228 KB; 1 KB static and 1 KB
+    // reserved per CTA)
+    static_assert(!TC || KQ || 3 * (L::total(G, PKV_DEFAULT_PARTITION) + 2048) <= 228 * 1024, "3 CTAs per SM");
     const int smem = L::total(G, p.partition_size);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -1080,20 +1142,24 @@ extern "C" PKV_API size_t pkv_decode_multi_workspace_size(int num_seqs, int tota
            align256(counters * sizeof(int));
 }
 
-extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                                  const int32_t *block_tables, const int32_t *context_lens,
-                                                  const int32_t *query_start, int num_seqs, int total_q,
-                                                  int max_query_len, int max_blocks_per_seq, int num_q_heads,
-                                                  int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                                                  float scale, void *workspace, size_t workspace_bytes,
-                                                  pkv_stream_t stream) {
+namespace {
+// pkv_decode_attention_multi, optionally appending the new tokens first (k_new/v_new non-null:
+// pkv_decode_step_multi, with its flags).
+int decode_multi_impl(void *out, const void *q, const void *k_new, const void *v_new, const void *k_cache,
+                      const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                      const int32_t *query_start, int num_seqs, int total_q, int max_query_len, int max_blocks_per_seq,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+                      void *workspace, size_t workspace_bytes, unsigned flags, pkv_stream_t stream) {
+    if (flags & ~PKV_STEP_OVERLAP) return PKV_ERR_INVALID_ARG;
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
     if (!out || !pkv_internal::aligned(out, 8) || !query_start || !pkv_internal::aligned(query_start, 4))
         return PKV_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+    if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
     if (total_q < 0 || max_query_len <= 0) return PKV_ERR_INVALID_ARG;
-    if (max_query_len > PKV_MAX_QUERY_LEN) return PKV_ERR_UNSUPPORTED;
+    if (max_query_len > (k_new ? PKV_MAX_STEP_QUERY_LEN : PKV_MAX_QUERY_LEN)) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0 || total_q == 0) return PKV_OK;
     const int group = num_q_heads / num_kv_heads;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
@@ -1120,6 +1186,11 @@ extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, cons
     p.max_query_len = max_query_len;
     p.n_row_groups = row_groups(max_query_len, group);
     p.mq_tiles = mq_tiles(max_query_len, group);
+    p.k_new = static_cast<const __half *>(k_new);
+    p.v_new = static_cast<const __half *>(v_new);
+    p.k_cache_w = static_cast<__half *>(const_cast<void *>(k_cache));
+    p.v_cache_w = static_cast<__half *>(const_cast<void *>(v_cache));
+    p.overlap = (k_new && (flags & PKV_STEP_OVERLAP)) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts > 1) {
         const size_t need = pkv_decode_multi_workspace_size(num_seqs, total_q, max_query_len, num_q_heads,
@@ -1133,6 +1204,32 @@ extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, cons
         p.counters = reinterpret_cast<int *>(ws + counters_offset(rows));
     }
     return dispatch_partition(p, num_seqs, group, s);
+}
+}  // namespace
+
+extern "C" PKV_API int pkv_decode_attention_multi(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                                  const int32_t *block_tables, const int32_t *context_lens,
+                                                  const int32_t *query_start, int num_seqs, int total_q,
+                                                  int max_query_len, int max_blocks_per_seq, int num_q_heads,
+                                                  int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                                  float scale, void *workspace, size_t workspace_bytes,
+                                                  pkv_stream_t stream) {
+    return decode_multi_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, query_start,
+                             num_seqs, total_q, max_query_len, max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                             block_size, num_blocks, scale, workspace, workspace_bytes, 0, stream);
+}
+
+extern "C" PKV_API int pkv_decode_step_multi(void *out, const void *q, const void *k_new, const void *v_new,
+                                             void *k_cache, void *v_cache, const int32_t *block_tables,
+                                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                                             int total_q, int max_query_len, int max_blocks_per_seq, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                             float scale, void *workspace, size_t workspace_bytes, unsigned flags,
+                                             pkv_stream_t stream) {
+    if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+    return decode_multi_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, query_start, num_seqs,
+                             total_q, max_query_len, max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                             block_size, num_blocks, scale, workspace, workspace_bytes, flags, stream);
 }
 
 // ------------------------------------------------------------------ int8 keys and values

@@ -128,8 +128,10 @@ constexpr int kMergeTile = 512;  // partitions whose weights the fused merge sta
 // KQ (int8 keys): the K tile is one 2 KB box of 16 int8 rows in the same swizzle, and each stage
 // also holds the chunk's 16 float32 key scales.
 constexpr int kHalfTile = kChunk * 128;
-// KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values.
-template <bool TC, int KQ = 0, int NT = 1, int NS = kStages>
+// KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values.  NR: new token rows staged for a fused
+// append (one for a single-token step; up to PKV_MAX_STEP_QUERY_LEN for a several-token step).
+// The 16-row engine (NT = 2) keeps P in registers and needs no per-warp weight buffer.
+template <bool TC, int KQ = 0, int NT = 1, int NS = kStages, int NR = 1>
 struct SmemLayout {
     static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
@@ -142,9 +144,11 @@ struct SmemLayout {
     static constexpr int scales = stages + stage_bytes;
     static constexpr int bars = scales + (KQ ? kWarps * NS * scale_stride : 0);
     static constexpr int probs = bars + kWarps * NS * kBarsPerStage * 8;
-    __host__ __device__ static constexpr int probs_per_warp(int g) { return TC ? NT * 2 * 8 * kChunk * 2 : kChunk * g * 4; }
+    __host__ __device__ static constexpr int probs_per_warp(int g) {
+        return TC ? (NT == 2 ? 0 : NT * 2 * 8 * kChunk * 2) : kChunk * g * 4;
+    }
     __host__ __device__ static constexpr int newrow(int g) { return probs + kWarps * probs_per_warp(g); }
-    __host__ __device__ static constexpr int table(int g) { return newrow(g) + 2 * kRowBytes; }
+    __host__ __device__ static constexpr int table(int g) { return newrow(g) + NR * 2 * kRowBytes; }
     __host__ __device__ static constexpr int total(int g, int partition_size) {
         return table(g) + (partition_size / kChunk + 1) * 4;
     }

@@ -217,6 +217,13 @@ def test_step_flags(lib):
                                      null) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_decode_step_int8kv(p, p, p, p, p, p, p, p, p, p, 0, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 8,
                                       null) == _lib.PKV_ERR_INVALID_ARG
+    # several-token step: unknown flags, missing new rows, drafts longer than PKV_MAX_STEP_QUERY_LEN
+    multi = lambda kn, maxq, flags, b=1: lib.pkv_decode_step_multi(p, p, kn, p, p, p, p, p, p, b, 4, maxq, 4, 1, 1,
+                                                                   128, 16, 4, 1.0, null, 0, flags, null)
+    assert multi(p, 4, 2) == _lib.PKV_ERR_INVALID_ARG
+    assert multi(null, 4, 0) == _lib.PKV_ERR_INVALID_ARG
+    assert multi(p, _lib.PKV_MAX_STEP_QUERY_LEN + 1, 0) == _lib.PKV_ERR_UNSUPPORTED
+    assert multi(p, _lib.PKV_MAX_STEP_QUERY_LEN, _lib.PKV_STEP_OVERLAP, b=0) == _lib.PKV_OK
 
 
 def test_multi_workspace_size(lib):
