@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         }
     }
 
-    static_assert((kWarps * NC * (kD + 3) + 2 * NC) * 4 <= L::stage_bytes, "combine area must fit the stages");
+    static_assert((kWarps * NC * (kAccStride + 3) + 2 * NC) * 4 <= L::stage_bytes, "combine area must fit the stages");
 
     if (late_q) {  // the history is in flight: now q and the new rows of the preceding kernel
         wait_preceding();
@@ -581,8 +581,8 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
 
     // ---- merge the 4 warps in shared memory (reusing the stage buffers)
     __syncthreads();
-    float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][NC][kD]
-    float *c_m = c_acc + kWarps * NC * kD;                           // [kWarps][NC]
+    float *c_acc = reinterpret_cast<float *>(smem);                  // [kWarps][NC][kAccStride]
+    float *c_m = c_acc + kWarps * NC * kAccStride;                   // [kWarps][NC]
     float *c_l = c_m + kWarps * NC;                                  // [kWarps][NC]
     float *c_f = c_l + kWarps * NC;                                  // [kWarps][NC] weight of each warp
     float *c_row = c_f + kWarps * NC;                                // [2][NC] row max, row sum
@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         float O[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float4 a = *reinterpret_cast<const float4 *>(c_acc + (w * NC + hh) * kD + d);
+            const float4 a = *reinterpret_cast<const float4 *>(c_acc + (w * NC + hh) * kAccStride + d);
             const float f = c_f[w * NC + hh];
             O[0] = fmaf(a.x, f, O[0]);
             O[1] = fmaf(a.y, f, O[1]);

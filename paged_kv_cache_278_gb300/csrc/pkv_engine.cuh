@@ -128,6 +128,9 @@ constexpr int kMergeTile = 512;  // partitions whose weights the fused merge sta
 // KQ (int8 keys): the K tile is one 2 KB box of 16 int8 rows in the same swizzle, and each stage
 // also holds the chunk's 16 float32 key scales.
 constexpr int kHalfTile = kChunk * 128;
+// Row stride (floats) of the warps' partial results in the combine area: 4 floats of padding so
+// the fragment-ordered stores of eight rows at once spread over all 32 banks.
+constexpr int kAccStride = kD + 4;
 // KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values.  NR: new token rows staged for a fused
 // append (one for a single-token step; up to PKV_MAX_STEP_QUERY_LEN for a several-token step).
 // The 16-row engine (NT = 2) keeps P in registers and needs no per-warp weight buffer.
@@ -543,7 +546,7 @@ struct FmaEngine {
                 for (int e = 0; e < 4; ++e) acc[hh][e] *= f;
                 m = top;
             }
-            *reinterpret_cast<float4 *>(c_acc + (warp * G + hh) * kD + lane * 4) =
+            *reinterpret_cast<float4 *>(c_acc + (warp * G + hh) * kAccStride + lane * 4) =
                 make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
             if (lane == 0) {
                 c_m[warp * G + hh] = m;
@@ -665,8 +668,8 @@ struct TcEngine {
                 o[mt][3] *= a1;
             }
         }
-        float p[4] = {exp2f(s[0] - m_ref[0]), exp2f(s[1] - m_ref[1]), exp2f(s[2] - m_ref[0]),
-                      exp2f(s[3] - m_ref[1])};
+        float p[4] = {pkv::exp2_approx(s[0] - m_ref[0]), pkv::exp2_approx(s[1] - m_ref[1]),
+                      pkv::exp2_approx(s[2] - m_ref[0]), pkv::exp2_approx(s[3] - m_ref[1])};
         if (kAnyMasked) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) p[e] = s[e] == -INFINITY ? 0.f : p[e];
@@ -738,7 +741,7 @@ struct TcEngine {
             for (int e = 0; e < 4; ++e) {
                 const int h = h0 + (e & 1);
                 const int dim = kPermDims ? 16 * g + 2 * mt + (e >> 1) : mt * 16 + g + (e >> 1) * 8;
-                if (h < G) c_acc[(warp * nc + c0 + h) * kD + dim] = o[mt][e] * f[e & 1];
+                if (h < G) c_acc[(warp * nc + c0 + h) * kAccStride + dim] = o[mt][e] * f[e & 1];
             }
         if (g == 0) {
 #pragma unroll
@@ -1045,7 +1048,7 @@ struct TcEngineR16 {
                 m = top[i];
             }
             const int row = g + 8 * i;
-            float *acc = c_acc + (warp * 16 + row) * kD + 2 * t;
+            float *acc = c_acc + (warp * 16 + row) * kAccStride + 2 * t;
 #pragma unroll
             for (int j = 0; j < kD / 8; ++j)
                 *reinterpret_cast<float2 *>(acc + 8 * j) = make_float2(o[j][2 * i] * f, o[j][2 * i + 1] * f);
