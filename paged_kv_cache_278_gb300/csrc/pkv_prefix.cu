@@ -37,14 +37,14 @@ namespace {
 __device__ int g_prefix_error;
 
 constexpr int kD = PKV_HEAD_DIM;       // 128
-// 128-token chunks (one CTA per SM, 104 KB of shared memory) measured 5.5 % faster end to end
-// than 64 (which doubles the CTAs and the prefix slots every merge reads), and 64 than 32.
+// 128-token chunks (with 8 warps, one CTA per SM and 104 KB of shared memory) measured 5.5 % faster
+// end to end than 64 (which doubles the CTAs and the prefix slots every merge reads), and 64 than 32.
 #ifndef PKV_PREFIX_CHUNK
 #define PKV_PREFIX_CHUNK 128
 #endif
-// Registers per thread of the prefix kernel: at 168 (no spills), one 8-warp prefix CTA and one
-// 4-warp suffix-pass CTA fit an SM's register file together, so the suffix pass streams on the
-// prefix kernel's SMs too.
+// Registers per thread of the prefix kernel: at 168 (no spills), a prefix CTA and a 4-warp
+// suffix-pass CTA fit an SM's register file together, so the suffix pass streams on the prefix
+// kernel's SMs too.
 #ifndef PKV_PREFIX_MAXNREG
 #define PKV_PREFIX_MAXNREG 168
 #endif
@@ -58,9 +58,16 @@ constexpr int kD = PKV_HEAD_DIM;       // 128
 constexpr int kChunkTok = PKV_PREFIX_CHUNK;  // prefix tokens per CTA (a multiple of 16)
 constexpr int kNT = kChunkTok / 8;           // 8-token MMA n-tiles of a chunk
 static_assert(kChunkTok % 16 == 0 && kChunkTok >= 16, "chunk of whole 16-token k-steps");
-// Warps per prefix CTA (16 query rows each, so 16 x warps rows per row tile).
+// Warps per prefix CTA (16 query rows each, so 16 x warps rows per row tile).  Four (64 rows, two
+// row tiles for the 128 rows of 32 requests x 4 heads: twice the CTAs, each with half the MMA work
+// and the same chunk loads from L2) measured 1.5 % faster on the shared-prefix step than eight, and
+// two 12 % slower.  The tcgen05 tile is 128 rows.
 #ifndef PKV_PREFIX_WARPS
-#define PKV_PREFIX_WARPS 8
+#ifdef PKV_PREFIX_TCGEN05
+#define PKV_PREFIX_WARPS (PKV_PREFIX_TCGEN05 ? 8 : 4)
+#else
+#define PKV_PREFIX_WARPS 4
+#endif
 #endif
 constexpr int kWarps = PKV_PREFIX_WARPS;  // 16 query rows per warp
 constexpr int kRows = kWarps * 16;     // query rows per CTA
