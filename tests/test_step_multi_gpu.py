@@ -154,3 +154,26 @@ def test_step_multi_refuses_long_drafts():
     qs, q, kn, vn, pos = new_rows(case, [17, 3], 1)
     with pytest.raises(pkv.PkvError):
         gpu_step_multi(case, qs, q, kn, vn, 17)
+
+
+def test_step_multi_bad_block_id_skips_the_write_and_is_recorded():
+    """A new token whose block id is outside the pool: its cache write is skipped (every access
+    stays in bounds), the error is recorded, the other requests' rows and results are exact, and
+    the context stays usable."""
+    pkv.device_error()  # clear
+    ctxs, ns = [300, 700, 40], [4, 3, 2]
+    case = workloads.random_case(1195, ctxs, 8, 2, block_size=16, extra_blocks=3)
+    qs, q, kn, vn, pos = new_rows(case, ns, 5)
+    ref, k, v = oracle_step_multi(case, qs, q, kn, vn, pos)
+    bad = case.to("cpu")
+    bad.block_tables[1, (ctxs[1] - 1) // 16] = case.num_blocks + 9   # the block of request 1's last new token
+    out, dev = gpu_step_multi(bad, qs, q, kn, vn, max(ns))
+    assert pkv.device_error() == pkv.PKV_DEV_BAD_BLOCK_ID
+    rows = np.repeat(np.arange(3), ns)
+    keep = rows != 1
+    assert max_err(out[torch.from_numpy(keep).cuda()], ref[keep]) <= ATTN_TOL
+    # the same step with the valid table, on a fresh copy of the pool, is exact
+    out2, dev2 = gpu_step_multi(case, qs, q, kn, vn, max(ns))
+    assert max_err(out2, ref) <= ATTN_TOL
+    check_pool(dev2, k, v)
+    assert_no_device_error()
