@@ -166,6 +166,7 @@ def test_step_multi_bad_block_id_skips_the_write_and_is_recorded():
     qs, q, kn, vn, pos = new_rows(case, ns, 5)
     ref, k, v = oracle_step_multi(case, qs, q, kn, vn, pos)
     bad = case.to("cpu")
+    bad.block_tables = case.block_tables.clone()  # (to("cpu") of a CPU case shares its tensors)
     bad.block_tables[1, (ctxs[1] - 1) // 16] = case.num_blocks + 9   # the block of request 1's last new token
     out, dev = gpu_step_multi(bad, qs, q, kn, vn, max(ns))
     assert pkv.device_error() == pkv.PKV_DEV_BAD_BLOCK_ID
