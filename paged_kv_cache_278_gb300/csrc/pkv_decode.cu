@@ -72,11 +72,92 @@ constexpr int new_rows_of() {
     return MQ == 2 ? PKV_MAX_STEP_QUERY_LEN : (MQ ? 8 : 1);
 }
 
-template <int G, int LPT, bool TC, int KQ, int MQ>
+// One prefix tile of the one-grid shared-prefix step: CTA (chunk c, kv head kvh, row tile rt) of
+// the first P.prefix_ctas.  Its eight 16-token K/V tiles of prefix tokens 128 c .. 128 c + 127 are
+// copied once into the stage buffers (swizzled 2-D tensor boxes, as the decode path's; in overlap
+// mode before the preceding kernel completes); each warp then runs the 16-row tensor-core engine
+// over all eight for its 16 of the tile's 64 query rows (row r of the B * G rows reading kvh is
+// request r / G, head r % G) and stores their partial as slot c.  The tile then counts once
+// toward the merge of every request it covers; where its arrival is the last, it merges.
+template <int G, class L, class Wait>
+__device__ __forceinline__ void prefix_tile(const DecodeParams &P, unsigned char *smem, int warp, int lane, bool overlap,
+                                         Wait wait_preceding) {
+    const int Hkv = P.num_kv_heads, Hq = P.num_q_heads, bs = P.block_size;
+    const int c = static_cast<int>(blockIdx.x) % P.prefix_chunks;
+    const int kvh = (static_cast<int>(blockIdx.x) / P.prefix_chunks) % Hkv;
+    const int rt = static_cast<int>(blockIdx.x) / (P.prefix_chunks * Hkv);
+    const int rows = P.num_seqs * G;
+    const int prefix_len = P.token_offset;
+    const int tok0 = c * 128;
+    const int nsub = min(128, prefix_len - tok0) / kChunk;  // the prefix is whole 16-token chunks
+    const uint32_t bars = pkv::smem_addr(smem + L::bars);
+    const uint32_t tiles = pkv::smem_addr(smem + L::stages);
+    const bool smem_ok = (pkv::smem_addr(smem) & 1023) == 0;
+    if (!smem_ok && threadIdx.x == 0) pkv::record_error(&g_decode_error, PKV_DEV_SMEM_MISALIGNED);
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < nsub; ++j) pkv::mbar_init(bars + 8 * j, 1);
+        pkv::fence_mbar_init();
+    }
+    __syncthreads();
+    if (smem_ok && static_cast<int>(threadIdx.x) < nsub) {  // thread j stages tile j (cache history)
+        const int j = threadIdx.x, tok = tok0 + j * kChunk;
+        int32_t id = __ldg(P.block_tables + tok / bs);  // every table starts with the prefix's blocks
+        if (id < 0 || id >= P.num_blocks) {
+            pkv::record_error(&g_decode_error, PKV_DEV_BAD_BLOCK_ID);
+            id = 0;
+        }
+        const int y = static_cast<int>((static_cast<int64_t>(id) * Hkv + kvh) * bs + tok % bs);
+        const uint32_t dst = tiles + j * L::stage, bar = bars + 8 * j;
+        pkv::mbar_arrive_expect_tx(bar, 4 * kHalfTile);
+        pkv::tma_load_2d(dst, &P.tmap_k, 0, y, bar);
+        pkv::tma_load_2d(dst + kHalfTile, &P.tmap_k, 64, y, bar);
+        pkv::tma_load_2d(dst + L::k_tile, &P.tmap_v, 0, y, bar);
+        pkv::tma_load_2d(dst + L::k_tile + kHalfTile, &P.tmap_v, 64, y, bar);
+    }
+    if (overlap) wait_preceding();  // q, the workspace and out from here on
+
+    const int rg16 = rt * 4 + warp;  // this warp's 16-row group of the B * G rows
+    if (smem_ok && rg16 * 16 < rows) {
+        TcEngineR16<G> e;
+        e.init(P, 0, 0, 0);
+        e.bind(P, kvh, lane, rg16, 0, P.num_seqs, 0x3fffffff);  // requests as rows; every prefix token visible
+        bool ok = true;
+        for (int j = 0; j < nsub && ok; ++j) {
+            ok = __all_sync(pkv::kFullMask, pkv::mbar_wait_bounded(bars + 8 * j, 0));
+            if (!ok) {
+                if (lane == 0) pkv::record_error(&g_decode_error, PKV_DEV_WAIT_TIMEOUT);
+                break;
+            }
+            const uint32_t kt = tiles + j * L::stage;
+            e.qk(kt, 0, kChunk, lane, nullptr, tok0 + j * kChunk);
+            e.pv(kt + L::k_tile, kChunk, lane, nullptr);
+        }
+        e.store_partial(P, lane, rg16, rows, kvh, c);
+    }
+    // nothing of this CTA's copies left in flight before the stage buffers are reused (bounded)
+    if (smem_ok && threadIdx.x == 0)
+        for (int j = 0; j < nsub; ++j) pkv::mbar_wait_bounded(bars + 8 * j, 0);
+    __syncthreads();  // every warp's partial stores before the arrivals
+
+    // ---- arrivals: one per request of the tile.  A tile never merges: where its arrival is the
+    // last piece of a (request, kv head), the count is left complete and the merge launch after the
+    // grid folds that pair (a tile's requests with short suffixes would otherwise queue many merges
+    // on one CTA).
+    const int b_lo = rt * 64 / G, b_hi = min(rt * 64 + 64, rows) / G;
+    for (int b = b_lo + static_cast<int>(threadIdx.x); b < b_hi; b += kThreads)
+        pkv::atomic_add_acq_rel_gpu(P.counters + static_cast<int64_t>(b) * Hkv + kvh, 1);
+    (void)Hq;
+}
+
+// SP: the shared-prefix step in one grid: the first P.prefix_ctas CTAs attend over the shared
+// prefix (one 128-token chunk, one kv head, 64 query rows each), the rest are the suffix pass; the
+// merge of each (request, kv head) is fused where the last of its pieces lands.
+template <int G, int LPT, bool TC, int KQ, int MQ, bool SP = false>
 __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS))
     decode_partition_kernel(const __grid_constant__ DecodeParams P) {
     static_assert(!KQ || TC, "int8 keys run on the tensor-core engine");
     static_assert(!MQ || (TC && !KQ), "several tokens per request run on the fp16 tensor-core engine");
+    static_assert(!SP || (TC && !KQ && !MQ), "the one-grid shared-prefix step reads fp16 K/V, one token per request");
     constexpr int kStages = stages_of<MQ>();  // this variant's ring depth
     using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, kStages, new_rows_of<MQ>()>;
     using Engine = EngineFor<G, LPT, TC, KQ, MQ>;
@@ -92,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     // preceding kernel does not write) and waits just before it touches q, the new token's rows or
     // any output.  Once past that point, the kernel after this one may start launching: it too
     // touches nothing written here before this grid completes.
-    const bool suffix_pass = P.slot_offset > 0;
+    const bool suffix_pass = !SP && P.slot_offset > 0;
     const bool overlap = P.overlap != 0;          // set by the step calls only
     const bool late_q = overlap && !suffix_pass;  // q read after the wait
     auto wait_preceding = [suffix_pass]() {
@@ -104,11 +185,18 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if constexpr (SP) {
+        if (static_cast<int>(blockIdx.x) < P.prefix_ctas) {
+            prefix_tile<G, L>(P, smem, warp, lane, overlap, wait_preceding);
+            return;
+        }
+    }
     const int n_rg = MQ ? P.n_row_groups : 1;
-    const int part = MQ ? blockIdx.x / n_rg : blockIdx.x;
-    const int rg = MQ ? blockIdx.x - part * n_rg : 0;  // row group (fastest: groups share K/V in L2)
-    const int kvh = blockIdx.y;
-    const int b = blockIdx.z;
+    const int lin_s = SP ? static_cast<int>(blockIdx.x) - P.prefix_ctas : 0;  // one-grid step: suffix CTA index
+    const int part = SP ? lin_s % P.grid_parts : (MQ ? blockIdx.x / n_rg : blockIdx.x);
+    const int rg = SP ? 0 : (MQ ? blockIdx.x - part * n_rg : 0);  // row group (fastest: groups share K/V in L2)
+    const int kvh = SP ? (lin_s / P.grid_parts) % P.num_kv_heads : blockIdx.y;
+    const int b = SP ? lin_s / (P.grid_parts * P.num_kv_heads) : blockIdx.z;
     const int Hq = P.num_q_heads;
     const int bs = P.block_size;
     int q_len = 1;
@@ -191,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                blockIdx.y == 0 && blockIdx.z == 0;
     };
     if (n_parts == 0) {  // shared-prefix pass: the whole context is the prefix, merge its chunks only
+        if (SP) return;  // the prefix tiles' last arrival merges
         if (part == 0 && P.counters != nullptr) {
             pkv::pdl_wait_primary();  // the prefix kernel's partials
             merge_group<G, L::stage_bytes>(P, HeadRows{static_cast<int64_t>(b) * Hq + kvh * G}, P.slot_offset, smem);
@@ -658,10 +747,11 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     __shared__ int s_last;
     __syncthreads();
     int *counter = P.counters + (static_cast<int64_t>(b) * P.num_kv_heads + kvh) * n_rg + rg;
-    if (threadIdx.x == 0) s_last = pkv::atomic_add_acq_rel_gpu(counter, 1) == n_parts - 1;
+    if (threadIdx.x == 0)
+        s_last = pkv::atomic_add_acq_rel_gpu(counter, 1) == n_parts + (SP ? P.prefix_chunks : 0) - 1;
     __syncthreads();
     if (!s_last) return;
-    if (P.slot_offset > 0) pkv::pdl_wait_primary();  // shared-prefix pass: the prefix kernel's partials
+    if (!SP && P.slot_offset > 0) pkv::pdl_wait_primary();  // shared-prefix pass: the prefix kernel's partials
     if constexpr (MQ)
         merge_group<NC, L::stage_bytes>(P, token_rows, P.slot_offset + n_parts, smem);
     else
@@ -685,8 +775,14 @@ __global__ void __launch_bounds__(kThreads) merge_groups_kernel(const __grid_con
     int ctx = __ldg(P.context_lens + b);
     ctx = max(min(ctx, cap), P.token_offset);
     const int n_parts = (ctx - P.token_offset + P.partition_size - 1) / P.partition_size;
+    int *counter = nullptr;
+    if (P.prefix_ctas > 0) {  // one-grid step: only pairs whose last piece was a prefix tile remain
+        counter = P.counters + static_cast<int64_t>(b) * P.num_kv_heads + kvh;
+        if (__ldcg(counter) != P.prefix_chunks + n_parts) return;  // 0: merged in the grid
+    }
     merge_group<G, kMergeStageBytes>(P, HeadRows{static_cast<int64_t>(b) * P.num_q_heads + kvh * G},
                                      P.slot_offset + n_parts, smem);
+    if (counter && threadIdx.x == 0) *counter = 0;
 }
 
 // One CTA per (q head, request); thread d owns output dim d.  Partitions are taken in tiles
@@ -811,11 +907,11 @@ int encode_code_map(CUtensorMap *map, const void *base, int64_t rows) {
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int G, int KQ, int MQ>
+template <int G, int KQ, int MQ, bool SP = false>
 int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream, int grid_parts) {
     constexpr int LPT = lanes_per_token<G>();
-    constexpr bool TC = KQ || MQ || (PKV_DECODE_TC && G >= PKV_DECODE_TC_MIN_GROUP);
-    auto kernel = decode_partition_kernel<G, LPT, TC, KQ, MQ>;
+    constexpr bool TC = SP || KQ || MQ || (PKV_DECODE_TC && G >= PKV_DECODE_TC_MIN_GROUP);
+    auto kernel = decode_partition_kernel<G, LPT, TC, KQ, MQ, SP>;
     DecodeParams p = p_in;
     if (TC) {
         const int64_t rows = p.num_blocks * p.num_kv_heads * p.block_size;
@@ -842,7 +938,14 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
     }
     const int64_t gx = static_cast<int64_t>(grid_parts > 0 ? grid_parts : p.max_partitions) * (MQ ? p.n_row_groups : 1);
     if (gx > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
-    const dim3 grid(static_cast<unsigned>(gx), p.num_kv_heads, num_seqs);
+    dim3 grid(static_cast<unsigned>(gx), p.num_kv_heads, num_seqs);
+    if (SP) {  // one dimension: the prefix tiles, then (partition, kv head, request) fastest first
+        const int64_t n = p.prefix_ctas + gx * p.num_kv_heads * num_seqs;
+        if (n > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+        p.grid_parts = static_cast<int>(gx);
+        p.num_seqs = num_seqs;
+        grid = dim3(static_cast<unsigned>(n));
+    }
     // Always a programmatic dependent of the preceding kernel: its CTAs may become resident while
     // that kernel drains (the kernel waits, see above).  The suffix pass after the shared-prefix
     // kernel streams the suffixes while the prefix kernel runs; only its merges wait for the prefix.
@@ -861,6 +964,7 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
 
 template <int G>
 int launch_mode(const DecodeParams &p, int num_seqs, cudaStream_t stream, int grid_parts) {
+    if (p.prefix_ctas > 0) return launch_partition<G, 0, 0, true>(p, num_seqs, stream, grid_parts);
     if (p.query_start)
         return p.mq_tiles == 2 ? launch_partition<G, 0, 2>(p, num_seqs, stream, grid_parts)
                                : launch_partition<G, 0, 1>(p, num_seqs, stream, grid_parts);
@@ -1377,11 +1481,14 @@ int launch_split_pass(const SplitPass &a, void *stream) {
     p.v_new = static_cast<const __half *>(a.v_new);
     p.k_cache_w = static_cast<__half *>(const_cast<void *>(a.k_cache));
     p.v_cache_w = static_cast<__half *>(const_cast<void *>(a.v_cache));
-    if (a.separate_merge) p.counters = nullptr;
+    p.prefix_ctas = a.prefix_ctas;
+    p.prefix_chunks = a.prefix_chunks;
+    p.overlap = a.overlap ? 1 : 0;
+    if (a.separate_merge && a.prefix_ctas == 0) p.counters = nullptr;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int group = a.num_q_heads / a.num_kv_heads;
     const int st = dispatch_partition(p, a.num_seqs, group, s, a.grid_partitions);
-    if (st != PKV_OK || !a.separate_merge) return st;
+    if (st != PKV_OK || (!a.separate_merge && a.prefix_ctas == 0)) return st;
     // the merge as a programmatic dependent of the pass: launched as the pass's CTAs drain
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(a.num_kv_heads, a.num_seqs);

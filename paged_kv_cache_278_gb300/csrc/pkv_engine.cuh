@@ -116,6 +116,10 @@ struct DecodeParams {
     const float *v_scale;     // int8 values too: float32 scale per (block, kv head, slot); null for fp16 values
     float *v_scale_w;
     int overlap;              // 1: stream the cache history before the preceding kernel completes
+    int prefix_ctas;          // shared-prefix step in one grid: CTAs [0, prefix_ctas) are prefix tiles
+    int prefix_chunks;        //   128-token prefix chunks (partial slots [0, prefix_chunks))
+    int grid_parts;           //   suffix partitions per (request, kv head) in the grid
+    int num_seqs;             //   requests
     CUtensorMap tmap_k;       // tensor-core engine: the caches as 2-D [NB*Hkv*bs rows][128] fp16,
     CUtensorMap tmap_v;       //   16 x 64 boxes, 128-byte swizzle (int8 keys: 16 x 128-byte boxes)
 };
@@ -1055,6 +1059,40 @@ struct TcEngineR16 {
             if (t == 0) {
                 c_m[warp * 16 + row] = m;
                 c_l[warp * 16 + row] = l;
+            }
+        }
+    }
+
+    // Where each warp owns distinct rows (a shared-prefix tile: row r of the B * G rows of one kv
+    // head is request r / G, head r % G, i.e. bound with qs = 0 and n = B), no warp combine: the
+    // rows' partial result (max in natural-log units, weight sum, o / l) is stored as `slot` of
+    // the split layout.  rg: the warp's 16-row group; rows past n_rows are not stored.
+    __device__ __forceinline__ void store_partial(const DecodeParams &P, int lane, int rg, int n_rows, int kvh,
+                                                  int slot) {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float l = l_part[i];
+            l += __shfl_xor_sync(pkv::kFullMask, l, 1);
+            l += __shfl_xor_sync(pkv::kFullMask, l, 2);
+            float m = m_ref[i], f = 1.f;
+            if (top[i] > -INFINITY) {  // m_ref <= top < m_ref + 2^8
+                f = exp2f(m_ref[i] - top[i]);
+                l *= f;
+                m = top[i];
+            }
+            const int r = rg * 16 + g + 8 * i;
+            if (r >= n_rows) continue;
+            const int64_t row = static_cast<int64_t>(r / G) * P.num_q_heads + kvh * G + r % G;
+            const int64_t prow = row * P.max_partitions + slot;
+            const float s = f / l;
+            float *o_out = P.o_part + prow * kD + 2 * t;
+#pragma unroll
+            for (int j = 0; j < kD / 8; ++j)
+                *reinterpret_cast<float2 *>(o_out + 8 * j) = make_float2(o[j][2 * i] * s, o[j][2 * i + 1] * s);
+            if (t == 0) {
+                P.m_part[prow] = m * kLn2;
+                P.l_part[prow] = l;
             }
         }
     }

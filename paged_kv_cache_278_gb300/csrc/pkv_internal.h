@@ -45,6 +45,9 @@ struct SplitPass {
     int *counters;
     const void *k_new, *v_new;  // non-null: fused append of the new token (caches are written)
     bool separate_merge;
+    int prefix_ctas = 0;    // > 0: the shared-prefix step in one grid, these prefix tiles first
+    int prefix_chunks = 0;  //   (128-token prefix chunks; the merge is fused, separate_merge false)
+    bool overlap = false;   //   PKV_STEP_OVERLAP
 };
 int launch_split_pass(const SplitPass &a, void *stream);
 

@@ -55,6 +55,12 @@ constexpr int kD = PKV_HEAD_DIM;       // 128
 #ifndef PKV_PREFIX_SEPARATE_MERGE
 #define PKV_PREFIX_SEPARATE_MERGE 1
 #endif
+// 1: the whole step is one launch of the decode kernel: its first CTAs are the prefix tiles (one
+// 128-token chunk, one kv head, 64 query rows each, on the 16-row tensor-core engine), the rest the
+// suffix pass, and the merge is fused where the last piece of a (request, kv head) lands.
+#ifndef PKV_PREFIX_ONE_GRID
+#define PKV_PREFIX_ONE_GRID 0
+#endif
 constexpr int kChunkTok = PKV_PREFIX_CHUNK;  // prefix tokens per CTA (a multiple of 16)
 constexpr int kNT = kChunkTok / 8;           // 8-token MMA n-tiles of a chunk
 static_assert(kChunkTok % 16 == 0 && kChunkTok >= 16, "chunk of whole 16-token k-steps");
@@ -652,7 +658,12 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev & 63);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-#if PKV_PREFIX_TCGEN05
+#if PKV_PREFIX_ONE_GRID
+    static_assert(kChunkTok == 128, "the one-grid prefix tiles are 128-token chunks");
+    (void)configured;
+    (void)bit;
+    (void)s;
+#elif PKV_PREFIX_TCGEN05
     static_assert(kChunkTok == tc5::kTok && kRows == tc5::kRowsT, "partial slots are 128-token chunks of 128 rows");
     const int64_t cache_rows = num_blocks * num_kv_heads * block_size;
     if (cache_rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
@@ -720,6 +731,12 @@ int shared_prefix_decode(void *out, const void *q, const void *k_cache, const vo
     a.k_new = k_new;
     a.v_new = v_new;
     a.separate_merge = PKV_PREFIX_SEPARATE_MERGE != 0;
+#if PKV_PREFIX_ONE_GRID
+    a.prefix_ctas = L.n_pre * num_kv_heads * ((rows + 63) / 64);
+    a.prefix_chunks = L.n_pre;
+    a.separate_merge = false;
+    a.overlap = overlap;
+#endif
     return pkv_internal::launch_split_pass(a, stream);
 }
 
