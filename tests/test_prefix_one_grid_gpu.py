@@ -4,7 +4,7 @@ launch, merged where their last piece lands), against the float64 oracle.
 Built with PKV_PREFIX_ONE_GRID=1 into libpkv_onegrid.so beside the product library: the prefix
 tiles run the 16-row tensor-core engine over eight TMA-staged 16-token tiles each and store their
 rows' partials; a pair whose last piece is a prefix tile is merged by the merge launch after the
-grid.  The product default is the three-launch cascade, measured faster; this build keeps the
+grid.  The product default is the three-launch cascade, measured faster; the variant library keeps the
 one-grid form checked on the same cases.
 """
 import os

@@ -5,7 +5,7 @@ The shared prefix's chunk is the one dense contraction on the path (128 query ro
 S = Q K^T and O = P V accumulated in tensor memory with V as an MN-major operand, the rows' softmax
 read back with tcgen05.ld -- is built with PKV_PREFIX_TCGEN05=1 (and the merge fused into the
 suffix pass) into libpkv_tc5.so beside the product library.  The product default is the mma.sync
-tile, measured faster on the shared-prefix step; this build keeps the tcgen05 form checked on the
+tile, measured faster on the shared-prefix step; the variant library keeps the tcgen05 form checked on the
 same cases as the default one.
 """
 import os
