@@ -441,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     if constexpr (MQ) {
         if (P.k_new != nullptr) {
             new_lo = max(start, ctx_full - q_len);
-            new_hi = min(start + n_tok, ctx_full);
+            // (at most q_len <= max_query_len rows, which the host bounds by the staging's capacity)
+            new_hi = min(min(start + n_tok, ctx_full), new_lo + new_rows_of<MQ>());
             const bool writer = rg == (q_len * G - 1) / NC;
             const int64_t t0 = qs_b - (ctx_full - q_len);  // k_new row of position p: t0 + p
             for (int idx = threadIdx.x; idx < (new_hi - new_lo) * 32; idx += kThreads) {
