@@ -178,3 +178,22 @@ def test_step_multi_bad_block_id_skips_the_write_and_is_recorded():
     assert max_err(out2, ref) <= ATTN_TOL
     check_pool(dev2, k, v)
     assert_no_device_error()
+
+
+def test_step_multi_binding_checks_shapes():
+    case = workloads.random_case(1197, [100, 200], 8, 2, block_size=16)
+    qs, q, kn, vn, pos = new_rows(case, [3, 2], 1)
+    dev = case.to("cuda")
+    qd, knd, vnd = (torch.from_numpy(a).cuda() for a in (q, kn, vn))
+    qsd = torch.from_numpy(qs).cuda()
+    out = torch.empty_like(qd)
+    with pytest.raises(ValueError):   # k_new must have one row per new token
+        pkv.decode_step_multi(out, qd, knd[:-1], vnd, dev.k_cache, dev.v_cache, dev.block_tables, dev.context_lens,
+                              qsd, 3, case.scale)
+    with pytest.raises(ValueError):   # query_start must have num_seqs + 1 entries
+        pkv.decode_step_multi(out, qd, knd, vnd, dev.k_cache, dev.v_cache, dev.block_tables, dev.context_lens,
+                              qsd[:-1], 3, case.scale)
+    with pytest.raises(pkv.PkvError):  # the one-launch step takes up to PKV_MAX_STEP_QUERY_LEN new tokens
+        pkv.decode_step_multi(out, qd, knd, vnd, dev.k_cache, dev.v_cache, dev.block_tables, dev.context_lens,
+                              qsd, pkv.PKV_MAX_STEP_QUERY_LEN + 1, case.scale)
+    assert_no_device_error()
