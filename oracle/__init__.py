@@ -20,11 +20,17 @@ passage of the pages it follows:
 * ``decode`` -- read every cached K/V, score, softmax, weighted sum
   ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.2);
 * ``decode_partition``, ``merge`` -- the same over consecutive token ranges,
-  recombined by the log-sum-exp identity (not on the pages; see the C file).
+  recombined by the log-sum-exp identity (not on the pages; see the C file);
+* ``quantize_k_row``, ``append_quant_k(v)``, ``decode_quant_k(v)`` -- the int8
+  cache ("推理优化这件事，为什么值得反复复盘", sec. 4.4);
+* ``e4m3_to_double``, ``e4m3_from_float``, ``quantize_fp8_row``,
+  ``append_fp8_kv``, ``decode_fp8_kv`` -- the 8-bit floating-point (E4M3) cache
+  ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 2 and 4.2).
 
 Every function is pinned by ``tests/test_oracle.py`` against something other
-than itself (numpy's binary16 decoder, a contiguous textbook softmax, closed
-forms, a pure-Python brute force, the pages' worked size example).
+than itself (numpy's binary16 decoder, torch's float8_e4m3fn conversions, a
+contiguous textbook softmax, closed forms, a pure-Python brute force, the
+pages' worked size example, hand-worked goldens).
 """
 from __future__ import annotations
 
@@ -46,6 +52,7 @@ _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _i8p = ctypes.POINTER(ctypes.c_int8)
 _f32p = ctypes.POINTER(ctypes.c_float)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 GCC_FLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c99", "-shared", "-fPIC"]
 
@@ -121,6 +128,17 @@ class Oracle:
         lib.oracle_append_quant_kv.argtypes = [_i8p, _f32p, _i8p, _f32p, _i64p, _u16p, _u16p] + [ctypes.c_int] * 4
         lib.oracle_decode_quant_kv.restype = None
         lib.oracle_decode_quant_kv.argtypes = [_f64p, _u16p, _i8p, _f32p, _i8p, _f32p, _i32p, _i32p] + \
+            [ctypes.c_int] * 6 + [ctypes.c_double]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_quantize_fp8_row.restype = None
+        lib.oracle_quantize_fp8_row.argtypes = [_u8p, ctypes.POINTER(ctypes.c_float), _u16p, ctypes.c_int]
+        lib.oracle_append_fp8_kv.restype = None
+        lib.oracle_append_fp8_kv.argtypes = [_u8p, _f32p, _u8p, _f32p, _i64p, _u16p, _u16p] + [ctypes.c_int] * 4
+        lib.oracle_decode_fp8_kv.restype = None
+        lib.oracle_decode_fp8_kv.argtypes = [_f64p, _u16p, _u8p, _f32p, _u8p, _f32p, _i32p, _i32p] + \
             [ctypes.c_int] * 6 + [ctypes.c_double]
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [_f64p, _f64p, _f64p, _f64p, _i32p] + [ctypes.c_int] * 5
@@ -247,6 +265,55 @@ class Oracle:
         self.lib.oracle_decode_quant_kv(_p(out, _f64p), _p(qb, _u16p), _p(kc, _i8p), _p(ks, _f32p), _p(vc, _i8p),
                                         _p(vs, _f32p), _p(bt, _i32p), _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs,
                                         float(scale))
+        return out
+
+    def e4m3_to_double(self, codes) -> np.ndarray:
+        """float64 values of E4M3 codes (uint8), elementwise."""
+        c = np.asarray(codes, dtype=np.uint8)
+        return np.array([self.lib.oracle_e4m3_to_double(int(x)) for x in c.ravel()], np.float64).reshape(c.shape)
+
+    def e4m3_from_float(self, y) -> np.ndarray:
+        """E4M3 codes (uint8) nearest to float32 values y (ties to even, clamped to +-448)."""
+        a = np.asarray(y, dtype=np.float32)
+        return np.array([self.lib.oracle_e4m3_from_float(float(x)) for x in a.ravel()], np.uint8).reshape(a.shape)
+
+    def quantize_fp8_row(self, row) -> tuple[np.ndarray, float]:
+        """(E4M3 codes uint8 [D], float32 scale) of one fp16 row."""
+        rb = _bits(np.ascontiguousarray(row))
+        codes = np.empty(rb.shape[0], np.uint8)
+        sc = ctypes.c_float(0.0)
+        self.lib.oracle_quantize_fp8_row(_p(codes, _u8p), ctypes.byref(sc), _p(rb, _u16p), rb.shape[0])
+        return codes, np.float32(sc.value)
+
+    def append_fp8_kv(self, k_codes, k_scale, v_codes, v_scale, slots, k_new, v_new) -> None:
+        """In place on the fp8 K + V cache: codes uint8 [NB,Hkv,bs,D], scales float32 [NB,Hkv,bs]."""
+        nb, hkv, bs, d = k_codes.shape
+        for a, dt in ((k_codes, np.uint8), (v_codes, np.uint8), (k_scale, np.float32), (v_scale, np.float32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        assert v_codes.shape == k_codes.shape and k_scale.shape == (nb, hkv, bs) and v_scale.shape == k_scale.shape
+        kn, vn = _bits(k_new), _bits(v_new)
+        sl = np.ascontiguousarray(slots, dtype=np.int64)
+        assert kn.shape == (sl.shape[0], hkv, d) and vn.shape == kn.shape
+        self.lib.oracle_append_fp8_kv(_p(k_codes, _u8p), _p(k_scale, _f32p), _p(v_codes, _u8p), _p(v_scale, _f32p),
+                                      _p(sl, _i64p), _p(kn, _u16p), _p(vn, _u16p), sl.shape[0], hkv, d, bs)
+
+    def decode_fp8_kv(self, q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens,
+                      scale: float) -> np.ndarray:
+        """float64 [B, Hq, D] decode over the fp8 K + V cache (both dequantised exactly)."""
+        qb = _bits(q)
+        kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+        vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        b, hq, d = qb.shape
+        nb, hkv, bs, d2 = kc.shape
+        assert d2 == d and hq % hkv == 0 and vc.shape == kc.shape and ks.shape == vs.shape == (nb, hkv, bs)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty((b, hq, d), np.float64)
+        self.lib.oracle_decode_fp8_kv(_p(out, _f64p), _p(qb, _u16p), _p(kc, _u8p), _p(ks, _f32p), _p(vc, _u8p),
+                                      _p(vs, _f32p), _p(bt, _i32p), _p(cl, _i32p), b, bt.shape[1], hq, hkv, d, bs,
+                                      float(scale))
         return out
 
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
@@ -385,3 +452,23 @@ def append_quant_k(k_codes, k_scale, v_cache, slots, k_new, v_new):
 
 def decode_quant_k(q, k_codes, k_scale, v_cache, block_tables, context_lens, scale):
     return default().decode_quant_k(q, k_codes, k_scale, v_cache, block_tables, context_lens, scale)
+
+
+def e4m3_to_double(codes):
+    return default().e4m3_to_double(codes)
+
+
+def e4m3_from_float(y):
+    return default().e4m3_from_float(y)
+
+
+def quantize_fp8_row(row):
+    return default().quantize_fp8_row(row)
+
+
+def append_fp8_kv(k_codes, k_scale, v_codes, v_scale, slots, k_new, v_new):
+    return default().append_fp8_kv(k_codes, k_scale, v_codes, v_scale, slots, k_new, v_new)
+
+
+def decode_fp8_kv(q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, scale):
+    return default().decode_fp8_kv(q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, scale)

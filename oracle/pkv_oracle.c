@@ -512,3 +512,140 @@ void oracle_merge(double *out, const double *o_part, const double *m_part, const
         }
     }
 }
+
+/*
+ * fp8 K + V cache.  The pages compress the cache to 8 bits per element (int8 in
+ * "推理优化这件事，为什么值得反复复盘", sec. 4.4, and "LLM推理优化：从硬件瓶颈到KV Cache的工程实践",
+ * sec. 4.2) and name FP8 as the 8-bit number format the hardware handles natively
+ * ("LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 2).  The reading taken for an 8-bit
+ * floating-point cache: every element is an E4M3 code (1 sign bit, 4 exponent bits
+ * with bias 7, 3 fraction bits; exponent field 0 holds subnormals; S.1111.111 is
+ * NaN; no infinities; largest finite magnitude 448), with one float32 scale per
+ * (token, kv head) row as for int8: s = max_d |x_d| / 448 and code_d = the E4M3
+ * value nearest to x_d / s (ties to the even code), both in float32, clamped to
+ * +-448; an all-zero row has s = 0 and zero codes.  Attention then uses
+ * x_d = value(code_d) * s exactly.
+ */
+
+/* Value of one E4M3 code, from the format's definition. */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int expo = (c >> 3) & 0xf;
+    int frac = c & 0x7;
+    double v;
+    if (expo == 0xf && frac == 0x7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);                 /* subnormal: frac/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(8 + frac), expo - 10);    /* (1 + frac/8) * 2^(expo-7) */
+    return sign ? -v : v;
+}
+
+/* The E4M3 code whose value is nearest to y (ties: the code with an even fraction),
+ * |y| clamped to 448 first; the sign bit is y's, as in any IEEE rounding (a negative y
+ * that rounds to zero gives -0, code 0x80).  Brute force over the 127 finite
+ * non-negative codes, whose values increase with the code, so "even fraction" is
+ * "even code". */
+uint8_t oracle_e4m3_from_float(float y)
+{
+    double a = fabs((double)y);
+    if (a > 448.0)
+        a = 448.0;
+    int best = 0;
+    double best_err = a;                       /* code 0 has value 0 */
+    for (int c = 1; c <= 0x7e; ++c) {
+        double err = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(signbit(y) ? (best | 0x80) : best);
+}
+
+/* One row of D binary16 values -> E4M3 codes and the row's float32 scale. */
+void oracle_quantize_fp8_row(uint8_t *codes, float *scale, const uint16_t *row, int D)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf((float)oracle_half_to_double(row[d]));
+        if (a > amax)
+            amax = a;
+    }
+    float s = amax / 448.0f;
+    *scale = s;
+    for (int d = 0; d < D; ++d)
+        codes[d] = s == 0.0f ? 0 : oracle_e4m3_from_float((float)oracle_half_to_double(row[d]) / s);
+}
+
+/* Append into the fp8 K + V cache: both rows quantised by oracle_quantize_fp8_row and
+ * stored with their scales at the slot.  Layouts: codes uint8
+ * [num_blocks][num_kv_heads][block_size][head_dim], scales float32
+ * [num_blocks][num_kv_heads][block_size].  Negative slots skip. */
+void oracle_append_fp8_kv(uint8_t *k_codes, float *k_scale, uint8_t *v_codes, float *v_scale,
+                          const int64_t *slot_mapping, const uint16_t *k_new, const uint16_t *v_new,
+                          int num_tokens, int num_kv_heads, int head_dim, int block_size)
+{
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t blk = slot / block_size;
+        int off = (int)(slot % block_size);
+        for (int j = 0; j < num_kv_heads; ++j) {
+            int64_t row = (int64_t)(blk * num_kv_heads + j) * block_size + off;
+            int64_t src = ((int64_t)t * num_kv_heads + j) * head_dim;
+            oracle_quantize_fp8_row(k_codes + row * head_dim, k_scale + row, k_new + src, head_dim);
+            oracle_quantize_fp8_row(v_codes + row * head_dim, v_scale + row, v_new + src, head_dim);
+        }
+    }
+}
+
+/* Decode attention over the fp8 K + V cache: every key and value dequantised,
+ * value(code) * scale in float64, then the plain definition (scores, softmax,
+ * weighted sum).  Same shapes, table and context rules as oracle_decode. */
+void oracle_decode_fp8_kv(double *out, const uint16_t *q, const uint8_t *k_codes, const float *k_scale,
+                          const uint8_t *v_codes, const float *v_scale, const int32_t *block_tables,
+                          const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size, double scale)
+{
+    int group = num_q_heads / num_kv_heads;
+    for (int b = 0; b < num_seqs; ++b) {
+        int ctx = context_lens[b];
+        const int32_t *bt_row = block_tables + (int64_t)b * max_blocks_per_seq;
+        double *s = (double *)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+        for (int h = 0; h < num_q_heads; ++h) {
+            int kvh = h / group;
+            double *o = out + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            if (ctx <= 0)
+                continue;
+            const uint16_t *q_row = q + ((int64_t)b * num_q_heads + h) * head_dim;
+            double m = -INFINITY;
+            for (int p = 0; p < ctx; ++p) {
+                int64_t row = ((int64_t)bt_row[p / block_size] * num_kv_heads + kvh) * block_size + p % block_size;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += oracle_half_to_double(q_row[d]) *
+                           (oracle_e4m3_to_double(k_codes[row * head_dim + d]) * k_scale[row]);
+                s[p] = scale * dot;
+                if (s[p] > m)
+                    m = s[p];
+            }
+            double l = 0.0;
+            for (int p = 0; p < ctx; ++p) {
+                int64_t row = ((int64_t)bt_row[p / block_size] * num_kv_heads + kvh) * block_size + p % block_size;
+                double w = exp(s[p] - m);
+                l += w;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] += w * (oracle_e4m3_to_double(v_codes[row * head_dim + d]) * v_scale[row]);
+            }
+            for (int d = 0; d < head_dim; ++d)
+                o[d] /= l;
+        }
+        free(s);
+    }
+}

@@ -305,6 +305,144 @@ def pin_quant_kv(orc):
     assert np.abs(got - ref).max() <= 1e-12
 
 
+def _torch_e4m3_values():
+    """float64 values of the 256 E4M3 codes by torch's own float8_e4m3fn type (a library
+    decoder, not the oracle's); None where torch lacks the type."""
+    import torch
+    if not hasattr(torch, "float8_e4m3fn"):
+        return None
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_e4m3_decoding(orc):
+    """All 256 codes against torch's float8_e4m3fn, and the format's landmarks by hand: 0, the
+    smallest subnormal 2^-9, the smallest normal 2^-6, 1.0, the largest finite 448, -0, NaN."""
+    got = orc.e4m3_to_double(np.arange(256, dtype=np.uint8))
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3c: 1.5,
+            0x77: 240.0, 0x7e: 448.0, 0xb8: -1.0, 0xfe: -448.0}
+    for c, v in hand.items():
+        assert got[c] == v, (hex(c), got[c])
+    assert got[0x80] == 0.0 and np.signbit(got[0x80])
+    assert np.isnan(got[0x7f]) and np.isnan(got[0xff]) and np.isfinite(np.delete(got, [0x7f, 0xff])).all()
+    ref = _torch_e4m3_values()
+    if ref is not None:
+        both_nan = np.isnan(ref) & np.isnan(got)
+        assert np.array_equal(got[~both_nan], ref[~both_nan]) and both_nan.sum() == 2
+
+
+def pin_e4m3_encoding(orc):
+    """Every finite code's value encodes back to that code; a point halfway between neighbours
+    goes to the even code and a hair off it to the nearer one; magnitudes past 448 clamp to 448;
+    random float32 values within +-448 agree with torch's round-to-nearest-even conversion."""
+    vals = orc.e4m3_to_double(np.arange(0x7f, dtype=np.uint8))
+    assert np.array_equal(orc.e4m3_from_float(vals.astype(np.float32)), np.arange(0x7f, dtype=np.uint8))
+    assert np.array_equal(orc.e4m3_from_float(-vals[1:].astype(np.float32)), np.arange(1, 0x7f, dtype=np.uint8) | 0x80)
+    mid = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    lower = np.arange(0x7e, dtype=np.uint8)
+    even = np.where(lower % 2 == 0, lower, lower + 1).astype(np.uint8)
+    assert np.array_equal(orc.e4m3_from_float(mid), even)
+    assert np.array_equal(orc.e4m3_from_float(np.nextafter(mid, np.float32(0))), lower)
+    assert np.array_equal(orc.e4m3_from_float(np.nextafter(mid, np.float32(1e9))), lower + 1)
+    assert orc.e4m3_from_float(np.float32(1e6)) == 0x7e and orc.e4m3_from_float(np.float32(-470.0)) == 0xfe
+    import torch
+    if hasattr(torch, "float8_e4m3fn"):
+        rng = np.random.default_rng(17)
+        y = (rng.standard_normal(4000) * 10.0 ** rng.uniform(-4, 2.6, 4000)).astype(np.float32)
+        y = np.clip(y, -448, 448)
+        ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(orc.e4m3_from_float(y), ref)
+
+
+def pin_quantize_fp8_golden(orc):
+    g = golden("quantize_fp8_rows.json")
+    for row in g["rows"]:
+        codes, sc = orc.quantize_fp8_row(np.array(row["x"], np.float16))
+        assert sc == np.float32(row["scale"]), (row["note"], sc)
+        assert codes.tolist() == row["codes"], (row["note"], codes)
+
+
+def pin_quantize_fp8_properties(orc):
+    """On random rows: the largest |x| maps to +-448, every code's value is within half a code
+    spacing of x / s, the codes equal torch's conversion of the float32 quotients, and doubling
+    the row doubles the scale and keeps the codes."""
+    import torch
+    rng = np.random.default_rng(19)
+    for i in range(40):
+        x = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 2)).astype(np.float16)
+        codes, sc = orc.quantize_fp8_row(x)
+        xd = x.astype(np.float64)
+        i_max = np.argmax(np.abs(xd))
+        assert codes[i_max] == (0x7e if xd[i_max] > 0 else 0xfe)
+        y = (x.astype(np.float32) / sc).astype(np.float64)
+        v = orc.e4m3_to_double(codes)
+        spacing = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))) - 3)
+        assert np.all(np.abs(y - v) <= spacing / 2)
+        if hasattr(torch, "float8_e4m3fn"):
+            q = torch.from_numpy(x.astype(np.float32) / np.float32(sc)).to(torch.float8_e4m3fn)
+            assert np.array_equal(q.view(torch.uint8).numpy(), codes)
+        codes2, sc2 = orc.quantize_fp8_row((x.astype(np.float32) * 2).astype(np.float16))
+        assert sc2 == 2 * sc and np.array_equal(codes2, codes)
+
+
+def pin_fp8_kv(orc):
+    """fp8 K + V: the append stores the quantiser's codes and scales for both rows and nothing
+    else; with power-of-two scales the dequantised cache is exactly fp16 and the decode equals the
+    fp16 decode of it; with arbitrary scales it equals a textbook attention over the cache
+    dequantised through torch's float8 decoder."""
+    import torch
+    rng = np.random.default_rng(37)
+    nb, hkv, bs, d = 6, 2, 4, 16
+    kc = np.zeros((nb, hkv, bs, d), np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.full((nb, hkv, bs), -1.0, np.float32)
+    vs = ks.copy()
+    slots = np.array([3, 22, -1, 9], np.int64)
+    kn = rng.standard_normal((4, hkv, d)).astype(np.float16)
+    vn = rng.standard_normal((4, hkv, d)).astype(np.float16)
+    orc.append_fp8_kv(kc, ks, vc, vs, slots, kn, vn)
+    written = np.zeros((nb, bs), bool)
+    for ti, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        written[sl // bs, sl % bs] = True
+        for j in range(hkv):
+            c, sc = orc.quantize_fp8_row(vn[ti, j])
+            assert np.array_equal(vc[sl // bs, j, sl % bs], c) and vs[sl // bs, j, sl % bs] == sc
+            c, sc = orc.quantize_fp8_row(kn[ti, j])
+            assert np.array_equal(kc[sl // bs, j, sl % bs], c) and ks[sl // bs, j, sl % bs] == sc
+    assert np.all(ks.transpose(0, 2, 1)[~written] == -1.0) and not vc.transpose(0, 2, 1, 3)[~written].any()
+    hq, ctxs = 4, [7, 0, 16, 1]
+    nb = 20
+    finite = np.delete(np.arange(256), [0x7f, 0xff])
+    kc = rng.choice(finite, size=(nb, hkv, bs, d)).astype(np.uint8)
+    vc = rng.choice(finite, size=(nb, hkv, bs, d)).astype(np.uint8)
+    ks = (2.0 ** rng.integers(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    vs = (2.0 ** rng.integers(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    bt = rng.permutation(nb)[:16].reshape(4, 4).astype(np.int32)
+    q = rng.standard_normal((4, hq, d)).astype(np.float16)
+    ctx = np.array(ctxs, np.int32)
+    table = _torch_e4m3_values()
+    if table is None:
+        table = orc.e4m3_to_double(np.arange(256, dtype=np.uint8))
+    k64 = table[kc] * ks[..., None]
+    v64 = table[vc] * vs[..., None]
+    k16, v16 = k64.astype(np.float16), v64.astype(np.float16)
+    assert np.array_equal(k16.astype(np.float64), k64) and np.array_equal(v16.astype(np.float64), v64)
+    got = orc.decode_fp8_kv(q, kc, ks, vc, vs, bt, ctx, 0.3)
+    assert np.abs(got - orc.decode(q, k16, v16, bt, ctx, 0.3)).max() <= 1e-15
+    ks = rng.uniform(1e-3, 5e-2, size=(nb, hkv, bs)).astype(np.float32)
+    vs = rng.uniform(1e-3, 5e-2, size=(nb, hkv, bs)).astype(np.float32)
+    k64 = table[kc] * ks[..., None].astype(np.float64)
+    v64 = table[vc] * vs[..., None].astype(np.float64)
+    got = orc.decode_fp8_kv(q, kc, ks, vc, vs, bt, ctx, 0.3)
+    kk = [np.stack([k64[bt[b, p // bs], :, p % bs] for p in range(c)], 1) if c else np.zeros((hkv, 0, d))
+          for b, c in enumerate(ctxs)]
+    vv = [np.stack([v64[bt[b, p // bs], :, p % bs] for p in range(c)], 1) if c else np.zeros((hkv, 0, d))
+          for b, c in enumerate(ctxs)]
+    ref = textbook_attention(q, kk, vv, 0.3)
+    assert np.abs(got - ref).max() <= 1e-12
+
+
 def pin_decode_multi_causal(orc):
     """Several new tokens per request: a textbook causal attention (scipy softmax over the
     scores with every later position masked) on contiguous K/V, and row by row the single-token
@@ -543,6 +681,11 @@ ALL_PINS = [
     pin_decode_quant_k,
     pin_decode_multi_causal,
     pin_quant_kv,
+    pin_e4m3_decoding,
+    pin_e4m3_encoding,
+    pin_quantize_fp8_golden,
+    pin_quantize_fp8_properties,
+    pin_fp8_kv,
     pin_slot_mapping_by_enumeration,
     pin_two_keys_golden,
     pin_textbook_contiguous,

@@ -32,7 +32,7 @@ MUTANTS = {
                              "block_tables[(int64_t)b * max_blocks_per_seq + (pos + 1) / block_size]"),
     "kv_bytes_missing_factor": ("return 2 * batch * L * H * D * S * elem_bytes;",
                                 "return batch * L * H * D * S * elem_bytes;"),
-    "max_not_subtracted_in_l": ("        l += w;\n", "        l += w * w;\n"),
+    "max_not_subtracted_in_l": ("        int off = p % bs;\n        l += w;\n", "        int off = p % bs;\n        l += w * w;\n"),
     "copy_blocks_drops_v": ("            v_cache[(int64_t)dst[i] * per_block + e] = v_cache[(int64_t)src[i] * per_block + e];\n",
                             ""),
     "quant_truncates": ("float r = rintf(", "float r = truncf("),
@@ -51,6 +51,17 @@ MUTANTS = {
                           "oracle_quantize_k_row(v_codes + row * head_dim, v_scale + row, k_new + src, head_dim);"),
     "copy_blocks_one_head": ("int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;",
                              "int64_t per_block = (int64_t)block_size * head_dim;"),
+    "e4m3_exponent_bias": ("v = ldexp((double)(8 + frac), expo - 10);", "v = ldexp((double)(8 + frac), expo - 11);"),
+    "e4m3_subnormal_step": ("v = ldexp((double)frac, -9);", "v = ldexp((double)frac, -10);"),
+    "e4m3_ties_to_odd": ("(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    "e4m3_sign_dropped": ("return (uint8_t)(signbit(y) ? (best | 0x80) : best);", "return (uint8_t)best;"),
+    "fp8_step_127": ("float s = amax / 448.0f;", "float s = amax / 127.0f;"),
+    "fp8_v_from_k": ("oracle_quantize_fp8_row(v_codes + row * head_dim, v_scale + row, v_new + src, head_dim);",
+                     "oracle_quantize_fp8_row(v_codes + row * head_dim, v_scale + row, k_new + src, head_dim);"),
+    "fp8_keys_use_value_scale": ("(oracle_e4m3_to_double(k_codes[row * head_dim + d]) * k_scale[row])",
+                                 "(oracle_e4m3_to_double(k_codes[row * head_dim + d]) * v_scale[row])"),
+    "fp8_values_drop_scale": ("(oracle_e4m3_to_double(v_codes[row * head_dim + d]) * v_scale[row])",
+                              "(oracle_e4m3_to_double(v_codes[row * head_dim + d]))"),
 }
 
 

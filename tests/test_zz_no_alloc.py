@@ -81,3 +81,32 @@ def test_noalloc_refuses_requests_beyond_its_scratch():
     c.block_tables = torch.zeros((b, maxb), dtype=torch.int32, device="cuda")
     out = torch.zeros_like(c.q)
     assert _noalloc(lib, out, c, max_blocks=maxb) == _lib.PKV_ERR_WORKSPACE
+
+
+def test_noalloc_captured_in_a_graph_and_replayed():
+    """The use the entry exists for: after one eager call (the address look-up), the call is
+    captured into a CUDA graph in global capture mode and replayed with new queries written into
+    the captured input buffer.  Each replay must clear the counters again (the captured memset)
+    and equal the workspace entry point's output on the same inputs."""
+    lib = _lib.load()
+    c = workloads.random_case(904, [5000, 1, 2049, 0, 700, 1025], 32, 8, block_size=16).to("cuda")
+    out = torch.zeros_like(c.q)
+    assert _noalloc(lib, out, c) == _lib.PKV_OK        # eager: caches the scratch address
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="global"):
+            assert _noalloc(lib, out, c) == _lib.PKV_OK
+    gen = torch.Generator(device="cuda").manual_seed(905)
+    for _ in range(2):
+        c.q.copy_(torch.randn(c.q.shape, generator=gen, device="cuda").half())
+        out.fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        ref = _with_workspace(c)
+        err = (out.float() - ref.float()).abs().max().item()
+        assert err <= ATTN_TOL, err
+    assert pkv.device_error() == pkv.PKV_DEV_OK
