@@ -219,11 +219,12 @@ def decode_bytes(ctx, num_kv_heads, num_q_heads, head_dim, bs, unique_prefix_tok
                  kv="fp16", q_len=1):
     """Algorithmic bytes of one decode-attention call: K and V of every cached token read once
     (a shared prefix once), q read, out written, block-table entries and context lengths read.
-    kv="int8k": a key row is head_dim int8 codes plus one float32 scale; kv="int8kv": value rows too."""
+    kv="int8k": a key row is head_dim int8 codes plus one float32 scale; kv="int8kv": value rows too;
+    kv="fp8kv": as int8kv with 8-bit floating-point (E4M3) codes."""
     b = len(ctx) if num_seqs is None else num_seqs
     tokens = sum(ctx) - unique_prefix_tokens * (b - 1) if unique_prefix_tokens else sum(ctx)
-    k_row = head_dim + 4 if kv in ("int8k", "int8kv") else head_dim * 2
-    v_row = head_dim + 4 if kv == "int8kv" else head_dim * 2
+    k_row = head_dim + 4 if kv in ("int8k", "int8kv", "fp8kv") else head_dim * 2
+    v_row = head_dim + 4 if kv in ("int8kv", "fp8kv") else head_dim * 2
     kv = tokens * num_kv_heads * (k_row + v_row)
     qo = 2 * b * q_len * num_q_heads * head_dim * 2
     tables = sum(-(-c // bs) for c in ctx) * 4 + 4 * b
@@ -261,16 +262,18 @@ def run_ours(args):
                       ("q", "k_cache", "v_cache", "k_new", "v_new", "block_tables", "context_lens", "positions")}
     int8k = args.kv == "int8k"
     int8kv = args.kv == "int8kv"
-    if int8kv:
-        # int8 K + V cache per layer: every pool row of the generated fp16 keys and values quantised by the
-        # library's own append kernel (set-up, outside the timed regions)
+    fp8kv = args.kv == "fp8kv"
+    if int8kv or fp8kv:
+        # 8-bit K + V cache per layer (int8 or E4M3 codes): every pool row of the generated fp16 keys and values
+        # quantised by the library's own append kernel (set-up, outside the timed regions)
+        empty = pkv.empty_fp8kv_cache if fp8kv else pkv.empty_int8kv_cache
+        append_q = pkv.append_fp8kv if fp8kv else pkv.append_int8kv
         for c in cases:
             nb_, hkv_, bs_, d_ = c.k_cache.shape
-            c.k_codes, c.k_scale, c.v_codes, c.v_scale = pkv.empty_int8kv_cache(nb_, hkv_, bs_, dev)
+            c.k_codes, c.k_scale, c.v_codes, c.v_scale = empty(nb_, hkv_, bs_, dev)
             rows_k = c.k_cache.permute(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_).contiguous()
             rows_v = c.v_cache.permute(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_).contiguous()
-            pkv.append_int8kv(c.k_codes, c.k_scale, c.v_codes, c.v_scale, torch.arange(nb_ * bs_, device=dev), rows_k,
-                              rows_v)
+            append_q(c.k_codes, c.k_scale, c.v_codes, c.v_scale, torch.arange(nb_ * bs_, device=dev), rows_k, rows_v)
             del rows_k, rows_v
             c.k_cache = c.v_cache = None
         torch.cuda.synchronize(dev)
@@ -359,6 +362,15 @@ def run_ours(args):
             else:
                 pkv.decode_step_int8kv(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_codes, c.v_scale,
                                        block_tables, ctx_cur, c.scale, workspace=ws, overlap=overlap)
+        elif fp8kv:
+            if args.separate_append:
+                if not attention_only:
+                    pkv.append_fp8kv(c.k_codes, c.k_scale, c.v_codes, c.v_scale, slot_cur, c.k_new, c.v_new)
+                pkv.decode_attention_fp8kv(out_all[l], c.q, c.k_codes, c.k_scale, c.v_codes, c.v_scale, block_tables,
+                                           ctx_cur, c.scale, workspace=ws)
+            else:
+                pkv.decode_step_fp8kv(out_all[l], c.q, c.k_new, c.v_new, c.k_codes, c.k_scale, c.v_codes, c.v_scale,
+                                      block_tables, ctx_cur, c.scale, workspace=ws, overlap=overlap)
         elif int8k:
             if args.separate_append:
                 if not attention_only:
@@ -594,8 +606,9 @@ def run_ours(args):
     achieved = kernel_bytes_avg / (kernel_avg_ms * 1e-3) / 1e9
     traffic = read_traffic(args.workload + ("" if args.kv == "fp16" else "/" + args.kv) + (f"/q{nq}" if nq > 1 else ""),
                            bs)
-    layer_cache_bytes = (cases[0].k_codes.numel() * (2 if int8kv else 1) + cases[0].k_scale.numel() * 4
-                         * (2 if int8kv else 1) + (0 if int8kv else cases[0].v_cache.numel() * 2)
+    both8 = int8kv or fp8kv
+    layer_cache_bytes = (cases[0].k_codes.numel() * (2 if both8 else 1) + cases[0].k_scale.numel() * 4
+                         * (2 if both8 else 1) + (0 if both8 else cases[0].v_cache.numel() * 2)
                          if args.kv != "fp16" else cases[0].v_cache.numel() * 4)
     line = {
         "metric": METRIC,
@@ -680,10 +693,11 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- CPU oracle
 
 KV_DTYPE = {"fp16": "f16", "int8k": "i8 keys (f32 row scales), f16 values",
-            "int8kv": "i8 keys and values (f32 row scales)"}
+            "int8kv": "i8 keys and values (f32 row scales)", "fp8kv": "e4m3 keys and values (f32 row scales)"}
 KV_TEXT = {"fp16": "fp16 K and V", "int8k": "int8 keys + float32 scale per (token, kv head), fp16 values",
-           "int8kv": "int8 keys and values, each + float32 scale per (token, kv head)"}
-KV_SUFFIX = {"fp16": "", "int8k": "_int8k", "int8kv": "_int8kv"}
+           "int8kv": "int8 keys and values, each + float32 scale per (token, kv head)",
+           "fp8kv": "fp8 (E4M3) keys and values, each + float32 scale per (token, kv head)"}
+KV_SUFFIX = {"fp16": "", "int8k": "_int8k", "int8kv": "_int8kv", "fp8kv": "_fp8kv"}
 
 
 def oracle_int8kv_pool(h):
@@ -697,6 +711,20 @@ def oracle_int8kv_pool(h):
             np.zeros((nb, hkv, bs, d), np.int8), np.zeros((nb, hkv, bs), np.float32))
     rows = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
     oracle.append_quant_kv(*pool, np.arange(nb * bs, dtype=np.int64), rows(h["k_cache"]), rows(h["v_cache"]))
+    return pool
+
+
+def oracle_fp8kv_pool(h):
+    """Host fp8 K + V pool (k_codes, k_scale, v_codes, v_scale) of the sample's fp16 rows, quantised
+    by the oracle."""
+    import numpy as np
+
+    import oracle
+    nb, hkv, bs, d = h["k_cache"].shape
+    pool = (np.zeros((nb, hkv, bs, d), np.uint8), np.zeros((nb, hkv, bs), np.float32),
+            np.zeros((nb, hkv, bs, d), np.uint8), np.zeros((nb, hkv, bs), np.float32))
+    rows = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    oracle.append_fp8_kv(*pool, np.arange(nb * bs, dtype=np.int64), rows(h["k_cache"]), rows(h["v_cache"]))
     return pool
 
 
@@ -730,6 +758,12 @@ def cpu_baseline(h, case, bs, hkv, hq, d, budget_s=15.0, max_requests=None, kv="
         oracle.append_quant_kv(*pool, slots, h["k_new"], h["v_new"])
         decode_one = lambda sl: oracle.decode_quant_kv(h["q"][sl], *pool, h["block_tables"][sl],
                                                        h["context_lens"][sl], case.scale)
+    elif kv == "fp8kv":
+        pool = oracle_fp8kv_pool(h)
+        t0 = time.perf_counter()
+        oracle.append_fp8_kv(*pool, slots, h["k_new"], h["v_new"])
+        decode_one = lambda sl: oracle.decode_fp8_kv(h["q"][sl], *pool, h["block_tables"][sl],
+                                                     h["context_lens"][sl], case.scale)
     elif kv == "int8k":
         codes, scales = oracle_int8k_pool(h)
         t0 = time.perf_counter()
@@ -808,6 +842,12 @@ def run_reference(args):
         def one():
             oracle.append_quant_kv(*pool, slots, h["k_new"][sl], h["v_new"][sl])
             oracle.decode_quant_kv(h["q"][sl], *pool, h["block_tables"][sl], h["context_lens"][sl], case.scale)
+    elif args.kv == "fp8kv":
+        pool = oracle_fp8kv_pool(h)
+
+        def one():
+            oracle.append_fp8_kv(*pool, slots, h["k_new"][sl], h["v_new"][sl])
+            oracle.decode_fp8_kv(h["q"][sl], *pool, h["block_tables"][sl], h["context_lens"][sl], case.scale)
     elif args.kv == "int8k":
         codes, scales = oracle_int8k_pool(h)
 
@@ -867,9 +907,9 @@ def main(argv=None):
     ap.add_argument("--no-cascade", action="store_true", help="shared_prefix: plain decode instead of the cascade")
     ap.add_argument("--separate-append", action="store_true",
                     help="two calls per layer (pkv_append, then attention) instead of pkv_decode_step")
-    ap.add_argument("--kv", choices=["fp16", "int8k", "int8kv"], default="fp16",
+    ap.add_argument("--kv", choices=["fp16", "int8k", "int8kv", "fp8kv"], default="fp16",
                     help="cache format: fp16 K/V; int8 keys with float32 row scales and fp16 values; "
-                         "or int8 keys and values, each with float32 row scales")
+                         "int8 keys and values, each with float32 row scales; or the same with fp8 (E4M3) codes")
     ap.add_argument("--query-len", type=int, default=1,
                     help="new tokens per request per step (>1: append them, then causal multi-token attention)")
     ap.add_argument("--partition", type=int, default=0,

@@ -464,6 +464,52 @@ PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const void *k_new, 
                                    int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
                                    unsigned flags, pkv_stream_t stream);
 
+/* ---- fp8 (E4M3) keys and values (optional) ---------------------------------
+ * The pages compress the cache to 8 bits per element ("推理优化这件事，为什么值得反复复盘",
+ * sec. 4.4; "LLM推理优化：从硬件瓶颈到KV Cache的工程实践", sec. 4.2) and name FP8 as the
+ * 8-bit number format the hardware handles natively (the latter page, sec. 2).
+ * This cache stores 8-bit floating-point codes in the layout of the int8 K + V
+ * cache: k_codes and v_codes uint8 [num_blocks][num_kv_heads][block_size][128],
+ * 16-byte aligned; k_scale and v_scale float32 [num_blocks][num_kv_heads]
+ * [block_size], 16-byte aligned for the decode calls.  Each code is E4M3 (sign,
+ * 4 exponent bits with bias 7, 3 fraction bits; exponent field 0 holds
+ * subnormals; 0x7F and 0xFF are NaN; largest finite 448).  Per row (token, kv
+ * head): scale = max_d |x_d| / 448 and code_d = the E4M3 value nearest to
+ * x_d / scale (ties to the even code; a negative quotient that rounds to zero
+ * gives -0, 0x80), both in float32, magnitudes clamped to 448; an all-zero row
+ * has scale 0 and codes 0.  Attention uses x_d = value(code_d) * scale.  Same
+ * bytes as int8 K + V (264 per cached token and kv head); a relative step of
+ * 2^-3 instead of int8's uniform max/127, so coarser for large elements and
+ * finer for small ones.  Rows the caller writes itself must hold no NaN code
+ * at positions below the context length. */
+
+/* Append into the fp8 K + V cache: both rows quantised at each slot.  Rules and
+ * errors as pkv_append_int8k. */
+PKV_API int pkv_append_fp8kv(void *k_codes, float *k_scale, void *v_codes, float *v_scale,
+                             const int64_t *slot_mapping, const void *k_new, const void *v_new, int num_tokens,
+                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                             pkv_stream_t stream);
+
+/* pkv_decode_attention over the fp8 K + V cache (keys and values dequantised).
+ * Workspace and errors as pkv_decode_attention_int8kv. */
+PKV_API int pkv_decode_attention_fp8kv(void *out, const void *q, const void *k_codes, const float *k_scale,
+                                       const void *v_codes, const float *v_scale, const int32_t *block_tables,
+                                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                       int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                       pkv_stream_t stream);
+
+/* pkv_decode_step over the fp8 K + V cache: the new token's key and value rows
+ * are quantised and written by the decode kernel, then attended.  Same as
+ * pkv_append_fp8kv at positions ctx - 1 followed by pkv_decode_attention_fp8kv.
+ * flags as pkv_decode_step. */
+PKV_API int pkv_decode_step_fp8kv(void *out, const void *q, const void *k_new, const void *v_new, void *k_codes,
+                                  float *k_scale, void *v_codes, float *v_scale, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                  unsigned flags, pkv_stream_t stream);
+
 /* ---- several new tokens per request ----------------------------------------
  * A verified draft (speculative decoding) or a prefill chunk: request b brings
  * n_b = query_start[b + 1] - query_start[b] new tokens whose K/V are already in

@@ -31,6 +31,7 @@ __all__ = [
     "decode_step", "make_step_workspace", "copy_blocks", "append_int8k", "decode_attention_int8k",
     "decode_step_int8k", "empty_int8k_cache", "decode_attention_multi", "decode_step_multi", "make_multi_workspace",
     "copy_blocks_between", "empty_int8kv_cache", "append_int8kv", "decode_attention_int8kv", "decode_step_int8kv",
+    "empty_fp8kv_cache", "append_fp8kv", "decode_attention_fp8kv", "decode_step_fp8kv",
     "device_error", "slot_mapping", "BlockPool", "PkvError", "library_path",
     "PKV_DEFAULT_PARTITION", "PKV_MAX_PARTITION", "PKV_HEAD_DIM",
     "PKV_DEV_OK", "PKV_DEV_BAD_BLOCK_ID", "PKV_DEV_BAD_CONTEXT", "PKV_DEV_BAD_SLOT", "PKV_DEV_WAIT_TIMEOUT",
@@ -442,10 +443,10 @@ def decode_step_int8k(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v
 
 # ---------------------------------------------------------------- int8 keys and values
 
-def _int8kv_shape(k_codes, k_scale, v_codes, v_scale):
-    _need(k_codes, "k_codes", torch.int8, 4)
+def _int8kv_shape(k_codes, k_scale, v_codes, v_scale, codes=torch.int8):
+    _need(k_codes, "k_codes", codes, 4)
     dev = k_codes.device
-    _need(v_codes, "v_codes", torch.int8, 4, dev)
+    _need(v_codes, "v_codes", codes, 4, dev)
     _need(k_scale, "k_scale", torch.float32, 3, dev)
     _need(v_scale, "v_scale", torch.float32, 3, dev)
     if v_codes.shape != k_codes.shape or k_scale.shape != k_codes.shape[:3] or v_scale.shape != k_scale.shape:
@@ -476,8 +477,9 @@ def append_int8kv(k_codes, k_scale, v_codes, v_scale, slot_mapping, k_new, v_new
     _lib.check(st, "pkv_append_int8kv")
 
 
-def _int8kv_inputs(q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, out, workspace):
-    nb, hkv, bs, d = _int8kv_shape(k_codes, k_scale, v_codes, v_scale)
+def _int8kv_inputs(q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, out, workspace,
+                   codes=torch.int8):
+    nb, hkv, bs, d = _int8kv_shape(k_codes, k_scale, v_codes, v_scale, codes)
     dev = k_codes.device
     _need(q, "q", torch.float16, 3, dev)
     _need(out, "out", torch.float16, 3, dev)
@@ -522,6 +524,63 @@ def decode_step_int8kv(out, q, k_new, v_new, k_codes, k_scale, v_codes, v_scale,
                                      block_tables.data_ptr(), context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv,
                                      d, bs, nb, float(scale), ws_ptr, ws_bytes, _flags(overlap), _stream(dev, stream))
     _lib.check(st, "pkv_decode_step_int8kv")
+    return out
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) keys and values
+# Codes are uint8 tensors holding E4M3 bit patterns (view them as torch.float8_e4m3fn to read
+# their values); scales float32 per (block, kv head, slot), as for the int8 K + V cache.
+
+def empty_fp8kv_cache(num_blocks: int, num_kv_heads: int, block_size: int, device, head_dim: int = PKV_HEAD_DIM):
+    """Zero-filled (k_codes, k_scale, v_codes, v_scale) for the fp8 K + V cache (codes uint8)."""
+    codes = lambda: torch.zeros((num_blocks, num_kv_heads, block_size, head_dim), dtype=torch.uint8, device=device)
+    scales = lambda: torch.zeros((num_blocks, num_kv_heads, block_size), dtype=torch.float32, device=device)
+    return codes(), scales(), codes(), scales()
+
+
+def append_fp8kv(k_codes, k_scale, v_codes, v_scale, slot_mapping, k_new, v_new, stream=None) -> None:
+    """Quantise k_new and v_new [T, Hkv, D] into the fp8 K + V cache at slot_mapping [T]."""
+    nb, hkv, bs, d = _int8kv_shape(k_codes, k_scale, v_codes, v_scale, torch.uint8)
+    dev = k_codes.device
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    t = slot_mapping.shape[0]
+    if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
+    st = _L().pkv_append_fp8kv(k_codes.data_ptr(), k_scale.data_ptr(), v_codes.data_ptr(), v_scale.data_ptr(),
+                               slot_mapping.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), t, hkv, d, bs, nb,
+                               _stream(dev, stream))
+    _lib.check(st, "pkv_append_fp8kv")
+
+
+def decode_attention_fp8kv(out, q, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens, scale: float,
+                           workspace=None, stream=None) -> torch.Tensor:
+    """decode_attention over the fp8 K + V cache."""
+    nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes = _int8kv_inputs(q, k_codes, k_scale, v_codes, v_scale, block_tables,
+                                                                  context_lens, out, workspace, torch.uint8)
+    st = _L().pkv_decode_attention_fp8kv(out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), k_scale.data_ptr(),
+                                         v_codes.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
+                                         context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv, d, bs, nb,
+                                         float(scale), ws_ptr, ws_bytes, _stream(dev, stream))
+    _lib.check(st, "pkv_decode_attention_fp8kv")
+    return out
+
+
+def decode_step_fp8kv(out, q, k_new, v_new, k_codes, k_scale, v_codes, v_scale, block_tables, context_lens,
+                      scale: float, workspace=None, stream=None, overlap: bool = False) -> torch.Tensor:
+    """decode_step over the fp8 K + V cache; overlap as decode_step's."""
+    nb, hkv, bs, d, b, hq, dev, ws_ptr, ws_bytes = _int8kv_inputs(q, k_codes, k_scale, v_codes, v_scale, block_tables,
+                                                                  context_lens, out, workspace, torch.uint8)
+    _need(k_new, "k_new", torch.float16, 3, dev)
+    _need(v_new, "v_new", torch.float16, 3, dev)
+    if k_new.shape != (b, hkv, d) or v_new.shape != (b, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{b}, {hkv}, {d}]")
+    st = _L().pkv_decode_step_fp8kv(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                    k_codes.data_ptr(), k_scale.data_ptr(), v_codes.data_ptr(), v_scale.data_ptr(),
+                                    block_tables.data_ptr(), context_lens.data_ptr(), b, block_tables.shape[1], hq, hkv,
+                                    d, bs, nb, float(scale), ws_ptr, ws_bytes, _flags(overlap), _stream(dev, stream))
+    _lib.check(st, "pkv_decode_step_fp8kv")
     return out
 
 

@@ -78,6 +78,11 @@ SIGNATURES = {
                                                                             c_void_p]),
     "pkv_decode_step_int8kv": (c_int, [c_void_p] * 10 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
                                                                         c_uint, c_void_p]),
+    "pkv_append_fp8kv": (c_int, [c_void_p] * 7 + [c_int] * 4 + [c_int64, c_void_p]),
+    "pkv_decode_attention_fp8kv": (c_int, [c_void_p] * 8 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
+                                                                           c_void_p]),
+    "pkv_decode_step_fp8kv": (c_int, [c_void_p] * 10 + [c_int] * 6 + [c_int64, c_float, c_void_p, c_size_t,
+                                                                       c_uint, c_void_p]),
     "pkv_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int64, c_void_p]),
     "pkv_slot_mapping": (c_int, [c_i64p, c_i32p, c_i32p, c_int, c_int, c_int]),
     "pkv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,

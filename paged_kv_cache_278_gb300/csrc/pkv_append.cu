@@ -104,6 +104,49 @@ __global__ void __launch_bounds__(kAppendThreads)
     if (lane == 0) k_scale[dst] = s;
 }
 
+// fp8 (E4M3) keys and values: one warp per (token, kv head) row, lane i holds dims 4i..4i+3.
+// Each row's scale is max|x| / 448 from a warp max; codes are the nearest E4M3 values of x / scale
+// (float32 division), by the hardware conversion with round-to-nearest-even and clamping to 448.
+__device__ __forceinline__ uint32_t quantize_row_part_e4m3(uint2 raw, float &scale) {
+    const float2 x01 = pkv::half2_bits_to_float2(raw.x);
+    const float2 x23 = pkv::half2_bits_to_float2(raw.y);
+    float amax = fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(pkv::kFullMask, amax, sh));
+    const float s = __fdiv_rn(amax, 448.f);
+    scale = s;
+    return pkv::quantize_e4m3x2(x01.x, x01.y, s) | (pkv::quantize_e4m3x2(x23.x, x23.y, s) << 16);
+}
+
+__global__ void __launch_bounds__(kAppendThreads)
+    append_fp8kv_kernel(uint32_t *__restrict__ k_codes, float *__restrict__ k_scale, uint32_t *__restrict__ v_codes,
+                        float *__restrict__ v_scale, const int64_t *__restrict__ slot_mapping,
+                        const uint2 *__restrict__ k_new, const uint2 *__restrict__ v_new, int64_t rows,
+                        int num_kv_heads, int block_size, int64_t num_slots) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerAppendBlock + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;  // warp-uniform
+    const int head = static_cast<int>(row % num_kv_heads);
+    const int64_t token = row / num_kv_heads;
+    const int64_t slot = __ldg(slot_mapping + token);
+    if (slot < 0) return;  // padding token
+    if (slot >= num_slots) {
+        if (lane == 0) pkv::record_error(&g_append_error, PKV_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t block = slot / block_size;
+    const int64_t dst = (block * num_kv_heads + head) * block_size + (slot - block * block_size);
+    float ks, vs;
+    const uint32_t kc = quantize_row_part_e4m3(__ldg(k_new + row * 32 + lane), ks);
+    const uint32_t vc = quantize_row_part_e4m3(__ldg(v_new + row * 32 + lane), vs);
+    k_codes[dst * 32 + lane] = kc;
+    v_codes[dst * 32 + lane] = vc;
+    if (lane == 0) {
+        k_scale[dst] = ks;
+        v_scale[dst] = vs;
+    }
+}
+
 // Whole-block copies (copy-on-write within a pool, swap between a device pool and host swap
 // space): one thread per 16-byte piece of a block (all kv heads), K then V.  Plain loads and
 // stores, so either side may be page-locked host memory the GPU addresses directly.
@@ -206,6 +249,30 @@ extern "C" PKV_API int pkv_append_int8kv(void *k_codes, float *k_scale, void *v_
                                 reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<uint32_t *>(k_codes), k_scale, v_codes, v_scale, slot_mapping, static_cast<const uint2 *>(k_new),
         static_cast<const uint2 *>(v_new), rows, num_kv_heads, block_size, num_blocks * block_size);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" PKV_API int pkv_append_fp8kv(void *k_codes, float *k_scale, void *v_codes, float *v_scale,
+                                        const int64_t *slot_mapping, const void *k_new, const void *v_new,
+                                        int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                                        int64_t num_blocks, pkv_stream_t stream) {
+    if (!k_codes || !k_scale || !v_codes || !v_scale || (num_tokens > 0 && (!slot_mapping || !k_new || !v_new)))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != PKV_HEAD_DIM) return PKV_ERR_UNSUPPORTED;
+    if (!pkv_internal::aligned16(k_codes) || !pkv_internal::aligned(k_scale, 4) || !pkv_internal::aligned16(v_codes) ||
+        !pkv_internal::aligned(v_scale, 4) ||
+        (num_tokens > 0 && (!pkv_internal::aligned(slot_mapping, 8) || !pkv_internal::aligned(k_new, 8) ||
+                            !pkv_internal::aligned(v_new, 8))))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads;
+    const int64_t blocks = (rows + kRowsPerAppendBlock - 1) / kRowsPerAppendBlock;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    append_fp8kv_kernel<<<static_cast<unsigned>(blocks), kAppendThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint32_t *>(k_codes), k_scale, static_cast<uint32_t *>(v_codes), v_scale, slot_mapping,
+        static_cast<const uint2 *>(k_new), static_cast<const uint2 *>(v_new), rows, num_kv_heads, block_size,
+        num_blocks * block_size);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         const uint32_t dst = stage0 + st * L::stage;
         // TC: whole 16-row boxes (a ragged tail's extra rows stay inside the block and are masked)
         const uint32_t k_bytes = KQ ? L::k_tile + kChunk * 4 : (TC ? 2 * kHalfTile : bytes);
-        const uint32_t v_bytes = KQ == 2 ? L::v_tile + kChunk * 4 : (TC ? 2 * kHalfTile : bytes);
+        const uint32_t v_bytes = KQ >= 2 ? L::v_tile + kChunk * 4 : (TC ? 2 * kHalfTile : bytes);
         if (lane != 0) return;
         if (kSplitKV) {
             if (parts & 1) pkv::mbar_arrive_expect_tx(bar_k, k_bytes);
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
             }
         }
         if (parts & 2) {
-            if constexpr (KQ == 2) {  // one 16-row box of int8 values and their 16 scales
+            if constexpr (KQ >= 2) {  // one 16-row box of 8-bit value codes and their 16 scales
                 pkv::tma_load_2d(dst + L::k_tile, tmap_v, 0, static_cast<int>(y), bar_v);
                 pkv::bulk_copy_g2s(scale0 + st * L::scale_stride + kChunk * 4, vsc + y, kChunk * 4, bar_v);
             } else if constexpr (TC) {
@@ -478,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         const bool id_ok = id >= 0 && id < P.num_blocks;
         const int64_t grow = (static_cast<int64_t>(id) * P.num_kv_heads + kvh) * bs + new_pos % bs;
         if constexpr (KQ) {
-            // Lanes 0-15 quantise the K row (8 dims each; scale from a 16-lane max), 16-31 move V.
+            // Lanes 0-15 quantise the K row (8 dims each; scale from a 16-lane max), 16-31 move V
+            // (or quantise it the same way).
             const uint32_t w[4] = {new_row.x, new_row.y, new_row.z, new_row.w};
             float f[8];
 #pragma unroll
@@ -492,13 +493,22 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
             for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
 #pragma unroll
             for (int sh = 8; sh >= 1; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(pkv::kFullMask, amax, sh));
-            const float sc = __fdiv_rn(amax, 127.f);
-            if (lane < 16) {
+            const float sc = __fdiv_rn(amax, KQ == 3 ? 448.f : 127.f);
+            // this lane's 8 codes, dims in byte order
+            auto encode = [&]() {
                 uint32_t c[2] = {0u, 0u};
+                if constexpr (KQ == 3) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    c[e >> 2] |= (static_cast<uint32_t>(pkv::quantize_int8(f[e], sc)) & 0xffu) << (8 * (e & 3));
-                const uint2 codes = make_uint2(c[0], c[1]);
+                    for (int e = 0; e < 8; e += 2) c[e >> 2] |= pkv::quantize_e4m3x2(f[e], f[e + 1], sc) << (8 * (e & 3));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        c[e >> 2] |= (static_cast<uint32_t>(pkv::quantize_int8(f[e], sc)) & 0xffu) << (8 * (e & 3));
+                }
+                return make_uint2(c[0], c[1]);
+            };
+            if (lane < 16) {
+                const uint2 codes = encode();
                 *reinterpret_cast<uint2 *>(s_newrow + lane * 8) = codes;
                 if (lane == 0) *reinterpret_cast<float *>(s_newrow + kD) = sc;
                 if (id_ok) {
@@ -506,13 +516,9 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                         codes;
                     if (lane == 0) P.k_scale_w[grow] = sc;
                 }
-            } else if (KQ == 2) {  // lanes 16-31 quantise the V row the same way
+            } else if (KQ >= 2) {  // lanes 16-31 quantise the V row the same way
                 const int l16 = lane & 15;
-                uint32_t c[2] = {0u, 0u};
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    c[e >> 2] |= (static_cast<uint32_t>(pkv::quantize_int8(f[e], sc)) & 0xffu) << (8 * (e & 3));
-                const uint2 codes = make_uint2(c[0], c[1]);
+                const uint2 codes = encode();
                 *reinterpret_cast<uint2 *>(s_newrow + 2 * kD + l16 * 8) = codes;
                 if (l16 == 0) *reinterpret_cast<float *>(s_newrow + 3 * kD) = sc;
                 if (id_ok) {
@@ -577,16 +583,23 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
         auto fix_v = [&]() {
             bool touched = false;
             // (int8 values need no clearing: codes are finite and the scaled weights of the unused
-            // rows are forced to zero)
-            if (TC && KQ != 2 && valid < kChunk) {
+            // rows are forced to zero; fp8 codes include NaN, so their unused rows are zeroed)
+            if (TC && KQ != 2 && KQ != 3 && valid < kChunk) {
                 for (int x = lane; x < (kChunk - valid) * 16; x += 32)
                     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + TcEngine<4>::swz(valid + x / 16, x % 16)),
                                  "r"(0)
                                  : "memory");
                 touched = true;
             }
+            if (KQ == 3 && valid < kChunk) {
+                for (int x = lane; x < (kChunk - valid) * 8; x += 32)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_tile + TcEngineQ<G>::swz8(valid + x / 8, x % 8)),
+                                 "r"(0)
+                                 : "memory");
+                touched = true;
+            }
             if (own) {
-                if (KQ == 2 && lane >= 16) {  // int8 value row (8 bytes a lane) and its scale
+                if (KQ >= 2 && lane >= 16) {  // 8-bit value row (8 bytes a lane) and its scale
                     const int l16 = lane & 15;
                     const uint2 nc = *reinterpret_cast<const uint2 *>(s_newrow + 2 * kD + l16 * 8);
                     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(v_tile + TcEngineQ<G>::swz8(nr_row, l16 >> 1) +
@@ -597,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
                         asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_tile + kChunk * 4 + nr_row * 4),
                                      "f"(*reinterpret_cast<const float *>(s_newrow + 3 * kD))
                                      : "memory");
-                } else if (KQ != 2 && lane >= 16) {
+                } else if (KQ < 2 && lane >= 16) {
                     const uint4 nr = *reinterpret_cast<const uint4 *>(s_newrow + lane * 16);
                     const uint32_t row = TC ? TcEngine<4>::swz(nr_row, lane & 15) : nr_row * kRow + (lane & 15) * 16;
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(v_tile + row), "r"(nr.x), "r"(nr.y),
@@ -919,7 +932,7 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
         if (rows >= 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // box row coordinates are signed 32-bit
         int st = KQ ? encode_code_map(&p.tmap_k, p.k_cache, rows) : encode_cache_map(&p.tmap_k, p.k_cache, rows);
         if (st == PKV_OK)
-            st = KQ == 2 ? encode_code_map(&p.tmap_v, p.v_cache, rows) : encode_cache_map(&p.tmap_v, p.v_cache, rows);
+            st = KQ >= 2 ? encode_code_map(&p.tmap_v, p.v_cache, rows) : encode_cache_map(&p.tmap_v, p.v_cache, rows);
         if (st != PKV_OK) return st;
     }
     using L = SmemLayout<TC, KQ, MQ == 2 ? 2 : 1, stages_of<MQ>(), new_rows_of<MQ>()>;
@@ -969,7 +982,9 @@ int launch_mode(const DecodeParams &p, int num_seqs, cudaStream_t stream, int gr
     if (p.query_start)
         return p.mq_tiles == 2 ? launch_partition<G, 0, 2>(p, num_seqs, stream, grid_parts)
                                : launch_partition<G, 0, 1>(p, num_seqs, stream, grid_parts);
-    if (p.k_scale && p.v_scale) return launch_partition<G, 2, 0>(p, num_seqs, stream, grid_parts);
+    if (p.k_scale && p.v_scale)
+        return p.kv_fp8 ? launch_partition<G, 3, 0>(p, num_seqs, stream, grid_parts)
+                        : launch_partition<G, 2, 0>(p, num_seqs, stream, grid_parts);
     if (p.k_scale) return launch_partition<G, 1, 0>(p, num_seqs, stream, grid_parts);
     return launch_partition<G, 0, 0>(p, num_seqs, stream, grid_parts);
 }
@@ -1081,20 +1096,22 @@ extern "C" PKV_API int pkv_merge(void *out, const float *o_part, const float *m_
 namespace {
 
 // pkv_decode_attention, optionally appending the new token first (k_new/v_new non-null).
-// k_scale non-null: k_cache holds int8 codes with these float32 row scales.
+// k_scale non-null: k_cache holds int8 codes with these float32 row scales (v_scale too: so does
+// v_cache).  kv_fp8 (with both scales): the codes are E4M3 instead of int8.
 int decode_attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                           int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, const void *k_new, const void *v_new, void *workspace,
                           size_t workspace_bytes, pkv_stream_t stream, const float *k_scale = nullptr,
                           int partition_size = PKV_DEFAULT_PARTITION, const float *v_scale = nullptr,
-                          unsigned flags = 0) {
+                          unsigned flags = 0, bool kv_fp8 = false) {
     if (flags & ~PKV_STEP_OVERLAP) return PKV_ERR_INVALID_ARG;
     int st = check_common(q, k_cache, v_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks);
     if (st != PKV_OK) return st;
     if (k_scale && !pkv_internal::aligned16(k_scale)) return PKV_ERR_INVALID_ARG;
     if (v_scale && (!k_scale || !pkv_internal::aligned16(v_scale))) return PKV_ERR_INVALID_ARG;
+    if (kv_fp8 && !v_scale) return PKV_ERR_INVALID_ARG;
     if (!out || !pkv_internal::aligned(out, 8)) return PKV_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
     if (k_new && (!pkv_internal::aligned16(k_new) || !pkv_internal::aligned16(v_new))) return PKV_ERR_INVALID_ARG;
@@ -1128,6 +1145,7 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     p.k_scale_w = const_cast<float *>(k_scale);
     p.v_scale = v_scale;
     p.v_scale_w = const_cast<float *>(v_scale);
+    p.kv_fp8 = kv_fp8 ? 1 : 0;
     p.overlap = (flags & PKV_STEP_OVERLAP) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
@@ -1363,6 +1381,35 @@ extern "C" PKV_API int pkv_decode_step_int8kv(void *out, const void *q, const vo
     return decode_attention_impl(out, q, k_codes, v_codes, block_tables, context_lens, num_seqs, max_blocks_per_seq,
                                  num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
                                  workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale, flags);
+}
+
+// ------------------------------------------------------------------ fp8 (E4M3) keys and values
+
+extern "C" PKV_API int pkv_decode_attention_fp8kv(void *out, const void *q, const void *k_codes,
+                                                  const float *k_scale, const void *v_codes, const float *v_scale,
+                                                  const int32_t *block_tables, const int32_t *context_lens,
+                                                  int num_seqs, int max_blocks_per_seq, int num_q_heads,
+                                                  int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                                  float scale, void *workspace, size_t workspace_bytes,
+                                                  pkv_stream_t stream) {
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_codes, v_codes, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, nullptr, nullptr,
+                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale, 0u, true);
+}
+
+extern "C" PKV_API int pkv_decode_step_fp8kv(void *out, const void *q, const void *k_new, const void *v_new,
+                                             void *k_codes, float *k_scale, void *v_codes, float *v_scale,
+                                             const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                             int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                                             int head_dim, int block_size, int64_t num_blocks, float scale,
+                                             void *workspace, size_t workspace_bytes, unsigned flags,
+                                             pkv_stream_t stream) {
+    if (!k_new || !v_new || !k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    return decode_attention_impl(out, q, k_codes, v_codes, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_new, v_new,
+                                 workspace, workspace_bytes, stream, k_scale, PKV_DEFAULT_PARTITION, v_scale, flags,
+                                 true);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

@@ -145,6 +145,26 @@ __device__ __forceinline__ int quantize_int8(float x, float s) {
     return c > 127 ? 127 : (c < -127 ? -127 : c);
 }
 
+// Four E4M3 codes (8-bit floating point: sign, 4 exponent bits with bias 7, 3 fraction bits,
+// largest finite 448) -> two fp16x2, exactly (every E4M3 value is an fp16 value): bytes 0, 1 go
+// to the low and high half of lo, bytes 2, 3 to those of hi.  One hardware conversion per pair.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// E4M3 codes of x / s for the row scale s = max|x| / 448: the nearest code (ties to the even
+// code, the sign kept when rounding to zero), |x / s| clamped to 448, with IEEE float32
+// division; code 0 when s == 0.  lo goes to bits 0-7, hi to bits 8-15.
+__device__ __forceinline__ uint32_t quantize_e4m3x2(float lo, float hi, float s) {
+    if (s == 0.f) return 0u;
+    const float ylo = __fdiv_rn(lo, s), yhi = __fdiv_rn(hi, s);
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(yhi), "f"(ylo));
+    return r;
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -115,6 +115,7 @@ struct DecodeParams {
     float *k_scale_w;         // writable view of k_scale for the fused append
     const float *v_scale;     // int8 values too: float32 scale per (block, kv head, slot); null for fp16 values
     float *v_scale_w;
+    int kv_fp8;               // with k_scale and v_scale: the codes are E4M3 (fp8), not int8
     int overlap;              // 1: stream the cache history before the preceding kernel completes
     int prefix_ctas;          // shared-prefix step in one grid: CTAs [0, prefix_ctas) are prefix tiles
     int prefix_chunks;        //   128-token prefix chunks (partial slots [0, prefix_chunks))
@@ -135,7 +136,7 @@ constexpr int kHalfTile = kChunk * 128;
 // Row stride (floats) of the warps' partial results in the combine area: 4 floats of padding so
 // the fragment-ordered stores of eight rows at once spread over all 32 banks.
 constexpr int kAccStride = kD + 4;
-// KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values.  NR: new token rows staged for a fused
+// KQ: 0 fp16 K/V, 1 int8 keys, 2 int8 keys and values, 3 fp8 (E4M3) keys and values.  NR: new token rows staged for a fused
 // append (one for a single-token step; up to PKV_MAX_STEP_QUERY_LEN for a several-token step).
 // The 16-row engine (NT = 2) keeps P in registers and needs no per-warp weight buffer.
 template <bool TC, int KQ = 0, int NT = 1, int NS = kStages, int NR = 1>
@@ -143,9 +144,9 @@ struct SmemLayout {
     static constexpr int row = kRowBytes;
     static constexpr int tile = kChunk * row;
     static constexpr int k_tile = KQ ? kChunk * kD : tile;
-    static constexpr int v_tile = KQ == 2 ? kChunk * kD : tile;
+    static constexpr int v_tile = KQ >= 2 ? kChunk * kD : tile;
     static constexpr int stage = k_tile + v_tile;
-    static constexpr int scale_stride = KQ == 2 ? 2 * kChunk * 4 : kChunk * 4;  // K scales (| V scales) per stage
+    static constexpr int scale_stride = KQ >= 2 ? 2 * kChunk * 4 : kChunk * 4;  // K scales (| V scales) per stage
     static constexpr int stages = 0;
     static constexpr int stage_bytes = kWarps * NS * stage;
     static constexpr int scales = stages + stage_bytes;
@@ -868,6 +869,73 @@ struct TcEngineQV : TcEngineQ<G> {
     }
 };
 
+// ---------------------------------------------------------------- fp8 (E4M3) keys and values
+// TcEngineQV's tiles, dim permutations, scales and weights with E4M3 codes: each code pair
+// becomes an fp16x2 MMA operand by one hardware conversion (exact), in place of the int8 codes'
+// sign flip, byte permute and fp16 subtract.  The value pairs are still formed across tokens by
+// one byte permute per A register pair.  Unused value rows of a ragged tail are cleared before
+// P.V (E4M3 has NaN codes, and NaN x 0 is NaN).
+template <int G>
+struct TcEngineF8 : TcEngineQ<G> {
+    __device__ __forceinline__ void qk(uint32_t k_tile, uint32_t s_tile, int valid, int lane, unsigned char *scratch,
+                                       int) {
+        const int g = lane >> 2, t = lane & 3;
+        const uint4 r0 = pkv::lds128(k_tile + TcEngineQ<G>::swz8(g, 2 * t));
+        const uint4 r1 = pkv::lds128(k_tile + TcEngineQ<G>::swz8(g, 2 * t + 1));
+        const uint4 r8 = pkv::lds128(k_tile + TcEngineQ<G>::swz8(g + 8, 2 * t));
+        const uint4 r9 = pkv::lds128(k_tile + TcEngineQ<G>::swz8(g + 8, 2 * t + 1));
+        const uint32_t wg[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const uint32_t w8[8] = {r8.x, r8.y, r8.z, r8.w, r9.x, r9.y, r9.z, r9.w};
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t a[4];
+            pkv::e4m3x4_to_h2x2(wg[ks], a[0], a[2]);
+            pkv::e4m3x4_to_h2x2(w8[ks], a[1], a[3]);
+            pkv::mma16816(s, a, this->qb[ks][0], this->qb[ks][1]);
+        }
+        const float fg = this->q_scale * pkv::lds32f(s_tile + 4 * g);
+        const float f8 = this->q_scale * pkv::lds32f(s_tile + 4 * (g + 8));
+        s[0] = g < valid ? s[0] * fg : -INFINITY;
+        s[1] = g < valid ? s[1] * fg : -INFINITY;
+        s[2] = g + 8 < valid ? s[2] * f8 : -INFINITY;
+        s[3] = g + 8 < valid ? s[3] * f8 : -INFINITY;
+        this->template softmax<false, true>(s, lane, scratch, s_tile + kChunk * 4);
+    }
+
+    __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *scratch) {
+        const __half *ph = reinterpret_cast<const __half *>(scratch);
+        const __half *pl = ph + 8 * kChunk;
+        const int g = lane >> 2, t = lane & 3, k0 = t * 2;
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0);
+        const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0 + 8);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0);
+        const uint32_t bl1 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0 + 8);
+        const uint4 r0 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t, g));
+        const uint4 r1 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 1, g));
+        const uint4 r8 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 8, g));
+        const uint4 r9 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 9, g));
+        const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+        const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w}, w9[4] = {r9.x, r9.y, r9.z, r9.w};
+#pragma unroll
+        for (int mt = 0; mt < kD / 16; ++mt) {
+            // bytes 2mt, 2mt+1 (dims 16g + 2mt, +1) of the two token rows, interleaved token-wise
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t xa = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
+            const uint32_t xb = __byte_perm(w8[mt >> 1], w9[mt >> 1], sel);
+            uint32_t a[4];
+            pkv::e4m3x4_to_h2x2(xa, a[0], a[1]);
+            pkv::e4m3x4_to_h2x2(xb, a[2], a[3]);
+            pkv::mma16816(this->o[mt], a, bh0, bh1);
+            pkv::mma16816(this->o[mt], a, bl0, bl1);
+        }
+    }
+
+    __device__ __forceinline__ void finish(int warp, int lane, float *c_acc, float *c_m, float *c_l) {
+        TcEngine<G>::template finish<true>(warp, lane, c_acc, c_m, c_l);
+    }
+};
+
 // ---------------------------------------------------------------- several new tokens per request
 // The 8 MMA columns carry (token, head) rows r = 8 rg + c of the request's n * G rows for this kv
 // head (token r / G, head r % G), so a verified draft or a prefill chunk is the same tile as a
@@ -1103,9 +1171,11 @@ using EngineFor = typename std::conditional<
     MQ == 2, TcEngineR16<G>,
     typename std::conditional<MQ == 1, TcEngineM<G>,
     typename std::conditional<
+        KQ == 3, TcEngineF8<G>,
+    typename std::conditional<
         KQ == 2, TcEngineQV<G>,
         typename std::conditional<
             KQ == 1, TcEngineQ<G>,
-            typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type>::type>::type;
+            typename std::conditional<TC, TcEngine<(TC ? G : 4)>, FmaEngine<G, LPT>>::type>::type>::type>::type>::type>::type;
 
 }  // namespace

@@ -78,8 +78,9 @@ def test_decode_bytes_model_by_hand():
     assert bench.decode_bytes(ctx, hkv, hq, d, bs) == fp16
     # int8 keys: a key row is 128 codes + a float32 scale; values stay fp16
     assert bench.decode_bytes(ctx, hkv, hq, d, bs, kv="int8k") == 53 * hkv * ((d + 4) + kv_row) + qo + tables
-    # int8 keys and values
+    # int8 keys and values; fp8 keys and values (the same bytes)
     assert bench.decode_bytes(ctx, hkv, hq, d, bs, kv="int8kv") == 53 * hkv * 2 * (d + 4) + qo + tables
+    assert bench.decode_bytes(ctx, hkv, hq, d, bs, kv="fp8kv") == 53 * hkv * 2 * (d + 4) + qo + tables
     # several new tokens per request: q and out counted per token
     assert bench.decode_bytes(ctx, hkv, hq, d, bs, q_len=3) == fp16 + 2 * qo
     # a shared 16-token prefix counted once: unique tokens = 20 + 33 - 16
@@ -97,6 +98,8 @@ def test_decode_bytes_of_the_mha7b_workload():
     ["--warmup", "2"],                                                   # fewer than 3 warm-up steps
     ["--workload", "shared_prefix", "--kv", "int8k"],                    # the cascade reads fp16 K/V
     ["--workload", "shared_prefix", "--kv", "int8kv"],
+    ["--workload", "shared_prefix", "--kv", "fp8kv"],
+    ["--query-len", "4", "--kv", "fp8kv"],
     ["--query-len", "4", "--kv", "int8k"],                               # several tokens: fp16 path only
     ["--query-len", "4", "--workload", "shared_prefix"],
     ["--query-len", "2", "--impl", "reference"],                         # the reference arm times single tokens

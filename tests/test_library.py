@@ -154,6 +154,20 @@ def test_int8k_multi_copy_invalid_arguments(lib):
     assert lib.pkv_decode_step_int8kv(p, p, p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 0,
                                       null) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_append_int8kv(p, p, p, p, null, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
+    # fp8 keys and values: the same argument rules
+    assert lib.pkv_append_fp8kv(p, p, p, null, p, p, p, 1, 1, 128, 16, 4, null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_append_fp8kv(p, p, p, p, p, p, p, 1, 1, 64, 16, 4, null) == _lib.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_decode_attention_fp8kv(p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_attention_fp8kv(p, p, p, p, p, bad, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_attention_fp8kv(p, p, p, null, p, p, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
+                                          null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_fp8kv(p, p, p, p, p, p, p, null, p, p, 1, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 0,
+                                     null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_step_fp8kv(p, p, p, p, p, p, p, p, p, p, 0, 1, 1, 1, 128, 16, 4, 1.0, null, 0, 8,
+                                     null) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_append_fp8kv(p, p, p, p, null, null, null, 0, 1, 128, 16, 4, null) == _lib.PKV_OK
     # several tokens per request: null query_start, query length beyond the limit, no workspace
     assert lib.pkv_decode_attention_multi(p, p, p, p, p, p, null, 1, 4, 4, 1, 1, 1, 128, 16, 4, 1.0, null, 0,
                                           null) == _lib.PKV_ERR_INVALID_ARG

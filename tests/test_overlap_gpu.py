@@ -15,6 +15,7 @@ from gpu_util import ATTN_TOL, assert_no_device_error, host_inputs, max_err, ora
 from test_shared_prefix_gpu import with_prefix
 import test_int8k_gpu as i8k
 import test_int8kv_gpu as i8kv
+import test_fp8kv_gpu as f8kv
 
 pytestmark = pytest.mark.gpu
 
@@ -166,6 +167,31 @@ def test_int8kv_steps():
         d, (kc, ks, vc, vs) = devs[l], pools[l]
         pkv.decode_step_int8kv(out, d.q, d.k_new, d.v_new, kc, ks, vc, vs, d.block_tables, d.context_lens, d.scale,
                                workspace=ws, overlap=overlap)
+
+    check_overlap(fn, outs, refs)
+
+
+def test_fp8kv_steps():
+    cases = [workloads.random_case(870 + l, LENS, 32, 8, block_size=16, extra_blocks=3) for l in range(LAYERS)]
+    refs, pools = [], []
+    for c in cases:
+        pool = f8kv.quantised_pool(c)
+        h = c.to("cpu")
+        bt = h.block_tables.numpy()
+        host = tuple(a.copy() for a in pool)
+        oracle.append_fp8_kv(*host, oracle.slot_mapping(bt, h.positions.numpy(), c.block_size),
+                             h.k_new.numpy(), h.v_new.numpy())
+        refs.append(oracle.decode_fp8_kv(h.q.numpy(), *host, bt, h.context_lens.numpy(), c.scale))
+        pools.append(f8kv.to_dev(*pool))
+    devs = [c.to("cuda") for c in cases]
+    c0 = cases[0]
+    ws = pkv.make_workspace(c0.num_seqs, c0.num_q_heads, c0.max_blocks_per_seq * 16, "cuda")
+    outs = [torch.empty_like(d.q) for d in devs]
+
+    def fn(l, out, overlap):
+        d, (kc, ks, vc, vs) = devs[l], pools[l]
+        pkv.decode_step_fp8kv(out, d.q, d.k_new, d.v_new, kc, ks, vc, vs, d.block_tables, d.context_lens, d.scale,
+                              workspace=ws, overlap=overlap)
 
     check_overlap(fn, outs, refs)
 
