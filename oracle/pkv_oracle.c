@@ -545,22 +545,41 @@ double oracle_e4m3_to_double(uint8_t c)
 
 /* The E4M3 code whose value is nearest to y (ties: the code with an even fraction),
  * |y| clamped to 448 first; the sign bit is y's, as in any IEEE rounding (a negative y
- * that rounds to zero gives -0, code 0x80).  Brute force over the 127 finite
- * non-negative codes, whose values increase with the code, so "even fraction" is
- * "even code". */
+ * that rounds to zero gives -0, code 0x80).  The finite non-negative codes 0 .. 0x7E
+ * have increasing values, so "even fraction" is "even code" and the nearest code is
+ * one of the two neighbours of |y| in that sorted table, found by bisection. */
+static double e4m3_table[0x7f];                /* value of codes 0 .. 0x7E, filled once */
+static int e4m3_table_ready;
+
+static double e4m3_value(int c)
+{
+    if (!e4m3_table_ready) {
+        for (int i = 0; i < 0x7f; ++i)
+            e4m3_table[i] = oracle_e4m3_to_double((uint8_t)i);
+        e4m3_table_ready = 1;
+    }
+    return e4m3_table[c];
+}
+
 uint8_t oracle_e4m3_from_float(float y)
 {
     double a = fabs((double)y);
     if (a > 448.0)
         a = 448.0;
-    int best = 0;
-    double best_err = a;                       /* code 0 has value 0 */
-    for (int c = 1; c <= 0x7e; ++c) {
-        double err = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
-        if (err < best_err || (err == best_err && (c & 1) == 0)) {
-            best = c;
-            best_err = err;
-        }
+    int lo = 0, hi = 0x7e;                     /* invariant: value(lo) <= a */
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (e4m3_value(mid) <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    int best = lo;
+    if (lo < 0x7e) {
+        double below = a - e4m3_value(lo);
+        double above = e4m3_value(lo + 1) - a;
+        if (above < below || (above == below && ((lo + 1) & 1) == 0))
+            best = lo + 1;
     }
     return (uint8_t)(signbit(y) ? (best | 0x80) : best);
 }

@@ -53,7 +53,8 @@ MUTANTS = {
                              "int64_t per_block = (int64_t)block_size * head_dim;"),
     "e4m3_exponent_bias": ("v = ldexp((double)(8 + frac), expo - 10);", "v = ldexp((double)(8 + frac), expo - 11);"),
     "e4m3_subnormal_step": ("v = ldexp((double)frac, -9);", "v = ldexp((double)frac, -10);"),
-    "e4m3_ties_to_odd": ("(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    "e4m3_ties_to_odd": ("(above == below && ((lo + 1) & 1) == 0)", "(above == below && ((lo + 1) & 1) == 1)"),
+    "e4m3_rounds_down": ("if (above < below || (above == below", "if (above < below - 1e300 || (above == below"),
     "e4m3_sign_dropped": ("return (uint8_t)(signbit(y) ? (best | 0x80) : best);", "return (uint8_t)best;"),
     "fp8_step_127": ("float s = amax / 448.0f;", "float s = amax / 127.0f;"),
     "fp8_v_from_k": ("oracle_quantize_fp8_row(v_codes + row * head_dim, v_scale + row, v_new + src, head_dim);",
