@@ -152,6 +152,7 @@ struct SmemLayout {
     static constexpr int scales = stages + stage_bytes;
     static constexpr int bars = scales + (KQ ? kWarps * NS * scale_stride : 0);
     static constexpr int probs = bars + kWarps * NS * kBarsPerStage * 8;
+    static_assert(probs % 16 == 0, "the weight rows are read by ldmatrix (16-byte rows)");
     __host__ __device__ static constexpr int probs_per_warp(int g) {
         return TC ? (NT == 2 ? 0 : NT * 2 * 8 * kChunk * 2) : kChunk * g * 4;
     }
@@ -686,29 +687,33 @@ struct TcEngine {
 #pragma unroll
             for (int e = 0; e < 4; ++e) p[e] = p[e] == 0.f ? 0.f : p[e] * (e < 2 ? vg : v8);  // masked rows: 0
         }
-        // P^T through shared memory as fp16 hi / lo: [2][8 heads][16 tokens]
-        __half *ph = reinterpret_cast<__half *>(scratch);
-        __half *pl = ph + 8 * kChunk;
-        const int h0 = (lane & 3) * 2;
+        // P^T through shared memory as fp16 hi / lo rows, [2][16 tokens][8 heads] (16 bytes a row):
+        // this lane's two columns of tokens g and g + 8, one 32-bit store each
+        const uint32_t base = pkv::smem_addr(scratch) + (lane & 3) * 4;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int idx = (h0 + (e & 1)) * kChunk + g + (e >> 1) * 8;
-            const __half hi = __float2half_rn(p[e]);
-            ph[idx] = hi;
-            pl[idx] = __float2half_rn(p[e] - __half2float(hi));
+        for (int r = 0; r < 2; ++r) {
+            const __half2 hi = __floats2half2_rn(p[2 * r], p[2 * r + 1]);
+            const __half2 lo = __floats2half2_rn(p[2 * r] - __low2float(hi), p[2 * r + 1] - __high2float(hi));
+            const uint32_t row = base + (g + 8 * r) * 16;
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(row), "r"(*reinterpret_cast<const uint32_t *>(&hi)) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(row + 256), "r"(*reinterpret_cast<const uint32_t *>(&lo))
+                         : "memory");
         }
         __syncwarp();
     }
 
+    // The B fragments of P^T (16 tokens x 8 heads; hi then lo) that softmax() left in scratch: one
+    // transposing matrix load, lanes 8m .. 8m + 7 addressing the rows of matrix m (hi tokens 0-7,
+    // hi 8-15, lo 0-7, lo 8-15), so each lane gets tokens 2t, 2t + 1 (and + 8) of head lane / 4.
+    __device__ __forceinline__ static void weights(uint32_t (&b)[4], int lane, const unsigned char *scratch) {
+        pkv::ldsm_x4_trans(b, pkv::smem_addr(scratch) + (lane >> 4) * 256 + ((lane >> 3) & 1) * 128 + (lane & 7) * 16);
+    }
+
     // O^T += V_tile^T . P^T with the weights softmax() left in scratch.
     __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *scratch) {
-        const __half *ph = reinterpret_cast<const __half *>(scratch);
-        const __half *pl = ph + 8 * kChunk;
-        const int n = lane >> 2, k0 = (lane & 3) * 2;
-        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + n * kChunk + k0);
-        const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + n * kChunk + k0 + 8);
-        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(pl + n * kChunk + k0);
-        const uint32_t bl1 = *reinterpret_cast<const uint32_t *>(pl + n * kChunk + k0 + 8);
+        uint32_t b[4];
+        weights(b, lane, scratch);
+        const uint32_t bh0 = b[0], bh1 = b[1], bl0 = b[2], bl1 = b[3];
 #pragma unroll
         for (int mt = 0; mt < kD / 16; ++mt) {
             uint32_t a[4];
@@ -838,13 +843,10 @@ struct TcEngineQV : TcEngineQ<G> {
     }
 
     __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *scratch) {
-        const __half *ph = reinterpret_cast<const __half *>(scratch);
-        const __half *pl = ph + 8 * kChunk;
-        const int g = lane >> 2, t = lane & 3, k0 = t * 2;
-        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0);
-        const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0 + 8);
-        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0);
-        const uint32_t bl1 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0 + 8);
+        const int g = lane >> 2, t = lane & 3;
+        uint32_t b[4];
+        TcEngine<G>::weights(b, lane, scratch);
+        const uint32_t bh0 = b[0], bh1 = b[1], bl0 = b[2], bl1 = b[3];
         const uint4 r0 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t, g));
         const uint4 r1 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 1, g));
         const uint4 r8 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 8, g));
@@ -904,13 +906,10 @@ struct TcEngineF8 : TcEngineQ<G> {
     }
 
     __device__ __forceinline__ void pv(uint32_t v_tile, int, int lane, unsigned char *scratch) {
-        const __half *ph = reinterpret_cast<const __half *>(scratch);
-        const __half *pl = ph + 8 * kChunk;
-        const int g = lane >> 2, t = lane & 3, k0 = t * 2;
-        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0);
-        const uint32_t bh1 = *reinterpret_cast<const uint32_t *>(ph + g * kChunk + k0 + 8);
-        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0);
-        const uint32_t bl1 = *reinterpret_cast<const uint32_t *>(pl + g * kChunk + k0 + 8);
+        const int g = lane >> 2, t = lane & 3;
+        uint32_t b[4];
+        TcEngine<G>::weights(b, lane, scratch);
+        const uint32_t bh0 = b[0], bh1 = b[1], bl0 = b[2], bl1 = b[3];
         const uint4 r0 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t, g));
         const uint4 r1 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 1, g));
         const uint4 r8 = pkv::lds128(v_tile + TcEngineQ<G>::swz8(2 * t + 8, g));
