@@ -216,7 +216,10 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     // The block ids of this warp's first chunks and q depend only on (b, kv head, partition):
     // load them now, in parallel with the context length.
     const int cap = P.max_blocks_per_seq * bs;
-    const int start = P.token_offset + part * P.partition_size;
+    // Partition p covers [first(p), first(p + 1)) with first(p) = offset + p * partition_size, less
+    // the stagger for odd p; the last partition ends at the context.
+    auto part_first = [&P](int p) { return P.token_offset + p * P.partition_size - ((p & 1) ? P.stagger : 0); };
+    const int start = part_first(part);
     int32_t first_ids[kStages];
 #pragma unroll
     for (int k = 0; k < kStages; ++k) {
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, (!TC && G >= 8) ? 2 : (KQ ? PKV_DECO
     }
     if (part >= n_parts) return;
 
-    const int n_tok = min(P.partition_size, ctx - start);
+    const int n_tok = (part == n_parts - 1 ? ctx : part_first(part + 1)) - start;
     const int n_chunks = (n_tok + kChunk - 1) / kChunk;
     const int lb0 = start / bs;
     const int n_bt = (start + n_tok - 1) / bs - lb0 + 1;
@@ -939,7 +942,7 @@ int launch_partition(const DecodeParams &p_in, int num_seqs, cudaStream_t stream
     // three fp16 tensor-core CTAs per SM at the default partition (228 KB; 1 KB static and 1 KB
     // reserved per CTA)
     static_assert(!TC || KQ || 3 * (L::total(G, PKV_DEFAULT_PARTITION) + 2048) <= 228 * 1024, "3 CTAs per SM");
-    const int smem = L::total(G, p.partition_size);
+    const int smem = L::total(G, p.partition_size + p.stagger);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     static std::atomic<uint64_t> configured{0};  // one bit per device
@@ -1021,6 +1024,9 @@ int check_common(const void *q, const void *k_cache, const void *v_cache, const 
 }
 
 using pkv_internal::align256;
+
+constexpr int kStaggerMinParts = 8;
+constexpr int kStaggerMinWaves = 3;
 
 // Split workspace layout: o_part | m_part | l_part | counters, each 256-byte aligned.
 size_t counters_offset(size_t rows) {
@@ -1149,6 +1155,20 @@ int decode_attention_impl(void *out, const void *q, const void *k_cache, const v
     p.overlap = (flags & PKV_STEP_OVERLAP) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_parts <= 1) return dispatch_partition(p, num_seqs, num_q_heads / num_kv_heads, s);
+    // Equal partitions in several waves start together and end together, and the SMs idle at every
+    // wave boundary until the next wave's first copies land; partitions of alternating length
+    // (P - P/4, P + P/4) end at staggered times.  Taken when a request can span kStaggerMinParts
+    // partitions and the grid fills kStaggerMinWaves waves of resident CTAs: with fewer, the longer
+    // partitions only lengthen the critical path.
+    const int stagger = part / 4 / kChunk * kChunk;
+    if (max_parts >= kStaggerMinParts && stagger > 0 && part + stagger <= PKV_MAX_PARTITION) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        const int64_t slots = static_cast<int64_t>(sms) * (k_scale ? PKV_DECODE_KQ_MIN_CTAS : PKV_DECODE_MIN_CTAS);
+        if (static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts >= kStaggerMinWaves * slots) p.stagger = stagger;
+    }
 
     const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, static_cast<int>(cap), part);
     if (!workspace || workspace_bytes < need || !pkv_internal::aligned(workspace, 256)) return PKV_ERR_WORKSPACE;

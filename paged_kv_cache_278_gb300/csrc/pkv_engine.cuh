@@ -117,6 +117,8 @@ struct DecodeParams {
     float *v_scale_w;
     int kv_fp8;               // with k_scale and v_scale: the codes are E4M3 (fp8), not int8
     int overlap;              // 1: stream the cache history before the preceding kernel completes
+    int stagger;              // automatic split: odd partitions start this many tokens early, so the
+                              //   partitions alternate partition_size -/+ stagger tokens (0: all equal)
     int prefix_ctas;          // shared-prefix step in one grid: CTAs [0, prefix_ctas) are prefix tiles
     int prefix_chunks;        //   128-token prefix chunks (partial slots [0, prefix_chunks))
     int grid_parts;           //   suffix partitions per (request, kv head) in the grid
