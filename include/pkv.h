@@ -50,6 +50,11 @@
  *     traps, asserts or spins without bound.
  *   * Thread safety: calls may be issued from several host threads; the
  *     pool object is not internally locked (one owner thread per pool).
+ *   * Cache formats: fp16 K and V (the calls without a suffix); int8 keys with
+ *     fp16 values (*_int8k); int8 keys and values (*_int8kv); fp8 (E4M3) keys
+ *     and values (*_fp8kv).  The 8-bit forms keep one float32 scale per
+ *     (token, kv head) row beside the codes; their sections below give the
+ *     layouts and the quantisation rule.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -299,7 +304,12 @@ PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int head
  * contexts are split into partitions of PKV_DEFAULT_PARTITION tokens that run
  * in parallel and are merged by log-sum-exp inside the same kernel (the last
  * partition of a request to finish merges them); requests that fit one
- * partition still finish in one pass.  The split needs
+ * partition still finish in one pass.  When a request can span at least 8
+ * partitions and the grid fills at least three waves of resident CTAs, odd
+ * partitions start a quarter partition early, so that partition lengths
+ * alternate (P - P/4, P + P/4; the count per request is unchanged) and the
+ * CTAs of one wave do not all end together; the result is the same up to
+ * rounding order.  The split needs
  * pkv_decode_workspace_size(num_seqs, num_q_heads, 128, max_blocks_per_seq *
  * block_size, PKV_DEFAULT_PARTITION) bytes of 256-byte-aligned workspace whose
  * counter region is zero when the workspace is first used (zero-fill a new
